@@ -1,0 +1,189 @@
+/*
+ * llama_layer.h -- C ABI of the GB300 (sm_103a) LLaMA-style pre-norm decoder layer.
+ *
+ * What is computed (pages cited by title and section):
+ *   h   = x + o_proj(GQA_causal(RoPE(q), RoPE(k), v)),  [q|k|v] = RMSNorm_1(x) W_qkv^T
+ *   out = h + down(SiLU(RMSNorm_2(h) W_gate^T) * (RMSNorm_2(h) W_up^T))
+ * "05 LLaMA3 Block — 从零件到发动机" §3.1 and §4.2 (pre-norm order, two separate norms);
+ * "12 · 从 Transformer 到 LLaMA 系列" §八 (RMSNorm, SwiGLU, GQA attention, LlamaModel);
+ * "第 10 章：现代 LLaMA 架构" §3 (even/odd RoPE pairs), §7 (KV-cache prefill/decode),
+ * §9 (llama_block(x, position_ids, past_kv)).
+ *
+ * Conventions for every entry point:
+ *  - Pointers named "device" are caller-owned device memory; the library never
+ *    allocates or frees device memory and never synchronises, except
+ *    llama_get_device_status().  Scratch space is the caller's `workspace`, sized
+ *    by the matching *_workspace_bytes() call.
+ *  - Work is enqueued asynchronously on `cuda_stream` (a cudaStream_t; NULL = the
+ *    legacy default stream) of the current device.
+ *  - Layouts are row-major.  Linear weights use the nn.Linear layout [out, in]:
+ *    wq [H*D, d], wk/wv [G*D, d], wo [d, H*D], w_gate/w_up [d_inter, d],
+ *    w_down [d, d_inter].  Norm gammas are [d].  Activations are [B, S, d].
+ *    The KV cache is K and V, each [B, G, max_T, D]; only G heads are stored.
+ *  - Element type of activations, weights, gammas and the cache = dims.dtype
+ *    (LLAMA_F32 or LLAMA_BF16); RoPE tables and logits are fp32.
+ *  - Device pointers must be 16-byte aligned.
+ *  - Return value: LLAMA_OK or a negative llama_status; errors never trap.
+ *    Errors found on the device (a wait that timed out, a position or token out
+ *    of range) are recorded in a per-device status word that
+ *    llama_get_device_status() returns and clears.
+ */
+#ifndef LLAMA_LAYER_H
+#define LLAMA_LAYER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LLAMA_OK = 0,
+  LLAMA_ERR_INVALID_ARG = -1,   /* null pointer, H % G != 0, odd D, S > max_pos or max_T, small workspace, misalignment */
+  LLAMA_ERR_UNSUPPORTED = -2,   /* a shape the tiled bf16 path does not cover (e.g. D != 128, d % 128 != 0) */
+  LLAMA_ERR_CUDA = -3,          /* a CUDA runtime error (launch failure, no device, ...) */
+  LLAMA_ERR_TIMEOUT = -4,       /* a bounded device-side wait expired; the kernel gave up and returned */
+  LLAMA_ERR_DEVICE_BOUNDS = -5  /* a device-side index check failed (position >= max_T or max_pos, token >= vocab) */
+} llama_status;
+
+typedef enum { LLAMA_F32 = 0, LLAMA_BF16 = 1 } llama_dtype;
+
+/* Layer hyper-parameters; mirrors the config fields of "第 10 章：现代 LLaMA 架构" §1
+ * (hidden_size, intermediate_size, num_attention_heads, num_key_value_heads, rms_norm_eps). */
+typedef struct {
+  int32_t d_model;     /* d */
+  int32_t n_heads;     /* H, query heads */
+  int32_t n_kv_heads;  /* G, key/value heads; H % G == 0 ("12 · 从 Transformer 到 LLaMA 系列" §八 Attention) */
+  int32_t head_dim;    /* D, even ("第 10 章：现代 LLaMA 架构" §3) */
+  int32_t d_inter;     /* SwiGLU hidden size */
+  float rms_eps;       /* inside the square root: rsqrt(mean(x^2) + eps) */
+  int32_t dtype;       /* llama_dtype */
+} llama_layer_dims;
+
+/* Device pointers of one layer's parameters (no biases). */
+typedef struct {
+  const void *attn_norm, *wq, *wk, *wv, *wo, *ffn_norm, *w_gate, *w_up, *w_down;
+} llama_layer_weights;
+
+/* One layer's cache: K and V device buffers, each [B, G, max_T, D] of dims.dtype. */
+typedef struct {
+  void *k, *v;
+  int32_t max_T;
+} llama_kv_cache;
+
+/* A stack of n_layers identical-shape layers plus embedding, final RMSNorm and an
+ * untied LM head ("12 · 从 Transformer 到 LLaMA 系列" §八 LlamaModel). */
+typedef struct {
+  int32_t n_layers;
+  int32_t vocab;
+  llama_layer_dims dims;
+  const llama_layer_weights *layers; /* HOST array of n_layers entries (device pointers inside) */
+  const void *final_norm;            /* [d] */
+  const void *embed;                 /* [vocab, d] */
+  const void *lm_head;               /* [vocab, d] */
+} llama_stack;
+
+/* ---------------------------------------------------------------- layer entry points */
+
+/* Workspace bytes that llama_layer_prefill needs for B sequences of S tokens. */
+int llama_layer_prefill_workspace_bytes(const llama_layer_dims *dims, int32_t B, int32_t S, size_t *bytes);
+
+/* Prefill: one decoder layer over B sequences of S tokens at positions 0..S-1
+ * ("12 · 从 Transformer 到 LLaMA 系列" §八 LlamaBlock.forward; "第 10 章：现代 LLaMA 架构" §7
+ * prefill).  x, out: device [B, S, d] (may not alias).  cos, sin: device fp32
+ * [max_pos, D/2] tables (angle p * base^(-2i/D), see llama_rope_tables).  The
+ * rotated K and the V of token s of sequence b are written to cache slot s
+ * (slots [0, S) of every sequence).  Requires S <= max_pos and S <= cache.max_T. */
+int llama_layer_prefill(const llama_layer_dims *dims, const llama_layer_weights *w, const void *x, void *out,
+                        const float *cos, const float *sin, int32_t max_pos, llama_kv_cache cache, int32_t B,
+                        int32_t S, void *workspace, size_t ws_bytes, void *cuda_stream);
+
+/* Workspace bytes that llama_layer_decode needs for B sequences and caches of max_T slots. */
+int llama_layer_decode_workspace_bytes(const llama_layer_dims *dims, int32_t B, int32_t max_T, size_t *bytes);
+
+/* Decode: one new token per sequence ("第 10 章：现代 LLaMA 架构" §7 decode and §3:
+ * position_id = past_len).  x, out: device [B, d].  positions: device int32 [B];
+ * token b sits at position p = positions[b], its rotated K and its V are written
+ * to cache slot p, and it attends to slots 0..p (p + 1 keys; the slots below p
+ * are the existing cache).  A p outside [0, min(max_T, max_pos)) is recorded as
+ * LLAMA_ERR_DEVICE_BOUNDS and that sequence's cache is left untouched. */
+int llama_layer_decode(const llama_layer_dims *dims, const llama_layer_weights *w, const void *x, void *out,
+                       const float *cos, const float *sin, int32_t max_pos, const int32_t *positions,
+                       llama_kv_cache cache, int32_t B, void *workspace, size_t ws_bytes, void *cuda_stream);
+
+/* Workspace bytes that llama_stack_forward needs. */
+int llama_stack_workspace_bytes(const llama_stack *stack, int32_t B, int32_t S, size_t *bytes);
+
+/* Stack forward: logits = lm_head(RMSNorm_final(layers(embed[tokens]))) ("12 · 从
+ * Transformer 到 LLaMA 系列" §八 LlamaModel.forward).  tokens: device int32 [B, S]
+ * (a token outside [0, vocab) is recorded as LLAMA_ERR_DEVICE_BOUNDS and embeds as
+ * zeros).  logits: device fp32 [B, S, vocab].  caches: NULL (K/V kept in the
+ * workspace) or a HOST array of n_layers caches that receive slots [0, S). */
+int llama_stack_forward(const llama_stack *stack, const int32_t *tokens, float *logits, const float *cos,
+                        const float *sin, int32_t max_pos, const llama_kv_cache *caches, int32_t B, int32_t S,
+                        void *workspace, size_t ws_bytes, void *cuda_stream);
+
+/* ---------------------------------------------------------------- the steps, one by one
+ * The layer entry points are compositions of these; they are exported so that each
+ * step can be checked and timed on its own. */
+
+/* y = gamma * x * rsqrt(mean(x^2) + eps) per row ("12 · 从 Transformer 到 LLaMA 系列" §八
+ * RMSNorm; "3.2 核心组件逐一拆解" §3.2.1: fp32 arithmetic).  x, y: device [rows, d];
+ * gamma: device [d]; all of dtype. */
+int llama_rmsnorm(const void *x, const void *gamma, void *y, int32_t rows, int32_t d, float eps, int32_t dtype,
+                  void *cuda_stream);
+
+/* C = A B^T ("12 · 从 Transformer 到 LLaMA 系列" §八: nn.Linear, y = x W^T).  A: device
+ * [M, K], B: device [N, K], both bf16; C: device [M, N], bf16 (c_f32 = 0) or fp32
+ * (c_f32 = 1).  K % 8 == 0. */
+int llama_linear_bf16(const void *A, const void *B, void *C, int32_t M, int32_t N, int32_t K, int32_t c_f32,
+                      void *cuda_stream);
+
+/* Causal grouped-query attention over a cache ("12 · 从 Transformer 到 LLaMA 系列" §八
+ * Attention; "深度学习进阶（三十）从 Transformer 到 LLaMA：现代 LLM 架构总览" §1.1
+ * softmax(QK^T / sqrt(D)) V).  q: device [B, H, S, D] at positions 0..S-1; cache
+ * slots [0, S) hold K, V; out: device [B, S, H*D].  Query head h reads KV head
+ * h / (H/G); key j is visible to query i iff j <= i. */
+int llama_attention_prefill(const llama_layer_dims *dims, const void *q, llama_kv_cache cache, void *out,
+                            int32_t B, int32_t S, void *cuda_stream);
+
+/* Workspace bytes of llama_attention_decode. */
+int llama_attention_decode_workspace_bytes(const llama_layer_dims *dims, int32_t B, int32_t max_T, size_t *bytes);
+
+/* One query per sequence at position positions[b] over cache slots 0..positions[b]
+ * ("第 10 章：现代 LLaMA 架构" §7: score shape [B, H, 1, T_cache + 1]).  q: device
+ * [B, H, D]; out: device [B, H*D]. */
+int llama_attention_decode(const llama_layer_dims *dims, const void *q, llama_kv_cache cache,
+                           const int32_t *positions, void *out, int32_t B, void *workspace, size_t ws_bytes,
+                           void *cuda_stream);
+
+/* ---------------------------------------------------------------- host helpers and status */
+
+/* RoPE tables on the HOST: cos/sin[p * (D/2) + i] = cos/sin(p * base^(-2i/D)), computed in
+ * double precision and rounded to nearest fp32 ("12 · 从 Transformer 到 LLaMA 系列" §八
+ * RotaryEmbedding; "深度学习进阶（三十）…" §4.2 theta_i = base^(-2i/d)).  cos_host, sin_host:
+ * caller-owned host arrays of max_pos * D/2 floats. */
+int llama_rope_tables(double base, int32_t head_dim, int32_t max_pos, float *cos_host, float *sin_host);
+
+/* Synchronises `cuda_stream`, then returns and clears the current device's status word
+ * (LLAMA_OK if no device-side error was recorded since the last call). */
+int llama_get_device_status(void *cuda_stream);
+
+/* Text of a status code (static storage). */
+const char *llama_status_string(int status);
+
+/* Test of the bounded-wait path: launches one CTA that waits on an mbarrier that
+ * nothing arrives at, for at most budget_ns nanoseconds (capped at 10 s), with the
+ * same wait routine the tensor-core kernels use; the wait then records
+ * LLAMA_ERR_TIMEOUT in the device status word and the kernel returns normally. */
+int llama_debug_wait_probe(uint64_t budget_ns, void *cuda_stream);
+
+/* Number of kernels the library enqueued on this process since load (for launch accounting). */
+uint64_t llama_kernel_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LLAMA_LAYER_H */

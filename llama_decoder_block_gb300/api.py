@@ -1,0 +1,165 @@
+"""Thin Python binding of the C ABI: torch tensors in, device pointers out.
+
+Every step runs in the library's CUDA kernels; this module only builds the argument
+structs, sizes workspaces and turns status codes into exceptions.  PyTorch provides
+device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+from . import _native as N
+
+DTYPES = {torch.float32: N.LLAMA_F32, torch.bfloat16: N.LLAMA_BF16}
+
+
+@dataclass(frozen=True)
+class Dims:
+    d_model: int
+    n_heads: int
+    n_kv_heads: int
+    head_dim: int
+    d_inter: int
+    rms_eps: float
+    dtype: torch.dtype
+
+    def c(self) -> N.LayerDims:
+        return N.LayerDims(self.d_model, self.n_heads, self.n_kv_heads, self.head_dim, self.d_inter,
+                           self.rms_eps, DTYPES[self.dtype])
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+
+
+def weights_struct(w: dict) -> N.LayerWeights:
+    return N.LayerWeights(*[_ptr(w[k]) for k in N.WEIGHT_FIELDS])
+
+
+def cache_struct(k: torch.Tensor, v: torch.Tensor) -> N.KVCache:
+    return N.KVCache(_ptr(k), _ptr(v), k.shape[2])
+
+
+def rope_tables(base: float, head_dim: int, max_pos: int) -> tuple[np.ndarray, np.ndarray]:
+    """Host cos/sin tables [max_pos, head_dim/2] fp32 (llama_rope_tables)."""
+    cos = np.empty((max_pos, head_dim // 2), dtype=np.float32)
+    sin = np.empty_like(cos)
+    N.check(N.lib().llama_rope_tables(base, head_dim, max_pos, cos.ctypes.data, sin.ctypes.data), "llama_rope_tables")
+    return cos, sin
+
+
+def prefill_workspace_bytes(dims: Dims, B: int, S: int) -> int:
+    n = ctypes.c_size_t()
+    d = dims.c()
+    N.check(N.lib().llama_layer_prefill_workspace_bytes(ctypes.byref(d), B, S, ctypes.byref(n)), "workspace")
+    return n.value
+
+
+def decode_workspace_bytes(dims: Dims, B: int, max_T: int) -> int:
+    n = ctypes.c_size_t()
+    d = dims.c()
+    N.check(N.lib().llama_layer_decode_workspace_bytes(ctypes.byref(d), B, max_T, ctypes.byref(n)), "workspace")
+    return n.value
+
+
+def workspace(nbytes: int, device) -> torch.Tensor:
+    return torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
+
+
+def layer_prefill(dims: Dims, w: dict, x, out, cos, sin, cache_k, cache_v, ws, stream=None) -> None:
+    B, S = x.shape[0], x.shape[1]
+    d = dims.c()
+    ww = weights_struct(w)
+    N.check(N.lib().llama_layer_prefill(ctypes.byref(d), ctypes.byref(ww), _ptr(x), _ptr(out), _ptr(cos), _ptr(sin),
+                                        cos.shape[0], cache_struct(cache_k, cache_v), B, S, _ptr(ws), ws.numel(),
+                                        _stream(stream)), "llama_layer_prefill")
+
+
+def layer_decode(dims: Dims, w: dict, x, out, cos, sin, positions, cache_k, cache_v, ws, stream=None) -> None:
+    d = dims.c()
+    ww = weights_struct(w)
+    N.check(N.lib().llama_layer_decode(ctypes.byref(d), ctypes.byref(ww), _ptr(x), _ptr(out), _ptr(cos), _ptr(sin),
+                                       cos.shape[0], _ptr(positions), cache_struct(cache_k, cache_v), x.shape[0],
+                                       _ptr(ws), ws.numel(), _stream(stream)), "llama_layer_decode")
+
+
+class StackArgs:
+    """Keeps the ctypes structs of a stack alive for as long as it is used."""
+
+    def __init__(self, dims: Dims, layers: list[dict], final_norm, embed, lm_head):
+        self.layer_structs = (N.LayerWeights * max(1, len(layers)))(*[weights_struct(w) for w in layers])
+        self.tensors = (layers, final_norm, embed, lm_head)
+        self.s = N.Stack(len(layers), embed.shape[0], dims.c(), self.layer_structs, _ptr(final_norm), _ptr(embed),
+                         _ptr(lm_head))
+
+    def workspace_bytes(self, B: int, S: int) -> int:
+        n = ctypes.c_size_t()
+        N.check(N.lib().llama_stack_workspace_bytes(ctypes.byref(self.s), B, S, ctypes.byref(n)), "workspace")
+        return n.value
+
+
+def stack_forward(st: StackArgs, tokens, logits, cos, sin, ws, caches=None, stream=None) -> None:
+    B, S = tokens.shape
+    cache_arr = None
+    if caches is not None:
+        cache_arr = (N.KVCache * len(caches))(*[cache_struct(k, v) for k, v in caches])
+    N.check(N.lib().llama_stack_forward(ctypes.byref(st.s), _ptr(tokens), _ptr(logits), _ptr(cos), _ptr(sin),
+                                        cos.shape[0], cache_arr, B, S, _ptr(ws), ws.numel(), _stream(stream)),
+            "llama_stack_forward")
+
+
+def rmsnorm(x, gamma, y, eps: float, stream=None) -> None:
+    d = x.shape[-1]
+    N.check(N.lib().llama_rmsnorm(_ptr(x), _ptr(gamma), _ptr(y), x.numel() // d, d, eps, DTYPES[x.dtype],
+                                  _stream(stream)), "llama_rmsnorm")
+
+
+def linear_bf16(a, b, c, stream=None) -> None:
+    M, K = a.shape
+    Nn = b.shape[0]
+    N.check(N.lib().llama_linear_bf16(_ptr(a), _ptr(b), _ptr(c), M, Nn, K, int(c.dtype == torch.float32),
+                                      _stream(stream)), "llama_linear_bf16")
+
+
+def attention_prefill(dims: Dims, q, cache_k, cache_v, out, stream=None) -> None:
+    B, _, S, _ = q.shape
+    d = dims.c()
+    N.check(N.lib().llama_attention_prefill(ctypes.byref(d), _ptr(q), cache_struct(cache_k, cache_v), _ptr(out), B, S,
+                                            _stream(stream)), "llama_attention_prefill")
+
+
+def attention_decode_workspace_bytes(dims: Dims, B: int, max_T: int) -> int:
+    n = ctypes.c_size_t()
+    d = dims.c()
+    N.check(N.lib().llama_attention_decode_workspace_bytes(ctypes.byref(d), B, max_T, ctypes.byref(n)), "workspace")
+    return n.value
+
+
+def attention_decode(dims: Dims, q, cache_k, cache_v, positions, out, ws, stream=None) -> None:
+    d = dims.c()
+    N.check(N.lib().llama_attention_decode(ctypes.byref(d), _ptr(q), cache_struct(cache_k, cache_v), _ptr(positions),
+                                           _ptr(out), q.shape[0], _ptr(ws), ws.numel(), _stream(stream)),
+            "llama_attention_decode")
+
+
+def device_status(stream=None) -> int:
+    """Synchronises the stream; returns and clears the device status word."""
+    return N.lib().llama_get_device_status(_stream(stream))
+
+
+def wait_probe(budget_ns: int, stream=None) -> None:
+    N.check(N.lib().llama_debug_wait_probe(budget_ns, _stream(stream)), "llama_debug_wait_probe")
+
+
+def launch_count() -> int:
+    return N.lib().llama_kernel_launch_count()

@@ -1,0 +1,419 @@
+// C entry points: argument validation, workspace carve-up and the order of the steps
+// of the pre-norm decoder layer ("05 LLaMA3 Block — 从零件到发动机" §4.2: save residual,
+// norm, sublayer, add back -- twice) on top of the kernels of the other files.
+#include <algorithm>
+#include <cstring>
+
+#include "common.cuh"
+#include "internal.h"
+
+using namespace llama;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Carves consecutive aligned regions out of the caller's workspace.
+struct Carver {
+  uint8_t* base;
+  size_t off = 0;
+  explicit Carver(void* b) : base(static_cast<uint8_t*>(b)) {}
+  void* take(size_t bytes) {
+    void* p = base ? base + off : nullptr;
+    off += align_up(bytes);
+    return p;
+  }
+};
+
+size_t esize(int dtype) { return dtype == LLAMA_BF16 ? 2 : 4; }
+
+int check_dims(const llama_layer_dims* d) {
+  if (d == nullptr) return LLAMA_ERR_INVALID_ARG;
+  if (d->d_model <= 0 || d->n_heads <= 0 || d->n_kv_heads <= 0 || d->head_dim <= 0 || d->d_inter <= 0)
+    return LLAMA_ERR_INVALID_ARG;
+  if (d->n_heads % d->n_kv_heads != 0) return LLAMA_ERR_INVALID_ARG;   // each KV head serves H/G query heads
+  if (d->head_dim % 2 != 0) return LLAMA_ERR_INVALID_ARG;              // RoPE rotates pairs
+  if (!(d->rms_eps >= 0.f)) return LLAMA_ERR_INVALID_ARG;
+  if (d->dtype != LLAMA_F32 && d->dtype != LLAMA_BF16) return LLAMA_ERR_INVALID_ARG;
+  if (d->dtype == LLAMA_BF16) {
+    // the tensor-core path: 128-wide head tiles and 128-row weight blocks
+    const int rep = d->n_heads / d->n_kv_heads;
+    if (d->head_dim != 128 || d->d_model % 128 != 0 || d->d_inter % 128 != 0) return LLAMA_ERR_UNSUPPORTED;
+    if (rep != 1 && rep != 2 && rep != 4 && rep != 8) return LLAMA_ERR_UNSUPPORTED;
+  } else {
+    if (d->head_dim > 256) return LLAMA_ERR_UNSUPPORTED;
+  }
+  return LLAMA_OK;
+}
+
+int check_weights(const llama_layer_weights* w) {
+  if (w == nullptr) return LLAMA_ERR_INVALID_ARG;
+  const void* ptrs[] = {w->attn_norm, w->wq, w->wk, w->wv, w->wo, w->ffn_norm, w->w_gate, w->w_up, w->w_down};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return LLAMA_ERR_INVALID_ARG;
+  return LLAMA_OK;
+}
+
+struct PrefillWs {
+  void *xn, *q, *o, *h, *a;
+};
+
+size_t prefill_ws(const llama_layer_dims* d, int B, int S, void* base, PrefillWs* out) {
+  const size_t es = esize(d->dtype);
+  const size_t M = static_cast<size_t>(B) * S;
+  Carver c(base);
+  PrefillWs w;
+  w.xn = c.take(M * d->d_model * es);                      // RMSNorm output (both norms)
+  w.q = c.take(M * d->n_heads * d->head_dim * es);         // [B, H, S, D]
+  w.o = c.take(M * d->n_heads * d->head_dim * es);         // attention output [B, S, H*D]
+  w.h = c.take(M * d->d_model * es);                       // attention half output
+  w.a = c.take(M * d->d_inter * es);                       // SiLU(gate) * up
+  if (out) *out = w;
+  return c.off;
+}
+
+struct DecodeWs {
+  void *xn, *q, *o, *h, *a, *part, *attn;
+};
+
+size_t decode_part_floats(const llama_layer_dims* d, int B, int num_sms) {
+  const int qkv = (d->n_heads + 2 * d->n_kv_heads) * d->head_dim;
+  const int Ns[4] = {qkv, d->d_model, 2 * d->d_inter, d->d_model};
+  const int Ks[4] = {d->d_model, d->n_heads * d->head_dim, d->d_model, d->d_inter};
+  size_t mx = 0;
+  for (int i = 0; i < 4; ++i) {
+    const size_t s = static_cast<size_t>(choose_splits(num_sms, Ns[i], Ks[i]));
+    mx = std::max(mx, s * B * Ns[i]);
+  }
+  return mx;
+}
+
+size_t decode_ws(const llama_layer_dims* d, int B, int max_T, int num_sms, void* base, DecodeWs* out) {
+  const size_t es = esize(d->dtype);
+  Carver c(base);
+  DecodeWs w;
+  w.xn = c.take(static_cast<size_t>(B) * d->d_model * es);
+  w.q = c.take(static_cast<size_t>(B) * d->n_heads * d->head_dim * es);
+  w.o = c.take(static_cast<size_t>(B) * d->n_heads * d->head_dim * es);
+  w.h = c.take(static_cast<size_t>(B) * d->d_model * es);
+  w.a = c.take(static_cast<size_t>(B) * d->d_inter * es);
+  if (d->dtype == LLAMA_BF16) {
+    w.part = c.take(decode_part_floats(d, B, num_sms) * sizeof(float));
+    w.attn = c.take(attn_decode_ws_bytes(B, d->n_heads, d->head_dim, max_T));
+  } else {
+    w.part = w.attn = nullptr;
+  }
+  if (out) *out = w;
+  return c.off;
+}
+
+int num_sms_current(int* sms) {
+  Ctx c;
+  int rc = make_ctx(nullptr, &c);
+  if (rc != LLAMA_OK) return rc;
+  *sms = c.num_sms;
+  return LLAMA_OK;
+}
+
+int prefill_impl(const Ctx& c, const llama_layer_dims* d, const llama_layer_weights* w, const void* x, void* out,
+                 const float* cos, const float* sin, int max_pos, llama_kv_cache cache, int B, int S, void* ws) {
+  PrefillWs p;
+  prefill_ws(d, B, S, ws, &p);
+  const int M = B * S, dm = d->d_model, H = d->n_heads, G = d->n_kv_heads, D = d->head_dim, I = d->d_inter;
+  int rc;
+  if (d->dtype == LLAMA_BF16) {
+    if ((rc = rmsnorm(c, x, w->attn_norm, p.xn, M, dm, d->rms_eps, d->dtype))) return rc;
+    if ((rc = gemm_qkv_rope(c, p.xn, w->wq, w->wk, w->wv, B, S, dm, H, G, D, cos, sin, p.q, cache.k, cache.v,
+                            cache.max_T)))
+      return rc;
+    if ((rc = attn_prefill_tc(c, p.q, cache.k, cache.v, p.o, B, S, H, G, D, cache.max_T))) return rc;
+    if ((rc = gemm_residual(c, p.o, w->wo, x, p.h, M, dm, H * D))) return rc;
+    if ((rc = rmsnorm(c, p.h, w->ffn_norm, p.xn, M, dm, d->rms_eps, d->dtype))) return rc;
+    if ((rc = gemm_swiglu(c, p.xn, w->w_gate, w->w_up, p.a, M, I, dm))) return rc;
+    return gemm_residual(c, p.a, w->w_down, p.h, out, M, dm, I);
+  }
+  const float* xf = static_cast<const float*>(x);
+  float* xn = static_cast<float*>(p.xn);
+  float* h = static_cast<float*>(p.h);
+  float* a = static_cast<float*>(p.a);
+  if ((rc = rmsnorm(c, x, w->attn_norm, p.xn, M, dm, d->rms_eps, d->dtype))) return rc;
+  if ((rc = simt_qkv_rope(c, xn, static_cast<const float*>(w->wq), static_cast<const float*>(w->wk),
+                          static_cast<const float*>(w->wv), B, S, dm, H, G, D, cos, sin, nullptr, max_pos,
+                          static_cast<float*>(p.q), static_cast<float*>(cache.k), static_cast<float*>(cache.v),
+                          cache.max_T)))
+    return rc;
+  if ((rc = simt_attention(c, static_cast<float*>(p.q), static_cast<float*>(cache.k), static_cast<float*>(cache.v),
+                           nullptr, static_cast<float*>(p.o), B, S, H, G, D, cache.max_T, max_pos)))
+    return rc;
+  if ((rc = simt_linear(c, 1, static_cast<float*>(p.o), static_cast<const float*>(w->wo), nullptr, nullptr, xf, h, M,
+                        dm, H * D)))
+    return rc;
+  if ((rc = rmsnorm(c, h, w->ffn_norm, xn, M, dm, d->rms_eps, d->dtype))) return rc;
+  if ((rc = simt_linear(c, 2, xn, static_cast<const float*>(w->w_gate), static_cast<const float*>(w->w_up), nullptr,
+                        nullptr, a, M, I, dm)))
+    return rc;
+  return simt_linear(c, 1, a, static_cast<const float*>(w->w_down), nullptr, nullptr, h, static_cast<float*>(out), M,
+                     dm, I);
+}
+
+int check_prefill_args(const llama_layer_dims* d, const llama_layer_weights* w, const void* x, const void* out,
+                       const float* cos, const float* sin, int max_pos, const llama_kv_cache& cache, int B, int S) {
+  int rc = check_dims(d);
+  if (rc) return rc;
+  if ((rc = check_weights(w))) return rc;
+  if (!x || !out || !cos || !sin || !cache.k || !cache.v) return LLAMA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(out) || !aligned16(cos) || !aligned16(sin) || !aligned16(cache.k) ||
+      !aligned16(cache.v))
+    return LLAMA_ERR_INVALID_ARG;
+  if (x == out) return LLAMA_ERR_INVALID_ARG;
+  if (B <= 0 || S <= 0 || max_pos <= 0 || cache.max_T <= 0) return LLAMA_ERR_INVALID_ARG;
+  if (S > max_pos || S > cache.max_T) return LLAMA_ERR_INVALID_ARG;
+  return LLAMA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int llama_layer_prefill_workspace_bytes(const llama_layer_dims* dims, int32_t B, int32_t S, size_t* bytes) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if (bytes == nullptr || B <= 0 || S <= 0) return LLAMA_ERR_INVALID_ARG;
+  *bytes = prefill_ws(dims, B, S, nullptr, nullptr);
+  return LLAMA_OK;
+}
+
+int llama_layer_prefill(const llama_layer_dims* dims, const llama_layer_weights* w, const void* x, void* out,
+                        const float* cos, const float* sin, int32_t max_pos, llama_kv_cache cache, int32_t B,
+                        int32_t S, void* workspace, size_t ws_bytes, void* cuda_stream) {
+  int rc = check_prefill_args(dims, w, x, out, cos, sin, max_pos, cache, B, S);
+  if (rc) return rc;
+  if (!workspace || !aligned16(workspace) || ws_bytes < prefill_ws(dims, B, S, nullptr, nullptr))
+    return LLAMA_ERR_INVALID_ARG;
+  Ctx c;
+  if ((rc = make_ctx(cuda_stream, &c))) return rc;
+  return prefill_impl(c, dims, w, x, out, cos, sin, max_pos, cache, B, S, workspace);
+}
+
+int llama_layer_decode_workspace_bytes(const llama_layer_dims* dims, int32_t B, int32_t max_T, size_t* bytes) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if (bytes == nullptr || B <= 0 || max_T <= 0) return LLAMA_ERR_INVALID_ARG;
+  int sms = 0;
+  if (dims->dtype == LLAMA_BF16 && (rc = num_sms_current(&sms))) return rc;
+  *bytes = decode_ws(dims, B, max_T, sms, nullptr, nullptr);
+  return LLAMA_OK;
+}
+
+int llama_layer_decode(const llama_layer_dims* dims, const llama_layer_weights* w, const void* x, void* out,
+                       const float* cos, const float* sin, int32_t max_pos, const int32_t* positions,
+                       llama_kv_cache cache, int32_t B, void* workspace, size_t ws_bytes, void* cuda_stream) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if ((rc = check_weights(w))) return rc;
+  if (!x || !out || !cos || !sin || !positions || !cache.k || !cache.v || !workspace) return LLAMA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(out) || !aligned16(cos) || !aligned16(sin) || !aligned16(cache.k) ||
+      !aligned16(cache.v) || !aligned16(workspace) || x == out)
+    return LLAMA_ERR_INVALID_ARG;
+  if (B <= 0 || max_pos <= 0 || cache.max_T <= 0) return LLAMA_ERR_INVALID_ARG;
+  Ctx c;
+  if ((rc = make_ctx(cuda_stream, &c))) return rc;
+  if (ws_bytes < decode_ws(dims, B, cache.max_T, c.num_sms, nullptr, nullptr)) return LLAMA_ERR_INVALID_ARG;
+  DecodeWs p;
+  decode_ws(dims, B, cache.max_T, c.num_sms, workspace, &p);
+  const int dm = dims->d_model, H = dims->n_heads, G = dims->n_kv_heads, D = dims->head_dim, I = dims->d_inter;
+  const int T = cache.max_T;
+  if (dims->dtype == LLAMA_BF16) {
+    float* P = static_cast<float*>(p.part);
+    const int qkv = (H + 2 * G) * D;
+    if ((rc = rmsnorm(c, x, w->attn_norm, p.xn, B, dm, dims->rms_eps, dims->dtype))) return rc;
+    {
+      const void* W3[3] = {w->wq, w->wk, w->wv};
+      const int R3[3] = {H * D, G * D, G * D};
+      const int s = choose_splits(c.num_sms, qkv, dm);
+      if ((rc = gemm_tokens_partial(c, W3, R3, 3, p.xn, B, dm, s, P))) return rc;
+      if ((rc = fix_qkv_rope(c, P, s, B, H, G, D, positions, max_pos, cos, sin, p.q, cache.k, cache.v, T))) return rc;
+    }
+    if ((rc = attn_decode(c, dims->dtype, p.q, cache.k, cache.v, positions, p.o, B, H, G, D, T, max_pos, p.attn)))
+      return rc;
+    {
+      const void* W1[1] = {w->wo};
+      const int R1[1] = {dm};
+      const int s = choose_splits(c.num_sms, dm, H * D);
+      if ((rc = gemm_tokens_partial(c, W1, R1, 1, p.o, B, H * D, s, P))) return rc;
+      if ((rc = fix_residual(c, P, s, B, dm, x, p.h))) return rc;
+    }
+    if ((rc = rmsnorm(c, p.h, w->ffn_norm, p.xn, B, dm, dims->rms_eps, dims->dtype))) return rc;
+    {
+      const void* W2[2] = {w->w_gate, w->w_up};
+      const int R2[2] = {I, I};
+      const int s = choose_splits(c.num_sms, 2 * I, dm);
+      if ((rc = gemm_tokens_partial(c, W2, R2, 2, p.xn, B, dm, s, P))) return rc;
+      if ((rc = fix_swiglu(c, P, s, B, I, p.a))) return rc;
+    }
+    {
+      const void* W1[1] = {w->w_down};
+      const int R1[1] = {dm};
+      const int s = choose_splits(c.num_sms, dm, I);
+      if ((rc = gemm_tokens_partial(c, W1, R1, 1, p.a, B, I, s, P))) return rc;
+      return fix_residual(c, P, s, B, dm, p.h, out);
+    }
+  }
+  float* xn = static_cast<float*>(p.xn);
+  float* h = static_cast<float*>(p.h);
+  float* a = static_cast<float*>(p.a);
+  if ((rc = rmsnorm(c, x, w->attn_norm, xn, B, dm, dims->rms_eps, dims->dtype))) return rc;
+  if ((rc = simt_qkv_rope(c, xn, static_cast<const float*>(w->wq), static_cast<const float*>(w->wk),
+                          static_cast<const float*>(w->wv), B, 1, dm, H, G, D, cos, sin, positions, max_pos,
+                          static_cast<float*>(p.q), static_cast<float*>(cache.k), static_cast<float*>(cache.v), T)))
+    return rc;
+  if ((rc = simt_attention(c, static_cast<float*>(p.q), static_cast<float*>(cache.k), static_cast<float*>(cache.v),
+                           positions, static_cast<float*>(p.o), B, 1, H, G, D, T, max_pos)))
+    return rc;
+  if ((rc = simt_linear(c, 1, static_cast<float*>(p.o), static_cast<const float*>(w->wo), nullptr, nullptr,
+                        static_cast<const float*>(x), h, B, dm, H * D)))
+    return rc;
+  if ((rc = rmsnorm(c, h, w->ffn_norm, xn, B, dm, dims->rms_eps, dims->dtype))) return rc;
+  if ((rc = simt_linear(c, 2, xn, static_cast<const float*>(w->w_gate), static_cast<const float*>(w->w_up), nullptr,
+                        nullptr, a, B, I, dm)))
+    return rc;
+  return simt_linear(c, 1, a, static_cast<const float*>(w->w_down), nullptr, nullptr, h, static_cast<float*>(out), B,
+                     dm, I);
+}
+
+int llama_stack_workspace_bytes(const llama_stack* st, int32_t B, int32_t S, size_t* bytes) {
+  if (st == nullptr || bytes == nullptr || B <= 0 || S <= 0) return LLAMA_ERR_INVALID_ARG;
+  int rc = check_dims(&st->dims);
+  if (rc) return rc;
+  const size_t es = esize(st->dims.dtype);
+  const size_t M = static_cast<size_t>(B) * S;
+  size_t total = 0;
+  total += 2 * align_up(M * st->dims.d_model * es);                                           // ping-pong activations
+  total += 2 * align_up(M * st->dims.n_kv_heads * st->dims.head_dim * es);                    // K/V if no caches
+  total += align_up(prefill_ws(&st->dims, B, S, nullptr, nullptr));
+  *bytes = total;
+  return LLAMA_OK;
+}
+
+int llama_stack_forward(const llama_stack* st, const int32_t* tokens, float* logits, const float* cos,
+                        const float* sin, int32_t max_pos, const llama_kv_cache* caches, int32_t B, int32_t S,
+                        void* workspace, size_t ws_bytes, void* cuda_stream) {
+  if (st == nullptr || tokens == nullptr || logits == nullptr || workspace == nullptr) return LLAMA_ERR_INVALID_ARG;
+  if (st->n_layers < 0 || st->vocab <= 0 || st->final_norm == nullptr || st->embed == nullptr ||
+      st->lm_head == nullptr || (st->n_layers > 0 && st->layers == nullptr))
+    return LLAMA_ERR_INVALID_ARG;
+  if (!aligned16(tokens) || !aligned16(logits) || !aligned16(workspace) || !aligned16(st->embed) ||
+      !aligned16(st->lm_head) || !aligned16(st->final_norm))
+    return LLAMA_ERR_INVALID_ARG;
+  size_t need = 0;
+  int rc = llama_stack_workspace_bytes(st, B, S, &need);
+  if (rc) return rc;
+  if (ws_bytes < need) return LLAMA_ERR_INVALID_ARG;
+  const llama_layer_dims* d = &st->dims;
+  if (d->dtype == LLAMA_BF16 && st->vocab % 8 != 0) return LLAMA_ERR_UNSUPPORTED;
+  if ((d->d_model * esize(d->dtype)) % 16 != 0) return LLAMA_ERR_UNSUPPORTED;
+  const size_t es = esize(d->dtype);
+  const size_t M = static_cast<size_t>(B) * S;
+  Carver cv(workspace);
+  void* xa = cv.take(M * d->d_model * es);
+  void* xb = cv.take(M * d->d_model * es);
+  void* ks = cv.take(M * d->n_kv_heads * d->head_dim * es);
+  void* vs = cv.take(M * d->n_kv_heads * d->head_dim * es);
+  void* lws = cv.take(prefill_ws(d, B, S, nullptr, nullptr));
+  for (int l = 0; l < st->n_layers; ++l) {
+    llama_kv_cache kc = caches ? caches[l] : llama_kv_cache{ks, vs, S};
+    if ((rc = check_prefill_args(d, &st->layers[l], xa, xb, cos, sin, max_pos, kc, B, S))) return rc;
+  }
+  if (st->n_layers == 0 && (S > max_pos || !cos || !sin)) return LLAMA_ERR_INVALID_ARG;
+  Ctx c;
+  if ((rc = make_ctx(cuda_stream, &c))) return rc;
+  if ((rc = embed_gather(c, tokens, st->embed, xa, static_cast<int>(M), static_cast<int>(d->d_model * es),
+                         st->vocab)))
+    return rc;
+  for (int l = 0; l < st->n_layers; ++l) {
+    llama_kv_cache kc = caches ? caches[l] : llama_kv_cache{ks, vs, S};
+    if ((rc = prefill_impl(c, d, &st->layers[l], xa, xb, cos, sin, max_pos, kc, B, S, lws))) return rc;
+    void* t = xa;
+    xa = xb;
+    xb = t;
+  }
+  // final RMSNorm (required by the pre-norm layout), then the untied LM head in fp32
+  if ((rc = rmsnorm(c, xa, st->final_norm, xb, static_cast<int>(M), d->d_model, d->rms_eps, d->dtype))) return rc;
+  if (d->dtype == LLAMA_BF16)
+    return gemm_plain(c, xb, st->lm_head, logits, static_cast<int>(M), st->vocab, d->d_model, true);
+  return simt_linear(c, 0, static_cast<const float*>(xb), static_cast<const float*>(st->lm_head), nullptr, nullptr,
+                     nullptr, logits, static_cast<int>(M), st->vocab, d->d_model);
+}
+
+int llama_rmsnorm(const void* x, const void* gamma, void* y, int32_t rows, int32_t d, float eps, int32_t dtype,
+                  void* cuda_stream) {
+  if (!x || !gamma || !y || rows < 0 || d <= 0 || !(eps >= 0.f) || (dtype != LLAMA_F32 && dtype != LLAMA_BF16))
+    return LLAMA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(gamma)) return LLAMA_ERR_INVALID_ARG;
+  Ctx c;
+  int rc = make_ctx(cuda_stream, &c);
+  if (rc) return rc;
+  return rmsnorm(c, x, gamma, y, rows, d, eps, dtype);
+}
+
+int llama_linear_bf16(const void* A, const void* B, void* C, int32_t M, int32_t N, int32_t K, int32_t c_f32,
+                      void* cuda_stream) {
+  if (!A || !B || !C || M <= 0 || N <= 0 || K <= 0) return LLAMA_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return LLAMA_ERR_INVALID_ARG;
+  if (K % 8 != 0 || N % 8 != 0) return LLAMA_ERR_UNSUPPORTED;
+  Ctx c;
+  int rc = make_ctx(cuda_stream, &c);
+  if (rc) return rc;
+  return gemm_plain(c, A, B, C, M, N, K, c_f32 != 0);
+}
+
+int llama_attention_prefill(const llama_layer_dims* dims, const void* q, llama_kv_cache cache, void* out, int32_t B,
+                            int32_t S, void* cuda_stream) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if (!q || !out || !cache.k || !cache.v || B <= 0 || S <= 0 || S > cache.max_T) return LLAMA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out) || !aligned16(cache.k) || !aligned16(cache.v)) return LLAMA_ERR_INVALID_ARG;
+  Ctx c;
+  if ((rc = make_ctx(cuda_stream, &c))) return rc;
+  if (dims->dtype == LLAMA_BF16)
+    return attn_prefill_tc(c, q, cache.k, cache.v, out, B, S, dims->n_heads, dims->n_kv_heads, dims->head_dim,
+                           cache.max_T);
+  return simt_attention(c, static_cast<const float*>(q), static_cast<const float*>(cache.k),
+                        static_cast<const float*>(cache.v), nullptr, static_cast<float*>(out), B, S, dims->n_heads,
+                        dims->n_kv_heads, dims->head_dim, cache.max_T, cache.max_T);
+}
+
+int llama_attention_decode_workspace_bytes(const llama_layer_dims* dims, int32_t B, int32_t max_T, size_t* bytes) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if (!bytes || B <= 0 || max_T <= 0) return LLAMA_ERR_INVALID_ARG;
+  *bytes = attn_decode_ws_bytes(B, dims->n_heads, dims->head_dim, max_T);
+  return LLAMA_OK;
+}
+
+int llama_attention_decode(const llama_layer_dims* dims, const void* q, llama_kv_cache cache,
+                           const int32_t* positions, void* out, int32_t B, void* workspace, size_t ws_bytes,
+                           void* cuda_stream) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if (!q || !out || !cache.k || !cache.v || !positions || B <= 0 || cache.max_T <= 0) return LLAMA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out) || !aligned16(cache.k) || !aligned16(cache.v)) return LLAMA_ERR_INVALID_ARG;
+  Ctx c;
+  if ((rc = make_ctx(cuda_stream, &c))) return rc;
+  if (dims->dtype == LLAMA_BF16) {
+    if (!workspace || !aligned16(workspace) ||
+        ws_bytes < attn_decode_ws_bytes(B, dims->n_heads, dims->head_dim, cache.max_T))
+      return LLAMA_ERR_INVALID_ARG;
+    return attn_decode(c, dims->dtype, q, cache.k, cache.v, positions, out, B, dims->n_heads, dims->n_kv_heads,
+                       dims->head_dim, cache.max_T, cache.max_T, workspace);
+  }
+  return simt_attention(c, static_cast<const float*>(q), static_cast<const float*>(cache.k),
+                        static_cast<const float*>(cache.v), positions, static_cast<float*>(out), B, 1, dims->n_heads,
+                        dims->n_kv_heads, dims->head_dim, cache.max_T, cache.max_T);
+}
+
+}  // extern "C"

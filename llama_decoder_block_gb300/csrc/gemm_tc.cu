@@ -1,0 +1,530 @@
+// Persistent, warp-specialised tcgen05 GEMM for sm_103a with fused epilogues.
+//
+// C = X W^T ("12 · 从 Transformer 到 LLaMA 系列" §八: every projection of the layer is an
+// nn.Linear without bias).  One CTA per SM walks a list of output tiles:
+//   warp 0     TMA producer: 128x64 A tile + BNx64 B tile per stage (128-byte swizzle)
+//   warp 1     TMEM allocator and MMA issuer: tcgen05.mma 128xBNx16 into a TMEM accumulator
+//   warps 2-5  epilogue: tcgen05.ld of the accumulator rows, fused op, stores to HBM
+// Two TMEM accumulators let the epilogue of tile i overlap the main loop of tile i+1.
+// Epilogues: plain store (bf16 / fp32), residual add (o_proj, down_proj;
+// "05 LLaMA3 Block — 从零件到发动机" §4.2 steps ④ ⑧), SiLU(gate) * up
+// ("3.2 核心组件逐一拆解" §3.2.2; gate and up tiles share one accumulator), QKV with
+// even/odd RoPE and the scatter of k, v into the cache layout ("第 10 章：现代 LLaMA 架构"
+// §3, §6), and fp32 split-K partials for the weight-streaming (few-token) form.
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace llama {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int A_TILE_BYTES = BM * BK * 2;
+constexpr int NUM_THREADS = 192;
+
+enum Epi : int { EPI_BF16 = 0, EPI_F32 = 1, EPI_RESID = 2, EPI_SWIGLU = 3, EPI_QKV = 4, EPI_PARTIAL = 5 };
+
+// How a 128-row block of an operand maps to one of the kernel's tensor maps.
+struct RowMap {
+  int nseg;          // 1..3 row-concatenated matrices
+  int seg_end[3];    // cumulative row ends (multiples of 128)
+  int interleave;    // 1: 256-row block j = [map0 rows 128j.. | map1 rows 128j..]
+};
+
+struct TMaps {
+  CUtensorMap m[4];
+};
+
+struct Params {
+  int M, N, K;                  // kernel frame: C[M, N] = A[M, K] B[N, K]^T
+  int num_mb, num_nb, num_splits, kb_per_split, num_kb;
+  int group_m;
+  RowMap amap, bmap;
+  int a_map0, b_map0;
+  void* out;
+  long long ldo;
+  const __nv_bfloat16* resid;
+  long long ldr;
+  // QKV + RoPE
+  const float* cos;
+  const float* sin;
+  int S, H, G, D, T_max;
+  __nv_bfloat16* q_out;
+  __nv_bfloat16* k_cache;
+  __nv_bfloat16* v_cache;
+  int* status;
+};
+
+__device__ __forceinline__ void resolve_rows(const RowMap& rm, int vrow, int& map, int& row) {
+  if (rm.interleave) {
+    map = (vrow >> 7) & 1;
+    row = (vrow >> 8) << 7;
+    return;
+  }
+  map = 0;
+  int start = 0;
+  if (rm.nseg > 1 && vrow >= rm.seg_end[0]) { map = 1; start = rm.seg_end[0]; }
+  if (rm.nseg > 2 && vrow >= rm.seg_end[1]) { map = 2; start = rm.seg_end[1]; }
+  row = vrow - start;
+}
+
+__device__ __forceinline__ void tile_coords(const Params& p, int t, int& mb, int& nb, int& split) {
+  split = t % p.num_splits;
+  t /= p.num_splits;
+  const int per_group = p.group_m * p.num_nb;
+  const int g = t / per_group, r = t % per_group;
+  const int first_m = g * p.group_m;
+  const int gm = min(p.group_m, p.num_mb - first_m);
+  mb = first_m + r % gm;
+  nb = r / gm;
+}
+
+// ------------------------------------------------------------------ epilogue helpers
+
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v, int valid) {
+  if (valid >= 32) {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      uint4 w;
+      w.x = pack_bf16(v[8 * g + 0], v[8 * g + 1]);
+      w.y = pack_bf16(v[8 * g + 2], v[8 * g + 3]);
+      w.z = pack_bf16(v[8 * g + 4], v[8 * g + 5]);
+      w.w = pack_bf16(v[8 * g + 6], v[8 * g + 7]);
+      d4[g] = w;
+    }
+  } else {
+    for (int i = 0; i < valid; ++i) dst[i] = __float2bfloat16_rn(v[i]);
+  }
+}
+
+__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float* v, int valid) {
+  if (valid >= 32) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const uint4 w = s4[g];
+      v[8 * g + 0] = bf16_lo(w.x); v[8 * g + 1] = bf16_hi(w.x);
+      v[8 * g + 2] = bf16_lo(w.y); v[8 * g + 3] = bf16_hi(w.y);
+      v[8 * g + 4] = bf16_lo(w.z); v[8 * g + 5] = bf16_hi(w.z);
+      v[8 * g + 6] = bf16_lo(w.w); v[8 * g + 7] = bf16_hi(w.w);
+    }
+  } else {
+    for (int i = 0; i < 32; ++i) v[i] = i < valid ? __bfloat162float(src[i]) : 0.f;
+  }
+}
+
+template <int BN, int EPI, int STAGES>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ TMaps tm, const Params p) {
+  constexpr int B_TILE_BYTES = BN * BK * 2;
+  constexpr int B_BOX_ROWS = BN >= 128 ? 128 : BN;
+  constexpr int B_BOXES = BN / B_BOX_ROWS;
+  constexpr uint32_t STAGE_TX = A_TILE_BYTES + B_TILE_BYTES;
+  constexpr uint32_t TMEM_COLS = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
+  constexpr uint32_t IDESC = idesc_bf16(BM, BN, false);
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_TILE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_TILE_BYTES);
+  uint64_t* full_bar = bars;
+  uint64_t* empty_bar = bars + STAGES;
+  uint64_t* tfull_bar = bars + 2 * STAGES;
+  uint64_t* tempty_bar = bars + 2 * STAGES + 2;
+  uint64_t* drain_bar = bars + 2 * STAGES + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int num_tiles = p.num_mb * p.num_nb * p.num_splits;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(smem_u32(full_bar + i), 1);
+      mbar_init(smem_u32(empty_bar + i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(tfull_bar + i), 1);
+      mbar_init(smem_u32(tempty_bar + i), 4);
+    }
+    mbar_init(smem_u32(drain_bar), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < 4; ++i) tma_prefetch_desc(&tm.m[i]);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ TMA producer
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t used_mask = 0, last_parity = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        int mb, nb, split;
+        tile_coords(p, t, mb, nb, split);
+        const int kb0 = split * p.kb_per_split;
+        const int kb1 = min(kb0 + p.kb_per_split, p.num_kb);
+        int a_map, a_row;
+        resolve_rows(p.amap, mb * BM, a_map, a_row);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(smem_u32(empty_bar + stage), phase ^ 1u, p.status, abort_flag)) { ok = false; break; }
+          const uint32_t fb = smem_u32(full_bar + stage);
+          mbar_expect_tx(fb, STAGE_TX);
+          tma_load_2d(smem_u32(sA + stage * A_TILE_BYTES), &tm.m[p.a_map0 + a_map], fb, kb * BK, a_row);
+#pragma unroll
+          for (int bx = 0; bx < B_BOXES; ++bx) {
+            int b_map, b_row;
+            resolve_rows(p.bmap, nb * BN + bx * B_BOX_ROWS, b_map, b_row);
+            tma_load_2d(smem_u32(sB + stage * B_TILE_BYTES + bx * B_BOX_ROWS * 128), &tm.m[p.b_map0 + b_map], fb,
+                        kb * BK, b_row);
+          }
+          used_mask |= 1u << stage;
+          last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        // leave no copy in flight: wait (bounded) for the last load into every stage used
+        for (int s = 0; s < STAGES; ++s)
+          if (used_mask & (1u << s))
+            mbar_wait_slow(smem_u32(full_bar + s), (last_parity >> s) & 1u, nullptr, nullptr, kWaitBudgetNs);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      bool issued = false;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        int mb, nb, split;
+        tile_coords(p, t, mb, nb, split);
+        const int kb0 = split * p.kb_per_split;
+        const int kb1 = min(kb0 + p.kb_per_split, p.num_kb);
+        if (!mbar_wait(smem_u32(tempty_bar + acc), acc_phase ^ 1u, p.status, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(smem_u32(full_bar + stage), phase, p.status, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(sA + stage * A_TILE_BYTES);
+          const uint32_t b_addr = smem_u32(sB + stage * B_TILE_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t ad = sdesc_sw128(a_addr + k * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(b_addr + k * 32, 16, 1024);
+            tc_mma_bf16(d_tmem, ad, bd, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+          }
+          issued = true;
+          tc_commit(smem_u32(empty_bar + stage));
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(smem_u32(tfull_bar + acc));
+        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      }
+      if (!ok && issued) {
+        // all MMAs of this thread must finish before the TMEM is released
+        tc_commit(smem_u32(drain_bar));
+        mbar_wait_slow(smem_u32(drain_bar), 0, nullptr, nullptr, kWaitBudgetNs);
+      }
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue warps 2..5
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+      int mb, nb, split;
+      tile_coords(p, t, mb, nb, split);
+      if (!mbar_wait(smem_u32(tfull_bar + acc), acc_phase, p.status, abort_flag)) break;
+      tc_fence_after();
+      const uint32_t t_acc = tmem_base + t_lane + static_cast<uint32_t>(acc * BN);
+      const int m = mb * BM + row;
+      uint32_t r[32];
+      float v[32];
+
+      if constexpr (EPI == EPI_BF16 || EPI == EPI_F32 || EPI == EPI_RESID) {
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          tmem_ld32(t_acc + c * 32, r);
+          const int n0 = nb * BN + c * 32;
+          const int valid = min(32, p.N - n0);
+          if (m < p.M && valid > 0) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+            if constexpr (EPI == EPI_F32) {
+              float* dst = static_cast<float*>(p.out) + m * p.ldo + n0;
+              if (valid >= 32) {
+                float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+                for (int g = 0; g < 8; ++g) d4[g] = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+              } else {
+                for (int i = 0; i < valid; ++i) dst[i] = v[i];
+              }
+            } else {
+              if constexpr (EPI == EPI_RESID) {
+                float rr[32];
+                load_bf16x32(p.resid + m * p.ldr + n0, rr, valid);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] += rr[i];
+              }
+              store_bf16x32(static_cast<__nv_bfloat16*>(p.out) + m * p.ldo + n0, v, valid);
+            }
+          }
+        }
+      } else if constexpr (EPI == EPI_SWIGLU) {
+        // columns [0,128) of the tile are gate rows 128*nb.., [128,256) the matching up rows
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t u[32];
+          tmem_ld32(t_acc + c * 32, r);
+          tmem_ld32(t_acc + 128 + c * 32, u);
+          const int n0 = nb * 128 + c * 32;
+          const int valid = min(32, p.N - n0);
+          if (m < p.M && valid > 0) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = silu_f(__uint_as_float(r[i])) * __uint_as_float(u[i]);
+            store_bf16x32(static_cast<__nv_bfloat16*>(p.out) + m * p.ldo + n0, v, valid);
+          }
+        }
+      } else if constexpr (EPI == EPI_QKV) {
+        // each 128-column half of the tile is one head of [q heads | k heads | v heads]
+        const int b = m / p.S, s = m - (m / p.S) * p.S;
+        const int half_d = p.D >> 1;
+#pragma unroll 1
+        for (int hf = 0; hf < 2; ++hf) {
+          const int hh = nb * 2 + hf;
+          if (hh >= p.H + 2 * p.G) break;
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            tmem_ld32(t_acc + hf * 128 + c * 32, r);
+            if (m >= p.M) continue;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+            __nv_bfloat16* dst;
+            if (hh < p.H + p.G) {
+              // RoPE on q and k: pair (2i, 2i+1) rotated by angle s * base^(-2i/D)
+              const float* cr = p.cos + static_cast<long long>(s) * half_d + c * 16;
+              const float* sr = p.sin + static_cast<long long>(s) * half_d + c * 16;
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const float cs = cr[i], sn = sr[i];
+                const float e = v[2 * i], o = v[2 * i + 1];
+                v[2 * i] = e * cs - o * sn;
+                v[2 * i + 1] = e * sn + o * cs;
+              }
+            }
+            if (hh < p.H)
+              dst = p.q_out + ((static_cast<long long>(b) * p.H + hh) * p.S + s) * p.D;
+            else if (hh < p.H + p.G)
+              dst = p.k_cache + ((static_cast<long long>(b) * p.G + (hh - p.H)) * p.T_max + s) * p.D;
+            else
+              dst = p.v_cache + ((static_cast<long long>(b) * p.G + (hh - p.H - p.G)) * p.T_max + s) * p.D;
+            store_bf16x32(dst + c * 32, v, 32);
+          }
+        }
+      } else if constexpr (EPI == EPI_PARTIAL) {
+        // kernel M = weight rows, N = tokens: P[split][token][row] in fp32
+        float* P = static_cast<float*>(p.out);
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          tmem_ld32(t_acc + c * 32, r);
+          if (m < p.M) {
+            const int n0 = nb * BN + c * 32;
+#pragma unroll 4
+            for (int i = 0; i < 32; ++i) {
+              const int n = n0 + i;
+              if (n < p.N) P[(static_cast<long long>(split) * p.N + n) * p.ldo + m] = __uint_as_float(r[i]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(tempty_bar + acc));
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+template <int BN, int EPI, int STAGES>
+constexpr size_t smem_bytes() {
+  return 1024 + STAGES * (A_TILE_BYTES + BN * BK * 2) + (2 * STAGES + 5) * 8 + 16;
+}
+
+template <int BN, int EPI, int STAGES>
+int launch(const Ctx& c, const TMaps& tm, Params p) {
+  auto kern = gemm_tc_kernel<BN, EPI, STAGES>;
+  constexpr size_t smem = smem_bytes<BN, EPI, STAGES>();
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  });
+  if (attr_err != cudaSuccess) return LLAMA_ERR_CUDA;
+  p.status = c.status;
+  const int tiles = p.num_mb * p.num_nb * p.num_splits;
+  if (tiles == 0) return LLAMA_OK;
+  const int grid = std::min(tiles, c.num_sms);
+  kern<<<grid, NUM_THREADS, smem, c.stream>>>(tm, p);
+  return after_launch();
+}
+
+Params base_params(int M, int N, int K, int BN) {
+  Params p{};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.num_mb = (M + BM - 1) / BM;
+  p.num_nb = (N + BN - 1) / BN;
+  p.num_kb = (K + BK - 1) / BK;
+  p.num_splits = 1;
+  p.kb_per_split = p.num_kb;
+  p.group_m = 8;
+  p.amap.nseg = 1;
+  p.amap.seg_end[0] = 1 << 30;
+  p.bmap.nseg = 1;
+  p.bmap.seg_end[0] = 1 << 30;
+  return p;
+}
+
+}  // namespace
+
+int gemm_plain(const Ctx& c, const void* X, const void* W, void* C, int M, int N, int K, bool c_f32) {
+  TMaps tm{};
+  if (!make_tmap_2d(&tm.m[0], X, K, M, K, 128) || !make_tmap_2d(&tm.m[1], W, K, N, K, 128))
+    return LLAMA_ERR_INVALID_ARG;
+  Params p = base_params(M, N, K, 256);
+  p.a_map0 = 0;
+  p.b_map0 = 1;
+  p.out = C;
+  p.ldo = N;
+  return c_f32 ? launch<256, EPI_F32, 4>(c, tm, p) : launch<256, EPI_BF16, 4>(c, tm, p);
+}
+
+int gemm_residual(const Ctx& c, const void* X, const void* W, const void* resid, void* out, int M, int N, int K) {
+  TMaps tm{};
+  if (!make_tmap_2d(&tm.m[0], X, K, M, K, 128) || !make_tmap_2d(&tm.m[1], W, K, N, K, 128))
+    return LLAMA_ERR_INVALID_ARG;
+  Params p = base_params(M, N, K, 256);
+  p.a_map0 = 0;
+  p.b_map0 = 1;
+  p.out = out;
+  p.ldo = N;
+  p.resid = static_cast<const __nv_bfloat16*>(resid);
+  p.ldr = N;
+  return launch<256, EPI_RESID, 4>(c, tm, p);
+}
+
+int gemm_swiglu(const Ctx& c, const void* X, const void* Wg, const void* Wu, void* out, int M, int I, int K) {
+  TMaps tm{};
+  if (!make_tmap_2d(&tm.m[0], X, K, M, K, 128) || !make_tmap_2d(&tm.m[1], Wg, K, I, K, 128) ||
+      !make_tmap_2d(&tm.m[2], Wu, K, I, K, 128))
+    return LLAMA_ERR_INVALID_ARG;
+  // kernel N runs over 256-column tiles, each = 128 gate rows + the same 128 up rows
+  Params p = base_params(M, 2 * ((I + 127) / 128) * 128, K, 256);
+  p.N = I;   // output width (used by the epilogue's bounds)
+  p.a_map0 = 0;
+  p.b_map0 = 1;
+  p.bmap.interleave = 1;
+  p.out = out;
+  p.ldo = I;
+  return launch<256, EPI_SWIGLU, 4>(c, tm, p);
+}
+
+int gemm_qkv_rope(const Ctx& c, const void* X, const void* Wq, const void* Wk, const void* Wv, int B, int S, int K,
+                  int H, int G, int D, const float* cos, const float* sin, void* q_out, void* k_cache,
+                  void* v_cache, int T_max) {
+  const int M = B * S;
+  TMaps tm{};
+  if (!make_tmap_2d(&tm.m[0], X, K, M, K, 128) || !make_tmap_2d(&tm.m[1], Wq, K, H * D, K, 128) ||
+      !make_tmap_2d(&tm.m[2], Wk, K, G * D, K, 128) || !make_tmap_2d(&tm.m[3], Wv, K, G * D, K, 128))
+    return LLAMA_ERR_INVALID_ARG;
+  Params p = base_params(M, (H + 2 * G) * D, K, 256);
+  p.a_map0 = 0;
+  p.b_map0 = 1;
+  p.bmap.nseg = 3;
+  p.bmap.seg_end[0] = H * D;
+  p.bmap.seg_end[1] = (H + G) * D;
+  p.bmap.seg_end[2] = (H + 2 * G) * D;
+  p.cos = cos;
+  p.sin = sin;
+  p.S = S;
+  p.H = H;
+  p.G = G;
+  p.D = D;
+  p.T_max = T_max;
+  p.q_out = static_cast<__nv_bfloat16*>(q_out);
+  p.k_cache = static_cast<__nv_bfloat16*>(k_cache);
+  p.v_cache = static_cast<__nv_bfloat16*>(v_cache);
+  return launch<256, EPI_QKV, 4>(c, tm, p);
+}
+
+int choose_splits(int num_sms, int w_rows_total, int K) {
+  const int tiles = (w_rows_total + BM - 1) / BM;
+  const int kb = (K + BK - 1) / BK;
+  int s = std::max(1, (num_sms + tiles - 1) / tiles);
+  s = std::min(s, std::max(1, kb / 4));   // keep at least 4 k-blocks per split
+  // the count actually used: every split gets ceil(kb / s) blocks and none is empty
+  const int per = (kb + s - 1) / s;
+  return (kb + per - 1) / per;
+}
+
+int gemm_tokens_partial(const Ctx& c, const void* const* W, const int* w_rows, int n_w, const void* X, int n_tok,
+                        int K, int splits, float* P) {
+  if (n_w < 1 || n_w > 3) return LLAMA_ERR_INVALID_ARG;
+  TMaps tm{};
+  int total = 0;
+  Params p = base_params(0, n_tok, K, 64);
+  for (int i = 0; i < n_w; ++i) {
+    if (!make_tmap_2d(&tm.m[i], W[i], K, w_rows[i], K, 128)) return LLAMA_ERR_INVALID_ARG;
+    total += w_rows[i];
+    p.amap.seg_end[i] = total;
+  }
+  if (!make_tmap_2d(&tm.m[n_w], X, K, n_tok, K, 64)) return LLAMA_ERR_INVALID_ARG;
+  p.M = total;
+  p.num_mb = (total + BM - 1) / BM;
+  p.amap.nseg = n_w;
+  p.a_map0 = 0;
+  p.b_map0 = n_w;
+  splits = std::max(1, std::min(splits, p.num_kb));
+  p.kb_per_split = (p.num_kb + splits - 1) / splits;
+  p.num_splits = (p.num_kb + p.kb_per_split - 1) / p.kb_per_split;   // every split non-empty
+  if (p.num_splits != splits) return LLAMA_ERR_INVALID_ARG;          // callers pass choose_splits()
+  p.out = P;
+  p.ldo = total;
+  return launch<64, EPI_PARTIAL, 8>(c, tm, p);
+}
+
+}  // namespace llama

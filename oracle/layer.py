@@ -34,6 +34,11 @@ def round_bf16(x) -> np.ndarray:
     return np.ldexp(np.rint(np.ldexp(m, 8)), e - 8)   # np.rint: ties to even
 
 
+def linear(x, w):
+    """nn.Linear without bias: y = x W^T with W in the [out, in] layout ([T2L] §八)."""
+    return x @ w.T
+
+
 def rms_norm(x, gamma, eps):
     """RMSNorm: gamma * x * rsqrt(mean(x^2) + eps) over the last axis.
 

@@ -1,0 +1,51 @@
+"""Helpers of the GPU parity tests: moving synth tensors to the device and the tolerance check."""
+import numpy as np
+import torch
+
+from llama_decoder_block_gb300 import api, synth
+
+# |gpu - ref| <= TOL * (1 + |ref|), elementwise
+TOL = {"f32": 1e-4, "bf16": 2e-2}
+TORCH_DT = {"f32": torch.float32, "bf16": torch.bfloat16}
+NAN_BF16 = np.uint16(0x7FC0)
+
+
+def to_dev(s: synth.Stored, device="cuda") -> torch.Tensor:
+    if s.dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(s.data).view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(s.data)).to(device)
+
+
+def f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def bf16_stored(a: np.ndarray) -> synth.Stored:
+    return synth.Stored(synth.f32_to_bf16_bits(a.astype(np.float32)), "bf16")
+
+
+def assert_close(gpu: np.ndarray, ref: np.ndarray, tol: float, what: str):
+    assert gpu.shape == ref.shape, (what, gpu.shape, ref.shape)
+    assert np.all(np.isfinite(gpu)), f"{what}: non-finite values in the GPU result"
+    err = np.abs(gpu - ref) / (1.0 + np.abs(ref))
+    worst = np.unravel_index(np.argmax(err), err.shape)
+    assert err.max() <= tol, (f"{what}: max |gpu-ref|/(1+|ref|) = {err.max():.3e} > {tol:.0e} at {worst} "
+                              f"(gpu {gpu[worst]!r}, ref {ref[worst]!r}); p99 {np.quantile(err, 0.99):.3e}")
+    return float(err.max())
+
+
+def dims_of(layer: synth.LayerShape) -> api.Dims:
+    return api.Dims(layer.d_model, layer.n_heads, layer.n_kv_heads, layer.head_dim, layer.d_inter, layer.rms_eps,
+                    TORCH_DT[layer.dtype])
+
+
+def tables(layer: synth.LayerShape, max_pos: int, oracle_mod, device="cuda"):
+    """RoPE tables made by the oracle in fp64 and rounded to fp32: the same input on both sides."""
+    c, s = oracle_mod.rope_tables(layer.rope_base, layer.head_dim, max_pos)
+    c32, s32 = c.astype(np.float32), s.astype(np.float32)
+    return (torch.from_numpy(c32).to(device), torch.from_numpy(s32).to(device),
+            c32.astype(np.float64), s32.astype(np.float64))
+
+
+def oracle_kw(layer: synth.LayerShape) -> dict:
+    return dict(n_heads=layer.n_heads, n_kv_heads=layer.n_kv_heads, head_dim=layer.head_dim, rms_eps=layer.rms_eps)

@@ -1,0 +1,125 @@
+"""Host-side checks of the C ABI: the library builds and loads, exports every symbol the
+header declares, and rejects bad arguments before touching a GPU (no compute calls here)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def native():
+    from llama_decoder_block_gb300 import build, _native
+    build.build()
+    return _native
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "llama_layer.h"), encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(llama_[a-z_0-9]+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for required in ("llama_layer_prefill", "llama_layer_decode", "llama_stack_forward", "llama_rope_tables",
+                     "llama_get_device_status"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(native):
+    lib = ctypes.CDLL(native.LIB_PATH)
+    names = _declared_functions()
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+    # the binding declares exactly the header's functions
+    assert sorted(native.SIGNATURES) == names
+
+
+def test_rope_tables_match_the_oracle(native):
+    from llama_decoder_block_gb300 import api
+    for base, D, P in ((1e4, 16, 64), (5e5, 128, 4096), (1e4, 128, 2048)):
+        cos, sin = api.rope_tables(base, D, P)
+        oc, os_ = oracle.rope_tables(base, D, P)
+        # both round an fp64 value to fp32; allow one fp32 ulp for libm differences
+        assert np.max(np.abs(cos - oc.astype(np.float32))) <= 2 ** -24
+        assert np.max(np.abs(sin - os_.astype(np.float32))) <= 2 ** -24
+
+
+def test_status_strings(native):
+    lib = native.lib()
+    for code in (0, -1, -2, -3, -4, -5):
+        assert lib.llama_status_string(code)
+    assert lib.llama_status_string(-99) == b"unknown status"
+
+
+def _dims(native, **kw):
+    base = dict(d_model=256, n_heads=4, n_kv_heads=2, head_dim=128, d_inter=384, rms_eps=1e-5, dtype=1)
+    base.update(kw)
+    return native.LayerDims(**base)
+
+
+def _bytes(native, dims, B=2, S=64):
+    n = ctypes.c_size_t()
+    rc = native.lib().llama_layer_prefill_workspace_bytes(ctypes.byref(dims), B, S, ctypes.byref(n))
+    return rc, n.value
+
+
+def test_workspace_sizes_and_dims_validation(native):
+    rc, n = _bytes(native, _dims(native))
+    assert rc == 0 and n >= 2 * 2 * 64 * (2 * 256 + 2 * 512 + 384)   # xn, h, q, o, a
+    assert _bytes(native, _dims(native, n_kv_heads=3))[0] == -1     # H % G != 0
+    assert _bytes(native, _dims(native, head_dim=15, dtype=0))[0] == -1   # odd D
+    assert _bytes(native, _dims(native, head_dim=64))[0] == -2      # bf16 tile path needs D = 128
+    assert _bytes(native, _dims(native, d_model=200))[0] == -2      # d % 128
+    assert _bytes(native, _dims(native, dtype=7))[0] == -1
+    assert _bytes(native, _dims(native, rms_eps=-1.0))[0] == -1
+    assert _bytes(native, _dims(native, n_heads=12, n_kv_heads=4))[0] == -2   # H/G = 3 not a tiled ratio
+    assert _bytes(native, _dims(native, head_dim=16, d_model=64, n_heads=4, n_kv_heads=2, d_inter=176,
+                                dtype=0))[0] == 0                     # the fp32 path takes any even D
+
+
+def test_prefill_rejects_bad_arguments_without_a_gpu(native):
+    lib = native.lib()
+    dims = _dims(native)
+    buf = (ctypes.c_uint8 * 4096)()
+    p = ctypes.addressof(buf)
+    p = (p + 255) // 256 * 256 - 256 + 256 if p % 256 else p
+    w = native.LayerWeights(*([p] * 9))
+    cache = native.KVCache(p, p, 64)
+
+    def call(dims=dims, w=w, x=p, out=p + 1024, cos=p, sin=p, max_pos=64, cache=cache, B=1, S=8, ws=p, n=1 << 40):
+        return lib.llama_layer_prefill(ctypes.byref(dims), ctypes.byref(w), x, out, cos, sin, max_pos, cache, B, S,
+                                       ws, n, None)
+
+    assert call(x=None) == -1
+    assert call(out=p) == -1                   # aliasing input and output
+    assert call(x=p + 8) == -1                 # not 16-byte aligned
+    assert call(S=65) == -1                    # S > max_T
+    assert call(max_pos=4) == -1               # S > max_pos
+    assert call(n=16) == -1                    # workspace too small
+    assert call(B=0) == -1
+    assert call(w=native.LayerWeights(*([p] * 8 + [None]))) == -1
+    assert call(dims=_dims(native, n_kv_heads=3)) == -1
+
+
+def test_decode_and_attention_reject_bad_arguments_without_a_gpu(native):
+    lib = native.lib()
+    dims = _dims(native)
+    buf = (ctypes.c_uint8 * 4096)()
+    p = (ctypes.addressof(buf) + 255) // 256 * 256
+    w = native.LayerWeights(*([p] * 9))
+    cache = native.KVCache(p, p, 64)
+    assert lib.llama_layer_decode(ctypes.byref(dims), ctypes.byref(w), p, p + 512, p, p, 64, None, cache, 1, p, 1 << 30,
+                                  None) == -1
+    assert lib.llama_layer_decode(ctypes.byref(dims), ctypes.byref(w), p, p, p, p, 64, p, cache, 1, p, 1 << 30,
+                                  None) == -1
+    assert lib.llama_attention_prefill(ctypes.byref(dims), p, native.KVCache(p, p, 4), p, 1, 8, None) == -1
+    assert lib.llama_linear_bf16(p, p, p, 4, 12, 30, 0, None) == -2    # K % 8
+    assert lib.llama_linear_bf16(None, p, p, 4, 16, 32, 0, None) == -1
+    assert lib.llama_rmsnorm(p, p, p, 4, 64, -1.0, 1, None) == -1
+    assert lib.llama_rope_tables(1e4, 7, 4, p, p) == -1

@@ -1,0 +1,150 @@
+"""GPU parity of each step against the fp64 oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import NAN_BF16, TOL, assert_close, bf16_stored, f64, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def api(cuda_dev):
+    from llama_decoder_block_gb300 import build, api as a
+    build.build()
+    assert a.device_status() == 0
+    return a
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def test_bounded_wait_gives_up_and_reports(api):
+    api.wait_probe(2_000_000)           # 2 ms: the probe waits on an mbarrier nothing arrives at
+    assert api.device_status() == -4    # LLAMA_ERR_TIMEOUT
+    assert api.device_status() == 0     # read-and-clear
+    x = torch.ones(4, 256, dtype=torch.bfloat16, device="cuda")
+    y = torch.empty_like(x)
+    api.rmsnorm(x, torch.ones(256, dtype=torch.bfloat16, device="cuda"), y, 1e-5)   # the context still works
+    torch.cuda.synchronize()
+    assert torch.allclose(y.float(), torch.ones_like(y.float()), atol=1e-2)
+
+
+@pytest.mark.parametrize("rows,d,dt", [(1, 4096, "bf16"), (37, 4096, "bf16"), (2048, 4096, "bf16"),
+                                       (64, 768, "bf16"), (40, 1024, "bf16"), (16, 64, "f32"), (33, 4096, "f32")])
+def test_rmsnorm(api, rows, d, dt):
+    rng = _rng(rows * 7 + d)
+    x = rng.standard_normal((rows, d)) * 3
+    g = 1 + 0.1 * rng.standard_normal(d)
+    if dt == "bf16":
+        xs, gs = bf16_stored(x), bf16_stored(g)
+    else:
+        from llama_decoder_block_gb300.synth import Stored
+        xs, gs = Stored(x.astype(np.float32), "f32"), Stored(g.astype(np.float32), "f32")
+    xd, gd = to_dev(xs), to_dev(gs)
+    y = torch.empty_like(xd)
+    api.rmsnorm(xd, gd, y, 1e-5)
+    ref = oracle.rms_norm(xs.f64(), gs.f64(), 1e-5)
+    assert_close(f64(y), ref, TOL[dt], "rmsnorm")
+    assert api.device_status() == 0
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (300, 520, 200), (1000, 2048, 4096), (64, 6144, 4096)])
+@pytest.mark.parametrize("out_f32", [False, True])
+def test_linear_bf16(api, M, N, K, out_f32):
+    rng = _rng(M + N + K)
+    a = bf16_stored(rng.standard_normal((M, K)))
+    b = bf16_stored(0.02 * rng.standard_normal((N, K)))
+    c = torch.empty(M, N, dtype=torch.float32 if out_f32 else torch.bfloat16, device="cuda")
+    api.linear_bf16(to_dev(a), to_dev(b), c)
+    ref = oracle.linear(a.f64(), b.f64())
+    # fp32 output: only fp32 accumulation error; bf16 output: the final rounding too
+    assert_close(f64(c), ref, 1e-3 if out_f32 else TOL["bf16"], f"linear {M}x{N}x{K}")
+    assert api.device_status() == 0
+
+
+def _attn_dims(api, H, G):
+    return api.Dims(H * 128, H, G, 128, 128, 1e-5, torch.bfloat16)
+
+
+def _cache_with_nan_tail(rng, B, G, T_max, valid):
+    """[B, G, T_max, 128] bf16 with N(0,1) in slots < valid[b] and NaN beyond (must never be read)."""
+    vals = rng.standard_normal((B, G, T_max, 128))
+    st = bf16_stored(vals)
+    for b in range(B):
+        st.data[b, :, valid[b]:, :] = NAN_BF16
+    return st
+
+
+@pytest.mark.parametrize("B,S,H,G", [(2, 300, 4, 2), (1, 128, 2, 2), (1, 520, 8, 1), (2, 256, 8, 2), (1, 1, 4, 4)])
+def test_attention_prefill(api, B, S, H, G):
+    rng = _rng(B * 1000 + S + H * 10 + G)
+    T_max = S + 37
+    q = bf16_stored(rng.standard_normal((B, H, S, 128)))
+    kc = _cache_with_nan_tail(rng, B, G, T_max, [S] * B)
+    vc = _cache_with_nan_tail(rng, B, G, T_max, [S] * B)
+    out = torch.empty(B, S, H * 128, dtype=torch.bfloat16, device="cuda")
+    api.attention_prefill(_attn_dims(api, H, G), to_dev(q), to_dev(kc), to_dev(vc), out)
+    pos = np.tile(np.arange(S), (B, 1))
+    ref = oracle.attention(q.f64(), kc.f64()[:, :, :S], vc.f64()[:, :, :S], pos, np.full(B, S))
+    gpu = f64(out).reshape(B, S, H, 128).transpose(0, 2, 1, 3)
+    assert_close(gpu, ref, TOL["bf16"], "attention prefill")
+    assert api.device_status() == 0
+
+
+def test_attention_prefill_mask_and_group_map_are_exact(api):
+    # q = 0: every visible key gets weight 1/(i+1).  V row j of group g is one-hot at column
+    # (j + 17 g) % 128, so the nonzero columns of O[b, h, i] name exactly the keys and the group read.
+    B, S, H, G = 1, 128, 8, 2
+    q = torch.zeros(B, H, S, 128, dtype=torch.bfloat16, device="cuda")
+    k = torch.randn(B, G, S, 128, device="cuda").to(torch.bfloat16)
+    v = torch.zeros(B, G, S, 128, dtype=torch.bfloat16, device="cuda")
+    for g in range(G):
+        for j in range(S):
+            v[0, g, j, (j + 17 * g) % 128] = 1.0
+    out = torch.empty(B, S, H * 128, dtype=torch.bfloat16, device="cuda")
+    api.attention_prefill(_attn_dims(api, H, G), q, k, v, out)
+    o = f64(out).reshape(S, H, 128)
+    for h in range(H):
+        g = h // (H // G)
+        for i in range(S):
+            expect = {(j + 17 * g) % 128 for j in range(i + 1)}
+            got = set(np.nonzero(o[i, h])[0].tolist())
+            assert got == expect, (h, i)
+            assert np.allclose(o[i, h][list(expect)], 1.0 / (i + 1), rtol=1e-2)
+
+
+@pytest.mark.parametrize("H,G", [(8, 2), (4, 4), (8, 1), (32, 8)])
+def test_attention_decode(api, H, G):
+    rng = _rng(H * 31 + G)
+    positions = np.array([0, 1, 127, 128, 511, 512, 1024, 1099], dtype=np.int32)
+    B, T_max = len(positions), 1100
+    q = bf16_stored(rng.standard_normal((B, H, 128)))
+    kc = _cache_with_nan_tail(rng, B, G, T_max, positions + 1)
+    vc = _cache_with_nan_tail(rng, B, G, T_max, positions + 1)
+    dims = _attn_dims(api, H, G)
+    ws = api.workspace(api.attention_decode_workspace_bytes(dims, B, T_max), "cuda")
+    out = torch.empty(B, H * 128, dtype=torch.bfloat16, device="cuda")
+    api.attention_decode(dims, to_dev(q), to_dev(kc), to_dev(vc), torch.from_numpy(positions).cuda(), out, ws)
+    k64, v64 = kc.f64(), vc.f64()
+    for b, p in enumerate(positions):
+        ref = oracle.attention(q.f64()[b:b + 1, :, None, :], k64[b:b + 1, :, :p + 1], v64[b:b + 1, :, :p + 1],
+                               np.array([[p]]), np.array([p + 1]))[0, :, 0, :]
+        assert_close(f64(out)[b].reshape(H, 128), ref, TOL["bf16"], f"decode attention b={b} p={p}")
+    assert api.device_status() == 0
+
+
+def test_attention_decode_reports_out_of_range_positions(api):
+    B, H, G, T_max = 3, 4, 2, 256
+    dims = _attn_dims(api, H, G)
+    q = torch.randn(B, H, 128, device="cuda").to(torch.bfloat16)
+    kc = torch.randn(B, G, T_max, 128, device="cuda").to(torch.bfloat16)
+    vc = torch.randn(B, G, T_max, 128, device="cuda").to(torch.bfloat16)
+    ws = api.workspace(api.attention_decode_workspace_bytes(dims, B, T_max), "cuda")
+    out = torch.empty(B, H * 128, dtype=torch.bfloat16, device="cuda")
+    pos = torch.tensor([5, T_max, 7], dtype=torch.int32, device="cuda")
+    api.attention_decode(dims, q, kc, vc, pos, out, ws)
+    assert api.device_status() == -5
+    assert torch.all(out[1] == 0) and torch.all(torch.isfinite(out.float()))

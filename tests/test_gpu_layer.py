@@ -1,0 +1,222 @@
+"""GPU parity of the whole layer (prefill, decode) and of the stack against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import NAN_BF16, TOL, assert_close, dims_of, f64, oracle_kw, tables, to_dev
+from llama_decoder_block_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def api(cuda_dev):
+    from llama_decoder_block_gb300 import build, api as a
+    build.build()
+    assert a.device_status() == 0
+    return a
+
+
+def _weights(wl, layer=0):
+    st = synth.layer_weights(wl, layer)
+    return st, {k: to_dev(v) for k, v in st.items()}
+
+
+def _run_prefill(api, wl, extra_T=5, max_pos=None):
+    L = wl.layer
+    B, S = wl.B, wl.S
+    T_max = S + extra_T
+    max_pos = max_pos or T_max
+    st, w = _weights(wl)
+    xs = synth.activations(wl)
+    x = to_dev(xs)
+    out = torch.empty_like(x)
+    cos, sin, c64, s64 = tables(L, max_pos, oracle)
+    dt = x.dtype
+    kc = torch.full((B, L.n_kv_heads, T_max, L.head_dim), float("nan"), dtype=dt, device="cuda")
+    vc = torch.full_like(kc, float("nan"))
+    dims = dims_of(L)
+    ws = api.workspace(api.prefill_workspace_bytes(dims, B, S), "cuda")
+    api.layer_prefill(dims, w, x, out, cos, sin, kc, vc, ws)
+    assert api.device_status() == 0
+    return st, xs, c64, s64, out, kc, vc
+
+
+def _check_prefill(api, wl, prefix=None):
+    L = wl.layer
+    st, xs, c64, s64, out, kc, vc = _run_prefill(api, wl)
+    x64 = xs.f64()
+    S_ref = prefix or wl.S
+    w64 = {k: v.f64() for k, v in st.items()}
+    ref, k_ref, v_ref = oracle.decoder_layer(x64[:, :S_ref], w64, c64, s64, store_bf16=(L.dtype == "bf16"),
+                                             **oracle_kw(L))
+    tol = TOL[L.dtype]
+    assert_close(f64(out)[:, :S_ref], ref, tol, f"{wl.name} out")
+    assert_close(f64(kc)[:, :, :S_ref], k_ref, tol, f"{wl.name} cache K")
+    assert_close(f64(vc)[:, :, :S_ref], v_ref, tol, f"{wl.name} cache V")
+    # slots >= S are never written
+    assert torch.isnan(kc[:, :, wl.S:].float()).all() and torch.isnan(vc[:, :, wl.S:].float()).all()
+
+
+def test_prefill_tiny_fp32_config(api):
+    _check_prefill(api, synth.WORKLOADS["tiny_f32_b1_s16"])
+
+
+@pytest.mark.parametrize("H,G,B,S", [(4, 2, 2, 200), (2, 2, 1, 128), (8, 1, 1, 300), (4, 4, 3, 65)])
+def test_prefill_bf16_small(api, H, G, B, S):
+    base = synth.WORKLOADS["gqa8b_bf16_b4_s4096"]
+    wl = synth.scaled(base, d_model=256, n_heads=H, n_kv_heads=G, d_inter=384, B=B, S=S,
+                      name=f"bf16_d256_h{H}_g{G}_b{B}_s{S}")
+    _check_prefill(api, wl)
+
+
+def test_prefill_fp32_gqa_ragged(api):
+    base = synth.WORKLOADS["tiny_f32_b1_s16"]
+    wl = synth.scaled(base, d_model=96, n_heads=6, n_kv_heads=3, head_dim=16, d_inter=160, B=2, S=37,
+                      name="f32_d96_h6_g3_b2_s37")
+    _check_prefill(api, wl)
+
+
+def test_prefill_mha7b_full_size(api):
+    _check_prefill(api, synth.WORKLOADS["mha7b_bf16_b1_s2048"])
+
+
+def test_prefill_gqa8b_full_size_causal_prefix(api):
+    # the GPU runs B=4, S=4096; rows < 256 depend only on tokens < 256 (causality), so the
+    # oracle's 256-token run is their exact reference
+    _check_prefill(api, synth.WORKLOADS["gqa8b_bf16_b4_s4096"], prefix=256)
+
+
+def _run_decode(api, wl, positions=None, nan_beyond=True, sample=None):
+    L = wl.layer
+    st, w = _weights(wl)
+    pos, ks, vs = synth.decode_state(wl)
+    if positions is not None:
+        pos = np.asarray(positions, dtype=np.int32)
+    if nan_beyond:
+        for b in range(wl.B):
+            ks.data[b, :, pos[b] + 1:] = NAN_BF16 if L.dtype == "bf16" else np.nan
+            vs.data[b, :, pos[b] + 1:] = NAN_BF16 if L.dtype == "bf16" else np.nan
+    xs = synth.activations(wl)
+    x = to_dev(xs)
+    out = torch.empty_like(x)
+    kc, vc = to_dev(ks), to_dev(vs)
+    cos, sin, c64, s64 = tables(L, wl.T_max, oracle)
+    dims = dims_of(L)
+    ws = api.workspace(api.decode_workspace_bytes(dims, wl.B, wl.T_max), "cuda")
+    api.layer_decode(dims, w, x, out, cos, sin, torch.from_numpy(pos).cuda(), kc, vc, ws)
+    assert api.device_status() == 0
+    w64 = {k: v.f64() for k, v in st.items()}
+    tol = TOL[L.dtype]
+    x64 = xs.f64()
+    out_h = f64(out)
+    for b in (range(wl.B) if sample is None else sample):
+        p = int(pos[b])
+        ks64 = synth.Stored(ks.data[b:b + 1], ks.dtype).f64()
+        vs64 = synth.Stored(vs.data[b:b + 1], vs.dtype).f64()
+        ref, k_new, v_new = oracle.decoder_layer(
+            x64[b:b + 1, None, :], w64, c64, s64, past_k=ks64, past_v=vs64,
+            past_len=np.array([p]), store_bf16=(L.dtype == "bf16"), **oracle_kw(L))
+        kc_h, vc_h = f64(kc[b]), f64(vc[b])
+        assert_close(out_h[b], ref[0, 0], tol, f"decode out b={b} p={p}")
+        assert_close(kc_h[:, p], k_new[0, :, 0], tol, f"decode cache K slot b={b} p={p}")
+        assert_close(vc_h[:, p], v_new[0, :, 0], tol, f"decode cache V slot b={b} p={p}")
+        # every other slot is untouched (bitwise, NaN included)
+        others = np.ones(wl.T_max, bool)
+        others[p] = False
+        assert np.array_equal(kc_h[:, others], ks64[0][:, others], equal_nan=True)
+        assert np.array_equal(vc_h[:, others], vs64[0][:, others], equal_nan=True)
+
+
+def test_decode_bf16_small_edge_positions(api):
+    base = synth.WORKLOADS["decode_gqa8b_bf16_b64_t4096"]
+    wl = synth.scaled(base, d_model=256, n_heads=8, n_kv_heads=2, d_inter=384, B=6, T_max=600,
+                      name="decode_bf16_d256_b6_t600")
+    _run_decode(api, wl, positions=[0, 1, 300, 511, 512, 599])
+
+
+def test_decode_fp32_small(api):
+    base = synth.WORKLOADS["tiny_f32_b1_s16"]
+    wl = synth.scaled(base, kind="decode", B=4, S=0, T_max=40, pos_lo=0, pos_hi=40, name="decode_f32_tiny_b4")
+    _run_decode(api, wl, positions=[0, 5, 17, 39])
+
+
+def test_decode_gqa8b_full_size_sampled(api):
+    wl = synth.WORKLOADS["decode_gqa8b_bf16_b64_t4096"]
+    pos = synth.decode_state(wl)[0]
+    order = np.argsort(pos)
+    _run_decode(api, wl, nan_beyond=False, sample=sorted({int(order[0]), int(order[-1]), 0, 17, 40, 63}))
+
+
+def test_decode_matches_prefill_row(api):
+    # "第 10 章：现代 LLaMA 架构" §7: decode of token t over the cache of tokens < t equals
+    # row t of the full prefill (here both on the GPU, at the scaled bf16 shape).
+    base = synth.WORKLOADS["gqa8b_bf16_b4_s4096"]
+    wl = synth.scaled(base, d_model=256, n_heads=4, n_kv_heads=2, d_inter=384, B=2, S=150, name="bf16_pd_b2_s150")
+    st, xs, c64, s64, out, kc, vc = _run_prefill(api, wl, extra_T=0)
+    L = wl.layer
+    _, w = _weights(wl)
+    t = wl.S - 1
+    x_t = to_dev(xs)[:, t].contiguous()
+    y = torch.empty_like(x_t)
+    kc2, vc2 = kc.clone(), vc.clone()
+    kc2[:, :, t:] = float("nan")
+    vc2[:, :, t:] = float("nan")
+    dims = dims_of(L)
+    cos, sin, _, _ = tables(L, wl.S, oracle)
+    ws = api.workspace(api.decode_workspace_bytes(dims, wl.B, wl.S), "cuda")
+    api.layer_decode(dims, w, x_t, y, cos, sin, torch.full((wl.B,), t, dtype=torch.int32, device="cuda"), kc2, vc2, ws)
+    assert api.device_status() == 0
+    assert_close(f64(y), f64(out)[:, t], TOL["bf16"], "decode vs prefill row")
+
+
+def test_decode_out_of_range_position_is_reported(api):
+    base = synth.WORKLOADS["decode_gqa8b_bf16_b64_t4096"]
+    wl = synth.scaled(base, d_model=256, n_heads=8, n_kv_heads=2, d_inter=384, B=3, T_max=64, name="decode_oob")
+    L = wl.layer
+    _, w = _weights(wl)
+    x = torch.randn(3, 256, device="cuda").to(torch.bfloat16)
+    out = torch.empty_like(x)
+    kc = torch.randn(3, 2, 64, 128, device="cuda").to(torch.bfloat16)
+    vc = torch.randn_like(kc)
+    k0, v0 = kc.clone(), vc.clone()
+    cos, sin, _, _ = tables(L, 64, oracle)
+    dims = dims_of(L)
+    ws = api.workspace(api.decode_workspace_bytes(dims, 3, 64), "cuda")
+    api.layer_decode(dims, w, x, out, cos, sin, torch.tensor([3, 64, -1], dtype=torch.int32, device="cuda"), kc, vc, ws)
+    assert api.device_status() == -5
+    assert torch.equal(kc[1:], k0[1:]) and torch.equal(vc[1:], v0[1:])   # bad sequences leave the cache alone
+
+
+def _stack_case(api, wl, n_layers, prefix=None):
+    L = wl.layer
+    layers_st = [synth.layer_weights(wl, l) for l in range(n_layers)]
+    glob = synth.stack_globals(wl)
+    dev_layers = [{k: to_dev(v) for k, v in st.items()} for st in layers_st]
+    fn, emb, lm = to_dev(glob["final_norm"]), to_dev(glob["embed"]), to_dev(glob["lm_head"])
+    st = api.StackArgs(dims_of(L), dev_layers, fn, emb, lm)
+    tokens = torch.from_numpy(glob["tokens"]).cuda()
+    logits = torch.empty(wl.B, wl.S, wl.vocab, dtype=torch.float32, device="cuda")
+    cos, sin, c64, s64 = tables(L, wl.S, oracle)
+    ws = api.workspace(st.workspace_bytes(wl.B, wl.S), "cuda")
+    api.stack_forward(st, tokens, logits, cos, sin, ws)
+    assert api.device_status() == 0
+    S_ref = prefix or wl.S
+    ref = oracle.stack_forward(glob["tokens"][:, :S_ref], ({k: v.f64() for k, v in s.items()} for s in layers_st),
+                               glob["final_norm"].f64(), glob["embed"].f64(), glob["lm_head"].f64(), c64, s64,
+                               store_bf16=(L.dtype == "bf16"), **oracle_kw(L))
+    assert_close(f64(logits)[:, :S_ref], ref, TOL[L.dtype], f"{wl.name} logits")
+
+
+def test_stack_bf16_small(api):
+    base = synth.WORKLOADS["stack32_gqa8b_bf16_s8192_v32000"]
+    wl = synth.scaled(base, d_model=256, n_heads=4, n_kv_heads=2, d_inter=384, S=130, vocab=1000, n_layers=3,
+                      name="stack3_bf16_d256_s130_v1000")
+    _stack_case(api, wl, 3)
+
+
+def test_stack_fp32_tiny(api):
+    base = synth.WORKLOADS["tiny_f32_b1_s16"]
+    wl = synth.scaled(base, kind="stack", B=2, S=16, vocab=96, n_layers=2, name="stack2_f32_tiny")
+    _stack_case(api, wl, 2)

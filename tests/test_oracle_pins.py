@@ -49,6 +49,16 @@ def test_round_bf16_ties_to_even():
     assert oracle.round_bf16(0.0) == 0.0
 
 
+# ------------------------------------------------------------------ linear
+
+def test_linear_uses_out_in_layout():
+    # W = [[1, 2], [3, 4], [5, 6]] maps 2 inputs to 3 outputs: y_j = sum_i W[j, i] x_i
+    y = oracle.linear(np.array([[1.0, -1.0]]), np.array([[1.0, 2.0], [3.0, 4.0], [5.0, 6.0]]))
+    assert np.array_equal(y, [[-1.0, -1.0, -1.0]])
+    y = oracle.linear(np.array([[2.0, 0.5]]), np.array([[1.0, 2.0], [3.0, 4.0], [5.0, 6.0]]))
+    assert np.array_equal(y, [[3.0, 8.0, 13.0]])
+
+
 # ------------------------------------------------------------------ RMSNorm
 
 def test_rmsnorm_worked_example():
