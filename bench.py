@@ -1,0 +1,488 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 decoder layer through its C ABI.
+
+Headline: prefill tokens/s of one MHA layer shaped like a 7B model (B=1, S=2048, d=4096,
+H=G=32, D=128, d_inter=11008, bf16 with fp32 accumulation).  Also measured: the decode
+step of the GQA 8B-shaped layer (B=64, cache [64, 8, 4096, 128]) in us/step and the GQA
+8B-shaped prefill (B=4, S=4096).  A step is one full pass of the layer.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One JSON line on rank 0.  Under torchrun each rank runs an independent replica on its own
+GPU (the layer has no exchange step); `value` sums the tokens of all ranks over the slowest
+rank's time.  `--impl reference` times the fp64 CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decoder-layer prefill tokens/s + decode µs/step on 1 GB300; % of TC/HBM roofline"
+MAIN = "mha7b_bf16_b1_s2048"
+PREFILL_KERNELS = ["rmsnorm_attn", "qkv_rope_gemm", "attention_prefill", "o_proj_residual_gemm", "rmsnorm_ffn",
+                   "gate_up_swiglu_gemm", "down_residual_gemm"]
+DECODE_KERNELS = ["rmsnorm_attn", "qkv_gemm_stream", "qkv_rope_fixup", "attention_decode_split",
+                  "attention_decode_combine", "o_proj_gemm_stream", "o_proj_residual_fixup", "rmsnorm_ffn",
+                  "gate_up_gemm_stream", "swiglu_fixup", "down_gemm_stream", "down_residual_fixup"]
+L2_FLUSH_BYTES = 256 << 20
+
+# DRAM bytes (read + write) per launch from ncu captures, keyed by kernel and the sha1 of
+# the source file it was measured on; a changed source makes the figure stale (null).
+NCU_TRAFFIC = {}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extra", action="store_true", help="only the headline workload")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16": d["bf16_tflops"], "bf16_sustained": d["bf16_tflops_sustained"],
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+def src_sha(name):
+    import hashlib
+    with open(os.path.join(ROOT, "llama_decoder_block_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha1(f.read()).hexdigest()[:12]
+
+
+# ------------------------------------------------------------------ clocks
+
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        import statistics
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ workloads on the GPU
+
+def dev_weights_from_synth(wl, dev):
+    import numpy as np
+    import torch
+    from llama_decoder_block_gb300 import synth
+    st = synth.layer_weights(wl)
+    return {k: torch.from_numpy(np.ascontiguousarray(v.data).view(np.int16)).to(dev).view(torch.bfloat16)
+            for k, v in st.items()}
+
+
+def dev_weights_random(wl, dev, seed):
+    """Same recipe drawn on the device (seeded torch generator): for the extra workloads."""
+    import torch
+    L = wl.layer
+    g = torch.Generator(device=dev).manual_seed(seed)
+    d, H, G, D, I = L.d_model, L.n_heads, L.n_kv_heads, L.head_dim, L.d_inter
+    shapes = {"wq": (H * D, d), "wk": (G * D, d), "wv": (G * D, d), "wo": (d, H * D), "w_gate": (I, d),
+              "w_up": (I, d), "w_down": (d, I)}
+    w = {k: (torch.randn(s, generator=g, device=dev) * 0.02).to(torch.bfloat16) for k, s in shapes.items()}
+    for k in ("attn_norm", "ffn_norm"):
+        w[k] = (1 + 0.1 * torch.randn(d, generator=g, device=dev)).to(torch.bfloat16)
+    return w
+
+
+def prefill_flops(L, B, S):
+    M = B * S
+    d, H, G, D, I = L.d_model, L.n_heads, L.n_kv_heads, L.head_dim, L.d_inter
+    return {
+        "qkv_rope_gemm": 2.0 * M * d * (H + 2 * G) * D,
+        "attention_prefill": 4.0 * D * H * B * S * (S + 1) / 2,
+        "o_proj_residual_gemm": 2.0 * M * H * D * d,
+        "gate_up_swiglu_gemm": 2.0 * M * d * 2 * I,
+        "down_residual_gemm": 2.0 * M * I * d,
+    }
+
+
+def bench_prefill(api, wl, steps, warmup, dev, pk, from_synth):
+    import numpy as np
+    import torch
+    L = wl.layer
+    B, S = wl.B, wl.S
+    w = dev_weights_from_synth(wl, dev) if from_synth else dev_weights_random(wl, dev, wl.seed)
+    if from_synth:
+        from llama_decoder_block_gb300 import synth
+        x = torch.from_numpy(synth.activations(wl).data.view(np.int16)).to(dev).view(torch.bfloat16)
+    else:
+        x = torch.randn(B, S, L.d_model, generator=torch.Generator(device=dev).manual_seed(wl.seed + 1),
+                        device=dev).to(torch.bfloat16)
+    out = torch.empty_like(x)
+    c, s = api.rope_tables(L.rope_base, L.head_dim, S)
+    cos, sin = torch.from_numpy(c).to(dev), torch.from_numpy(s).to(dev)
+    kc = torch.empty(B, L.n_kv_heads, S, L.head_dim, dtype=torch.bfloat16, device=dev)
+    vc = torch.empty_like(kc)
+    dims = api.Dims(L.d_model, L.n_heads, L.n_kv_heads, L.head_dim, L.d_inter, L.rms_eps, torch.bfloat16)
+    ws = api.workspace(api.prefill_workspace_bytes(dims, B, S), dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        api.layer_prefill(dims, w, x, out, cos, sin, kc, vc, ws, stream)
+
+    for _ in range(warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert api.device_status(stream) == 0
+    traces = [api.KernelTrace(len(PREFILL_KERNELS), stream) for _ in range(steps)]
+    barrier()
+    torch.cuda.synchronize()
+    n0 = api.launch_count()
+    t0 = time.perf_counter()
+    for tr in traces:
+        flush.zero_()
+        with tr:
+            step()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    launches = api.launch_count() - n0
+    barrier()
+    assert api.device_status(stream) == 0
+    per_kernel = np.array([tr.kernel_ms() for tr in traces])           # [steps, kernels]
+    step_ms = per_kernel.sum(axis=1)
+    res = {"ms_per_step": float(step_ms.mean()), "tokens_per_step": B * S, "wall_s": wall, "launches": launches,
+           "kernel_ms": {n: float(per_kernel[:, i].mean()) for i, n in enumerate(PREFILL_KERNELS)}}
+    flops = prefill_flops(L, B, S)
+    res["tflops_total"] = sum(flops.values()) / (res["ms_per_step"] * 1e-3) / 1e12
+    dom = max(flops, key=lambda k: res["kernel_ms"][k])
+    t = res["kernel_ms"][dom] * 1e-3
+    achieved = flops[dom] / t / 1e12
+    res["roofline"] = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1),
+                       "peak": pk["bf16_sustained"], "unit": "TFLOP/s",
+                       "frac": round(achieved / pk["bf16_sustained"], 4),
+                       "frac_of_burst_peak": round(achieved / pk["bf16"], 4),
+                       "peak_kind": f"{pk['source']} sustained bf16", "flop_per_launch": flops[dom],
+                       "traffic": NCU_TRAFFIC.get((dom, src_sha("gemm_tc.cu"))),
+                       "traffic_unit": "bytes per launch (ncu dram read+write)"}
+    res["kernel_tflops"] = {k: round(v / (res["kernel_ms"][k] * 1e-3) / 1e12, 1) for k, v in flops.items()}
+
+    # end to end through the C ABI: pinned host input -> device, the layer, device -> pinned host output
+    xh = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+    xh.copy_(x.cpu())
+    oh = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    xd = torch.empty_like(x)
+    e2e = []
+    for i in range(warmup + steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        xd.copy_(xh, non_blocking=True)
+        api.layer_prefill(dims, w, xd, out, cos, sin, kc, vc, ws, stream)
+        oh.copy_(out, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        if i >= warmup:
+            e2e.append(e0.elapsed_time(e1))
+    res["e2e_ms"] = float(np.mean(e2e))
+    res["h2d_bytes"] = x.numel() * 2
+    res["d2h_bytes"] = out.numel() * 2
+    del w, ws, flush, kc, vc
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_decode(api, wl, steps, warmup, dev, pk):
+    import numpy as np
+    import torch
+    from llama_decoder_block_gb300 import synth
+    L = wl.layer
+    B, T = wl.B, wl.T_max
+    w = dev_weights_random(wl, dev, wl.seed)
+    g = torch.Generator(device=dev).manual_seed(wl.seed + 2)
+    kc = torch.randn(B, L.n_kv_heads, T, L.head_dim, generator=g, device=dev).to(torch.bfloat16)
+    vc = torch.randn(B, L.n_kv_heads, T, L.head_dim, generator=g, device=dev).to(torch.bfloat16)
+    pos_h = synth.decode_positions(wl)
+    pos = torch.from_numpy(pos_h.astype(np.int32)).to(dev)
+    x = torch.randn(B, L.d_model, generator=g, device=dev).to(torch.bfloat16)
+    out = torch.empty_like(x)
+    c, s = api.rope_tables(L.rope_base, L.head_dim, T)
+    cos, sin = torch.from_numpy(c).to(dev), torch.from_numpy(s).to(dev)
+    dims = api.Dims(L.d_model, L.n_heads, L.n_kv_heads, L.head_dim, L.d_inter, L.rms_eps, torch.bfloat16)
+    ws = api.workspace(api.decode_workspace_bytes(dims, B, T), dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        api.layer_decode(dims, w, x, out, cos, sin, pos, kc, vc, ws, stream)
+
+    for _ in range(warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert api.device_status(stream) == 0
+    traces = [api.KernelTrace(len(DECODE_KERNELS), stream) for _ in range(steps)]
+    for tr in traces:
+        flush.zero_()
+        with tr:
+            step()
+    torch.cuda.synchronize()
+    assert api.device_status(stream) == 0
+    per_kernel = np.array([tr.kernel_ms() for tr in traces])
+    step_ms = per_kernel.sum(axis=1)
+    d, H, G, D, I = L.d_model, L.n_heads, L.n_kv_heads, L.head_dim, L.d_inter
+    w_bytes = 2 * (d * (H + 2 * G) * D + H * D * d + 3 * d * I + 2 * d)
+    kv_read = int(np.sum(pos_h + 1)) * G * D * 2 * 2
+    step_bytes = w_bytes + kv_read + B * (H + 2 * G) * D * 2
+    us = float(step_ms.mean() * 1e3)
+    km = {n: float(per_kernel[:, i].mean()) for i, n in enumerate(DECODE_KERNELS)}
+    attn_ms = km["attention_decode_split"]
+    attn_gbs = kv_read / (attn_ms * 1e-3) / 1e9
+    res = {"workload": wl.name, "us_per_step": round(us, 1), "bytes_per_step": step_bytes,
+           "hbm_GBps": round(step_bytes / (us * 1e-6) / 1e9, 1),
+           "frac_of_hbm": round(step_bytes / (us * 1e-6) / 1e9 / pk["hbm_gbs"], 4),
+           "kernel_us": {k: round(v * 1e3, 1) for k, v in km.items()},
+           "attention_roofline": {"bound": "hbm", "achieved": round(attn_gbs, 1), "peak": pk["hbm_gbs"],
+                                  "unit": "GB/s", "frac": round(attn_gbs / pk["hbm_gbs"], 4),
+                                  "bytes_per_launch": kv_read}}
+    del w, kc, vc, ws, flush
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_rmsnorm(api, dev, pk, rows=16384, d=4096, reps=20):
+    import torch
+    xs = [torch.randn(rows, d, device=dev).to(torch.bfloat16) for _ in range(2)]
+    g = torch.ones(d, dtype=torch.bfloat16, device=dev)
+    y = torch.empty_like(xs[0])
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    ts = []
+    for i in range(reps + 3):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        api.rmsnorm(xs[i % 2], g, y, 1e-5)
+        e1.record()
+        e1.synchronize()
+        if i >= 3:
+            ts.append(e0.elapsed_time(e1))
+    ms = sorted(ts)[len(ts) // 2]
+    gbs = 2 * rows * d * 2 / (ms * 1e-3) / 1e9
+    return {"rows": rows, "d": d, "us": round(ms * 1e3, 1), "GBps": round(gbs, 1),
+            "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4)}
+
+
+# ------------------------------------------------------------------ the oracle on the host cores
+
+class OracleSample:
+    """The fp64 oracle (as it stands) on a causal prefix of a prefill workload, on the host cores."""
+
+    def __init__(self, wl):
+        import numpy as np
+        import oracle
+        from llama_decoder_block_gb300 import synth
+        L = wl.layer
+        self.wl, self.oracle = wl, oracle
+        self.w64 = {k: v.f64() for k, v in synth.layer_weights(wl).items()}
+        self.x64 = synth.activations(wl).f64()
+        c, s = oracle.rope_tables(L.rope_base, L.head_dim, wl.S)
+        self.c, self.s = c.astype(np.float32).astype(np.float64), s.astype(np.float32).astype(np.float64)
+        self.kw = dict(n_heads=L.n_heads, n_kv_heads=L.n_kv_heads, head_dim=L.head_dim, rms_eps=L.rms_eps,
+                       store_bf16=True)
+
+    def run(self, n):
+        t = time.perf_counter()
+        self.oracle.decoder_layer(self.x64[:, :n], self.w64, self.c, self.s, **self.kw)
+        return time.perf_counter() - t
+
+    def calibrate(self, seconds):
+        """Largest power-of-two prefix (128 .. S tokens) whose run takes about `seconds`."""
+        n = 128
+        dt = self.run(n)
+        while dt < seconds / 2 and n < self.wl.S:
+            n = min(self.wl.S, n * 2)
+            dt = self.run(n)
+        return n
+
+
+def oracle_prefill_sample(wl, target_s=15.0):
+    """Times the oracle for about `target_s` seconds; returns (tokens/s, tokens per run, seconds per run)."""
+    o = OracleSample(wl)
+    n = o.calibrate(target_s / 3)
+    total, reps = 0.0, 0
+    while total < target_s and reps < 8:
+        total += o.run(n)
+        reps += 1
+    per = total / reps
+    return wl.B * n / per, n, per
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+_DIST = {"on": False}
+
+
+def barrier():
+    if _DIST["on"]:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(v: float) -> float:
+    if not _DIST["on"]:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    from llama_decoder_block_gb300 import synth
+    wl = synth.WORKLOADS[MAIN]
+    L = wl.layer
+    cfg = {"workload": MAIN, "B": wl.B, "S": wl.S, "d": L.d_model, "H": L.n_heads, "G": L.n_kv_heads,
+           "D": L.head_dim, "d_inter": L.d_inter, "layers": 1, "global_batch": wl.B * max(world, 1),
+           "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+           "l2": "flushed between timed steps (256 MiB write); weights 404 MB > L2"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        # each step: the oracle on a causal prefix sized so that W + K steps take a few minutes
+        o = OracleSample(wl)
+        n = o.calibrate(max(1.0, min(10.0, 150.0 / max(1, args.steps + args.warmup))))
+        for _ in range(args.warmup):
+            o.run(n)
+        total = sum(o.run(n) for _ in range(args.steps))
+        per = total / max(1, args.steps)
+        tps = wl.B * n / per
+        line = {"impl": "reference", "metric": METRIC, "value": round(tps, 2), "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per * 1e3, 1),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": cfg,
+                "cpu_baseline": {"value": round(tps, 2), "unit": "tokens/s", "cores": cores(), "kind": "oracle",
+                                 "sample": f"fp64 numpy oracle, one layer, first {n} tokens of the B=1 S=2048 "
+                                           "prefill (exact causal prefix), bf16 storage points"},
+                "e2e": {"value": round(tps, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        _DIST["on"] = True
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", local if world > 1 else 0)
+    import __graft_entry__
+    __graft_entry__.build()
+    from llama_decoder_block_gb300 import api
+    pk = peaks()
+
+    with Clocks(dev.index) as clk:
+        main_res = bench_prefill(api, wl, args.steps, args.warmup, dev, pk, from_synth=True)
+    ms = reduce_max(main_res["ms_per_step"])
+    e2e_ms = reduce_max(main_res["e2e_ms"])
+    value = world * main_res["tokens_per_step"] / (ms * 1e-3)
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded PCG64: x ~ N(0,1), W ~ N(0,0.02), gamma ~ 1+N(0,0.1))",
+            "config": cfg, "roofline": main_res["roofline"],
+            "e2e": {"value": round(world * main_res["tokens_per_step"] / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+                    "h2d_bytes_per_step": main_res["h2d_bytes"], "d2h_bytes_per_step": main_res["d2h_bytes"]},
+            "gpu_launches": main_res["launches"], "clocks": clk.summary(),
+            "prefill_tflops": round(main_res["tflops_total"], 1),
+            "kernel_ms": {k: round(v, 4) for k, v in main_res["kernel_ms"].items()},
+            "kernel_tflops": main_res["kernel_tflops"]}
+    if not args.no_extra:
+        torch.cuda.empty_cache()
+        line["decode"] = bench_decode(api, synth.WORKLOADS["decode_gqa8b_bf16_b64_t4096"], max(10, args.steps // 2),
+                                      args.warmup, dev, pk)
+        g8 = synth.WORKLOADS["gqa8b_bf16_b4_s4096"]
+        r8 = bench_prefill(api, g8, max(5, args.steps // 4), args.warmup, dev, pk, from_synth=False)
+        line["gqa8b_prefill"] = {"workload": g8.name, "tokens_per_s": round(g8.B * g8.S / (r8["ms_per_step"] * 1e-3), 1),
+                                 "ms_per_step": round(r8["ms_per_step"], 3), "tflops": round(r8["tflops_total"], 1),
+                                 "frac_of_sustained_peak": round(r8["tflops_total"] / pk["bf16_sustained"], 4),
+                                 "kernel_ms": {k: round(v, 3) for k, v in r8["kernel_ms"].items()},
+                                 "kernel_tflops": r8["kernel_tflops"]}
+        line["rmsnorm"] = bench_rmsnorm(api, dev, pk)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tps, n, per = oracle_prefill_sample(wl)
+        line["cpu_baseline"] = {"value": round(tps, 2), "unit": "tokens/s", "cores": cores(), "kind": "oracle",
+                                "sample": f"fp64 numpy oracle, one layer, first {n} tokens of the B=1 S=2048 prefill "
+                                          f"(exact causal prefix), {per:.1f} s per run"}
+    if rank == 0:
+        print(json.dumps(line))
+    if _DIST["on"]:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

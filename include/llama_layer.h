@@ -140,6 +140,26 @@ int llama_rmsnorm(const void *x, const void *gamma, void *y, int32_t rows, int32
 int llama_linear_bf16(const void *A, const void *B, void *C, int32_t M, int32_t N, int32_t K, int32_t c_f32,
                       void *cuda_stream);
 
+/* out = resid + A W^T (o_proj and down_proj with the residual add, "05 LLaMA3 Block — 从零件到
+ * 发动机" §4.2 steps ④ and ⑧).  A: device [M, K]; W: device [N, K]; resid, out: device [M, N];
+ * all bf16; resid and out may be the same buffer.  K % 8 == 0, N % 128 == 0. */
+int llama_linear_residual(const void *A, const void *W, const void *resid, void *out, int32_t M, int32_t N,
+                          int32_t K, void *cuda_stream);
+
+/* out = SiLU(A W_gate^T) * (A W_up^T) ("3.2 核心组件逐一拆解" §3.2.2; "05 LLaMA3 Block — 从零件到
+ * 发动机" §4.1).  A: device [M, K]; W_gate, W_up: device [I, K]; out: device [M, I]; bf16.
+ * K % 8 == 0, I % 128 == 0. */
+int llama_linear_swiglu(const void *A, const void *W_gate, const void *W_up, void *out, int32_t M, int32_t I,
+                        int32_t K, void *cuda_stream);
+
+/* [q|k|v] = xn [Wq;Wk;Wv]^T with RoPE on q and k ("第 10 章：现代 LLaMA 架构" §3 even/odd pairs,
+ * §9 q_proj/k_proj/v_proj then apply_rope) for B sequences of S tokens at positions 0..S-1.
+ * xn: device [B, S, d]; q_out: device [B, H, S, D]; k and v go to cache slots [0, S).  bf16
+ * layers only (dims.dtype = LLAMA_BF16).  S <= max_pos and S <= cache.max_T. */
+int llama_qkv_rope(const llama_layer_dims *dims, const void *xn, const void *wq, const void *wk, const void *wv,
+                   const float *cos, const float *sin, int32_t max_pos, llama_kv_cache cache, void *q_out, int32_t B,
+                   int32_t S, void *cuda_stream);
+
 /* Causal grouped-query attention over a cache ("12 · 从 Transformer 到 LLaMA 系列" §八
  * Attention; "深度学习进阶（三十）从 Transformer 到 LLaMA：现代 LLM 架构总览" §1.1
  * softmax(QK^T / sqrt(D)) V).  q: device [B, H, S, D] at positions 0..S-1; cache
@@ -181,6 +201,14 @@ int llama_debug_wait_probe(uint64_t budget_ns, void *cuda_stream);
 
 /* Number of kernels the library enqueued on this process since load (for launch accounting). */
 uint64_t llama_kernel_launch_count(void);
+
+/* Per-thread kernel trace for measurement.  events: caller-owned cudaEvent_t handles
+ * (n_events of them).  llama_trace_begin records events[0] on cuda_stream; afterwards,
+ * until llama_trace_end, every kernel that this thread's calls enqueue is followed by
+ * the next event, recorded on that call's stream (the i-th kernel runs between events
+ * i and i+1).  llama_trace_end stops tracing and returns how many events were recorded. */
+int llama_trace_begin(void *const *events, int32_t n_events, void *cuda_stream);
+int32_t llama_trace_end(void);
 
 #ifdef __cplusplus
 }

@@ -54,6 +54,11 @@ SIGNATURES = {
                                       c_int32, c_int32, c_void_p, c_size_t, c_void_p]),
     "llama_rmsnorm": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_float, c_int32, c_void_p]),
     "llama_linear_bf16": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32, c_void_p]),
+    "llama_linear_residual": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32,
+                                        c_void_p]),
+    "llama_linear_swiglu": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_void_p]),
+    "llama_qkv_rope": (c_int32, [P(LayerDims), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int32,
+                                 KVCache, c_void_p, c_int32, c_int32, c_void_p]),
     "llama_attention_prefill": (c_int32, [P(LayerDims), c_void_p, KVCache, c_void_p, c_int32, c_int32, c_void_p]),
     "llama_attention_decode_workspace_bytes": (c_int32, [P(LayerDims), c_int32, c_int32, P(c_size_t)]),
     "llama_attention_decode": (c_int32, [P(LayerDims), c_void_p, KVCache, c_void_p, c_void_p, c_int32, c_void_p,
@@ -63,6 +68,8 @@ SIGNATURES = {
     "llama_status_string": (ctypes.c_char_p, [c_int32]),
     "llama_debug_wait_probe": (c_int32, [c_uint64, c_void_p]),
     "llama_kernel_launch_count": (c_uint64, []),
+    "llama_trace_begin": (c_int32, [ctypes.POINTER(c_void_p), c_int32, c_void_p]),
+    "llama_trace_end": (c_int32, []),
 }
 
 _lib = None

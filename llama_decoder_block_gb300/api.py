@@ -131,6 +131,26 @@ def linear_bf16(a, b, c, stream=None) -> None:
                                       _stream(stream)), "llama_linear_bf16")
 
 
+def linear_residual(a, w, resid, out, stream=None) -> None:
+    M, K = a.shape
+    N.check(N.lib().llama_linear_residual(_ptr(a), _ptr(w), _ptr(resid), _ptr(out), M, w.shape[0], K,
+                                          _stream(stream)), "llama_linear_residual")
+
+
+def linear_swiglu(a, w_gate, w_up, out, stream=None) -> None:
+    M, K = a.shape
+    N.check(N.lib().llama_linear_swiglu(_ptr(a), _ptr(w_gate), _ptr(w_up), _ptr(out), M, w_gate.shape[0], K,
+                                        _stream(stream)), "llama_linear_swiglu")
+
+
+def qkv_rope(dims: Dims, xn, wq, wk, wv, cos, sin, cache_k, cache_v, q_out, stream=None) -> None:
+    B, S = xn.shape[0], xn.shape[1]
+    d = dims.c()
+    N.check(N.lib().llama_qkv_rope(ctypes.byref(d), _ptr(xn), _ptr(wq), _ptr(wk), _ptr(wv), _ptr(cos), _ptr(sin),
+                                   cos.shape[0], cache_struct(cache_k, cache_v), _ptr(q_out), B, S, _stream(stream)),
+            "llama_qkv_rope")
+
+
 def attention_prefill(dims: Dims, q, cache_k, cache_v, out, stream=None) -> None:
     B, _, S, _ = q.shape
     d = dims.c()
@@ -163,3 +183,28 @@ def wait_probe(budget_ns: int, stream=None) -> None:
 
 def launch_count() -> int:
     return N.lib().llama_kernel_launch_count()
+
+
+class KernelTrace:
+    """Times every kernel that the library enqueues inside a ``with`` block (CUDA events
+    recorded by the library on its launch stream after each kernel)."""
+
+    def __init__(self, max_kernels: int = 64, stream=None):
+        self.stream = stream or torch.cuda.current_stream()
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(max_kernels + 1)]
+        for e in self.events:           # torch creates the CUDA event on first record
+            e.record(self.stream)
+        self.handles = (ctypes.c_void_p * len(self.events))(*[e.cuda_event for e in self.events])
+        self.n = 0
+
+    def __enter__(self):
+        N.check(N.lib().llama_trace_begin(self.handles, len(self.events), self.stream.cuda_stream), "trace_begin")
+        return self
+
+    def __exit__(self, *exc):
+        self.n = N.lib().llama_trace_end()
+        return False
+
+    def kernel_ms(self) -> list[float]:
+        """Duration of each traced kernel, after the stream has been synchronised."""
+        return [self.events[i].elapsed_time(self.events[i + 1]) for i in range(self.n - 1)]

@@ -371,6 +371,45 @@ int llama_linear_bf16(const void* A, const void* B, void* C, int32_t M, int32_t 
   return gemm_plain(c, A, B, C, M, N, K, c_f32 != 0);
 }
 
+int llama_linear_residual(const void* A, const void* W, const void* resid, void* out, int32_t M, int32_t N, int32_t K,
+                          void* cuda_stream) {
+  if (!A || !W || !resid || !out || M <= 0 || N <= 0 || K <= 0) return LLAMA_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(W) || !aligned16(resid) || !aligned16(out)) return LLAMA_ERR_INVALID_ARG;
+  if (K % 8 != 0 || N % 128 != 0) return LLAMA_ERR_UNSUPPORTED;
+  Ctx c;
+  int rc = make_ctx(cuda_stream, &c);
+  if (rc) return rc;
+  return gemm_residual(c, A, W, resid, out, M, N, K);
+}
+
+int llama_linear_swiglu(const void* A, const void* W_gate, const void* W_up, void* out, int32_t M, int32_t I, int32_t K,
+                        void* cuda_stream) {
+  if (!A || !W_gate || !W_up || !out || M <= 0 || I <= 0 || K <= 0) return LLAMA_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(W_gate) || !aligned16(W_up) || !aligned16(out)) return LLAMA_ERR_INVALID_ARG;
+  if (K % 8 != 0 || I % 128 != 0) return LLAMA_ERR_UNSUPPORTED;
+  Ctx c;
+  int rc = make_ctx(cuda_stream, &c);
+  if (rc) return rc;
+  return gemm_swiglu(c, A, W_gate, W_up, out, M, I, K);
+}
+
+int llama_qkv_rope(const llama_layer_dims* dims, const void* xn, const void* wq, const void* wk, const void* wv,
+                   const float* cos, const float* sin, int32_t max_pos, llama_kv_cache cache, void* q_out, int32_t B,
+                   int32_t S, void* cuda_stream) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if (dims->dtype != LLAMA_BF16) return LLAMA_ERR_UNSUPPORTED;
+  if (!xn || !wq || !wk || !wv || !cos || !sin || !cache.k || !cache.v || !q_out) return LLAMA_ERR_INVALID_ARG;
+  if (!aligned16(xn) || !aligned16(wq) || !aligned16(wk) || !aligned16(wv) || !aligned16(cache.k) ||
+      !aligned16(cache.v) || !aligned16(q_out))
+    return LLAMA_ERR_INVALID_ARG;
+  if (B <= 0 || S <= 0 || S > max_pos || S > cache.max_T) return LLAMA_ERR_INVALID_ARG;
+  Ctx c;
+  if ((rc = make_ctx(cuda_stream, &c))) return rc;
+  return gemm_qkv_rope(c, xn, wq, wk, wv, B, S, dims->d_model, dims->n_heads, dims->n_kv_heads, dims->head_dim, cos,
+                       sin, q_out, cache.k, cache.v, cache.max_T);
+}
+
 int llama_attention_prefill(const llama_layer_dims* dims, const void* q, llama_kv_cache cache, void* out, int32_t B,
                             int32_t S, void* cuda_stream) {
   int rc = check_dims(dims);

@@ -232,11 +232,11 @@ int attn_decode(const Ctx& c, int dtype, const void* q, const void* k_cache, con
     case 8: attn_decode_split_kernel<8><<<grid, WARPS * 32, 0, c.stream>>>(qq, kk, vv, positions, o_part, m_part, l_part, H, G, T_max, max_pos, n_split, sl, c.status); break;
     default: return LLAMA_ERR_UNSUPPORTED;
   }
-  int rc = after_launch();
+  int rc = after_launch(c);
   if (rc != LLAMA_OK) return rc;
   attn_decode_combine_kernel<<<B * H, HD, 0, c.stream>>>(o_part, m_part, l_part, static_cast<__nv_bfloat16*>(out),
                                                          n_split);
-  return after_launch();
+  return after_launch(c);
 }
 
 }  // namespace llama

@@ -311,7 +311,7 @@ int attn_prefill_tc(const Ctx& c, const void* q, const void* k_cache, const void
   p.out = static_cast<__nv_bfloat16*>(out);
   p.status = c.status;
   attn_prefill_kernel<<<dim3(p.n_qt, H, B), NUM_THREADS, kSmemBytes, c.stream>>>(tq, tk, tv, p);
-  return after_launch();
+  return after_launch(c);
 }
 
 }  // namespace llama

@@ -398,7 +398,7 @@ int launch(const Ctx& c, const TMaps& tm, Params p) {
   if (tiles == 0) return LLAMA_OK;
   const int grid = std::min(tiles, c.num_sms);
   kern<<<grid, NUM_THREADS, smem, c.stream>>>(tm, p);
-  return after_launch();
+  return after_launch(c);
 }
 
 Params base_params(int M, int N, int K, int BN) {

@@ -20,8 +20,8 @@ struct Ctx {
 
 // Fills `c` for the current device; returns LLAMA_OK or LLAMA_ERR_CUDA.
 int make_ctx(void* stream, Ctx* c);
-// Checks cudaGetLastError after a launch and counts the launch.
-int after_launch();
+// Checks cudaGetLastError after a launch, counts it and records the next trace event.
+int after_launch(const Ctx& c);
 
 // ---------------------------------------------------------------- tensor maps (tmap.cu)
 // 2-D bf16 row-major matrix [rows, cols] with row stride `ld` elements; box = 64 columns

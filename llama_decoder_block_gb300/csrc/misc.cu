@@ -91,7 +91,7 @@ int embed_gather(const Ctx& c, const int32_t* tokens, const void* table, void* x
   const int vec = row_bytes / 16;
   embed_kernel<<<(n_tok + 7) / 8, 256, 0, c.stream>>>(tokens, static_cast<const uint4*>(table),
                                                       static_cast<uint4*>(x), n_tok, vec, vocab, c.status);
-  return after_launch();
+  return after_launch(c);
 }
 
 int fix_qkv_rope(const Ctx& c, const float* P, int splits, int n_tok, int H, int G, int D, const int32_t* positions,
@@ -102,7 +102,7 @@ int fix_qkv_rope(const Ctx& c, const float* P, int splits, int n_tok, int H, int
   fix_qkv_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, c.stream>>>(
       P, splits, n_tok, H, G, D, positions, max_pos, cos, sin, static_cast<__nv_bfloat16*>(q_out),
       static_cast<__nv_bfloat16*>(k_cache), static_cast<__nv_bfloat16*>(v_cache), T_max, c.status);
-  return after_launch();
+  return after_launch(c);
 }
 
 int fix_residual(const Ctx& c, const float* P, int splits, int n_tok, int N, const void* resid, void* out) {
@@ -110,7 +110,7 @@ int fix_residual(const Ctx& c, const float* P, int splits, int n_tok, int N, con
   if (total == 0) return LLAMA_OK;
   fix_residual_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, c.stream>>>(
       P, splits, n_tok, N, static_cast<const __nv_bfloat16*>(resid), static_cast<__nv_bfloat16*>(out));
-  return after_launch();
+  return after_launch(c);
 }
 
 int fix_swiglu(const Ctx& c, const float* P, int splits, int n_tok, int I, void* out) {
@@ -118,7 +118,7 @@ int fix_swiglu(const Ctx& c, const float* P, int splits, int n_tok, int I, void*
   if (total == 0) return LLAMA_OK;
   fix_swiglu_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, c.stream>>>(
       P, splits, n_tok, I, static_cast<__nv_bfloat16*>(out));
-  return after_launch();
+  return after_launch(c);
 }
 
 }  // namespace llama

@@ -108,7 +108,7 @@ int rmsnorm(const Ctx& c, const void* x, const void* gamma, void* y, int rows, i
     rmsnorm_generic_kernel<float><<<grid, block, 0, c.stream>>>(
         static_cast<const float*>(x), static_cast<const float*>(gamma), static_cast<float*>(y), rows, d, eps);
   }
-  return after_launch();
+  return after_launch(c);
 }
 
 }  // namespace llama

@@ -61,9 +61,20 @@ int make_ctx(void* stream, Ctx* c) {
   return LLAMA_OK;
 }
 
-int after_launch() {
+namespace {
+// Optional per-thread trace: caller-owned CUDA events recorded on the launch stream
+// once when tracing starts and after every kernel launch (for timing kernel by kernel).
+thread_local void* const* t_events = nullptr;
+thread_local int t_n = 0;
+thread_local int t_next = 0;
+}  // namespace
+
+int after_launch(const Ctx& c) {
   g_launches.fetch_add(1, std::memory_order_relaxed);
-  return cudaGetLastError() == cudaSuccess ? LLAMA_OK : LLAMA_ERR_CUDA;
+  const bool ok = cudaGetLastError() == cudaSuccess;
+  if (t_events != nullptr && t_next < t_n)
+    cudaEventRecord(static_cast<cudaEvent_t>(t_events[t_next++]), c.stream);
+  return ok ? LLAMA_OK : LLAMA_ERR_CUDA;
 }
 
 bool make_tmap_2d(CUtensorMap* tm, const void* base, uint64_t cols, uint64_t rows, uint64_t ld, uint32_t box_rows) {
@@ -147,10 +158,28 @@ int llama_debug_wait_probe(uint64_t budget_ns, void* cuda_stream) {
   if (rc != LLAMA_OK) return rc;
   const uint64_t cap = 10ull * 1000ull * 1000ull * 1000ull;
   wait_probe_kernel<<<1, 32, 0, c.stream>>>(budget_ns < cap ? budget_ns : cap, c.status);
-  return after_launch();
+  return after_launch(c);
 }
 
 uint64_t llama_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int llama_trace_begin(void* const* events, int32_t n_events, void* cuda_stream) {
+  if (events == nullptr || n_events < 1) return LLAMA_ERR_INVALID_ARG;
+  t_events = events;
+  t_n = n_events;
+  t_next = 0;
+  if (cudaEventRecord(static_cast<cudaEvent_t>(events[t_next++]), static_cast<cudaStream_t>(cuda_stream)) !=
+      cudaSuccess)
+    return LLAMA_ERR_CUDA;
+  return LLAMA_OK;
+}
+
+int32_t llama_trace_end(void) {
+  const int n = t_next;
+  t_events = nullptr;
+  t_n = t_next = 0;
+  return n;
+}
 
 int llama_rope_tables(double base, int32_t head_dim, int32_t max_pos, float* cos_host, float* sin_host) {
   if (cos_host == nullptr || sin_host == nullptr || head_dim <= 0 || (head_dim & 1) || max_pos <= 0 ||

@@ -141,7 +141,7 @@ int simt_linear(const Ctx& c, int mode, const float* X, const float* W0, const f
   if (total == 0) return LLAMA_OK;
   simt_linear_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, c.stream>>>(mode, X, W0, W1, resid, out,
                                                                                       M, N, K);
-  return after_launch();
+  return after_launch(c);
 }
 
 int simt_qkv_rope(const Ctx& c, const float* X, const float* Wq, const float* Wk, const float* Wv, int B, int S,
@@ -151,7 +151,7 @@ int simt_qkv_rope(const Ctx& c, const float* X, const float* Wq, const float* Wk
   if (total == 0) return LLAMA_OK;
   simt_qkv_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, c.stream>>>(
       X, Wq, Wk, Wv, B, S, K, H, G, D, cos, sin, positions, max_pos, q_out, k_cache, v_cache, T_max, c.status);
-  return after_launch();
+  return after_launch(c);
 }
 
 int simt_attention(const Ctx& c, const float* q, const float* k_cache, const float* v_cache,
@@ -162,7 +162,7 @@ int simt_attention(const Ctx& c, const float* q, const float* k_cache, const flo
   if (threads == 0) return LLAMA_OK;
   simt_attention_kernel<<<static_cast<unsigned>((threads + 127) / 128), 128, 0, c.stream>>>(
       q, k_cache, v_cache, positions, out, B, S, H, G, D, T_max, max_pos, c.status);
-  return after_launch();
+  return after_launch(c);
 }
 
 }  // namespace llama

@@ -156,10 +156,15 @@ def activations(wl: Workload, rows: int | None = None) -> Stored:
     return _store(_normal(rng(wl.seed, 0, _X), shape, 1.0, L.dtype), L.dtype)
 
 
+def decode_positions(wl: Workload) -> np.ndarray:
+    """New-token positions ``[B]`` int32, uniform in [pos_lo, pos_hi)."""
+    return rng(wl.seed, 0, _POSITIONS).integers(wl.pos_lo, wl.pos_hi, size=wl.B).astype(np.int32)
+
+
 def decode_state(wl: Workload) -> tuple[np.ndarray, Stored, Stored]:
     """positions ``[B]`` int32 and the pre-filled caches K, V ``[B, G, T_max, D]``."""
     L = wl.layer
-    pos = rng(wl.seed, 0, _POSITIONS).integers(wl.pos_lo, wl.pos_hi, size=wl.B).astype(np.int32)
+    pos = decode_positions(wl)
     shape = (wl.B, L.n_kv_heads, wl.T_max, L.head_dim)
     k = _store(_normal(rng(wl.seed, 0, _CACHE_K), shape, 1.0, L.dtype), L.dtype)
     v = _store(_normal(rng(wl.seed, 0, _CACHE_V), shape, 1.0, L.dtype), L.dtype)

@@ -15,9 +15,9 @@ Pages cited (by title):
 Readings taken where the pages disagree or are silent (see also the design
 notes): eps inside the square root; even/odd RoPE pairs; theta_i =
 base^(-2i/D); key j visible to query i iff pos_j <= pos_i; head h uses KV
-group h // (H/G); SiLU on the gate projection; K/V (and, in a stack, each
-layer's output) rounded to bf16 where the configuration stores them in bf16,
-nowhere else.
+group h // (H/G); SiLU on the gate projection; for bf16 layers, every
+activation passed from one step to the next rounded to bf16 where it is
+produced, and nowhere else.
 """
 from __future__ import annotations
 
@@ -82,13 +82,18 @@ def silu(z):
     return z / (1.0 + np.exp(-z))
 
 
-def swiglu_mlp(x, w_gate, w_up, w_down):
+def _keep(a):
+    return a
+
+
+def swiglu_mlp(x, w_gate, w_up, w_down, store=_keep):
     """SwiGLU MLP: down(SiLU(x W_gate^T) * (x W_up^T)), no bias.
 
     [CORE] §3.2.2 ``SwiGLUFFN``; [L3B] §4.1 ``LlamaMLP`` and §6 (the SiLU goes on
-    the gate projection, not on up); [MOD] §5.
+    the gate projection, not on up); [MOD] §5.  ``store`` is applied to the gated
+    product, the activation handed to the down projection.
     """
-    return (silu(x @ w_gate.T) * (x @ w_up.T)) @ w_down.T
+    return store(silu(x @ w_gate.T) * (x @ w_up.T)) @ w_down.T
 
 
 def attention(q, k, v, q_pos, k_len):
@@ -133,9 +138,16 @@ def decoder_layer(x, w, cos, sin, *, n_heads, n_kv_heads, head_dim, rms_eps,
     (``wq [H*D, d]`` ...).  New tokens of sequence b sit at positions
     ``past_len[b] + s`` ([MOD] §3: position_id = past_len); ``past_k/v``
     ``[B, G, T, D]`` hold the cache, slots ``[0, past_len[b])`` valid.
-    With ``store_bf16`` the new K/V are rounded to bf16 as the cache stores them.
+
+    ``store_bf16``: the layer keeps its activations in bf16 (the configurations'
+    "bf16 weights and activations, fp32 accumulation").  Every tensor handed from
+    one step of the layer to the next is then rounded to bf16 once, where it is
+    produced: the normed input, q and k after RoPE, v (the cache), the attention
+    output, h, the normed h and the gated MLP activation.  Arithmetic inside a step
+    stays exact.
     Returns ``(out [B,S,d], k_new [B,G,S,D], v_new [B,G,S,D])``.
     """
+    st = round_bf16 if store_bf16 else _keep
     B, S, d = x.shape
     H, G, D = n_heads, n_kv_heads, head_dim
     if past_len is None:
@@ -145,17 +157,15 @@ def decoder_layer(x, w, cos, sin, *, n_heads, n_kv_heads, head_dim, rms_eps,
 
     # attention half
     residual = x
-    xn = rms_norm(x, w["attn_norm"], rms_eps)
+    xn = st(rms_norm(x, w["attn_norm"], rms_eps))
     q = (xn @ w["wq"].T).reshape(B, S, H, D).transpose(0, 2, 1, 3)       # [B, H, S, D]
     k = (xn @ w["wk"].T).reshape(B, S, G, D).transpose(0, 2, 1, 3)       # [B, G, S, D]
     v = (xn @ w["wv"].T).reshape(B, S, G, D).transpose(0, 2, 1, 3)
     c = cos[pos][:, None, :, :]                                          # [B, 1, S, D/2]
     s = sin[pos][:, None, :, :]
-    q = apply_rope(q, c, s)                                              # RoPE on q and k only
-    k = apply_rope(k, c, s)
-    if store_bf16:
-        k = round_bf16(k)
-        v = round_bf16(v)
+    q = st(apply_rope(q, c, s))                                          # RoPE on q and k only
+    k = st(apply_rope(k, c, s))
+    v = st(v)
 
     # keys of sequence b: cached slots [0, past_len[b]) then the S new ones
     T = int((past_len + S).max())
@@ -168,14 +178,14 @@ def decoder_layer(x, w, cos, sin, *, n_heads, n_kv_heads, head_dim, rms_eps,
             vv[b, :, :P] = past_v[b, :, :P]
         kk[b, :, P:P + S] = k[b]
         vv[b, :, P:P + S] = v[b]
-    o = attention(q, kk, vv, pos, past_len + S)                           # [B, H, S, D]
+    o = st(attention(q, kk, vv, pos, past_len + S))                       # [B, H, S, D]
     o = o.transpose(0, 2, 1, 3).reshape(B, S, H * D)
-    h = residual + o @ w["wo"].T
+    h = st(residual + o @ w["wo"].T)
 
     # MLP half
     residual = h
-    hn = rms_norm(h, w["ffn_norm"], rms_eps)
-    out = residual + swiglu_mlp(hn, w["w_gate"], w["w_up"], w["w_down"])
+    hn = st(rms_norm(h, w["ffn_norm"], rms_eps))
+    out = residual + swiglu_mlp(hn, w["w_gate"], w["w_up"], w["w_down"], store=st)
     return out, k, v
 
 
@@ -184,8 +194,8 @@ def stack_forward(tokens, layers, final_norm, embed, lm_head, cos, sin, *, n_hea
     """embed -> layers -> final RMSNorm -> untied LM head ([T2L] §八 ``LlamaModel.forward``).
 
     ``layers`` yields one weight dict per layer (so callers can stream them).
-    With ``store_bf16`` each layer's output is rounded to bf16 (the stored
-    activation between layers) and so are the K/V inside each layer.
+    With ``store_bf16`` the activations are bf16 (see ``decoder_layer``): each
+    layer's output and the final normed activation are rounded once too.
     Returns logits ``[B, S, V]``.
     """
     x = embed[tokens]
@@ -195,6 +205,8 @@ def stack_forward(tokens, layers, final_norm, embed, lm_head, cos, sin, *, n_hea
         if store_bf16:
             x = round_bf16(x)
     xn = rms_norm(x, final_norm, rms_eps)                                 # the final norm Pre-LN needs
+    if store_bf16:
+        xn = round_bf16(xn)
     return xn @ lm_head.T
 
 

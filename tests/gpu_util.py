@@ -34,6 +34,29 @@ def assert_close(gpu: np.ndarray, ref: np.ndarray, tol: float, what: str):
     return float(err.max())
 
 
+# Whole bf16 layer at full width (d = 4096, d_inter = 11008 / 14336): bf16 storage of the
+# activations makes two correct implementations differ by more than TOL at a few elements.
+# The oracle itself, with fp32-sized noise (2e-7 relative) before each bf16 storage rounding,
+# moves by up to 3.4e-2, p99.9 1.7e-2, 3.5e-4 of the elements above 2e-2 and 2.7e-3 normwise
+# (tests/test_oracle_sensitivity.py).  Gate: TOL on all but 1e-3 of the elements, ENVELOPE
+# everywhere, NORMWISE on the whole tensor.
+LAYER_FULL = {"tol": 2e-2, "max_frac_over_tol": 1e-3, "envelope": 6e-2, "normwise": 5e-3}
+
+
+def assert_close_layer_full(gpu: np.ndarray, ref: np.ndarray, what: str):
+    g = LAYER_FULL
+    assert gpu.shape == ref.shape, (what, gpu.shape, ref.shape)
+    assert np.all(np.isfinite(gpu)), f"{what}: non-finite values in the GPU result"
+    err = np.abs(gpu - ref) / (1.0 + np.abs(ref))
+    frac = float(np.mean(err > g["tol"]))
+    norm = float(np.linalg.norm(gpu - ref) / np.linalg.norm(ref))
+    msg = (f"{what}: max {err.max():.3e} (envelope {g['envelope']:.0e}), fraction over {g['tol']:.0e} = {frac:.2e} "
+           f"(limit {g['max_frac_over_tol']:.0e}), normwise {norm:.2e} (limit {g['normwise']:.0e}), "
+           f"p99 {np.quantile(err, 0.99):.2e}")
+    assert err.max() <= g["envelope"] and frac <= g["max_frac_over_tol"] and norm <= g["normwise"], msg
+    return msg
+
+
 def dims_of(layer: synth.LayerShape) -> api.Dims:
     return api.Dims(layer.d_model, layer.n_heads, layer.n_kv_heads, layer.head_dim, layer.d_inter, layer.rms_eps,
                     TORCH_DT[layer.dtype])

@@ -16,16 +16,18 @@ MUTANTS = {
                         "x_even = x[..., :x.shape[-1]//2]\n    x_odd = x[..., x.shape[-1]//2:]"),
     "rope_sign": ("y[..., 0::2] = x_even * cos - x_odd * sin", "y[..., 0::2] = x_even * cos + x_odd * sin"),
     "rope_frequency": ("theta = np.power(float(base), -2.0 * i / head_dim)", "theta = np.power(float(base), -1.0 * i / head_dim)"),
-    "rope_on_v": ("    if store_bf16:\n        k = round_bf16(k)", "    v = apply_rope(v, c, s)\n    if store_bf16:\n        k = round_bf16(k)"),
+    "rope_on_v": ("    v = st(v)\n", "    v = st(apply_rope(v, c, s))\n"),
     "group_map_modulo": ("g = h // rep", "g = h % G"),
     "mask_strict": ("allowed = np.arange(T)[None, :] <= np.asarray(q_pos[b])[:, None]",
                     "allowed = np.arange(T)[None, :] < np.maximum(np.asarray(q_pos[b])[:, None], 1)"),
     "scale_1_over_D": ("scores = (q[b, h] @ k[b, g, :T].T) / np.sqrt(D)", "scores = (q[b, h] @ k[b, g, :T].T) / D"),
-    "silu_on_up": ("return (silu(x @ w_gate.T) * (x @ w_up.T)) @ w_down.T", "return (silu(x @ w_up.T) * (x @ w_gate.T)) @ w_down.T"),
+    "silu_on_up": ("return store(silu(x @ w_gate.T) * (x @ w_up.T)) @ w_down.T",
+                   "return store(silu(x @ w_up.T) * (x @ w_gate.T)) @ w_down.T"),
     "bf16_truncates": ("return np.ldexp(np.rint(np.ldexp(m, 8)), e - 8)", "return np.ldexp(np.trunc(np.ldexp(m, 8)), e - 8)"),
-    "residual_after_norm": ("    residual = x\n    xn = rms_norm(x, w[\"attn_norm\"], rms_eps)",
-                            "    xn = rms_norm(x, w[\"attn_norm\"], rms_eps)\n    residual = xn"),
-    "shared_norm_gamma": ("hn = rms_norm(h, w[\"ffn_norm\"], rms_eps)", "hn = rms_norm(h, w[\"attn_norm\"], rms_eps)"),
+    "residual_after_norm": ("    residual = x\n    xn = st(rms_norm(x, w[\"attn_norm\"], rms_eps))",
+                            "    xn = st(rms_norm(x, w[\"attn_norm\"], rms_eps))\n    residual = xn"),
+    "shared_norm_gamma": ("hn = st(rms_norm(h, w[\"ffn_norm\"], rms_eps))",
+                          "hn = st(rms_norm(h, w[\"attn_norm\"], rms_eps))"),
     "no_final_norm": ("xn = rms_norm(x, final_norm, rms_eps)", "xn = x"),
     "decode_positions_restart": ("pos = past_len[:, None] + np.arange(S)[None, :]",
                                  "pos = np.zeros_like(past_len)[:, None] + np.arange(S)[None, :]"),

@@ -1,0 +1,41 @@
+"""Derivation of the whole-layer tolerance at full width (d = 4096, d_inter = 11008).
+
+With bf16 activations, a result that differs from the oracle by fp32 accumulation error
+(about 1e-7 relative) before each bf16 storage rounding lands on a neighbouring bf16 value
+at a few elements; those flips cascade through attention and the gated MLP, and the
+d_inter-long down projection sums them.  The oracle itself, perturbed that way, already
+leaves the elementwise 2e-2 * (1 + |ref|) band at some elements, but stays inside the
+full-width gate that the GPU tests apply (gpu_util.LAYER_FULL).
+"""
+import numpy as np
+
+import oracle
+from gpu_util import LAYER_FULL
+from llama_decoder_block_gb300 import synth
+from oracle import layer as oracle_layer
+
+
+def test_fp32_sized_noise_at_the_storage_points_moves_the_full_width_layer(monkeypatch):
+    wl = synth.WORKLOADS["mha7b_bf16_b1_s2048"]
+    L = wl.layer
+    S = 64                                       # a causal prefix keeps this on the CPU
+    w = {k: v.f64() for k, v in synth.layer_weights(wl).items()}
+    x = synth.activations(wl).f64()[:, :S]
+    c, s = oracle.rope_tables(L.rope_base, L.head_dim, S)
+    c, s = c.astype(np.float32).astype(np.float64), s.astype(np.float32).astype(np.float64)
+    kw = dict(n_heads=L.n_heads, n_kv_heads=L.n_kv_heads, head_dim=L.head_dim, rms_eps=L.rms_eps, store_bf16=True)
+    ref, _, _ = oracle.decoder_layer(x, w, c, s, **kw)
+
+    exact = oracle_layer.round_bf16
+    rng = np.random.default_rng(0)
+    monkeypatch.setattr(oracle_layer, "round_bf16",
+                        lambda v: exact(np.asarray(v, np.float64) * (1 + 2e-7 * rng.standard_normal(np.shape(v)))))
+    out, _, _ = oracle.decoder_layer(x, w, c, s, **kw)
+
+    err = np.abs(out - ref) / (1 + np.abs(ref))
+    frac = np.mean(err > LAYER_FULL["tol"])
+    norm = np.linalg.norm(out - ref) / np.linalg.norm(ref)
+    assert err.max() > LAYER_FULL["tol"]                       # the plain band is too tight here
+    assert err.max() <= LAYER_FULL["envelope"]
+    assert frac <= LAYER_FULL["max_frac_over_tol"]
+    assert norm <= LAYER_FULL["normwise"]
