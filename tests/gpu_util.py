@@ -36,11 +36,12 @@ def assert_close(gpu: np.ndarray, ref: np.ndarray, tol: float, what: str):
 
 # Whole bf16 layer at full width (d = 4096, d_inter = 11008 / 14336): bf16 storage of the
 # activations makes two correct implementations differ by more than TOL at a few elements.
-# The oracle itself, with fp32-sized noise (2e-7 relative) before each bf16 storage rounding,
-# moves by up to 3.4e-2, p99.9 1.7e-2, 3.5e-4 of the elements above 2e-2 and 2.7e-3 normwise
-# (tests/test_oracle_sensitivity.py).  Gate: TOL on all but 1e-3 of the elements, ENVELOPE
-# everywhere, NORMWISE on the whole tensor.
-LAYER_FULL = {"tol": 2e-2, "max_frac_over_tol": 1e-3, "envelope": 6e-2, "normwise": 5e-3}
+# The oracle itself, computed the way a tensor-core implementation does (fp32-sized noise,
+# 2e-7 relative, before each bf16 storage rounding; softmax probabilities rounded to bf16
+# before they multiply V), moves at the GQA 8B shape by up to 4.3e-2, with 1.2e-3 of the
+# elements above 2e-2 and 3.2e-3 normwise (tests/test_oracle_sensitivity.py).  Gate: TOL on
+# all but 3e-3 of the elements, ENVELOPE everywhere, NORMWISE on the whole tensor.
+LAYER_FULL = {"tol": 2e-2, "max_frac_over_tol": 3e-3, "envelope": 6e-2, "normwise": 5e-3}
 
 
 def assert_close_layer_full(gpu: np.ndarray, ref: np.ndarray, what: str):
