@@ -46,6 +46,10 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true", help="only the headline workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", choices=["attention", "gate_up", "down", "qkv", "decode_attention", "decode_layer",
+                                       "rmsnorm"],
+                    help="time one step alone (W + K launches, CUDA events) instead of the layer")
+    ap.add_argument("--workload", default=MAIN, help="workload whose shapes --case uses")
     return ap.parse_args()
 
 
@@ -321,6 +325,93 @@ def bench_rmsnorm(api, dev, pk, rows=16384, d=4096, reps=20):
             "frac_of_hbm": round(gbs / pk["hbm_gbs"], 4)}
 
 
+def bench_case(api, case, wl, steps, warmup, dev, pk):
+    """One step alone at the workload's shapes: mean launch time over `steps` launches."""
+    import numpy as np
+    import torch
+    L = wl.layer
+    d, H, G, D, I = L.d_model, L.n_heads, L.n_kv_heads, L.head_dim, L.d_inter
+    dims = api.Dims(d, H, G, D, I, L.rms_eps, torch.bfloat16)
+    g = torch.Generator(device=dev).manual_seed(7)
+
+    def rnd(*shape, std=1.0):
+        return (torch.randn(*shape, generator=g, device=dev) * std).to(torch.bfloat16)
+
+    B, S = wl.B, max(wl.S, 1)
+    M = B * S
+    if case == "attention":
+        q, k, v = rnd(B, H, S, D), rnd(B, G, S, D), rnd(B, G, S, D)
+        o = torch.empty(B, S, H * D, dtype=torch.bfloat16, device=dev)
+        fn = lambda: api.attention_prefill(dims, q, k, v, o)
+        work, unit = 4.0 * D * H * B * S * (S + 1) / 2, "flop"
+    elif case == "gate_up":
+        x, wg, wu = rnd(M, d), rnd(I, d, std=0.02), rnd(I, d, std=0.02)
+        a = torch.empty(M, I, dtype=torch.bfloat16, device=dev)
+        fn = lambda: api.linear_swiglu(x, wg, wu, a)
+        work, unit = 2.0 * M * d * 2 * I, "flop"
+    elif case == "down":
+        a, wd, r = rnd(M, I), rnd(d, I, std=0.02), rnd(M, d)
+        out = torch.empty(M, d, dtype=torch.bfloat16, device=dev)
+        fn = lambda: api.linear_residual(a, wd, r, out)
+        work, unit = 2.0 * M * I * d, "flop"
+    elif case == "qkv":
+        x, wq, wk, wv = rnd(B, S, d), rnd(H * D, d, std=0.02), rnd(G * D, d, std=0.02), rnd(G * D, d, std=0.02)
+        q = torch.empty(B, H, S, D, dtype=torch.bfloat16, device=dev)
+        kc = torch.empty(B, G, S, D, dtype=torch.bfloat16, device=dev)
+        vc = torch.empty_like(kc)
+        c, s = api.rope_tables(L.rope_base, D, S)
+        cos, sin = torch.from_numpy(c).to(dev), torch.from_numpy(s).to(dev)
+        fn = lambda: api.qkv_rope(dims, x, wq, wk, wv, cos, sin, kc, vc, q)
+        work, unit = 2.0 * M * d * (H + 2 * G) * D, "flop"
+    elif case in ("decode_attention", "decode_layer"):
+        from llama_decoder_block_gb300 import synth
+        dw = synth.WORKLOADS["decode_gqa8b_bf16_b64_t4096"] if wl.kind != "decode" else wl
+        B, T = dw.B, dw.T_max
+        pos_h = synth.decode_positions(dw)
+        pos = torch.from_numpy(pos_h).to(dev)
+        kc, vc = rnd(B, G, T, D), rnd(B, G, T, D)
+        kv = int(np.sum(pos_h + 1)) * G * D * 2 * 2
+        if case == "decode_attention":
+            q = rnd(B, H, D)
+            o = torch.empty(B, H * D, dtype=torch.bfloat16, device=dev)
+            ws = api.workspace(api.attention_decode_workspace_bytes(dims, B, T), dev)
+            fn = lambda: api.attention_decode(dims, q, kc, vc, pos, o, ws)
+            work, unit = kv, "byte"
+        else:
+            w = dev_weights_random(dw, dev, 3)
+            x = rnd(B, d)
+            y = torch.empty_like(x)
+            c, s = api.rope_tables(L.rope_base, D, T)
+            cos, sin = torch.from_numpy(c).to(dev), torch.from_numpy(s).to(dev)
+            ws = api.workspace(api.decode_workspace_bytes(dims, B, T), dev)
+            fn = lambda: api.layer_decode(dims, w, x, y, cos, sin, pos, kc, vc, ws)
+            work, unit = kv + 2 * (d * (H + 2 * G) * D + H * D * d + 3 * d * I), "byte"
+    else:   # rmsnorm
+        x, gm = rnd(M, d), rnd(d)
+        y = torch.empty_like(x)
+        fn = lambda: api.rmsnorm(x, gm, y, L.rms_eps)
+        work, unit = 2.0 * M * d * 2, "byte"
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    ts = []
+    for i in range(warmup + steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        e1.synchronize()
+        if i >= warmup:
+            ts.append(e0.elapsed_time(e1))
+    assert api.device_status() == 0
+    ms = float(np.mean(ts))
+    rate = work / (ms * 1e-3)
+    if unit == "flop":
+        return {"case": case, "workload": wl.name, "ms": round(ms, 4), "TFLOPs": round(rate / 1e12, 1),
+                "frac_of_sustained_bf16": round(rate / 1e12 / pk["bf16_sustained"], 4)}
+    return {"case": case, "workload": wl.name, "ms": round(ms, 4), "GBps": round(rate / 1e9, 1),
+            "frac_of_hbm": round(rate / 1e9 / pk["hbm_gbs"], 4)}
+
+
 # ------------------------------------------------------------------ the oracle on the host cores
 
 class OracleSample:
@@ -443,6 +534,9 @@ def main():
     __graft_entry__.build()
     from llama_decoder_block_gb300 import api
     pk = peaks()
+    if args.case:
+        print(json.dumps(bench_case(api, args.case, synth.WORKLOADS[args.workload], args.steps, args.warmup, dev, pk)))
+        return
 
     with Clocks(dev.index) as clk:
         main_res = bench_prefill(api, wl, args.steps, args.warmup, dev, pk, from_synth=True)
