@@ -329,6 +329,9 @@ def bench_case(api, case, wl, steps, warmup, dev, pk):
     """One step alone at the workload's shapes: mean launch time over `steps` launches."""
     import numpy as np
     import torch
+    from llama_decoder_block_gb300 import synth
+    if case.startswith("decode") and wl.kind != "decode":
+        wl = synth.WORKLOADS["decode_gqa8b_bf16_b64_t4096"]
     L = wl.layer
     d, H, G, D, I = L.d_model, L.n_heads, L.n_kv_heads, L.head_dim, L.d_inter
     dims = api.Dims(d, H, G, D, I, L.rms_eps, torch.bfloat16)
@@ -364,8 +367,7 @@ def bench_case(api, case, wl, steps, warmup, dev, pk):
         fn = lambda: api.qkv_rope(dims, x, wq, wk, wv, cos, sin, kc, vc, q)
         work, unit = 2.0 * M * d * (H + 2 * G) * D, "flop"
     elif case in ("decode_attention", "decode_layer"):
-        from llama_decoder_block_gb300 import synth
-        dw = synth.WORKLOADS["decode_gqa8b_bf16_b64_t4096"] if wl.kind != "decode" else wl
+        dw = wl
         B, T = dw.B, dw.T_max
         pos_h = synth.decode_positions(dw)
         pos = torch.from_numpy(pos_h).to(dev)

@@ -5,15 +5,19 @@
 // repeated along dim 1; "深度学习进阶（三十）…" §1.1; "第 10 章：现代 LLaMA 架构" §6: K/V stay
 // G heads in the cache and are shared logically, never copied H/G times).
 //
-// One CTA per (128-query tile, head, sequence), tiles with the most keys first.
-//   warp 0     TMA: the Q tile once, then K_j, V_j tiles (128 keys) into a 2-stage ring,
-//              read straight from the [B, G, max_T, D] cache
-//   warp 1     TMEM allocator and MMA issuer: S_j = Q K_j^T (into one of two TMEM S
-//              buffers, so S_{j+1} is computed while the softmax of S_j runs), then
-//              O += P_j V_j with V as an MN-major operand
-//   warps 2-5  online softmax (one query row per thread, exp2 with the scale folded in),
-//              P_j as bf16 into 128-byte-swizzled shared memory, rescale of O in TMEM
-//              when the running max moves, and the final O / l epilogue
+// One CTA per (pair of 128-query blocks 2i and 2i+1, head, sequence), pairs with the most
+// keys first.  Both query tiles read every K/V tile once from shared memory.
+//   warp 0      TMA: both Q tiles once, then K_j, V_j (128 keys each) into a 2-stage ring
+//               straight from the [B, G, max_T, D] cache
+//   warp 1      TMEM allocator and MMA issuer, ping-pong between the two tiles:
+//               S_t = Q_t K_j^T into TMEM; once the softmax of tile t has written P_t,
+//               O_t += P_t V_j with P_t read from TMEM and V as an MN-major smem operand,
+//               then at once S_t for the next K tile, so one tile's softmax overlaps the
+//               other tile's MMAs
+//   warps 4-7   softmax of tile A, warps 8-11 softmax of tile B: one query row per thread;
+//               the row max, exp2 with the scale folded in, P as bf16 written over S in
+//               TMEM; O is rescaled only when the running max grows by more than 2^8
+//               (the final O / l uses the same reference max, so the result is exact)
 // fp32 statistics and accumulators; D = 128.
 #include <mutex>
 
@@ -28,11 +32,12 @@ constexpr int BKV = 128;
 constexpr int HD = 128;
 constexpr int CHUNK = 128 * 128;      // one 64-column half of a 128-row bf16 tile
 constexpr int TILE = 2 * CHUNK;       // 128 rows x 128 columns bf16
-constexpr int NUM_THREADS = 192;
-constexpr uint32_t TMEM_COLS = 512;   // S0 [0,128), S1 [128,256), O [256,384)
+constexpr int NUM_THREADS = 384;
+constexpr uint32_t TMEM_COLS = 512;   // S/P of tile t at [128t, 128t+128), O of tile t at 256 + 128t
+constexpr float kRescaleLog2 = 8.0f;  // rescale O when the max grows by more than 2^8
 
 struct AttnParams {
-  int B, S, H, G, n_qt;
+  int B, S, H, G, n_qt, n_pairs;
   float scale_log2;                   // log2(e) / sqrt(D)
   __nv_bfloat16* out;                 // [B, S, H*D]
   int* status;
@@ -43,27 +48,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem;
-  uint8_t* sK = smem + TILE;            // 2 stages
-  uint8_t* sV = smem + 3 * TILE;        // 2 stages
-  uint8_t* sP = smem + 5 * TILE;
+  uint8_t* sQ = smem;                   // 2 tiles
+  uint8_t* sK = smem + 2 * TILE;        // 2 stages
+  uint8_t* sV = smem + 4 * TILE;        // 2 stages
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 6 * TILE);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;         // [2]
-  uint64_t* kv_empty = bars + 3;        // [2]
-  uint64_t* s_full = bars + 5;          // [2]
-  uint64_t* p_full = bars + 7;
-  uint64_t* o_done = bars + 8;
-  uint64_t* drain = bars + 9;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
+  uint64_t* kv_full = bars + 1;         // [2] per stage
+  uint64_t* kv_empty = bars + 3;        // [2] per stage
+  uint64_t* s_full = bars + 5;          // [2] per tile
+  uint64_t* p_full = bars + 7;          // [2] per tile
+  uint64_t* o_done = bars + 9;          // [2] per tile
+  uint64_t* drain = bars + 11;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qt = p.n_qt - 1 - static_cast<int>(blockIdx.x);
+  const int pair = p.n_pairs - 1 - static_cast<int>(blockIdx.x);
   const int h = blockIdx.y, b = blockIdx.z;
   const int g = h / (p.H / p.G);
-  const int q0 = qt * BQ;
-  const int nt = qt + 1;                // key tiles 0..qt
+  const int qb[2] = {2 * pair, 2 * pair + 1};
+  const bool hasB = qb[1] < p.n_qt;
+  const int nt = hasB ? qb[1] + 1 : qb[0] + 1;   // key tiles 0 .. last diagonal
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(q_full), 1);
@@ -71,9 +76,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(smem_u32(kv_full + i), 1);
       mbar_init(smem_u32(kv_empty + i), 1);
       mbar_init(smem_u32(s_full + i), 1);
+      mbar_init(smem_u32(p_full + i), 4);
+      mbar_init(smem_u32(o_done + i), 1);
     }
-    mbar_init(smem_u32(p_full), 4);
-    mbar_init(smem_u32(o_done), 1);
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -97,10 +102,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // ------------------------------------------------------------ TMA producer
       bool ok = true;
       int issued = 0;
-      const uint32_t qb = smem_u32(q_full);
-      mbar_expect_tx(qb, TILE);
-      tma_load_3d(smem_u32(sQ), &tmQ, qb, 0, q0, b * p.H + h);
-      tma_load_3d(smem_u32(sQ + CHUNK), &tmQ, qb, 64, q0, b * p.H + h);
+      const uint32_t qbar = smem_u32(q_full);
+      const int qplane = b * p.H + h;
+      mbar_expect_tx(qbar, hasB ? 2 * TILE : TILE);
+      for (int t = 0; t < (hasB ? 2 : 1); ++t) {
+        tma_load_3d(smem_u32(sQ + t * TILE), &tmQ, qbar, 0, qb[t] * BQ, qplane);
+        tma_load_3d(smem_u32(sQ + t * TILE + CHUNK), &tmQ, qbar, 64, qb[t] * BQ, qplane);
+      }
       for (int j = 0; j < nt; ++j) {
         const int st = j & 1;
         if (!mbar_wait(smem_u32(kv_empty + st), ((j >> 1) & 1) ^ 1u, p.status, abort_flag)) { ok = false; break; }
@@ -114,7 +122,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ++issued;
       }
       if (!ok) {
-        mbar_wait_slow(qb, 0, nullptr, nullptr, kWaitBudgetNs);
+        mbar_wait_slow(qbar, 0, nullptr, nullptr, kWaitBudgetNs);
         for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j)
           mbar_wait_slow(smem_u32(kv_full + (j & 1)), (j >> 1) & 1, nullptr, nullptr, kWaitBudgetNs);
       }
@@ -124,148 +132,157 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // ------------------------------------------------------------ MMA issuer
       constexpr uint32_t IDESC_QK = idesc_bf16(128, 128, false);
       constexpr uint32_t IDESC_PV = idesc_bf16(128, 128, true);
-      const uint32_t aq = smem_u32(sQ), ap = smem_u32(sP);
-      bool ok = mbar_wait(smem_u32(q_full), 0, p.status, abort_flag) &&
-                mbar_wait(smem_u32(kv_full), 0, p.status, abort_flag);
-      bool issued = false;
-      auto issue_qk = [&](int sbuf, int st) {
-        const uint32_t bk = smem_u32(sK + st * TILE);
+      auto active = [&](int t, int j) { return (t == 0 || hasB) && j <= qb[t]; };
+      auto issue_s = [&](int t, int j) {
+        const uint32_t aq = smem_u32(sQ + t * TILE), bk = smem_u32(sK + (j & 1) * TILE);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * CHUNK + (kk & 3) * 32;
-          tc_mma_bf16(tmem_base + sbuf * 128, sdesc_sw128(aq + off, 16, 1024), sdesc_sw128(bk + off, 16, 1024),
+          tc_mma_bf16(tmem_base + t * 128, sdesc_sw128(aq + off, 16, 1024), sdesc_sw128(bk + off, 16, 1024),
                       IDESC_QK, kk > 0 ? 1u : 0u);
         }
+        tc_commit(smem_u32(s_full + t));
       };
-      if (ok) {
-        tc_fence_after();
-        issue_qk(0, 0);
-        issued = true;
-        tc_commit(smem_u32(s_full));
-      }
-      for (int j = 0; j < nt && ok; ++j) {
-        if (j + 1 < nt) {
-          const int st1 = (j + 1) & 1;
-          if (!mbar_wait(smem_u32(kv_full + st1), ((j + 1) >> 1) & 1, p.status, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-          issue_qk(st1, st1);
-          tc_commit(smem_u32(s_full + st1));
-        }
-        if (!mbar_wait(smem_u32(p_full), j & 1, p.status, abort_flag)) { ok = false; break; }
-        tc_fence_after();
+      auto issue_pv = [&](int t, int j) {
         const uint32_t bv = smem_u32(sV + (j & 1) * TILE);
 #pragma unroll
         for (int kk = 0; kk < BKV / 16; ++kk) {
-          const uint64_t ad = sdesc_sw128(ap + (kk >> 2) * CHUNK + (kk & 3) * 32, 16, 1024);
-          // V tile: 128 key rows of 128 bytes per 64-wide d half; K step = 16 rows = 2048 bytes,
+          // V: 128 key rows of 128 bytes per 64-wide d half; K step = 16 rows = 2048 bytes,
           // the second d half is CHUNK bytes further (leading byte offset), 8-row groups 1024 apart
-          const uint64_t bd = sdesc_sw128(bv + kk * 2048, CHUNK, 1024);
-          tc_mma_bf16(tmem_base + 256, ad, bd, IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_bf16_ts(tmem_base + 256 + t * 128, tmem_base + t * 128 + kk * 8,
+                         sdesc_sw128(bv + kk * 2048, CHUNK, 1024), IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
         }
-        tc_commit(smem_u32(o_done));
-        tc_commit(smem_u32(kv_empty + (j & 1)));
+        tc_commit(smem_u32(o_done + t));
+      };
+      bool ok = mbar_wait(smem_u32(q_full), 0, p.status, abort_flag) &&
+                mbar_wait(smem_u32(kv_full), 0, p.status, abort_flag);
+      bool issued = false;
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        if (hasB) issue_s(1, 0);
+        issued = true;
+      }
+      for (int j = 0; j < nt && ok; ++j) {
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (!active(t, j)) continue;
+          if (!mbar_wait(smem_u32(p_full + t), j & 1, p.status, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv(t, j);
+          if (active(t, j + 1)) {
+            if (!mbar_wait(smem_u32(kv_full + ((j + 1) & 1)), ((j + 1) >> 1) & 1, p.status, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(t, j + 1);
+          }
+        }
+        if (ok) tc_commit(smem_u32(kv_empty + (j & 1)));
       }
       if (!ok && issued) {
         tc_commit(smem_u32(drain));
         mbar_wait_slow(smem_u32(drain), 0, nullptr, nullptr, kWaitBudgetNs);
       }
     }
-  } else {
-    // -------------------------------------------------------------- softmax warps 2..5
-    const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;
-    const int qi = q0 + row;
-    const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
-    const float sl = p.scale_log2;
-    float m_run = -INFINITY, l_run = 0.f;
-    uint32_t r[32];
-    bool ok = true;
-    uint8_t* prow = sP + row * 128;
-    const uint32_t swz = static_cast<uint32_t>(row & 7);
-    for (int j = 0; j < nt; ++j) {
-      const int sb = j & 1;
-      if (!mbar_wait(smem_u32(s_full + sb), (j >> 1) & 1, p.status, abort_flag)) { ok = false; break; }
-      tc_fence_after();
-      const uint32_t tS = tmem_base + t_lane + sb * 128;
-      const bool diag = (j == qt);
-      const int kbase = j * BKV;
-      float mx = -INFINITY;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        tmem_ld32(tS + c * 32, r);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          float s = __uint_as_float(r[i]);
-          const int key = kbase + c * 32 + i;
-          if (diag && (key > qi || key >= p.S)) s = -INFINITY;
-          mx = fmaxf(mx, s);
-        }
-      }
-      const float m_new = fmaxf(m_run, mx * sl);
-      const float alpha = exp2f(m_run - m_new);
-      if (j > 0) {
-        // P_{j-1} V_{j-1} must be complete before O is rescaled and P is overwritten
-        if (!mbar_wait(smem_u32(o_done), (j - 1) & 1, p.status, abort_flag)) { ok = false; break; }
+  } else if (warp >= 4) {
+    // -------------------------------------------------------------- softmax of tile t
+    const int t = (warp - 4) >> 2;
+    if (t == 0 || hasB) {
+      const int quarter = warp & 3;
+      const int row = quarter * 32 + lane;
+      const int qi = qb[t] * BQ + row;
+      const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
+      const uint32_t tS = tmem_base + t_lane + t * 128;        // S, and P written over it
+      const uint32_t tO = tmem_base + t_lane + 256 + t * 128;
+      const float sl = p.scale_log2;
+      float m_run = -INFINITY, l_run = 0.f;
+      uint32_t r[64];
+      bool ok = true;
+      const int n_t = qb[t] + 1;
+      for (int j = 0; j < n_t; ++j) {
+        if (!mbar_wait(smem_u32(s_full + t), j & 1, p.status, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+        const bool diag = (j == qb[t]);
+        const int kbase = j * BKV;
+        float mx = -INFINITY;
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            tmem_ld32(tmem_base + t_lane + 256 + c * 32, r);
+        for (int hlf = 0; hlf < 2; ++hlf) {
+          tmem_ld64(tS + hlf * 64, r);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-            tmem_st32(tmem_base + t_lane + 256 + c * 32, r);
+          for (int i = 0; i < 64; ++i) {
+            float s = __uint_as_float(r[i]);
+            const int key = kbase + hlf * 64 + i;
+            if (diag && (key > qi || key >= p.S)) s = -INFINITY;
+            mx = fmaxf(mx, s);
           }
         }
-      }
-      float rowsum = 0.f;
+        const float mxs = mx * sl;
+        const bool need = mxs > m_run + kRescaleLog2;    // also true on the first tile
+        if (__any_sync(0xffffffffu, need)) {
+          const float m_new = need ? mxs : m_run;
+          const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
+          if (j > 0) {
+            // P_{j-1} V_{j-1} must have landed before O is rescaled
+            if (!mbar_wait(smem_u32(o_done + t), (j - 1) & 1, p.status, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            uint32_t o32[32];
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        tmem_ld32(tS + c * 32, r);
-        float pv[32];
+            for (int c = 0; c < 4; ++c) {
+              tmem_ld32(tO + c * 32, o32);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int key = kbase + c * 32 + i;
-          const bool masked = diag && (key > qi || key >= p.S);
-          pv[i] = masked ? 0.f : exp2f(fmaf(__uint_as_float(r[i]), sl, -m_new));
-          rowsum += pv[i];
+              for (int i = 0; i < 32; ++i) o32[i] = __float_as_uint(__uint_as_float(o32[i]) * alpha);
+              tmem_st32(tO + c * 32, o32);
+            }
+          }
+          l_run *= alpha;
+          m_run = m_new;
         }
-        // keys c*32 .. c*32+31 live in 64-key chunk (c >> 1), 16-byte units (c & 1)*4 + u
-        uint8_t* base = prow + (c >> 1) * CHUNK;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint32_t unit = static_cast<uint32_t>((c & 1) * 4 + u) ^ swz;
-          uint4 w;
-          w.x = pack_bf16(pv[8 * u + 0], pv[8 * u + 1]);
-          w.y = pack_bf16(pv[8 * u + 2], pv[8 * u + 3]);
-          w.z = pack_bf16(pv[8 * u + 4], pv[8 * u + 5]);
-          w.w = pack_bf16(pv[8 * u + 6], pv[8 * u + 7]);
-          *reinterpret_cast<uint4*>(base + unit * 16) = w;
-        }
-      }
-      l_run = l_run * alpha + rowsum;
-      m_run = m_new;
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(p_full));
-    }
-    if (ok && mbar_wait(smem_u32(o_done), (nt - 1) & 1, p.status, abort_flag)) {
-      tc_fence_after();
-      const float inv_l = 1.0f / l_run;
-      __nv_bfloat16* dst = p.out + (static_cast<long long>(b) * p.S + qi) * (static_cast<long long>(p.H) * HD) + h * HD;
+        float rowsum = 0.f;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        tmem_ld32(tmem_base + t_lane + 256 + c * 32, r);
-        if (qi < p.S) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+        for (int hlf = 0; hlf < 2; ++hlf) {
+          tmem_ld64(tS + hlf * 64, r);
+          uint32_t pk[32];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            uint4 w;
-            w.x = pack_bf16(__uint_as_float(r[8 * u + 0]) * inv_l, __uint_as_float(r[8 * u + 1]) * inv_l);
-            w.y = pack_bf16(__uint_as_float(r[8 * u + 2]) * inv_l, __uint_as_float(r[8 * u + 3]) * inv_l);
-            w.z = pack_bf16(__uint_as_float(r[8 * u + 4]) * inv_l, __uint_as_float(r[8 * u + 5]) * inv_l);
-            w.w = pack_bf16(__uint_as_float(r[8 * u + 6]) * inv_l, __uint_as_float(r[8 * u + 7]) * inv_l);
-            d4[u] = w;
+          for (int i = 0; i < 32; ++i) {
+            const int key = kbase + hlf * 64 + 2 * i;
+            float p0 = ex2_approx(fmaf(__uint_as_float(r[2 * i]), sl, -m_run));
+            float p1 = ex2_approx(fmaf(__uint_as_float(r[2 * i + 1]), sl, -m_run));
+            if (diag) {
+              if (key > qi || key >= p.S) p0 = 0.f;
+              if (key + 1 > qi || key + 1 >= p.S) p1 = 0.f;
+            }
+            rowsum += p0 + p1;
+            pk[i] = pack_bf16(p0, p1);
+          }
+          // keys 64*hlf .. 64*hlf+63 as 32 packed columns over S columns already read
+          tmem_st32(tS + hlf * 32, pk);
+        }
+        l_run += rowsum;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(p_full + t));
+      }
+      if (ok && mbar_wait(smem_u32(o_done + t), (n_t - 1) & 1, p.status, abort_flag)) {
+        tc_fence_after();
+        const float inv_l = 1.0f / l_run;
+        __nv_bfloat16* dst =
+            p.out + (static_cast<long long>(b) * p.S + qi) * (static_cast<long long>(p.H) * HD) + h * HD;
+        uint32_t o32[32];
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          tmem_ld32(tO + c * 32, o32);
+          if (qi < p.S) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              uint4 w;
+              w.x = pack_bf16(__uint_as_float(o32[8 * u + 0]) * inv_l, __uint_as_float(o32[8 * u + 1]) * inv_l);
+              w.y = pack_bf16(__uint_as_float(o32[8 * u + 2]) * inv_l, __uint_as_float(o32[8 * u + 3]) * inv_l);
+              w.z = pack_bf16(__uint_as_float(o32[8 * u + 4]) * inv_l, __uint_as_float(o32[8 * u + 5]) * inv_l);
+              w.w = pack_bf16(__uint_as_float(o32[8 * u + 6]) * inv_l, __uint_as_float(o32[8 * u + 7]) * inv_l);
+              d4[u] = w;
+            }
           }
         }
       }
@@ -281,7 +298,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
-constexpr size_t kSmemBytes = 1024 + 6 * TILE + 11 * 8 + 16;
+constexpr size_t kSmemBytes = 1024 + 6 * TILE + 13 * 8 + 16;
 
 }  // namespace
 
@@ -307,10 +324,11 @@ int attn_prefill_tc(const Ctx& c, const void* q, const void* k_cache, const void
   p.H = H;
   p.G = G;
   p.n_qt = (S + BQ - 1) / BQ;
+  p.n_pairs = (p.n_qt + 1) / 2;
   p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
   p.out = static_cast<__nv_bfloat16*>(out);
   p.status = c.status;
-  attn_prefill_kernel<<<dim3(p.n_qt, H, B), NUM_THREADS, kSmemBytes, c.stream>>>(tq, tk, tv, p);
+  attn_prefill_kernel<<<dim3(p.n_pairs, H, B), NUM_THREADS, kSmemBytes, c.stream>>>(tq, tk, tv, p);
   return after_launch(c);
 }
 
