@@ -44,7 +44,8 @@ typedef enum {
   LLAMA_ERR_UNSUPPORTED = -2,   /* a shape the tiled bf16 path does not cover (e.g. D != 128, d % 128 != 0) */
   LLAMA_ERR_CUDA = -3,          /* a CUDA runtime error (launch failure, no device, ...) */
   LLAMA_ERR_TIMEOUT = -4,       /* a bounded device-side wait expired; the kernel gave up and returned */
-  LLAMA_ERR_DEVICE_BOUNDS = -5  /* a device-side index check failed (position >= max_T or max_pos, token >= vocab) */
+  LLAMA_ERR_DEVICE_BOUNDS = -5, /* a device-side index check failed (position >= max_T or max_pos, token >= vocab) */
+  LLAMA_ERR_SCRATCH_LIMIT = -6  /* the request needs more than llama_attention_decode_static's fixed scratch */
 } llama_status;
 
 typedef enum { LLAMA_F32 = 0, LLAMA_BF16 = 1 } llama_dtype;
@@ -177,6 +178,21 @@ int llama_attention_decode_workspace_bytes(const llama_layer_dims *dims, int32_t
 int llama_attention_decode(const llama_layer_dims *dims, const void *q, llama_kv_cache cache,
                            const int32_t *positions, void *out, int32_t B, void *workspace, size_t ws_bytes,
                            void *cuda_stream);
+
+/* Decode attention without a workspace argument, for callers that cannot allocate device
+ * memory: code whose device memory is owned entirely by another allocator (a framework's
+ * caching pool, a fixed memory budget) and latency-critical loops where cudaMalloc or cudaFree
+ * would synchronise the device.  The pages have no counterpart to this entry point; it computes
+ * what llama_attention_decode computes, with the same arguments minus the workspace.
+ * Its scratch is a fixed 16 MiB device array inside the library (every device that loads the
+ * library holds one until the process exits), enough for B * H * ceil(max_T / 512) * (D + 2)
+ * floats; a larger request returns LLAMA_ERR_SCRATCH_LIMIT.  All calls on a device share that
+ * array: calls that may overlap on the GPU (unordered streams) race on it.  Nothing in it needs
+ * to start at zero.  The first call on each device looks up the array's device address (a host
+ * query, no allocation); make that first call before any stream capture.  Never allocates or
+ * frees device memory.  bf16 layers with D = 128 only. */
+int llama_attention_decode_static(const llama_layer_dims *dims, const void *q, llama_kv_cache cache,
+                                  const int32_t *positions, void *out, int32_t B, void *cuda_stream);
 
 /* ---------------------------------------------------------------- host helpers and status */
 

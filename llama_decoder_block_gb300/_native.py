@@ -15,7 +15,7 @@ c_double, c_uint64 = ctypes.c_double, ctypes.c_uint64
 
 LLAMA_F32, LLAMA_BF16 = 0, 1
 STATUS = {0: "LLAMA_OK", -1: "LLAMA_ERR_INVALID_ARG", -2: "LLAMA_ERR_UNSUPPORTED", -3: "LLAMA_ERR_CUDA",
-          -4: "LLAMA_ERR_TIMEOUT", -5: "LLAMA_ERR_DEVICE_BOUNDS"}
+          -4: "LLAMA_ERR_TIMEOUT", -5: "LLAMA_ERR_DEVICE_BOUNDS", -6: "LLAMA_ERR_SCRATCH_LIMIT"}
 
 
 class LayerDims(ctypes.Structure):
@@ -63,6 +63,8 @@ SIGNATURES = {
     "llama_attention_decode_workspace_bytes": (c_int32, [P(LayerDims), c_int32, c_int32, P(c_size_t)]),
     "llama_attention_decode": (c_int32, [P(LayerDims), c_void_p, KVCache, c_void_p, c_void_p, c_int32, c_void_p,
                                          c_size_t, c_void_p]),
+    "llama_attention_decode_static": (c_int32, [P(LayerDims), c_void_p, KVCache, c_void_p, c_void_p, c_int32,
+                                                c_void_p]),
     "llama_rope_tables": (c_int32, [c_double, c_int32, c_int32, c_void_p, c_void_p]),
     "llama_get_device_status": (c_int32, [c_void_p]),
     "llama_status_string": (ctypes.c_char_p, [c_int32]),

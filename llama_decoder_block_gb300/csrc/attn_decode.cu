@@ -240,3 +240,60 @@ int attn_decode(const Ctx& c, int dtype, const void* q, const void* k_cache, con
 }
 
 }  // namespace llama
+
+// ---------------------------------------------------------------------------------------
+// Decode attention with its scratch in a fixed device array, for callers that cannot
+// allocate device memory: code whose device memory is owned entirely by another allocator
+// (a framework's caching pool, a fixed memory budget) and latency-critical loops in which
+// cudaMalloc / cudaFree would synchronise the device.  The caller passes inputs and outputs
+// only; the split partials live in g_decode_scratch below.
+
+#include <atomic>
+
+namespace llama {
+namespace {
+
+// Largest scratch the fixed-array entry point serves: the split partials of
+// B * H * ceil(max_T / 512) (query head, key split) pairs, (D + 2) floats each.  At B = 64,
+// H = 32, max_T = 4096, D = 128 that is 8.5 MB.
+constexpr size_t kDecodeScratchBytes = 16u << 20;
+
+// File-scope device array: every device that loads the library holds its own copy until the
+// process exits, and all calls on a device share it.  Each call writes every slot it later
+// reads (empty key splits write their neutral (m, l) entry), so nothing needs clearing, but
+// two calls that overlap on the GPU (different streams, no ordering) race on it.
+static __device__ __align__(256) unsigned char g_decode_scratch[kDecodeScratchBytes];
+
+// Device address of g_decode_scratch, looked up once per device (host code must not use
+// the symbol itself: on the host it only names a stand-in).
+std::atomic<void*> g_decode_scratch_addr[64];
+
+}  // namespace
+}  // namespace llama
+
+extern "C" int llama_attention_decode_static(const llama_layer_dims* dims, const void* q, llama_kv_cache cache,
+                                             const int32_t* positions, void* out, int32_t B, void* cuda_stream) {
+  using namespace llama;
+  if (dims == nullptr || q == nullptr || out == nullptr || positions == nullptr || cache.k == nullptr ||
+      cache.v == nullptr || B <= 0 || cache.max_T <= 0)
+    return LLAMA_ERR_INVALID_ARG;
+  if (dims->n_heads <= 0 || dims->n_kv_heads <= 0 || dims->n_heads % dims->n_kv_heads != 0)
+    return LLAMA_ERR_INVALID_ARG;
+  auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
+  if (misaligned(q) || misaligned(out) || misaligned(cache.k) || misaligned(cache.v)) return LLAMA_ERR_INVALID_ARG;
+  if (dims->dtype != LLAMA_BF16 || dims->head_dim != HD) return LLAMA_ERR_UNSUPPORTED;
+  if (attn_decode_ws_bytes(B, dims->n_heads, dims->head_dim, cache.max_T) > kDecodeScratchBytes)
+    return LLAMA_ERR_SCRATCH_LIMIT;
+  Ctx c;
+  int rc = make_ctx(cuda_stream, &c);
+  if (rc != LLAMA_OK) return rc;
+  void* scratch = g_decode_scratch_addr[c.device].load(std::memory_order_acquire);
+  if (scratch == nullptr) {
+    // first call on this device (which is current): look the array's device address up
+    if (cudaGetSymbolAddress(&scratch, g_decode_scratch) != cudaSuccess || scratch == nullptr)
+      return LLAMA_ERR_CUDA;
+    g_decode_scratch_addr[c.device].store(scratch, std::memory_order_release);
+  }
+  return attn_decode(c, dims->dtype, q, cache.k, cache.v, positions, out, B, dims->n_heads, dims->n_kv_heads,
+                     dims->head_dim, cache.max_T, cache.max_T, scratch);
+}

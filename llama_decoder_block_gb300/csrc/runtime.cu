@@ -148,6 +148,7 @@ const char* llama_status_string(int s) {
     case LLAMA_ERR_CUDA: return "CUDA error";
     case LLAMA_ERR_TIMEOUT: return "device-side wait timed out";
     case LLAMA_ERR_DEVICE_BOUNDS: return "device-side index out of range";
+    case LLAMA_ERR_SCRATCH_LIMIT: return "request exceeds the fixed scratch of llama_attention_decode_static";
     default: return "unknown status";
   }
 }
