@@ -142,8 +142,52 @@ def dev_weights_random(wl, dev, seed):
               "w_up": (I, d), "w_down": (d, I)}
     w = {k: (torch.randn(s, generator=g, device=dev) * 0.02).to(torch.bfloat16) for k, s in shapes.items()}
     for k in ("attn_norm", "ffn_norm"):
-        w[k] = (1 + 0.1 * torch.randn(d, generator=g, device=dev)).to(torch.bfloat16)
+        if L.gamma == "ones":
+            w[k] = torch.ones(d, dtype=torch.bfloat16, device=dev)
+        else:
+            w[k] = (1 + 0.1 * torch.randn(d, generator=g, device=dev)).to(torch.bfloat16)
     return w
+
+
+def bench_stack(api, wl, steps, warmup, dev, pk):
+    """The full stack: embedding, n_layers layers, final RMSNorm, fp32 LM head, one step = one forward."""
+    import numpy as np
+    import torch
+    L = wl.layer
+    B, S, V = wl.B, wl.S, wl.vocab
+    layers = [dev_weights_random(wl, dev, wl.seed * 1000 + l) for l in range(wl.n_layers)]
+    g = torch.Generator(device=dev).manual_seed(wl.seed)
+    embed = (torch.randn(V, L.d_model, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    lm_head = (torch.randn(V, L.d_model, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    final_norm = torch.ones(L.d_model, dtype=torch.bfloat16, device=dev)
+    tokens = torch.randint(0, V, (B, S), generator=g, device=dev, dtype=torch.int32)
+    dims = api.Dims(L.d_model, L.n_heads, L.n_kv_heads, L.head_dim, L.d_inter, L.rms_eps, torch.bfloat16)
+    st = api.StackArgs(dims, layers, final_norm, embed, lm_head)
+    logits = torch.empty(B, S, V, dtype=torch.float32, device=dev)
+    c, s = api.rope_tables(L.rope_base, L.head_dim, S)
+    cos, sin = torch.from_numpy(c).to(dev), torch.from_numpy(s).to(dev)
+    ws = api.workspace(st.workspace_bytes(B, S), dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    ts = []
+    for i in range(warmup + steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        api.stack_forward(st, tokens, logits, cos, sin, ws)
+        e1.record()
+        e1.synchronize()
+        if i >= warmup:
+            ts.append(e0.elapsed_time(e1))
+    assert api.device_status() == 0
+    ms = float(np.mean(ts))
+    flops = wl.n_layers * sum(prefill_flops(L, B, S).values()) + 2.0 * B * S * L.d_model * V
+    res = {"workload": wl.name, "ms_per_forward": round(ms, 2), "tokens_per_s": round(B * S / (ms * 1e-3), 1),
+           "tflops": round(flops / (ms * 1e-3) / 1e12, 1),
+           "frac_of_sustained_peak": round(flops / (ms * 1e-3) / 1e12 / pk["bf16_sustained"], 4),
+           "weights_GB": round(sum(t.numel() for w in layers for t in w.values()) * 2 / 1e9, 2)}
+    del layers, st, logits, ws, flush
+    torch.cuda.empty_cache()
+    return res
 
 
 def prefill_flops(L, B, S):
@@ -568,6 +612,7 @@ def main():
                                  "kernel_ms": {k: round(v, 3) for k, v in r8["kernel_ms"].items()},
                                  "kernel_tflops": r8["kernel_tflops"]}
         line["rmsnorm"] = bench_rmsnorm(api, dev, pk)
+        line["stack32_forward"] = bench_stack(api, synth.WORKLOADS["stack32_gqa8b_bf16_s8192_v32000"], 3, 2, dev, pk)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tps, n, per = oracle_prefill_sample(wl)
         line["cpu_baseline"] = {"value": round(tps, 2), "unit": "tokens/s", "cores": cores(), "kind": "oracle",

@@ -86,7 +86,7 @@ size_t decode_part_floats(const llama_layer_dims* d, int B, int num_sms) {
   const int Ks[4] = {d->d_model, d->n_heads * d->head_dim, d->d_model, d->d_inter};
   size_t mx = 0;
   for (int i = 0; i < 4; ++i) {
-    const size_t s = static_cast<size_t>(choose_splits(num_sms, Ns[i], Ks[i]));
+    const size_t s = static_cast<size_t>(choose_splits(num_sms, Ns[i], Ks[i], B));
     mx = std::max(mx, s * B * Ns[i]);
   }
   return mx;
@@ -234,7 +234,7 @@ int llama_layer_decode(const llama_layer_dims* dims, const llama_layer_weights* 
     {
       const void* W3[3] = {w->wq, w->wk, w->wv};
       const int R3[3] = {H * D, G * D, G * D};
-      const int s = choose_splits(c.num_sms, qkv, dm);
+      const int s = choose_splits(c.num_sms, qkv, dm, B);
       if ((rc = gemm_tokens_partial(c, W3, R3, 3, p.xn, B, dm, s, P))) return rc;
       if ((rc = fix_qkv_rope(c, P, s, B, H, G, D, positions, max_pos, cos, sin, p.q, cache.k, cache.v, T))) return rc;
     }
@@ -243,7 +243,7 @@ int llama_layer_decode(const llama_layer_dims* dims, const llama_layer_weights* 
     {
       const void* W1[1] = {w->wo};
       const int R1[1] = {dm};
-      const int s = choose_splits(c.num_sms, dm, H * D);
+      const int s = choose_splits(c.num_sms, dm, H * D, B);
       if ((rc = gemm_tokens_partial(c, W1, R1, 1, p.o, B, H * D, s, P))) return rc;
       if ((rc = fix_residual(c, P, s, B, dm, x, p.h))) return rc;
     }
@@ -251,14 +251,14 @@ int llama_layer_decode(const llama_layer_dims* dims, const llama_layer_weights* 
     {
       const void* W2[2] = {w->w_gate, w->w_up};
       const int R2[2] = {I, I};
-      const int s = choose_splits(c.num_sms, 2 * I, dm);
+      const int s = choose_splits(c.num_sms, 2 * I, dm, B);
       if ((rc = gemm_tokens_partial(c, W2, R2, 2, p.xn, B, dm, s, P))) return rc;
       if ((rc = fix_swiglu(c, P, s, B, I, p.a))) return rc;
     }
     {
       const void* W1[1] = {w->w_down};
       const int R1[1] = {dm};
-      const int s = choose_splits(c.num_sms, dm, I);
+      const int s = choose_splits(c.num_sms, dm, I, B);
       if ((rc = gemm_tokens_partial(c, W1, R1, 1, p.a, B, I, s, P))) return rc;
       return fix_residual(c, P, s, B, dm, p.h, out);
     }

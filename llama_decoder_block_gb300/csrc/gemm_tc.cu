@@ -411,7 +411,13 @@ Params base_params(int M, int N, int K, int BN) {
   p.num_kb = (K + BK - 1) / BK;
   p.num_splits = 1;
   p.kb_per_split = p.num_kb;
-  p.group_m = 8;
+  // tile order: a group of group_m row blocks walks all column blocks, so that group's rows
+  // of A stay in L2 while the weights stream; take every row block when all of A fits in
+  // 48 MB (the weights then stream from DRAM once), else about 32 MB of A per group
+  const size_t a_block_bytes = static_cast<size_t>(BM) * K * 2;
+  const size_t a_bytes = a_block_bytes * p.num_mb;
+  p.group_m = a_bytes <= (48u << 20) ? std::max(1, p.num_mb)
+                                     : std::max(8, static_cast<int>((32u << 20) / std::max<size_t>(a_block_bytes, 1)));
   p.amap.nseg = 1;
   p.amap.seg_end[0] = 1 << 30;
   p.bmap.nseg = 1;
@@ -491,14 +497,27 @@ int gemm_qkv_rope(const Ctx& c, const void* X, const void* Wq, const void* Wk, c
   return launch<256, EPI_QKV, 4>(c, tm, p);
 }
 
-int choose_splits(int num_sms, int w_rows_total, int K) {
-  const int tiles = (w_rows_total + BM - 1) / BM;
+int choose_splits(int num_sms, int w_rows_total, int K, int n_tok) {
+  // Cost of streaming the weights once with s splits, relative to a perfectly balanced
+  // stream: the slowest SM handles ceil(tiles / SMs) tiles of ceil(kb / s) k-blocks; the fp32
+  // partials add 2 * s * n_tok * rows * 4 bytes (written, then read by the fixup kernel)
+  // against rows * K * 2 bytes of weights.
+  const int mb = (w_rows_total + BM - 1) / BM;
   const int kb = (K + BK - 1) / BK;
-  int s = std::max(1, (num_sms + tiles - 1) / tiles);
-  s = std::min(s, std::max(1, kb / 4));   // keep at least 4 k-blocks per split
-  // the count actually used: every split gets ceil(kb / s) blocks and none is empty
-  const int per = (kb + s - 1) / s;
-  return (kb + per - 1) / per;
+  int best = 1;
+  double best_cost = 1e30;
+  for (int s = 1; s <= std::max(1, kb / 4); ++s) {
+    const int per = (kb + s - 1) / s;
+    const int se = (kb + per - 1) / per;   // the count actually used: no empty split
+    const int rounds = (mb * se + num_sms - 1) / num_sms;
+    const double cost = static_cast<double>(rounds) * per * num_sms / (static_cast<double>(mb) * kb) +
+                        4.0 * se * n_tok / static_cast<double>(K);
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = se;
+    }
+  }
+  return best;
 }
 
 int gemm_tokens_partial(const Ctx& c, const void* const* W, const int* w_rows, int n_w, const void* X, int n_tok,

@@ -53,7 +53,7 @@ int gemm_qkv_rope(const Ctx& c, const void* X, const void* Wq, const void* Wk, c
 int gemm_tokens_partial(const Ctx& c, const void* const* W, const int* w_rows, int n_w, const void* X,
                         int n_tok, int K, int splits, float* P);
 // Split count for the weight-streaming form (exactly the count that gemm_tokens_partial uses).
-int choose_splits(int num_sms, int w_rows_total, int K);
+int choose_splits(int num_sms, int w_rows_total, int K, int n_tok);
 
 // ---------------------------------------------------------------- attention
 int attn_prefill_tc(const Ctx& c, const void* q, const void* k_cache, const void* v_cache, void* out, int B,

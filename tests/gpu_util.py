@@ -1,4 +1,6 @@
 """Helpers of the GPU parity tests: moving synth tensors to the device and the tolerance check."""
+import contextlib
+
 import numpy as np
 import torch
 
@@ -56,6 +58,54 @@ def assert_close_layer_full(gpu: np.ndarray, ref: np.ndarray, what: str):
            f"p99 {np.quantile(err, 0.99):.2e}")
     assert err.max() <= g["envelope"] and frac <= g["max_frac_over_tol"] and norm <= g["normwise"], msg
     return msg
+
+
+def attention_bf16_probabilities(q, k, v, q_pos, k_len):
+    """The oracle's attention with the probabilities rounded to bf16 before the product with
+    V and the normaliser summed from the unrounded ones (flash-attention numerics)."""
+    import oracle
+    B, H, S, D = q.shape
+    rep = H // k.shape[1]
+    out = np.empty_like(q)
+    for b in range(B):
+        T = int(k_len[b])
+        allowed = np.arange(T)[None, :] <= np.asarray(q_pos[b])[:, None]
+        for h in range(H):
+            g = h // rep
+            scores = np.where(allowed, (q[b, h] @ k[b, g, :T].T) / np.sqrt(D), -np.inf)
+            p = np.exp(scores - scores.max(axis=-1, keepdims=True))
+            out[b, h] = (oracle.round_bf16(p) @ v[b, g, :T]) / p.sum(axis=-1, keepdims=True)
+    return out
+
+
+@contextlib.contextmanager
+def tensor_core_numerics(seed=0):
+    """Within the block the oracle computes the way a tensor-core implementation does:
+    fp32-sized relative noise (2e-7) before each bf16 storage rounding, and bf16 softmax
+    probabilities.  Comparing it with the exact oracle measures how far a correct bf16
+    implementation lands from the oracle for a given workload."""
+    from oracle import layer as oracle_layer
+    exact_round, exact_attention = oracle_layer.round_bf16, oracle_layer.attention
+    rng = np.random.default_rng(seed)
+    oracle_layer.round_bf16 = lambda v: exact_round(np.asarray(v, np.float64) *
+                                                    (1 + 2e-7 * rng.standard_normal(np.shape(v))))
+    oracle_layer.attention = attention_bf16_probabilities
+    try:
+        yield
+    finally:
+        oracle_layer.round_bf16, oracle_layer.attention = exact_round, exact_attention
+
+
+def deviation(a: np.ndarray, ref: np.ndarray) -> dict:
+    err = np.abs(a - ref) / (1.0 + np.abs(ref))
+    return {"max": float(err.max()), "p99": float(np.quantile(err, 0.99)),
+            "normwise": float(np.linalg.norm(a - ref) / np.linalg.norm(ref))}
+
+
+def gen_layer(args):
+    """Process-pool worker: one layer's weights of a workload (storage format)."""
+    wl, layer = args
+    return synth.layer_weights(wl, layer)
 
 
 def dims_of(layer: synth.LayerShape) -> api.Dims:

@@ -11,29 +11,11 @@ gate that the GPU tests apply (gpu_util.LAYER_FULL).
 import numpy as np
 
 import oracle
-from gpu_util import LAYER_FULL
+from gpu_util import LAYER_FULL, tensor_core_numerics
 from llama_decoder_block_gb300 import synth
-from oracle import layer as oracle_layer
 
 
-def _attention_bf16_probabilities(q, k, v, q_pos, k_len):
-    """The oracle's attention with the probabilities rounded to bf16 before the product with
-    V and the normaliser summed from the unrounded ones (flash-attention numerics)."""
-    B, H, S, D = q.shape
-    rep = H // k.shape[1]
-    out = np.empty_like(q)
-    for b in range(B):
-        T = int(k_len[b])
-        allowed = np.arange(T)[None, :] <= np.asarray(q_pos[b])[:, None]
-        for h in range(H):
-            g = h // rep
-            scores = np.where(allowed, (q[b, h] @ k[b, g, :T].T) / np.sqrt(D), -np.inf)
-            p = np.exp(scores - scores.max(axis=-1, keepdims=True))
-            out[b, h] = (oracle.round_bf16(p) @ v[b, g, :T]) / p.sum(axis=-1, keepdims=True)
-    return out
-
-
-def test_tensor_core_numerics_move_the_full_width_layer_inside_the_gate(monkeypatch):
+def test_tensor_core_numerics_move_the_full_width_layer_inside_the_gate():
     wl = synth.WORKLOADS["gqa8b_bf16_b4_s4096"]
     L = wl.layer
     S = 128                                      # one sequence, a causal prefix: stays on the CPU
@@ -44,12 +26,8 @@ def test_tensor_core_numerics_move_the_full_width_layer_inside_the_gate(monkeypa
     kw = dict(n_heads=L.n_heads, n_kv_heads=L.n_kv_heads, head_dim=L.head_dim, rms_eps=L.rms_eps, store_bf16=True)
     ref, _, _ = oracle.decoder_layer(x, w, c, s, **kw)
 
-    exact = oracle_layer.round_bf16
-    rng = np.random.default_rng(0)
-    monkeypatch.setattr(oracle_layer, "round_bf16",
-                        lambda v: exact(np.asarray(v, np.float64) * (1 + 2e-7 * rng.standard_normal(np.shape(v)))))
-    monkeypatch.setattr(oracle_layer, "attention", _attention_bf16_probabilities)
-    out, _, _ = oracle.decoder_layer(x, w, c, s, **kw)
+    with tensor_core_numerics():
+        out, _, _ = oracle.decoder_layer(x, w, c, s, **kw)
 
     err = np.abs(out - ref) / (1 + np.abs(ref))
     frac = np.mean(err > LAYER_FULL["tol"])
