@@ -29,7 +29,7 @@ MAIN = "mha7b_bf16_b1_s2048"
 PREFILL_KERNELS = ["rmsnorm_attn", "qkv_rope_gemm", "attention_prefill", "o_proj_residual_gemm", "rmsnorm_ffn",
                    "gate_up_swiglu_gemm", "down_residual_gemm"]
 DECODE_KERNELS = ["rmsnorm_attn", "qkv_gemm_stream", "qkv_rope_fixup", "attention_decode_split",
-                  "attention_decode_combine", "o_proj_gemm_stream", "o_proj_residual_fixup", "rmsnorm_ffn",
+                  "attention_decode_combine", "o_proj_gemm_stream", "o_proj_residual_rmsnorm_fixup",
                   "gate_up_gemm_stream", "swiglu_fixup", "down_gemm_stream", "down_residual_fixup"]
 L2_FLUSH_BYTES = 256 << 20
 

@@ -185,7 +185,7 @@ int llama_attention_decode(const llama_layer_dims *dims, const void *q, llama_kv
  * would synchronise the device.  The pages have no counterpart to this entry point; it computes
  * what llama_attention_decode computes, with the same arguments minus the workspace.
  * Its scratch is a fixed 16 MiB device array inside the library (every device that loads the
- * library holds one until the process exits), enough for B * H * ceil(max_T / 512) * (D + 2)
+ * library holds one until the process exits), enough for B * H * ceil(max_T / 1024) * (D + 2)
  * floats; a larger request returns LLAMA_ERR_SCRATCH_LIMIT.  All calls on a device share that
  * array: calls that may overlap on the GPU (unordered streams) race on it.  Nothing in it needs
  * to start at zero.  The first call on each device looks up the array's device address (a host

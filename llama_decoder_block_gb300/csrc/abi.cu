@@ -245,9 +245,9 @@ int llama_layer_decode(const llama_layer_dims* dims, const llama_layer_weights* 
       const int R1[1] = {dm};
       const int s = choose_splits(c.num_sms, dm, H * D, B);
       if ((rc = gemm_tokens_partial(c, W1, R1, 1, p.o, B, H * D, s, P))) return rc;
-      if ((rc = fix_residual(c, P, s, B, dm, x, p.h))) return rc;
+      // h = x + O Wo^T, then the MLP's RMSNorm of h, in one pass over each token's row
+      if ((rc = fix_residual_rmsnorm(c, P, s, B, dm, x, w->ffn_norm, dims->rms_eps, p.h, p.xn))) return rc;
     }
-    if ((rc = rmsnorm(c, p.h, w->ffn_norm, p.xn, B, dm, dims->rms_eps, dims->dtype))) return rc;
     {
       const void* W2[2] = {w->w_gate, w->w_up};
       const int R2[2] = {I, I};

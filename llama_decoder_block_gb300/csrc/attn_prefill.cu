@@ -46,6 +46,7 @@ struct AttnParams {
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+  pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;                   // 2 tiles
@@ -96,6 +97,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();   // inputs written by the previous kernel are read from here on
 
   if (warp == 0) {
     if (lane == 0) {
@@ -328,7 +330,7 @@ int attn_prefill_tc(const Ctx& c, const void* q, const void* k_cache, const void
   p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
   p.out = static_cast<__nv_bfloat16*>(out);
   p.status = c.status;
-  attn_prefill_kernel<<<dim3(p.n_pairs, H, B), NUM_THREADS, kSmemBytes, c.stream>>>(tq, tk, tv, p);
+  launch_pdl(c, attn_prefill_kernel, dim3(p.n_pairs, H, B), dim3(NUM_THREADS), kSmemBytes, tq, tk, tv, p);
   return after_launch(c);
 }
 

@@ -128,6 +128,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   constexpr uint32_t IDESC = idesc_bf16(BM, BN, false);
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
 
+  pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -168,6 +169,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();   // inputs written by the previous kernel are read from here on
 
   if (warp == 0) {
     if (lane == 0) {
@@ -397,7 +399,7 @@ int launch(const Ctx& c, const TMaps& tm, Params p) {
   const int tiles = p.num_mb * p.num_nb * p.num_splits;
   if (tiles == 0) return LLAMA_OK;
   const int grid = std::min(tiles, c.num_sms);
-  kern<<<grid, NUM_THREADS, smem, c.stream>>>(tm, p);
+  launch_pdl(c, kern, dim3(grid), dim3(NUM_THREADS), smem, tm, p);
   return after_launch(c);
 }
 

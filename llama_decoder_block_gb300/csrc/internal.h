@@ -20,6 +20,23 @@ struct Ctx {
 
 // Fills `c` for the current device; returns LLAMA_OK or LLAMA_ERR_CUDA.
 int make_ctx(void* stream, Ctx* c);
+
+// Launches `kern` on c.stream with programmatic stream serialisation (the kernel calls
+// pdl_trigger / pdl_wait, see common.cuh).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(const Ctx& c, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = c.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
 // Checks cudaGetLastError after a launch, counts it and records the next trace event.
 int after_launch(const Ctx& c);
 
@@ -84,6 +101,9 @@ int fix_qkv_rope(const Ctx& c, const float* P, int splits, int n_tok, int H, int
                  const int32_t* positions, int max_pos, const float* cos, const float* sin, void* q_out,
                  void* k_cache, void* v_cache, int T_max);
 int fix_residual(const Ctx& c, const float* P, int splits, int n_tok, int N, const void* resid, void* out);
+// h = resid + sum of the splits (bf16), then hn = RMSNorm(h) with gamma (bf16); one CTA per token.
+int fix_residual_rmsnorm(const Ctx& c, const float* P, int splits, int n_tok, int N, const void* resid,
+                         const void* gamma, float eps, void* h_out, void* hn_out);
 int fix_swiglu(const Ctx& c, const float* P, int splits, int n_tok, int I, void* out);
 
 }  // namespace llama

@@ -10,6 +10,8 @@ namespace {
 // x[t, :] = table[tokens[t], :] ("12 · 从 Transformer 到 LLaMA 系列" §八 nn.Embedding), one warp per token.
 __global__ void embed_kernel(const int32_t* __restrict__ tokens, const uint4* __restrict__ table,
                              uint4* __restrict__ x, int n_tok, int vec_per_row, int vocab, int* status) {
+  pdl_trigger();
+  pdl_wait();
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= n_tok) return;
@@ -24,63 +26,134 @@ __global__ void embed_kernel(const int32_t* __restrict__ tokens, const uint4* __
   for (int i = lane; i < vec_per_row; i += 32) dst[i] = __ldg(src + i);
 }
 
-__device__ __forceinline__ float split_sum(const float* P, int splits, long long stride, long long idx) {
-  float a = 0.f;
-  for (int s = 0; s < splits; ++s) a += P[s * stride + idx];
+// Sum over the splits of 4 consecutive fp32 partials (16-byte aligned).
+__device__ __forceinline__ float4 split_sum4(const float* P, int splits, long long stride, long long idx) {
+  float4 a = *reinterpret_cast<const float4*>(P + idx);
+  for (int s = 1; s < splits; ++s) {
+    const float4 b = *reinterpret_cast<const float4*>(P + s * stride + idx);
+    a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+  }
   return a;
 }
 
-// one thread per (token, column pair) of [q heads | k heads | v heads]
+__device__ __forceinline__ void store_bf16x4(__nv_bfloat16* dst, float a, float b, float c, float d) {
+  uint2 w;
+  w.x = pack_bf16(a, b);
+  w.y = pack_bf16(c, d);
+  *reinterpret_cast<uint2*>(dst) = w;
+}
+
+// grid (ceil(N / 1024), n_tok): 4 consecutive columns of [q heads | k heads | v heads] per thread
 __global__ void fix_qkv_kernel(const float* __restrict__ P, int splits, int n_tok, int H, int G, int D,
                                const int32_t* __restrict__ positions, int max_pos, const float* __restrict__ cos,
                                const float* __restrict__ sin, __nv_bfloat16* __restrict__ q_out,
                                __nv_bfloat16* __restrict__ k_cache, __nv_bfloat16* __restrict__ v_cache, int T_max,
                                int* status) {
+  pdl_trigger();
+  pdl_wait();
   const int N = (H + 2 * G) * D;
-  const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (idx >= static_cast<long long>(n_tok) * (N / 2)) return;
-  const int t = static_cast<int>(idx / (N / 2));
-  const int col = static_cast<int>(idx % (N / 2)) * 2;
+  const int t = blockIdx.y;
+  const int col = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (col >= N) return;
   const int pos = positions[t];
   if (pos < 0 || pos >= max_pos || pos >= T_max) {
     if (col == 0) report(status, LLAMA_ERR_DEVICE_BOUNDS);
     return;
   }
-  const long long stride = static_cast<long long>(n_tok) * N;
-  float e = split_sum(P, splits, stride, static_cast<long long>(t) * N + col);
-  float o = split_sum(P, splits, stride, static_cast<long long>(t) * N + col + 1);
-  const int hh = col / D, j = col % D;
-  if (hh < H + G) {   // RoPE at the token's own position
-    const float c = cos[static_cast<long long>(pos) * (D / 2) + j / 2];
-    const float sn = sin[static_cast<long long>(pos) * (D / 2) + j / 2];
-    const float re = e * c - o * sn, ro = e * sn + o * c;
-    e = re;
-    o = ro;
+  const float4 v = split_sum4(P, splits, static_cast<long long>(n_tok) * N, static_cast<long long>(t) * N + col);
+  float e0 = v.x, o0 = v.y, e1 = v.z, o1 = v.w;
+  const int hh = col / D, j = col - hh * D;
+  if (hh < H + G) {   // RoPE at the token's own position, pairs (j, j+1) and (j+2, j+3)
+    const float* cr = cos + static_cast<long long>(pos) * (D / 2) + j / 2;
+    const float* sr = sin + static_cast<long long>(pos) * (D / 2) + j / 2;
+    const float c0 = cr[0], s0 = sr[0], c1 = cr[1], s1 = sr[1];
+    const float r0 = e0 * c0 - o0 * s0, r1 = e0 * s0 + o0 * c0;
+    const float r2 = e1 * c1 - o1 * s1, r3 = e1 * s1 + o1 * c1;
+    e0 = r0; o0 = r1; e1 = r2; o1 = r3;
   }
   __nv_bfloat16* dst;
   if (hh < H) dst = q_out + (static_cast<long long>(t) * H + hh) * D;
   else if (hh < H + G) dst = k_cache + ((static_cast<long long>(t) * G + (hh - H)) * T_max + pos) * D;
   else dst = v_cache + ((static_cast<long long>(t) * G + (hh - H - G)) * T_max + pos) * D;
-  *reinterpret_cast<__nv_bfloat162*>(dst + j) = __floats2bfloat162_rn(e, o);
+  store_bf16x4(dst + j, e0, o0, e1, o1);
 }
 
+// grid (ceil(N / 1024), n_tok): out = resid + sum of the splits, 4 columns per thread
 __global__ void fix_residual_kernel(const float* __restrict__ P, int splits, int n_tok, int N,
                                     const __nv_bfloat16* __restrict__ resid, __nv_bfloat16* __restrict__ out) {
-  const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const long long total = static_cast<long long>(n_tok) * N;
-  if (idx >= total) return;
-  out[idx] = __float2bfloat16_rn(__bfloat162float(resid[idx]) + split_sum(P, splits, total, idx));
+  pdl_trigger();
+  pdl_wait();
+  const int t = blockIdx.y;
+  const int col = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (col >= N) return;
+  const long long idx = static_cast<long long>(t) * N + col;
+  const float4 v = split_sum4(P, splits, static_cast<long long>(n_tok) * N, idx);
+  const uint2 r = *reinterpret_cast<const uint2*>(resid + idx);
+  store_bf16x4(out + idx, bf16_lo(r.x) + v.x, bf16_hi(r.x) + v.y, bf16_lo(r.y) + v.z, bf16_hi(r.y) + v.w);
 }
 
+// One CTA per token: h = resid + sum of the splits (stored in bf16), then hn = RMSNorm(h) from
+// the stored h ("12 · 从 Transformer 到 LLaMA 系列" §八 RMSNorm; fp32 arithmetic).
+__global__ void __launch_bounds__(256) fix_residual_rmsnorm_kernel(const float* __restrict__ P, int splits,
+                                                                   int n_tok, int N,
+                                                                   const __nv_bfloat16* __restrict__ resid,
+                                                                   const __nv_bfloat16* __restrict__ gamma, float eps,
+                                                                   __nv_bfloat16* __restrict__ h_out,
+                                                                   __nv_bfloat16* __restrict__ hn_out) {
+  pdl_trigger();
+  pdl_wait();
+  constexpr int MAXV = 8;   // 4-column groups per thread: N <= 256 * 4 * 8 = 8192
+  __shared__ float red[8];
+  const int t = blockIdx.x;
+  const long long row = static_cast<long long>(t) * N;
+  float hv[MAXV][4];
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const int col = (i * blockDim.x + threadIdx.x) * 4;
+    if (col < N) {
+      const float4 v = split_sum4(P, splits, static_cast<long long>(n_tok) * N, row + col);
+      const uint2 r = *reinterpret_cast<const uint2*>(resid + row + col);
+      const uint32_t w0 = pack_bf16(bf16_lo(r.x) + v.x, bf16_hi(r.x) + v.y);
+      const uint32_t w1 = pack_bf16(bf16_lo(r.y) + v.z, bf16_hi(r.y) + v.w);
+      *reinterpret_cast<uint2*>(h_out + row + col) = make_uint2(w0, w1);
+      hv[i][0] = bf16_lo(w0); hv[i][1] = bf16_hi(w0); hv[i][2] = bf16_lo(w1); hv[i][3] = bf16_hi(w1);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) ss = fmaf(hv[i][e], hv[i][e], ss);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) tot += red[w];
+  const float r = rsqrtf(tot / static_cast<float>(N) + eps);
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const int col = (i * blockDim.x + threadIdx.x) * 4;
+    if (col < N) {
+      const uint2 g = *reinterpret_cast<const uint2*>(gamma + col);
+      store_bf16x4(hn_out + row + col, bf16_lo(g.x) * (hv[i][0] * r), bf16_hi(g.x) * (hv[i][1] * r),
+                   bf16_lo(g.y) * (hv[i][2] * r), bf16_hi(g.y) * (hv[i][3] * r));
+    }
+  }
+}
+
+// grid (ceil(I / 1024), n_tok): a = SiLU(gate) * up from the split sums, 4 columns per thread
 __global__ void fix_swiglu_kernel(const float* __restrict__ P, int splits, int n_tok, int I,
                                   __nv_bfloat16* __restrict__ out) {
-  const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (idx >= static_cast<long long>(n_tok) * I) return;
-  const int t = static_cast<int>(idx / I), n = static_cast<int>(idx % I);
+  pdl_trigger();
+  pdl_wait();
+  const int t = blockIdx.y;
+  const int n = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (n >= I) return;
   const long long stride = static_cast<long long>(n_tok) * 2 * I;
-  const float gsum = split_sum(P, splits, stride, static_cast<long long>(t) * 2 * I + n);
-  const float usum = split_sum(P, splits, stride, static_cast<long long>(t) * 2 * I + I + n);
-  out[idx] = __float2bfloat16_rn(silu_f(gsum) * usum);
+  const float4 gs = split_sum4(P, splits, stride, static_cast<long long>(t) * 2 * I + n);
+  const float4 us = split_sum4(P, splits, stride, static_cast<long long>(t) * 2 * I + I + n);
+  store_bf16x4(out + static_cast<long long>(t) * I + n, silu_f(gs.x) * us.x, silu_f(gs.y) * us.y,
+               silu_f(gs.z) * us.z, silu_f(gs.w) * us.w);
 }
 
 }  // namespace
@@ -89,35 +162,43 @@ int embed_gather(const Ctx& c, const int32_t* tokens, const void* table, void* x
                  int vocab) {
   if (n_tok == 0) return LLAMA_OK;
   const int vec = row_bytes / 16;
-  embed_kernel<<<(n_tok + 7) / 8, 256, 0, c.stream>>>(tokens, static_cast<const uint4*>(table),
-                                                      static_cast<uint4*>(x), n_tok, vec, vocab, c.status);
+  launch_pdl(c, embed_kernel, dim3((n_tok + 7) / 8), dim3(256), 0, tokens, static_cast<const uint4*>(table),
+             static_cast<uint4*>(x), n_tok, vec, vocab, c.status);
   return after_launch(c);
 }
 
 int fix_qkv_rope(const Ctx& c, const float* P, int splits, int n_tok, int H, int G, int D, const int32_t* positions,
                  int max_pos, const float* cos, const float* sin, void* q_out, void* k_cache, void* v_cache,
                  int T_max) {
-  const long long total = static_cast<long long>(n_tok) * ((H + 2 * G) * D / 2);
-  if (total == 0) return LLAMA_OK;
-  fix_qkv_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, c.stream>>>(
+  const int N = (H + 2 * G) * D;
+  if (n_tok == 0) return LLAMA_OK;
+  launch_pdl(c, fix_qkv_kernel, dim3((N / 4 + 255) / 256, n_tok), dim3(256), 0,
       P, splits, n_tok, H, G, D, positions, max_pos, cos, sin, static_cast<__nv_bfloat16*>(q_out),
       static_cast<__nv_bfloat16*>(k_cache), static_cast<__nv_bfloat16*>(v_cache), T_max, c.status);
   return after_launch(c);
 }
 
 int fix_residual(const Ctx& c, const float* P, int splits, int n_tok, int N, const void* resid, void* out) {
-  const long long total = static_cast<long long>(n_tok) * N;
-  if (total == 0) return LLAMA_OK;
-  fix_residual_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, c.stream>>>(
+  if (n_tok == 0) return LLAMA_OK;
+  launch_pdl(c, fix_residual_kernel, dim3((N / 4 + 255) / 256, n_tok), dim3(256), 0,
       P, splits, n_tok, N, static_cast<const __nv_bfloat16*>(resid), static_cast<__nv_bfloat16*>(out));
   return after_launch(c);
 }
 
+int fix_residual_rmsnorm(const Ctx& c, const float* P, int splits, int n_tok, int N, const void* resid,
+                         const void* gamma, float eps, void* h_out, void* hn_out) {
+  if (n_tok == 0) return LLAMA_OK;
+  if (N % 4 != 0 || N > 256 * 4 * 8) return LLAMA_ERR_UNSUPPORTED;
+  launch_pdl(c, fix_residual_rmsnorm_kernel, dim3(n_tok), dim3(256), 0,
+      P, splits, n_tok, N, static_cast<const __nv_bfloat16*>(resid), static_cast<const __nv_bfloat16*>(gamma), eps,
+      static_cast<__nv_bfloat16*>(h_out), static_cast<__nv_bfloat16*>(hn_out));
+  return after_launch(c);
+}
+
 int fix_swiglu(const Ctx& c, const float* P, int splits, int n_tok, int I, void* out) {
-  const long long total = static_cast<long long>(n_tok) * I;
-  if (total == 0) return LLAMA_OK;
-  fix_swiglu_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, c.stream>>>(
-      P, splits, n_tok, I, static_cast<__nv_bfloat16*>(out));
+  if (n_tok == 0) return LLAMA_OK;
+  launch_pdl(c, fix_swiglu_kernel, dim3((I / 4 + 255) / 256, n_tok), dim3(256), 0, P, splits, n_tok, I,
+             static_cast<__nv_bfloat16*>(out));
   return after_launch(c);
 }
 

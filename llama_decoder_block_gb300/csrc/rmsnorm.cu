@@ -24,6 +24,8 @@ template <int VPL>
 __global__ void __launch_bounds__(kWarpsPerCta * 32)
     rmsnorm_bf16_kernel(const uint4* __restrict__ x, const uint4* __restrict__ gamma, uint4* __restrict__ y, int rows,
                         float inv_d, float eps) {
+  pdl_trigger();
+  pdl_wait();
   const int row = blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
@@ -63,6 +65,8 @@ template <typename T>
 __global__ void __launch_bounds__(kWarpsPerCta * 32)
     rmsnorm_generic_kernel(const T* __restrict__ x, const T* __restrict__ gamma, T* __restrict__ y, int rows, int d,
                            float eps) {
+  pdl_trigger();
+  pdl_wait();
   const int row = blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
@@ -90,23 +94,21 @@ int rmsnorm(const Ctx& c, const void* x, const void* gamma, void* y, int rows, i
     uint4* yv = static_cast<uint4*>(y);
     const float inv_d = 1.0f / static_cast<float>(d);
     switch (d / 256) {
-      case 1: rmsnorm_bf16_kernel<1><<<grid, block, 0, c.stream>>>(xv, gv, yv, rows, inv_d, eps); break;
-      case 2: rmsnorm_bf16_kernel<2><<<grid, block, 0, c.stream>>>(xv, gv, yv, rows, inv_d, eps); break;
-      case 4: rmsnorm_bf16_kernel<4><<<grid, block, 0, c.stream>>>(xv, gv, yv, rows, inv_d, eps); break;
-      case 8: rmsnorm_bf16_kernel<8><<<grid, block, 0, c.stream>>>(xv, gv, yv, rows, inv_d, eps); break;
-      case 16: rmsnorm_bf16_kernel<16><<<grid, block, 0, c.stream>>>(xv, gv, yv, rows, inv_d, eps); break;
+      case 1: launch_pdl(c, rmsnorm_bf16_kernel<1>, grid, block, 0, xv, gv, yv, rows, inv_d, eps); break;
+      case 2: launch_pdl(c, rmsnorm_bf16_kernel<2>, grid, block, 0, xv, gv, yv, rows, inv_d, eps); break;
+      case 4: launch_pdl(c, rmsnorm_bf16_kernel<4>, grid, block, 0, xv, gv, yv, rows, inv_d, eps); break;
+      case 8: launch_pdl(c, rmsnorm_bf16_kernel<8>, grid, block, 0, xv, gv, yv, rows, inv_d, eps); break;
+      case 16: launch_pdl(c, rmsnorm_bf16_kernel<16>, grid, block, 0, xv, gv, yv, rows, inv_d, eps); break;
       default:
-        rmsnorm_generic_kernel<__nv_bfloat16><<<grid, block, 0, c.stream>>>(
-            static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(gamma),
-            static_cast<__nv_bfloat16*>(y), rows, d, eps);
+        launch_pdl(c, rmsnorm_generic_kernel<__nv_bfloat16>, grid, block, 0, static_cast<const __nv_bfloat16*>(x),
+                   static_cast<const __nv_bfloat16*>(gamma), static_cast<__nv_bfloat16*>(y), rows, d, eps);
     }
   } else if (dtype == LLAMA_BF16) {
-    rmsnorm_generic_kernel<__nv_bfloat16><<<grid, block, 0, c.stream>>>(
-        static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(gamma),
-        static_cast<__nv_bfloat16*>(y), rows, d, eps);
+    launch_pdl(c, rmsnorm_generic_kernel<__nv_bfloat16>, grid, block, 0, static_cast<const __nv_bfloat16*>(x),
+               static_cast<const __nv_bfloat16*>(gamma), static_cast<__nv_bfloat16*>(y), rows, d, eps);
   } else {
-    rmsnorm_generic_kernel<float><<<grid, block, 0, c.stream>>>(
-        static_cast<const float*>(x), static_cast<const float*>(gamma), static_cast<float*>(y), rows, d, eps);
+    launch_pdl(c, rmsnorm_generic_kernel<float>, grid, block, 0, static_cast<const float*>(x),
+               static_cast<const float*>(gamma), static_cast<float*>(y), rows, d, eps);
   }
   return after_launch(c);
 }
