@@ -47,7 +47,7 @@ def parse():
     ap.add_argument("--no-extra", action="store_true", help="only the headline workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", choices=["attention", "gate_up", "down", "qkv", "decode_attention", "decode_layer",
-                                       "rmsnorm"],
+                                       "rmsnorm", "layernorm"],
                     help="time one step alone (W + K launches, CUDA events) instead of the layer")
     ap.add_argument("--workload", default=MAIN, help="workload whose shapes --case uses")
     return ap.parse_args()
@@ -347,18 +347,24 @@ def bench_decode(api, wl, steps, warmup, dev, pk):
     return res
 
 
-def bench_rmsnorm(api, dev, pk, rows=16384, d=4096, reps=20):
+def bench_norm(api, dev, pk, kind, rows=16384, d=4096, reps=20):
+    """RMSNorm or LayerNorm alone on [rows, d] bf16, L2 flushed before each run."""
     import torch
     xs = [torch.randn(rows, d, device=dev).to(torch.bfloat16) for _ in range(2)]
     g = torch.ones(d, dtype=torch.bfloat16, device=dev)
+    bt = torch.zeros(d, dtype=torch.bfloat16, device=dev)
     y = torch.empty_like(xs[0])
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    if kind == "rmsnorm":
+        fn = lambda x: api.rmsnorm(x, g, y, 1e-5)
+    else:
+        fn = lambda x: api.layernorm(x, g, bt, y, 1e-5)
     ts = []
     for i in range(reps + 3):
         flush.zero_()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        api.rmsnorm(xs[i % 2], g, y, 1e-5)
+        fn(xs[i % 2])
         e1.record()
         e1.synchronize()
         if i >= 3:
@@ -432,6 +438,11 @@ def bench_case(api, case, wl, steps, warmup, dev, pk):
             ws = api.workspace(api.decode_workspace_bytes(dims, B, T), dev)
             fn = lambda: api.layer_decode(dims, w, x, y, cos, sin, pos, kc, vc, ws)
             work, unit = kv + 2 * (d * (H + 2 * G) * D + H * D * d + 3 * d * I), "byte"
+    elif case == "layernorm":
+        x, gm, bt = rnd(M, d), rnd(d), rnd(d)
+        y = torch.empty_like(x)
+        fn = lambda: api.layernorm(x, gm, bt, y, L.rms_eps)
+        work, unit = 2.0 * M * d * 2, "byte"
     else:   # rmsnorm
         x, gm = rnd(M, d), rnd(d)
         y = torch.empty_like(x)
@@ -611,7 +622,9 @@ def main():
                                  "frac_of_sustained_peak": round(r8["tflops_total"] / pk["bf16_sustained"], 4),
                                  "kernel_ms": {k: round(v, 3) for k, v in r8["kernel_ms"].items()},
                                  "kernel_tflops": r8["kernel_tflops"]}
-        line["rmsnorm"] = bench_rmsnorm(api, dev, pk)
+        line["rmsnorm"] = bench_norm(api, dev, pk, "rmsnorm")
+        line["layernorm"] = bench_norm(api, dev, pk, "layernorm")
+        line["layernorm"]["time_vs_rmsnorm"] = round(line["layernorm"]["us"] / line["rmsnorm"]["us"], 3)
         line["stack32_forward"] = bench_stack(api, synth.WORKLOADS["stack32_gqa8b_bf16_s8192_v32000"], 3, 2, dev, pk)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tps, n, per = oracle_prefill_sample(wl)

@@ -135,6 +135,14 @@ int llama_stack_forward(const llama_stack *stack, const int32_t *tokens, float *
 int llama_rmsnorm(const void *x, const void *gamma, void *y, int32_t rows, int32_t d, float eps, int32_t dtype,
                   void *cuda_stream);
 
+/* y = gamma * (x - mu) / sqrt(sigma^2 + eps) + beta per row, mu the row mean and sigma^2 the
+ * biased row variance ("3.2 核心组件逐一拆解" §3.2.1, LayerNorm).  Not a step of the decoder
+ * layer (which uses RMSNorm); exported so that the two normalisations can be compared on the
+ * same rows.  x, y: device [rows, d]; gamma, beta: device [d]; all of dtype; 16-byte aligned.
+ * fp32 arithmetic, one rounding to dtype.  rows == 0 is a no-op. */
+int llama_layernorm(const void *x, const void *gamma, const void *beta, void *y, int32_t rows, int32_t d, float eps,
+                    int32_t dtype, void *cuda_stream);
+
 /* C = A B^T ("12 · 从 Transformer 到 LLaMA 系列" §八: nn.Linear, y = x W^T).  A: device
  * [M, K], B: device [N, K], both bf16; C: device [M, N], bf16 (c_f32 = 0) or fp32
  * (c_f32 = 1).  K % 8 == 0. */
@@ -174,7 +182,9 @@ int llama_attention_decode_workspace_bytes(const llama_layer_dims *dims, int32_t
 
 /* One query per sequence at position positions[b] over cache slots 0..positions[b]
  * ("第 10 章：现代 LLaMA 架构" §7: score shape [B, H, 1, T_cache + 1]).  q: device
- * [B, H, D]; out: device [B, H*D]. */
+ * [B, H, D]; out: device [B, H*D].  A sequence whose position lies outside the cache (or
+ * max_pos) gets a zero output row and LLAMA_ERR_DEVICE_BOUNDS in the status word.  bf16
+ * layers need D = 128 and H / G in {1, 2, 4, 8}. */
 int llama_attention_decode(const llama_layer_dims *dims, const void *q, llama_kv_cache cache,
                            const int32_t *positions, void *out, int32_t B, void *workspace, size_t ws_bytes,
                            void *cuda_stream);
@@ -185,8 +195,9 @@ int llama_attention_decode(const llama_layer_dims *dims, const void *q, llama_kv
  * would synchronise the device.  The pages have no counterpart to this entry point; it computes
  * what llama_attention_decode computes, with the same arguments minus the workspace.
  * Its scratch is a fixed 16 MiB device array inside the library (every device that loads the
- * library holds one until the process exits), enough for B * H * ceil(max_T / 1024) * (D + 2)
- * floats; a larger request returns LLAMA_ERR_SCRATCH_LIMIT.  All calls on a device share that
+ * library holds one until the process exits); a request needs (min(B, 1024) * G + 256) * (H / G)
+ * * (D + 2) floats plus min(B, 1024) + 1 ints of it, and one that needs more returns
+ * LLAMA_ERR_SCRATCH_LIMIT.  All calls on a device share that
  * array: calls that may overlap on the GPU (unordered streams) race on it.  Nothing in it needs
  * to start at zero.  The first call on each device looks up the array's device address (a host
  * query, no allocation); make that first call before any stream capture.  Never allocates or

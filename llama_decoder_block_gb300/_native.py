@@ -53,6 +53,8 @@ SIGNATURES = {
     "llama_stack_forward": (c_int32, [P(Stack), c_void_p, c_void_p, c_void_p, c_void_p, c_int32, P(KVCache),
                                       c_int32, c_int32, c_void_p, c_size_t, c_void_p]),
     "llama_rmsnorm": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_float, c_int32, c_void_p]),
+    "llama_layernorm": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_float, c_int32,
+                                  c_void_p]),
     "llama_linear_bf16": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32, c_void_p]),
     "llama_linear_residual": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32,
                                         c_void_p]),

@@ -124,6 +124,12 @@ def rmsnorm(x, gamma, y, eps: float, stream=None) -> None:
                                   _stream(stream)), "llama_rmsnorm")
 
 
+def layernorm(x, gamma, beta, y, eps: float, stream=None) -> None:
+    d = x.shape[-1]
+    N.check(N.lib().llama_layernorm(_ptr(x), _ptr(gamma), _ptr(beta), _ptr(y), x.numel() // d, d, eps,
+                                    DTYPES[x.dtype], _stream(stream)), "llama_layernorm")
+
+
 def linear_bf16(a, b, c, stream=None) -> None:
     M, K = a.shape
     Nn = b.shape[0]

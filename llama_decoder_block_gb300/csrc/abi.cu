@@ -103,7 +103,7 @@ size_t decode_ws(const llama_layer_dims* d, int B, int max_T, int num_sms, void*
   w.a = c.take(static_cast<size_t>(B) * d->d_inter * es);
   if (d->dtype == LLAMA_BF16) {
     w.part = c.take(decode_part_floats(d, B, num_sms) * sizeof(float));
-    w.attn = c.take(attn_decode_ws_bytes(B, d->n_heads, d->head_dim, max_T));
+    w.attn = c.take(attn_decode_ws_bytes(B, d->n_heads, d->n_kv_heads, d->head_dim));
   } else {
     w.part = w.attn = nullptr;
   }
@@ -360,6 +360,17 @@ int llama_rmsnorm(const void* x, const void* gamma, void* y, int32_t rows, int32
   return rmsnorm(c, x, gamma, y, rows, d, eps, dtype);
 }
 
+int llama_layernorm(const void* x, const void* gamma, const void* beta, void* y, int32_t rows, int32_t d, float eps,
+                    int32_t dtype, void* cuda_stream) {
+  if (!x || !gamma || !beta || !y || rows < 0 || d <= 0 || !(eps >= 0.f) || (dtype != LLAMA_F32 && dtype != LLAMA_BF16))
+    return LLAMA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(gamma) || !aligned16(beta)) return LLAMA_ERR_INVALID_ARG;
+  Ctx c;
+  int rc = make_ctx(cuda_stream, &c);
+  if (rc) return rc;
+  return layernorm(c, x, gamma, beta, y, rows, d, eps, dtype);
+}
+
 int llama_linear_bf16(const void* A, const void* B, void* C, int32_t M, int32_t N, int32_t K, int32_t c_f32,
                       void* cuda_stream) {
   if (!A || !B || !C || M <= 0 || N <= 0 || K <= 0) return LLAMA_ERR_INVALID_ARG;
@@ -430,7 +441,7 @@ int llama_attention_decode_workspace_bytes(const llama_layer_dims* dims, int32_t
   int rc = check_dims(dims);
   if (rc) return rc;
   if (!bytes || B <= 0 || max_T <= 0) return LLAMA_ERR_INVALID_ARG;
-  *bytes = attn_decode_ws_bytes(B, dims->n_heads, dims->head_dim, max_T);
+  *bytes = attn_decode_ws_bytes(B, dims->n_heads, dims->n_kv_heads, dims->head_dim);
   return LLAMA_OK;
 }
 
@@ -445,7 +456,7 @@ int llama_attention_decode(const llama_layer_dims* dims, const void* q, llama_kv
   if ((rc = make_ctx(cuda_stream, &c))) return rc;
   if (dims->dtype == LLAMA_BF16) {
     if (!workspace || !aligned16(workspace) ||
-        ws_bytes < attn_decode_ws_bytes(B, dims->n_heads, dims->head_dim, cache.max_T))
+        ws_bytes < attn_decode_ws_bytes(B, dims->n_heads, dims->n_kv_heads, dims->head_dim))
       return LLAMA_ERR_INVALID_ARG;
     return attn_decode(c, dims->dtype, q, cache.k, cache.v, positions, out, B, dims->n_heads, dims->n_kv_heads,
                        dims->head_dim, cache.max_T, cache.max_T, workspace);

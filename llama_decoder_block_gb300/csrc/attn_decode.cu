@@ -5,14 +5,17 @@
 // [B, H, 1, T_cache + 1]; §6: the G cached K/V heads are shared by H/G query heads).
 //
 // HBM-bound: the cache is read once, by TMA, 128 keys (32 KB of K and 32 KB of V) per
-// tile through a 3-stage ring.  A persistent CTA walks work items (sequence b, KV head g,
-// 1024-key split) and keeps the ring full across items.  The products run on the tensor
+// tile through a 3-stage ring.  The work is balanced over the persistent CTAs: all
+// (sequence b, KV head g, key tile) triples are laid out on one axis, ordered by b, then g,
+// then tile, and CTA c takes the c-th of gridDim.x equal ranges of it.  A CTA's range falls
+// into segments, one per (b, g) it touches, and the ring stays full across segments.  The products run on the tensor
 // cores with the keys as the 128-row dimension: S^T = K Q^T (M = 128 keys, N = 16 query-head
 // columns of which H/G are real) and O^T += V^T P^T (M = 128 head dims, V read as an
 // MN-major operand straight from the cache layout), so the SIMT work per key is one row of
 // the online softmax per thread.  P^T and the TMEM S^T are double-buffered, so the softmax
 // of tile t overlaps the products of tile t-1.  Each item leaves (m, l, O) for its split;
-// the combine kernel merges the splits.
+// each segment leaves (m, l, O) in its own slot and the combine kernel merges the segments
+// of each (b, g).
 #include <algorithm>
 #include <mutex>
 
@@ -23,7 +26,6 @@ namespace llama {
 namespace {
 
 constexpr int HD = 128;
-constexpr int SPLIT = 1024;                 // keys per work item
 constexpr int KT = 128;                     // keys per tile
 constexpr int NQ = 16;                      // query-head columns of the MMAs (H/G <= 8 real)
 constexpr int STAGES = 3;
@@ -35,36 +37,50 @@ constexpr int P_CHUNK = NQ * 128;           // 64 keys of 16 query rows: 2 KB
 constexpr int P_TILE = 2 * P_CHUNK;
 constexpr int DEC_THREADS = 192;            // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
 constexpr uint32_t DEC_TMEM_COLS = 64;      // S^T buffers at 0 and 16, O^T buffers at 32 and 48
-constexpr int POS_CACHE = 1024;             // positions staged in shared memory (larger B reads global)
+constexpr int POS_CACHE = 1024;             // sequences per launch (positions and tile prefix sums in smem)
+constexpr int kDecMaxCtas = 256;            // upper bound of the grid (one CTA per SM)
 constexpr float kDecRescaleLog2 = 8.0f;
 
 struct DecParams {
   const int32_t* positions;
-  float* o_part;
-  float* m_part;
-  float* l_part;
-  int B, H, G, T_max, max_pos, n_split, n_items;
+  float* o_part;   // [slot][REP][HD]
+  float* m_part;   // [slot][REP]
+  float* l_part;   // [slot][REP]
+  int* prefix;     // [B + 1] tile prefix sums over the sequences, for the combine
+  int B, H, G, T_max, max_pos;
   float scale_log2;
   int* status;
 };
 
+// One segment: tiles [k_begin / KT, k_begin / KT + ntile) of (b, g), keys [k_begin, k_end).
+// Its partials go to slot b * G + g + blockIdx.x: along the axis both b * G + g and the CTA
+// index never decrease and one of them grows from one segment to the next, so slots are
+// unique and fewer than B * G + gridDim.x.
 struct DecItem {
-  int b, g, c, k_begin, k_end, ntile;
-  bool bad_position;
+  int b, g, k_begin, k_end, ntile, slot;
 };
 
-__device__ __forceinline__ DecItem dec_item(const DecParams& p, const int* pos_s, int it) {
+// Segment starting at axis position `pos` of a CTA whose range ends at `end`.  pre_s[b] is
+// the number of tiles of sequences before b (one KV head), so (b, g, tile) sits at
+// G * pre_s[b] + g * n_b + tile with n_b = pre_s[b + 1] - pre_s[b].
+__device__ __forceinline__ DecItem dec_seg(const DecParams& p, const int* pre_s, const int* pos_s, long long pos,
+                                           long long end) {
+  int lo = 0, hi = p.B - 1;   // the last sequence whose first tile is at or before pos
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (static_cast<long long>(p.G) * pre_s[mid] <= pos) lo = mid;
+    else hi = mid - 1;
+  }
   DecItem d;
-  d.c = it % p.n_split;
-  d.g = (it / p.n_split) % p.G;
-  d.b = it / (p.n_split * p.G);
-  const int pos = d.b < POS_CACHE ? pos_s[d.b] : p.positions[d.b];
-  const bool ok = pos >= 0 && pos < p.T_max && pos < p.max_pos;
-  d.bad_position = !ok;
-  const int n_keys = ok ? pos + 1 : 0;
-  d.k_begin = d.c * SPLIT;
-  d.k_end = min(d.k_begin + SPLIT, n_keys);
-  d.ntile = d.k_end > d.k_begin ? (d.k_end - d.k_begin + KT - 1) / KT : 0;
+  d.b = lo;
+  const int n_b = pre_s[lo + 1] - pre_s[lo];   // >= 1: pos lies inside this sequence's tiles
+  const long long local = pos - static_cast<long long>(p.G) * pre_s[lo];
+  d.g = static_cast<int>(local / n_b);
+  const int t = static_cast<int>(local - static_cast<long long>(d.g) * n_b);
+  d.ntile = static_cast<int>(min(static_cast<long long>(n_b - t), end - pos));
+  d.k_begin = t * KT;
+  d.k_end = min((t + d.ntile) * KT, pos_s[lo] + 1);
+  d.slot = lo * p.G + d.g + static_cast<int>(blockIdx.x);
   return d;
 }
 
@@ -81,7 +97,8 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
   uint8_t* sP = sQ + 2 * Q_TILE;                         // 2 buffers of P^T: 16 rows x 128 keys
   float* red = reinterpret_cast<float*>(sP + 2 * P_TILE);   // [2 buffers][4 warps][8 heads]
   int* pos_s = reinterpret_cast<int*>(red + 64);            // [POS_CACHE]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(pos_s + POS_CACHE);
+  int* pre_s = pos_s + POS_CACHE;                           // [POS_CACHE + 1], padded to + 2
+  uint64_t* bars = reinterpret_cast<uint64_t*>(pre_s + POS_CACHE + 2);
   uint64_t* kv_full = bars;                  // [STAGES]
   uint64_t* kv_empty = bars + STAGES;        // [STAGES]
   uint64_t* q_full = bars + 2 * STAGES;      // [2]
@@ -114,8 +131,6 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
-  pdl_wait();   // positions may come from the previous kernel
-  for (int i = threadIdx.x; i < min(p.B, POS_CACHE); i += DEC_THREADS) pos_s[i] = p.positions[i];
   // P^T rows beyond H/G stay zero (their O^T columns are never read)
   for (int i = threadIdx.x; i < 2 * P_TILE / 16; i += DEC_THREADS)
     reinterpret_cast<uint4*>(sP)[i] = make_uint4(0, 0, 0, 0);
@@ -128,21 +143,50 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     tmem_alloc(smem_u32(tmem_slot), DEC_TMEM_COLS);
     tmem_relinquish();
   }
+  pdl_wait();   // inputs written by the previous kernel (positions, q, the cache) are read from here on
+  for (int i = threadIdx.x; i < p.B; i += DEC_THREADS) pos_s[i] = p.positions[i];
+  __syncthreads();
+  if (warp == 0) {   // tiles per sequence (0 for a position outside the cache), prefix-summed
+    int run = 0;
+    for (int base = 0; base < p.B; base += 32) {
+      const int b = base + lane;
+      int n = 0;
+      if (b < p.B) {
+        const int pos = pos_s[b];
+        const bool ok = pos >= 0 && pos < p.T_max && pos < p.max_pos;
+        if (!ok && blockIdx.x == 0) report(p.status, LLAMA_ERR_DEVICE_BOUNDS);
+        n = ok ? pos / KT + 1 : 0;
+      }
+      int incl = n;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (b < p.B) pre_s[b + 1] = run + incl;
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) pre_s[0] = 0;
+  }
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  pdl_wait();   // inputs written by the previous kernel are read from here on
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i <= p.B; i += DEC_THREADS) p.prefix[i] = pre_s[i];
+  // this CTA's range of the (b, g, tile) axis
+  const long long axis = static_cast<long long>(p.G) * pre_s[p.B];
+  const long long r0 = axis * blockIdx.x / gridDim.x, r1 = axis * (blockIdx.x + 1) / gridDim.x;
 
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ TMA producer
       uint32_t tcount = 0, icount = 0;
       bool ok = true;
-      for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x) {
-        const DecItem d = dec_item(p, pos_s, it);
-        if (d.ntile == 0) continue;
+      for (long long pos = r0; pos < r1 && ok;) {
+        const DecItem d = dec_seg(p, pre_s, pos_s, pos, r1);
+        pos += d.ntile;
         const uint32_t qs = icount & 1;
         if (!mbar_wait(smem_u32(q_empty + qs), ((icount >> 1) & 1) ^ 1u, p.status, abort_flag)) { ok = false; break; }
         mbar_expect_tx(smem_u32(q_full + qs), Q_TILE);
@@ -200,9 +244,9 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
         tc_commit(smem_u32(kv_empty + (tc % STAGES)));
         return true;
       };
-      for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x) {
-        const DecItem d = dec_item(p, pos_s, it);
-        if (d.ntile == 0) continue;
+      for (long long pos = r0; pos < r1 && ok;) {
+        const DecItem d = dec_seg(p, pre_s, pos_s, pos, r1);
+        pos += d.ntile;
         const uint32_t qs = icount & 1;
         if (!mbar_wait(smem_u32(q_full + qs), (icount >> 1) & 1, p.status, abort_flag)) { ok = false; break; }
         const uint32_t aq = smem_u32(sQ + qs * Q_TILE);
@@ -241,17 +285,10 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     const float sl = p.scale_log2;
     uint32_t tcount = 0, icount = 0;
     bool ok = true;
-    for (int it = blockIdx.x; it < p.n_items && ok; it += gridDim.x) {
-      const DecItem d = dec_item(p, pos_s, it);
-      const long long part = (static_cast<long long>(d.b) * p.H + d.g * REP) * p.n_split + d.c;
-      if (d.ntile == 0) {   // empty split: the neutral element of the merge
-        if (d.bad_position && d.c == 0 && d.g == 0 && sw == 0 && lane == 0) report(p.status, LLAMA_ERR_DEVICE_BOUNDS);
-        if (sw == 0 && lane < REP) {
-          p.m_part[part + lane * p.n_split] = -INFINITY;
-          p.l_part[part + lane * p.n_split] = 0.f;
-        }
-        continue;
-      }
+    for (long long pos = r0; pos < r1 && ok;) {
+      const DecItem d = dec_seg(p, pre_s, pos_s, pos, r1);
+      pos += d.ntile;
+      const long long part = static_cast<long long>(d.slot) * REP;
       float m_run[REP], lsum[REP];
 #pragma unroll
       for (int h = 0; h < REP; ++h) {
@@ -350,7 +387,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
         if (lane == 0) mbar_arrive(smem_u32(p_full));
       }
       if (!ok) break;
-      // item epilogue: wait for the last product, write this split's (m, l, O)
+      // segment epilogue: wait for the last product, write this segment's (m, l, O)
       const uint32_t last = tcount - 1;
       if (!mbar_wait(smem_u32(o_done + (last & 1)), (last >> 1) & 1, p.status, abort_flag)) { ok = false; break; }
       tc_fence_after();
@@ -373,13 +410,13 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
 #pragma unroll
       for (int h = 0; h < REP; ++h) {
         const float o = h < 4 ? __uint_as_float(oa[h]) : __uint_as_float(ob[h - 4]);
-        p.o_part[(part + h * p.n_split) * HD + row] = o;
+        p.o_part[(part + h) * HD + row] = o;
         if (row == 0) {
-          p.m_part[part + h * p.n_split] = m_run[h];
-          p.l_part[part + h * p.n_split] = rb[h] + rb[8 + h] + rb[16 + h] + rb[24 + h];
+          p.m_part[part + h] = m_run[h];
+          p.l_part[part + h] = rb[h] + rb[8 + h] + rb[16 + h] + rb[24 + h];
         }
       }
-      named_barrier(1, 128);   // rb is reused by the next item's first tiles
+      named_barrier(1, 128);   // rb is reused by the next segment's first tiles
       ++icount;
     }
   }
@@ -393,31 +430,50 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
   }
 }
 
-constexpr size_t kDecSmemBytes = 1024 + 2 * STAGES * KV_TILE + 2 * Q_TILE + 2 * P_TILE + 64 * 4 + POS_CACHE * 4 +
-                                 (2 * STAGES + 13) * 8 + 16;
+constexpr size_t kDecSmemBytes = 1024 + 2 * STAGES * KV_TILE + 2 * Q_TILE + 2 * P_TILE + 64 * 4 +
+                                 (2 * POS_CACHE + 2) * 4 + (2 * STAGES + 13) * 8 + 16;
+static_assert(kDecSmemBytes <= 232448, "decode attention exceeds the shared memory of one CTA");
 
-// out[b, h*D + d] = sum_s e^(m_s - M) O_s[d] / sum_s e^(m_s - M) l_s
+// out[b, h*D + d] = sum_s e^(m_s - M) O_s[d] / sum_s e^(m_s - M) l_s over the segments s of
+// (b, g = h / rep): the CTAs whose ranges meet the tiles [G pre[b] + g n_b, ... + n_b) of the
+// axis.  CTA c's range starts at floor(c T / n_ctas), so the CTA holding tile t is
+// floor(((t + 1) n_ctas - 1) / T).  A sequence with no tiles (position outside the cache)
+// gets zeros.
 __global__ void __launch_bounds__(HD) attn_decode_combine_kernel(const float* __restrict__ o_part,
                                                                  const float* __restrict__ m_part,
                                                                  const float* __restrict__ l_part,
-                                                                 __nv_bfloat16* __restrict__ out, int n_split) {
+                                                                 const int* __restrict__ prefix,
+                                                                 __nv_bfloat16* __restrict__ out, int B, int H, int G,
+                                                                 int n_ctas) {
   pdl_trigger();
   pdl_wait();
-  const long long bh = blockIdx.x;
+  const int bh = blockIdx.x, b = bh / H, h = bh - b * H, rep = H / G, g = h / rep, hr = h - g * rep;
   const int d = threadIdx.x;
-  float mm = -INFINITY;
-  for (int s = 0; s < n_split; ++s) mm = fmaxf(mm, m_part[bh * n_split + s]);
-  float l = 0.f, o = 0.f;
-  if (mm != -INFINITY) {
-    for (int s = 0; s < n_split; ++s) {
-      const float ms = m_part[bh * n_split + s];
-      if (ms == -INFINITY) continue;
-      const float a = exp2f(ms - mm);
-      l += l_part[bh * n_split + s] * a;
-      o += o_part[(bh * n_split + s) * HD + d] * a;
+  const int n_b = prefix[b + 1] - prefix[b];
+  float res = 0.f;
+  if (n_b > 0) {
+    const long long T = static_cast<long long>(G) * prefix[B];
+    const long long first = static_cast<long long>(G) * prefix[b] + static_cast<long long>(g) * n_b;
+    const long long last = first + n_b - 1;
+    const int c0 = static_cast<int>(((first + 1) * n_ctas - 1) / T);
+    const int c1 = static_cast<int>(((last + 1) * n_ctas - 1) / T);
+    const long long slot0 = static_cast<long long>(b) * G + g;
+    // a CTA with an empty range (fewer tiles than CTAs) wrote no slot
+    auto empty = [&](int c) { return T * c / n_ctas == T * (c + 1) / n_ctas; };
+    float mm = -INFINITY;
+    for (int c = c0; c <= c1; ++c)
+      if (!empty(c)) mm = fmaxf(mm, m_part[(slot0 + c) * rep + hr]);
+    float l = 0.f, o = 0.f;
+    for (int c = c0; c <= c1; ++c) {
+      if (empty(c)) continue;
+      const long long i = (slot0 + c) * rep + hr;
+      const float a = exp2f(m_part[i] - mm);
+      l += l_part[i] * a;
+      o += o_part[i * HD + d] * a;
     }
+    res = l > 0.f ? o / l : 0.f;
   }
-  out[bh * HD + d] = __float2bfloat16_rn(l > 0.f ? o / l : 0.f);
+  out[static_cast<long long>(bh) * HD + d] = __float2bfloat16_rn(res);
 }
 
 template <int REP>
@@ -430,16 +486,19 @@ cudaError_t launch_decode(const Ctx& c, const CUtensorMap& tq, const CUtensorMap
                                     static_cast<int>(kDecSmemBytes));
   });
   if (attr_err != cudaSuccess) return attr_err;
-  return launch_pdl(c, attn_decode_tc_kernel<REP>, dim3(std::min(p.n_items, c.num_sms)), dim3(DEC_THREADS),
+  return launch_pdl(c, attn_decode_tc_kernel<REP>, dim3(std::min(c.num_sms, kDecMaxCtas)), dim3(DEC_THREADS),
                     kDecSmemBytes, tq, tk, tv, p);
 }
 
 }  // namespace
 
-size_t attn_decode_ws_bytes(int B, int H, int D, int T_max) {
-  const size_t n_split = (T_max + SPLIT - 1) / SPLIT;
-  const size_t parts = static_cast<size_t>(B) * H * n_split;
-  return parts * D * sizeof(float) + 2 * parts * sizeof(float) + 256;
+size_t attn_decode_ws_bytes(int B, int H, int G, int D) {
+  // one launch per POS_CACHE sequences, all reusing the same workspace
+  // (callers validate H % G == 0 before launching; an invalid G still gets a finite size)
+  const size_t bc = static_cast<size_t>(std::max(0, std::min(B, POS_CACHE)));
+  const size_t g = G > 0 ? static_cast<size_t>(G) : 1, rep = static_cast<size_t>(std::max(H, 1)) / g;
+  const size_t slots = bc * g + kDecMaxCtas;
+  return slots * rep * (D + 2) * sizeof(float) + (bc + 1) * sizeof(int) + 256;
 }
 
 int attn_decode(const Ctx& c, int dtype, const void* q, const void* k_cache, const void* v_cache,
@@ -447,43 +506,51 @@ int attn_decode(const Ctx& c, int dtype, const void* q, const void* k_cache, con
   if (dtype != LLAMA_BF16) return LLAMA_ERR_UNSUPPORTED;
   const int rep = H / G;
   if (D != HD) return LLAMA_ERR_UNSUPPORTED;
-  const int n_split = (T_max + SPLIT - 1) / SPLIT;
-  const size_t parts = static_cast<size_t>(B) * H * n_split;
+  if (rep != 1 && rep != 2 && rep != 4 && rep != 8) return LLAMA_ERR_UNSUPPORTED;
+  const int n_ctas = std::min(c.num_sms, kDecMaxCtas);
+  const size_t bmax = static_cast<size_t>(std::min(B, POS_CACHE));
+  const size_t slots = bmax * G + kDecMaxCtas;
   DecParams p;
   p.o_part = static_cast<float*>(ws);
-  p.m_part = p.o_part + parts * D;
-  p.l_part = p.m_part + parts;
-  p.positions = positions;
-  p.B = B;
+  p.m_part = p.o_part + slots * rep * D;
+  p.l_part = p.m_part + slots * rep;
+  p.prefix = reinterpret_cast<int*>(p.l_part + slots * rep);
   p.H = H;
   p.G = G;
   p.T_max = T_max;
   p.max_pos = max_pos;
-  p.n_split = n_split;
-  p.n_items = B * G * n_split;
   p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
   p.status = c.status;
-  CUtensorMap tq, tk, tv;
-  // Q [B*H][D] in 16-row boxes (the group's H/G heads, then padding rows that are ignored);
-  // K, V [B*G][T_max][D] in 128-key boxes (keys past T_max read as 0)
-  if (!make_tmap_2d(&tq, q, HD, static_cast<uint64_t>(B) * H, HD, NQ) ||
-      !make_tmap_3d(&tk, k_cache, HD, T_max, static_cast<uint64_t>(B) * G, HD, static_cast<uint64_t>(T_max) * HD, KT) ||
-      !make_tmap_3d(&tv, v_cache, HD, T_max, static_cast<uint64_t>(B) * G, HD, static_cast<uint64_t>(T_max) * HD, KT))
-    return LLAMA_ERR_INVALID_ARG;
-  cudaError_t err;
-  switch (rep) {
-    case 1: err = launch_decode<1>(c, tq, tk, tv, p); break;
-    case 2: err = launch_decode<2>(c, tq, tk, tv, p); break;
-    case 4: err = launch_decode<4>(c, tq, tk, tv, p); break;
-    case 8: err = launch_decode<8>(c, tq, tk, tv, p); break;
-    default: return LLAMA_ERR_UNSUPPORTED;
+  for (int b0 = 0; b0 < B; b0 += POS_CACHE) {
+    const int bc = std::min(POS_CACHE, B - b0);
+    const size_t q_off = static_cast<size_t>(b0) * H * D * 2, kv_off = static_cast<size_t>(b0) * G * T_max * D * 2;
+    const uint8_t* qc = static_cast<const uint8_t*>(q) + q_off;
+    const uint8_t* kc = static_cast<const uint8_t*>(k_cache) + kv_off;
+    const uint8_t* vc = static_cast<const uint8_t*>(v_cache) + kv_off;
+    p.positions = positions + b0;
+    p.B = bc;
+    CUtensorMap tq, tk, tv;
+    // Q [B*H][D] in 16-row boxes (the group's H/G heads, then padding rows that are ignored);
+    // K, V [B*G][T_max][D] in 128-key boxes (keys past T_max read as 0)
+    if (!make_tmap_2d(&tq, qc, HD, static_cast<uint64_t>(bc) * H, HD, NQ) ||
+        !make_tmap_3d(&tk, kc, HD, T_max, static_cast<uint64_t>(bc) * G, HD, static_cast<uint64_t>(T_max) * HD, KT) ||
+        !make_tmap_3d(&tv, vc, HD, T_max, static_cast<uint64_t>(bc) * G, HD, static_cast<uint64_t>(T_max) * HD, KT))
+      return LLAMA_ERR_INVALID_ARG;
+    cudaError_t err;
+    switch (rep) {
+      case 1: err = launch_decode<1>(c, tq, tk, tv, p); break;
+      case 2: err = launch_decode<2>(c, tq, tk, tv, p); break;
+      case 4: err = launch_decode<4>(c, tq, tk, tv, p); break;
+      default: err = launch_decode<8>(c, tq, tk, tv, p); break;
+    }
+    if (err != cudaSuccess) return LLAMA_ERR_CUDA;
+    int rc = after_launch(c);
+    if (rc != LLAMA_OK) return rc;
+    launch_pdl(c, attn_decode_combine_kernel, dim3(bc * H), dim3(HD), 0, p.o_part, p.m_part, p.l_part, p.prefix,
+               reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(out) + q_off), bc, H, G, n_ctas);
+    if ((rc = after_launch(c)) != LLAMA_OK) return rc;
   }
-  if (err != cudaSuccess) return LLAMA_ERR_CUDA;
-  int rc = after_launch(c);
-  if (rc != LLAMA_OK) return rc;
-  launch_pdl(c, attn_decode_combine_kernel, dim3(B * H), dim3(HD), 0, p.o_part, p.m_part, p.l_part,
-             static_cast<__nv_bfloat16*>(out), n_split);
-  return after_launch(c);
+  return LLAMA_OK;
 }
 
 }  // namespace llama
@@ -500,15 +567,16 @@ int attn_decode(const Ctx& c, int dtype, const void* q, const void* k_cache, con
 namespace llama {
 namespace {
 
-// Largest scratch the fixed-array entry point serves: the split partials of
-// B * H * ceil(max_T / 1024) (query head, key split) pairs, (D + 2) floats each.  At B = 64,
-// H = 32, max_T = 4096, D = 128 that is 4.3 MB.
+// Largest scratch the fixed-array entry point serves: the segment partials of
+// (min(B, 1024) * G + 256) * (H / G) (query head, segment) pairs, (D + 2) floats each, and
+// min(B, 1024) + 1 ints.  At B = 64, H = 32, G = 8, D = 128 that is 2.1 MB.
 constexpr size_t kDecodeScratchBytes = 16u << 20;
 
 // File-scope device array: every device that loads the library holds its own copy until the
 // process exits, and all calls on a device share it.  Each call writes every slot it later
-// reads (empty key splits write their neutral (m, l) entry), so nothing needs clearing, but
-// two calls that overlap on the GPU (different streams, no ordering) race on it.
+// reads (the combine reads only the segments that the same call's CTAs wrote), so nothing
+// needs clearing, but two calls that overlap on the GPU (different streams, no ordering)
+// race on it.
 static __device__ __align__(256) unsigned char g_decode_scratch[kDecodeScratchBytes];
 
 // Device address of g_decode_scratch, looked up once per device (host code must not use
@@ -529,7 +597,7 @@ extern "C" int llama_attention_decode_static(const llama_layer_dims* dims, const
   auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
   if (misaligned(q) || misaligned(out) || misaligned(cache.k) || misaligned(cache.v)) return LLAMA_ERR_INVALID_ARG;
   if (dims->dtype != LLAMA_BF16 || dims->head_dim != HD) return LLAMA_ERR_UNSUPPORTED;
-  if (attn_decode_ws_bytes(B, dims->n_heads, dims->head_dim, cache.max_T) > kDecodeScratchBytes)
+  if (attn_decode_ws_bytes(B, dims->n_heads, dims->n_kv_heads, dims->head_dim) > kDecodeScratchBytes)
     return LLAMA_ERR_SCRATCH_LIMIT;
   Ctx c;
   int rc = make_ctx(cuda_stream, &c);

@@ -53,6 +53,11 @@ bool make_tmap_3d(CUtensorMap* tm, const void* base, uint64_t n0, uint64_t n1, u
 // ---------------------------------------------------------------- RMSNorm (rmsnorm.cu)
 int rmsnorm(const Ctx& c, const void* x, const void* gamma, void* y, int rows, int d, float eps, int dtype);
 
+// ---------------------------------------------------------------- LayerNorm (layernorm.cu)
+// y = gamma * (x - mean) * rsqrt(biased variance + eps) + beta per row.
+int layernorm(const Ctx& c, const void* x, const void* gamma, const void* beta, void* y, int rows, int d, float eps,
+              int dtype);
+
 // ---------------------------------------------------------------- tcgen05 GEMMs (gemm_tc.cu)
 // All compute C = X W^T with X [M, K] and W [N, K] bf16 row-major, fp32 accumulation.
 int gemm_plain(const Ctx& c, const void* X, const void* W, void* C, int M, int N, int K, bool c_f32);
@@ -75,7 +80,7 @@ int choose_splits(int num_sms, int w_rows_total, int K, int n_tok);
 // ---------------------------------------------------------------- attention
 int attn_prefill_tc(const Ctx& c, const void* q, const void* k_cache, const void* v_cache, void* out, int B,
                     int S, int H, int G, int D, int T_max);
-size_t attn_decode_ws_bytes(int B, int H, int D, int T_max);
+size_t attn_decode_ws_bytes(int B, int H, int G, int D);
 int attn_decode(const Ctx& c, int dtype, const void* q, const void* k_cache, const void* v_cache,
                 const int32_t* positions, void* out, int B, int H, int G, int D, int T_max, int max_pos,
                 void* ws);

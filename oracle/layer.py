@@ -50,6 +50,19 @@ def rms_norm(x, gamma, eps):
     return gamma * (x * (1.0 / np.sqrt(ms + eps)))
 
 
+def layer_norm(x, gamma, beta, eps):
+    """LayerNorm: gamma * (x - mu) / sqrt(sigma^2 + eps) + beta over the last axis.
+
+    [CORE] §3.2.1 "LayerNorm": mu is the mean over the hidden dimension and
+    sigma^2 the biased variance (divided by d, not d - 1); eps sits inside the
+    square root.  Not on the decoder layer's path: the pages contrast it with
+    RMSNorm, which drops the centring and beta.
+    """
+    mu = np.mean(x, axis=-1, keepdims=True)
+    var = np.mean((x - mu) ** 2, axis=-1, keepdims=True)
+    return gamma * ((x - mu) / np.sqrt(var + eps)) + beta
+
+
 def rope_tables(base, head_dim, max_pos):
     """cos/sin tables ``[max_pos, D/2]``: angle(p, i) = p * base^(-2i/D).
 

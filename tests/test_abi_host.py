@@ -122,4 +122,7 @@ def test_decode_and_attention_reject_bad_arguments_without_a_gpu(native):
     assert lib.llama_linear_bf16(p, p, p, 4, 12, 30, 0, None) == -2    # K % 8
     assert lib.llama_linear_bf16(None, p, p, 4, 16, 32, 0, None) == -1
     assert lib.llama_rmsnorm(p, p, p, 4, 64, -1.0, 1, None) == -1
+    assert lib.llama_layernorm(p, p, None, p, 4, 64, 1e-5, 1, None) == -1
+    assert lib.llama_layernorm(p, p, p + 8, p, 4, 64, 1e-5, 1, None) == -1     # beta not 16-byte aligned
+    assert lib.llama_layernorm(p, p, p, p, 4, 64, 1e-5, 7, None) == -1        # unknown dtype
     assert lib.llama_rope_tables(1e4, 7, 4, p, p) == -1

@@ -51,6 +51,28 @@ def test_rmsnorm(api, rows, d, dt):
     assert api.device_status() == 0
 
 
+@pytest.mark.parametrize("rows,d,dt", [(1, 4096, "bf16"), (37, 4096, "bf16"), (2048, 4096, "bf16"),
+                                       (64, 768, "bf16"), (40, 1024, "bf16"), (9, 100, "bf16"), (16, 64, "f32"),
+                                       (33, 4096, "f32")])
+def test_layernorm(api, rows, d, dt):
+    # rows with a large common offset: the centring must happen before the square
+    rng = _rng(rows * 11 + d)
+    x = 4.0 + rng.standard_normal((rows, d)) * 2
+    g = 1 + 0.1 * rng.standard_normal(d)
+    bt = 0.1 * rng.standard_normal(d)
+    if dt == "bf16":
+        xs, gs, bs = bf16_stored(x), bf16_stored(g), bf16_stored(bt)
+    else:
+        from llama_decoder_block_gb300.synth import Stored
+        xs, gs, bs = (Stored(v.astype(np.float32), "f32") for v in (x, g, bt))
+    xd, gd, bd = to_dev(xs), to_dev(gs), to_dev(bs)
+    y = torch.empty_like(xd)
+    api.layernorm(xd, gd, bd, y, 1e-5)
+    ref = oracle.layer_norm(xs.f64(), gs.f64(), bs.f64(), 1e-5)
+    assert_close(f64(y), ref, TOL[dt], "layernorm")
+    assert api.device_status() == 0
+
+
 @pytest.mark.parametrize("M,N,K", [(128, 256, 64), (300, 520, 200), (1000, 2048, 4096), (64, 6144, 4096)])
 @pytest.mark.parametrize("out_f32", [False, True])
 def test_linear_bf16(api, M, N, K, out_f32):
@@ -134,6 +156,51 @@ def test_attention_decode(api, H, G):
                                np.array([[p]]), np.array([p + 1]))[0, :, 0, :]
         assert_close(f64(out)[b].reshape(H, 128), ref, TOL["bf16"], f"decode attention b={b} p={p}")
     assert api.device_status() == 0
+
+
+@pytest.mark.parametrize("H,G,positions", [(8, 1, [4095, 0, 2000]), (32, 8, [4095, 3, 130, 4000]),
+                                           (4, 4, [255, 256, 257])])
+def test_attention_decode_long_and_short_sequences(api, H, G, positions):
+    # the CTAs split the (sequence, KV head, key tile) axis evenly, so a long sequence next to
+    # short ones is cut into many segments that the combine kernel merges
+    rng = _rng(H + 7 * G + len(positions))
+    positions = np.array(positions, dtype=np.int32)
+    B, T_max = len(positions), 4096
+    q = bf16_stored(rng.standard_normal((B, H, 128)))
+    kc = _cache_with_nan_tail(rng, B, G, T_max, positions + 1)
+    vc = _cache_with_nan_tail(rng, B, G, T_max, positions + 1)
+    dims = _attn_dims(api, H, G)
+    ws = api.workspace(api.attention_decode_workspace_bytes(dims, B, T_max), "cuda")
+    out = torch.empty(B, H * 128, dtype=torch.bfloat16, device="cuda")
+    api.attention_decode(dims, to_dev(q), to_dev(kc), to_dev(vc), torch.from_numpy(positions).cuda(), out, ws)
+    k64, v64 = kc.f64(), vc.f64()
+    for b, p in enumerate(positions):
+        ref = oracle.attention(q.f64()[b:b + 1, :, None, :], k64[b:b + 1, :, :p + 1], v64[b:b + 1, :, :p + 1],
+                               np.array([[p]]), np.array([p + 1]))[0, :, 0, :]
+        assert_close(f64(out)[b].reshape(H, 128), ref, TOL["bf16"], f"decode attention b={b} p={p}")
+    assert api.device_status() == 0
+
+
+def test_attention_decode_more_sequences_than_one_launch_holds(api):
+    # 1030 sequences: the library runs them as launches of at most 1024 sequences
+    B, H, G, T_max = 1030, 8, 2, 200
+    rng = _rng(1030)
+    positions = rng.integers(0, T_max, size=B).astype(np.int32)
+    positions[[0, 1023, 1024, 1029]] = [T_max - 1, 0, T_max - 1, 5]
+    q = torch.from_numpy(rng.standard_normal((B, H, 128)).astype(np.float32)).to(torch.bfloat16).cuda()
+    kc = torch.from_numpy(rng.standard_normal((B, G, T_max, 128)).astype(np.float32)).to(torch.bfloat16).cuda()
+    vc = torch.from_numpy(rng.standard_normal((B, G, T_max, 128)).astype(np.float32)).to(torch.bfloat16).cuda()
+    dims = _attn_dims(api, H, G)
+    ws = api.workspace(api.attention_decode_workspace_bytes(dims, B, T_max), "cuda")
+    out = torch.empty(B, H * 128, dtype=torch.bfloat16, device="cuda")
+    api.attention_decode(dims, q, kc, vc, torch.from_numpy(positions).cuda(), out, ws)
+    assert api.device_status() == 0
+    o = f64(out).reshape(B, H, 128)
+    for b in [0, 1, 511, 1022, 1023, 1024, 1025, 1029] + rng.integers(0, B, size=12).tolist():
+        p = int(positions[b])
+        ref = oracle.attention(f64(q[b:b + 1])[:, :, None, :], f64(kc[b:b + 1, :, :p + 1]),
+                               f64(vc[b:b + 1, :, :p + 1]), np.array([[p]]), np.array([p + 1]))[0, :, 0, :]
+        assert_close(o[b], ref, TOL["bf16"], f"decode attention b={b} p={p}")
 
 
 def test_attention_decode_reports_out_of_range_positions(api):

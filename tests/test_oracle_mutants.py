@@ -12,6 +12,12 @@ MUTANTS = {
     "eps_outside_sqrt": ("return gamma * (x * (1.0 / np.sqrt(ms + eps)))", "return gamma * (x / (np.sqrt(ms) + eps))"),
     "norm_subtracts_mean": ("ms = np.mean(x * x, axis=-1, keepdims=True)",
                             "x = x - x.mean(-1, keepdims=True); ms = np.mean(x * x, axis=-1, keepdims=True)"),
+    "layernorm_unbiased_variance": ("var = np.mean((x - mu) ** 2, axis=-1, keepdims=True)",
+                                    "var = np.sum((x - mu) ** 2, axis=-1, keepdims=True) / (x.shape[-1] - 1)"),
+    "layernorm_eps_outside_sqrt": ("return gamma * ((x - mu) / np.sqrt(var + eps)) + beta",
+                                   "return gamma * ((x - mu) / (np.sqrt(var) + eps)) + beta"),
+    "layernorm_beta_scaled": ("return gamma * ((x - mu) / np.sqrt(var + eps)) + beta",
+                              "return gamma * ((x - mu) / np.sqrt(var + eps) + beta)"),
     "rope_half_split": ("x_even = x[..., 0::2]\n    x_odd = x[..., 1::2]",
                         "x_even = x[..., :x.shape[-1]//2]\n    x_odd = x[..., x.shape[-1]//2:]"),
     "rope_sign": ("y[..., 0::2] = x_even * cos - x_odd * sin", "y[..., 0::2] = x_even * cos + x_odd * sin"),

@@ -102,6 +102,56 @@ def test_rmsnorm_statistics_of_normal_input():
     assert abs(y.mean()) < 0.03 and abs(y.std() - 1) < 0.03
 
 
+# ------------------------------------------------------------------ LayerNorm
+
+def test_layernorm_two_element_closed_form():
+    # "3.2 核心组件逐一拆解" §3.2.1: x = [1, 3] has mean 2 and biased variance 1, so with
+    # eps = 0 the output is [-1, 1]; with eps = 3, [-1, 1] / sqrt(1 + 3) = [-0.5, 0.5].
+    one, zero = np.ones(2), np.zeros(2)
+    assert np.array_equal(oracle.layer_norm(np.array([1.0, 3.0]), one, zero, 0.0), [-1.0, 1.0])
+    assert np.array_equal(oracle.layer_norm(np.array([1.0, 3.0]), one, zero, 3.0), [-0.5, 0.5])
+    # gamma scales the normalised value, beta is added after it
+    y = oracle.layer_norm(np.array([1.0, 3.0]), np.array([2.0, -4.0]), np.array([0.25, 0.5]), 0.0)
+    assert np.array_equal(y, [-1.75, -3.5])
+
+
+def test_layernorm_output_moments_closed_form():
+    # gamma = 1, beta = 0: each row has mean 0 and variance var / (var + eps) exactly.
+    x = 3.0 + 2.0 * RNG.standard_normal((6, 1000))
+    for eps in (1e-5, 0.5):
+        y = oracle.layer_norm(x, np.ones(1000), np.zeros(1000), eps)
+        var = np.var(x, axis=-1)
+        assert np.allclose(y.mean(-1), 0.0, atol=1e-13)
+        assert np.allclose(np.mean(y * y, axis=-1), var / (var + eps), rtol=1e-13, atol=0)
+
+
+def test_layernorm_shift_and_scale_invariance():
+    # re-centring removes any constant shift; with eps = 0 a positive scale cancels too
+    x = RNG.standard_normal((4, 96))
+    g, b = RNG.standard_normal(96), RNG.standard_normal(96)
+    base = oracle.layer_norm(x, g, b, 1e-5)
+    assert np.allclose(oracle.layer_norm(x + 7.25, g, b, 1e-5), base, rtol=1e-11, atol=1e-12)
+    assert np.allclose(oracle.layer_norm(3.0 * x, g, b, 0.0), oracle.layer_norm(x, g, b, 0.0), rtol=1e-12,
+                       atol=1e-13)
+
+
+def test_layernorm_is_rmsnorm_of_the_centred_row_plus_beta():
+    # the biased variance is the mean square of x - mu, so LN(x) = RMSNorm(x - mu) + beta
+    x = RNG.standard_normal((5, 128)) + 0.7
+    g, b = RNG.standard_normal(128), RNG.standard_normal(128)
+    centred = x - x.mean(-1, keepdims=True)
+    assert np.allclose(oracle.layer_norm(x, g, b, 1e-5), oracle.rms_norm(centred, g, 1e-5) + b, rtol=1e-12,
+                       atol=1e-13)
+
+
+def test_layernorm_matches_torch_layer_norm_in_fp64():
+    x = RNG.standard_normal((9, 257))
+    g, b = RNG.standard_normal(257), RNG.standard_normal(257)
+    ref = torch.nn.functional.layer_norm(torch.from_numpy(x), (257,), torch.from_numpy(g), torch.from_numpy(b),
+                                         1e-5).numpy()
+    assert np.allclose(oracle.layer_norm(x, g, b, 1e-5), ref, rtol=1e-12, atol=1e-12)
+
+
 # ------------------------------------------------------------------ RoPE
 
 def test_rope_special_frequencies():

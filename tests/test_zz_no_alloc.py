@@ -53,10 +53,12 @@ def test_fixed_scratch_decode_attention_matches_the_workspace_form(api):
 
 
 def test_fixed_scratch_refuses_requests_beyond_its_size(api):
-    H, G, B, T_max = 32, 8, 512, 4096     # 512 * 32 * 8 splits * 130 floats > 16 MiB
+    # (1024 * 8 + 256) segment slots * 4 heads * 130 floats > 16 MiB; the cache is real (small
+    # T_max) so that the arguments are valid apart from the scratch size
+    H, G, B, T_max = 32, 8, 1024, 16
     dims = api.Dims(H * 128, H, G, 128, 128, 1e-5, torch.bfloat16)
     q = torch.zeros(B, H, 128, dtype=torch.bfloat16, device="cuda")
-    kv = torch.zeros(16, dtype=torch.bfloat16, device="cuda")
+    kv = torch.zeros(B, G, T_max, 128, dtype=torch.bfloat16, device="cuda")
     pos = torch.zeros(B, dtype=torch.int32, device="cuda")
     out = torch.empty(B, H * 128, dtype=torch.bfloat16, device="cuda")
     from llama_decoder_block_gb300 import _native as N
