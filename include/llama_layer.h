@@ -50,6 +50,13 @@ typedef enum {
 
 typedef enum { LLAMA_F32 = 0, LLAMA_BF16 = 1 } llama_dtype;
 
+/* Which head dimensions RoPE rotates together.  Both use the angle p * base^(-2i/D) for pair
+ * i < D/2. */
+typedef enum {
+  LLAMA_ROPE_EVEN_ODD = 0, /* pairs (2i, 2i+1): "第 10 章：现代 LLaMA 架构" §2-§3 */
+  LLAMA_ROPE_HALF = 1      /* pairs (i, i + D/2): "12 · 从 Transformer 到 LLaMA 系列" §八 apply_rope */
+} llama_rope_style;
+
 /* Layer hyper-parameters; mirrors the config fields of "第 10 章：现代 LLaMA 架构" §1
  * (hidden_size, intermediate_size, num_attention_heads, num_key_value_heads, rms_norm_eps). */
 typedef struct {
@@ -60,6 +67,7 @@ typedef struct {
   int32_t d_inter;     /* SwiGLU hidden size */
   float rms_eps;       /* inside the square root: rsqrt(mean(x^2) + eps) */
   int32_t dtype;       /* llama_dtype */
+  int32_t rope_style;  /* llama_rope_style */
 } llama_layer_dims;
 
 /* Device pointers of one layer's parameters (no biases). */
@@ -184,7 +192,7 @@ int llama_attention_decode_workspace_bytes(const llama_layer_dims *dims, int32_t
  * ("第 10 章：现代 LLaMA 架构" §7: score shape [B, H, 1, T_cache + 1]).  q: device
  * [B, H, D]; out: device [B, H*D].  A sequence whose position lies outside the cache (or
  * max_pos) gets a zero output row and LLAMA_ERR_DEVICE_BOUNDS in the status word.  bf16
- * layers need D = 128 and H / G in {1, 2, 4, 8}. */
+ * layers need D = 128 and H / G in {1, 2, 4} or a multiple of 8. */
 int llama_attention_decode(const llama_layer_dims *dims, const void *q, llama_kv_cache cache,
                            const int32_t *positions, void *out, int32_t B, void *workspace, size_t ws_bytes,
                            void *cuda_stream);
@@ -195,9 +203,9 @@ int llama_attention_decode(const llama_layer_dims *dims, const void *q, llama_kv
  * would synchronise the device.  The pages have no counterpart to this entry point; it computes
  * what llama_attention_decode computes, with the same arguments minus the workspace.
  * Its scratch is a fixed 16 MiB device array inside the library (every device that loads the
- * library holds one until the process exits); a request needs (min(B, 1024) * G + 256) * (H / G)
- * * (D + 2) floats plus min(B, 1024) + 1 ints of it, and one that needs more returns
- * LLAMA_ERR_SCRATCH_LIMIT.  All calls on a device share that
+ * library holds one until the process exits); a request needs (min(B, 1024) * H + 256 * R)
+ * * (D + 2) floats, R = min(H / G, 8), plus min(B, 1024) + 1 ints of it, and one that needs
+ * more returns LLAMA_ERR_SCRATCH_LIMIT.  All calls on a device share that
  * array: calls that may overlap on the GPU (unordered streams) race on it.  Nothing in it needs
  * to start at zero.  The first call on each device looks up the array's device address (a host
  * query, no allocation); make that first call before any stream capture.  Never allocates or

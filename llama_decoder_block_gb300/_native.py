@@ -20,7 +20,7 @@ STATUS = {0: "LLAMA_OK", -1: "LLAMA_ERR_INVALID_ARG", -2: "LLAMA_ERR_UNSUPPORTED
 
 class LayerDims(ctypes.Structure):
     _fields_ = [("d_model", c_int32), ("n_heads", c_int32), ("n_kv_heads", c_int32), ("head_dim", c_int32),
-                ("d_inter", c_int32), ("rms_eps", c_float), ("dtype", c_int32)]
+                ("d_inter", c_int32), ("rms_eps", c_float), ("dtype", c_int32), ("rope_style", c_int32)]
 
 
 WEIGHT_FIELDS = ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up", "w_down")

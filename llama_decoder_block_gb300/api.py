@@ -26,10 +26,11 @@ class Dims:
     d_inter: int
     rms_eps: float
     dtype: torch.dtype
+    rope_style: int = 0     # 0: pairs (2i, 2i+1); 1: pairs (i, i + D/2)
 
     def c(self) -> N.LayerDims:
         return N.LayerDims(self.d_model, self.n_heads, self.n_kv_heads, self.head_dim, self.d_inter,
-                           self.rms_eps, DTYPES[self.dtype])
+                           self.rms_eps, DTYPES[self.dtype], self.rope_style)
 
 
 def _ptr(t) -> int | None:

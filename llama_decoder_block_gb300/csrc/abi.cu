@@ -39,11 +39,13 @@ int check_dims(const llama_layer_dims* d) {
   if (d->head_dim % 2 != 0) return LLAMA_ERR_INVALID_ARG;              // RoPE rotates pairs
   if (!(d->rms_eps >= 0.f)) return LLAMA_ERR_INVALID_ARG;
   if (d->dtype != LLAMA_F32 && d->dtype != LLAMA_BF16) return LLAMA_ERR_INVALID_ARG;
+  if (d->rope_style != LLAMA_ROPE_EVEN_ODD && d->rope_style != LLAMA_ROPE_HALF) return LLAMA_ERR_INVALID_ARG;
   if (d->dtype == LLAMA_BF16) {
-    // the tensor-core path: 128-wide head tiles and 128-row weight blocks
+    // the tensor-core path: 128-wide head tiles and 128-row weight blocks; decode attention
+    // takes query heads in groups of up to 8 per KV head
     const int rep = d->n_heads / d->n_kv_heads;
     if (d->head_dim != 128 || d->d_model % 128 != 0 || d->d_inter % 128 != 0) return LLAMA_ERR_UNSUPPORTED;
-    if (rep != 1 && rep != 2 && rep != 4 && rep != 8) return LLAMA_ERR_UNSUPPORTED;
+    if (rep != 1 && rep != 2 && rep != 4 && rep % 8 != 0) return LLAMA_ERR_UNSUPPORTED;
   } else {
     if (d->head_dim > 256) return LLAMA_ERR_UNSUPPORTED;
   }
@@ -128,7 +130,7 @@ int prefill_impl(const Ctx& c, const llama_layer_dims* d, const llama_layer_weig
   if (d->dtype == LLAMA_BF16) {
     if ((rc = rmsnorm(c, x, w->attn_norm, p.xn, M, dm, d->rms_eps, d->dtype))) return rc;
     if ((rc = gemm_qkv_rope(c, p.xn, w->wq, w->wk, w->wv, B, S, dm, H, G, D, cos, sin, p.q, cache.k, cache.v,
-                            cache.max_T)))
+                            cache.max_T, d->rope_style)))
       return rc;
     if ((rc = attn_prefill_tc(c, p.q, cache.k, cache.v, p.o, B, S, H, G, D, cache.max_T))) return rc;
     if ((rc = gemm_residual(c, p.o, w->wo, x, p.h, M, dm, H * D))) return rc;
@@ -144,7 +146,7 @@ int prefill_impl(const Ctx& c, const llama_layer_dims* d, const llama_layer_weig
   if ((rc = simt_qkv_rope(c, xn, static_cast<const float*>(w->wq), static_cast<const float*>(w->wk),
                           static_cast<const float*>(w->wv), B, S, dm, H, G, D, cos, sin, nullptr, max_pos,
                           static_cast<float*>(p.q), static_cast<float*>(cache.k), static_cast<float*>(cache.v),
-                          cache.max_T)))
+                          cache.max_T, d->rope_style)))
     return rc;
   if ((rc = simt_attention(c, static_cast<float*>(p.q), static_cast<float*>(cache.k), static_cast<float*>(cache.v),
                            nullptr, static_cast<float*>(p.o), B, S, H, G, D, cache.max_T, max_pos)))
@@ -236,7 +238,9 @@ int llama_layer_decode(const llama_layer_dims* dims, const llama_layer_weights* 
       const int R3[3] = {H * D, G * D, G * D};
       const int s = choose_splits(c.num_sms, qkv, dm, B);
       if ((rc = gemm_tokens_partial(c, W3, R3, 3, p.xn, B, dm, s, P))) return rc;
-      if ((rc = fix_qkv_rope(c, P, s, B, H, G, D, positions, max_pos, cos, sin, p.q, cache.k, cache.v, T))) return rc;
+      if ((rc = fix_qkv_rope(c, P, s, B, H, G, D, positions, max_pos, cos, sin, p.q, cache.k, cache.v, T,
+                             dims->rope_style)))
+        return rc;
     }
     if ((rc = attn_decode(c, dims->dtype, p.q, cache.k, cache.v, positions, p.o, B, H, G, D, T, max_pos, p.attn)))
       return rc;
@@ -269,7 +273,8 @@ int llama_layer_decode(const llama_layer_dims* dims, const llama_layer_weights* 
   if ((rc = rmsnorm(c, x, w->attn_norm, xn, B, dm, dims->rms_eps, dims->dtype))) return rc;
   if ((rc = simt_qkv_rope(c, xn, static_cast<const float*>(w->wq), static_cast<const float*>(w->wk),
                           static_cast<const float*>(w->wv), B, 1, dm, H, G, D, cos, sin, positions, max_pos,
-                          static_cast<float*>(p.q), static_cast<float*>(cache.k), static_cast<float*>(cache.v), T)))
+                          static_cast<float*>(p.q), static_cast<float*>(cache.k), static_cast<float*>(cache.v), T,
+                          dims->rope_style)))
     return rc;
   if ((rc = simt_attention(c, static_cast<float*>(p.q), static_cast<float*>(cache.k), static_cast<float*>(cache.v),
                            positions, static_cast<float*>(p.o), B, 1, H, G, D, T, max_pos)))
@@ -418,7 +423,7 @@ int llama_qkv_rope(const llama_layer_dims* dims, const void* xn, const void* wq,
   Ctx c;
   if ((rc = make_ctx(cuda_stream, &c))) return rc;
   return gemm_qkv_rope(c, xn, wq, wk, wv, B, S, dims->d_model, dims->n_heads, dims->n_kv_heads, dims->head_dim, cos,
-                       sin, q_out, cache.k, cache.v, cache.max_T);
+                       sin, q_out, cache.k, cache.v, cache.max_T, dims->rope_style);
 }
 
 int llama_attention_prefill(const llama_layer_dims* dims, const void* q, llama_kv_cache cache, void* out, int32_t B,

@@ -47,7 +47,10 @@ struct DecParams {
   float* m_part;   // [slot][REP]
   float* l_part;   // [slot][REP]
   int* prefix;     // [B + 1] tile prefix sums over the sequences, for the combine
-  int B, H, G, T_max, max_pos;
+  int B, H;
+  int G;           // kernel groups per sequence: KV heads x chunks
+  int chunks;      // groups of REP query heads per KV head (H / G_kv / REP)
+  int T_max, max_pos;
   float scale_log2;
   int* status;
 };
@@ -193,7 +196,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
         const int qrow = d.b * p.H + d.g * REP;
         tma_load_2d(smem_u32(sQ + qs * Q_TILE), &tmQ, smem_u32(q_full + qs), 0, qrow);
         tma_load_2d(smem_u32(sQ + qs * Q_TILE + Q_CHUNK), &tmQ, smem_u32(q_full + qs), 64, qrow);
-        const int plane = d.b * p.G + d.g;
+        const int plane = (d.b * p.G + d.g) / p.chunks;   // the cache plane of KV head g / chunks
         for (int t = 0; t < d.ntile; ++t, ++tcount) {
           const uint32_t st = tcount % STAGES;
           if (!mbar_wait(smem_u32(kv_empty + st), ((tcount / STAGES) & 1) ^ 1u, p.status, abort_flag)) {
@@ -492,31 +495,44 @@ cudaError_t launch_decode(const Ctx& c, const CUtensorMap& tq, const CUtensorMap
 
 }  // namespace
 
+// Query heads per kernel group (at most 8) and kernel groups per KV head.
+void dec_groups(int H, int G, int* rep_k, int* chunks) {
+  const int rep = (G > 0 && H >= G) ? H / G : 1;
+  *chunks = rep > 8 ? rep / 8 : 1;
+  *rep_k = rep / *chunks;
+}
+
 size_t attn_decode_ws_bytes(int B, int H, int G, int D) {
   // one launch per POS_CACHE sequences, all reusing the same workspace
-  // (callers validate H % G == 0 before launching; an invalid G still gets a finite size)
+  int rep_k, chunks;
+  dec_groups(H, G, &rep_k, &chunks);
   const size_t bc = static_cast<size_t>(std::max(0, std::min(B, POS_CACHE)));
-  const size_t g = G > 0 ? static_cast<size_t>(G) : 1, rep = static_cast<size_t>(std::max(H, 1)) / g;
-  const size_t slots = bc * g + kDecMaxCtas;
-  return slots * rep * (D + 2) * sizeof(float) + (bc + 1) * sizeof(int) + 256;
+  const size_t slots = bc * static_cast<size_t>(std::max(G, 1)) * chunks + kDecMaxCtas;
+  return slots * rep_k * (D + 2) * sizeof(float) + (bc + 1) * sizeof(int) + 256;
 }
 
 int attn_decode(const Ctx& c, int dtype, const void* q, const void* k_cache, const void* v_cache,
                 const int32_t* positions, void* out, int B, int H, int G, int D, int T_max, int max_pos, void* ws) {
   if (dtype != LLAMA_BF16) return LLAMA_ERR_UNSUPPORTED;
-  const int rep = H / G;
   if (D != HD) return LLAMA_ERR_UNSUPPORTED;
-  if (rep != 1 && rep != 2 && rep != 4 && rep != 8) return LLAMA_ERR_UNSUPPORTED;
+  const int rep_full = H / G;
+  if (rep_full != 1 && rep_full != 2 && rep_full != 4 && rep_full % 8 != 0) return LLAMA_ERR_UNSUPPORTED;
+  // more than 8 query heads per KV head: the kernel takes them 8 at a time, as `chunks`
+  // groups that read the same cache plane
+  int rep, chunks;
+  dec_groups(H, G, &rep, &chunks);
+  const int Gk = G * chunks;
   const int n_ctas = std::min(c.num_sms, kDecMaxCtas);
   const size_t bmax = static_cast<size_t>(std::min(B, POS_CACHE));
-  const size_t slots = bmax * G + kDecMaxCtas;
+  const size_t slots = bmax * Gk + kDecMaxCtas;
   DecParams p;
   p.o_part = static_cast<float*>(ws);
   p.m_part = p.o_part + slots * rep * D;
   p.l_part = p.m_part + slots * rep;
   p.prefix = reinterpret_cast<int*>(p.l_part + slots * rep);
   p.H = H;
-  p.G = G;
+  p.G = Gk;
+  p.chunks = chunks;
   p.T_max = T_max;
   p.max_pos = max_pos;
   p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(D));
@@ -547,7 +563,7 @@ int attn_decode(const Ctx& c, int dtype, const void* q, const void* k_cache, con
     int rc = after_launch(c);
     if (rc != LLAMA_OK) return rc;
     launch_pdl(c, attn_decode_combine_kernel, dim3(bc * H), dim3(HD), 0, p.o_part, p.m_part, p.l_part, p.prefix,
-               reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(out) + q_off), bc, H, G, n_ctas);
+               reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(out) + q_off), bc, H, Gk, n_ctas);
     if ((rc = after_launch(c)) != LLAMA_OK) return rc;
   }
   return LLAMA_OK;
@@ -568,8 +584,8 @@ namespace llama {
 namespace {
 
 // Largest scratch the fixed-array entry point serves: the segment partials of
-// (min(B, 1024) * G + 256) * (H / G) (query head, segment) pairs, (D + 2) floats each, and
-// min(B, 1024) + 1 ints.  At B = 64, H = 32, G = 8, D = 128 that is 2.1 MB.
+// min(B, 1024) * H + 256 * min(H / G, 8) (query head, segment) pairs, (D + 2) floats each,
+// and min(B, 1024) + 1 ints.  At B = 64, H = 32, G = 8, D = 128 that is 2.1 MB.
 constexpr size_t kDecodeScratchBytes = 16u << 20;
 
 // File-scope device array: every device that loads the library holds its own copy until the

@@ -52,6 +52,7 @@ struct Params {
   const float* cos;
   const float* sin;
   int S, H, G, D, T_max;
+  int rope_half;                // pairs (i, i + D/2) instead of (2i, 2i+1)
   __nv_bfloat16* q_out;
   __nv_bfloat16* k_cache;
   __nv_bfloat16* v_cache;
@@ -320,6 +321,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int hf = 0; hf < 2; ++hf) {
           const int hh = nb * 2 + hf;
           if (hh >= p.H + 2 * p.G) break;
+          if (p.rope_half && hh < p.H + p.G) {
+            // half-split pairs: columns 32c + i and 64 + 32c + i, angle index 32c + i
+            __nv_bfloat16* dst = hh < p.H
+                ? p.q_out + ((static_cast<long long>(b) * p.H + hh) * p.S + s) * p.D
+                : p.k_cache + ((static_cast<long long>(b) * p.G + (hh - p.H)) * p.T_max + s) * p.D;
+#pragma unroll 1
+            for (int c = 0; c < 2; ++c) {
+              uint32_t r2[32];
+              tmem_ld32(t_acc + hf * 128 + c * 32, r);
+              tmem_ld32(t_acc + hf * 128 + 64 + c * 32, r2);
+              if (m >= p.M) continue;
+              const float* cr = p.cos + static_cast<long long>(s) * half_d + c * 32;
+              const float* sr = p.sin + static_cast<long long>(s) * half_d + c * 32;
+              float w2[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                const float cs = cr[i], sn = sr[i];
+                const float x1 = __uint_as_float(r[i]), x2 = __uint_as_float(r2[i]);
+                v[i] = x1 * cs - x2 * sn;
+                w2[i] = x2 * cs + x1 * sn;
+              }
+              store_bf16x32(dst + c * 32, v, 32);
+              store_bf16x32(dst + 64 + c * 32, w2, 32);
+            }
+            continue;
+          }
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             tmem_ld32(t_acc + hf * 128 + c * 32, r);
@@ -473,7 +500,7 @@ int gemm_swiglu(const Ctx& c, const void* X, const void* Wg, const void* Wu, voi
 
 int gemm_qkv_rope(const Ctx& c, const void* X, const void* Wq, const void* Wk, const void* Wv, int B, int S, int K,
                   int H, int G, int D, const float* cos, const float* sin, void* q_out, void* k_cache,
-                  void* v_cache, int T_max) {
+                  void* v_cache, int T_max, int rope_half) {
   const int M = B * S;
   TMaps tm{};
   if (!make_tmap_2d(&tm.m[0], X, K, M, K, 128) || !make_tmap_2d(&tm.m[1], Wq, K, H * D, K, 128) ||
@@ -493,6 +520,7 @@ int gemm_qkv_rope(const Ctx& c, const void* X, const void* Wq, const void* Wk, c
   p.G = G;
   p.D = D;
   p.T_max = T_max;
+  p.rope_half = rope_half;
   p.q_out = static_cast<__nv_bfloat16*>(q_out);
   p.k_cache = static_cast<__nv_bfloat16*>(k_cache);
   p.v_cache = static_cast<__nv_bfloat16*>(v_cache);

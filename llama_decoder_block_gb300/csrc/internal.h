@@ -67,9 +67,10 @@ int gemm_residual(const Ctx& c, const void* X, const void* W, const void* resid,
 int gemm_swiglu(const Ctx& c, const void* X, const void* Wg, const void* Wu, void* out, int M, int I, int K);
 // [q|k|v] = X [Wq;Wk;Wv]^T for B sequences of S tokens at positions 0..S-1; RoPE on q, k;
 // q -> q_out [B, H, S, D]; k, v -> cache slots [0, S) of [B, G, T_max, D].
+// rope_half: pairs (i, i + D/2) instead of (2i, 2i+1).
 int gemm_qkv_rope(const Ctx& c, const void* X, const void* Wq, const void* Wk, const void* Wv, int B, int S,
                   int K, int H, int G, int D, const float* cos, const float* sin, void* q_out, void* k_cache,
-                  void* v_cache, int T_max);
+                  void* v_cache, int T_max, int rope_half);
 // Weight-streaming form for few tokens: P[s][t][n] = sum over split s of W[n, k] X[t, k] in fp32,
 // with W the row-concatenation of up to three matrices (rows multiples of 128).
 int gemm_tokens_partial(const Ctx& c, const void* const* W, const int* w_rows, int n_w, const void* X,
@@ -92,7 +93,7 @@ int simt_linear(const Ctx& c, int mode, const float* X, const float* W0, const f
                 const float* resid, float* out, int M, int N, int K);
 int simt_qkv_rope(const Ctx& c, const float* X, const float* Wq, const float* Wk, const float* Wv, int B, int S,
                   int K, int H, int G, int D, const float* cos, const float* sin, const int32_t* positions,
-                  int max_pos, float* q_out, float* k_cache, float* v_cache, int T_max);
+                  int max_pos, float* q_out, float* k_cache, float* v_cache, int T_max, int rope_half);
 int simt_attention(const Ctx& c, const float* q, const float* k_cache, const float* v_cache,
                    const int32_t* positions, float* out, int B, int S, int H, int G, int D, int T_max,
                    int max_pos);
@@ -104,7 +105,7 @@ int embed_gather(const Ctx& c, const int32_t* tokens, const void* table, void* x
 // Decode epilogues on the fp32 split partials P [splits][n_tok][N].
 int fix_qkv_rope(const Ctx& c, const float* P, int splits, int n_tok, int H, int G, int D,
                  const int32_t* positions, int max_pos, const float* cos, const float* sin, void* q_out,
-                 void* k_cache, void* v_cache, int T_max);
+                 void* k_cache, void* v_cache, int T_max, int rope_half);
 int fix_residual(const Ctx& c, const float* P, int splits, int n_tok, int N, const void* resid, void* out);
 // h = resid + sum of the splits (bf16), then hn = RMSNorm(h) with gamma (bf16); one CTA per token.
 int fix_residual_rmsnorm(const Ctx& c, const float* P, int splits, int n_tok, int N, const void* resid,

@@ -43,12 +43,14 @@ __device__ __forceinline__ void store_bf16x4(__nv_bfloat16* dst, float a, float 
   *reinterpret_cast<uint2*>(dst) = w;
 }
 
-// grid (ceil(N / 1024), n_tok): 4 consecutive columns of [q heads | k heads | v heads] per thread
+// grid (ceil(N / 1024), n_tok): 4 consecutive columns of [q heads | k heads | v heads] per thread.
+// With half-split pairs a thread of the first half of a q or k head also takes the partner
+// columns j + D/2 ... j + D/2 + 3, and threads of the second half have nothing to do.
 __global__ void fix_qkv_kernel(const float* __restrict__ P, int splits, int n_tok, int H, int G, int D,
                                const int32_t* __restrict__ positions, int max_pos, const float* __restrict__ cos,
                                const float* __restrict__ sin, __nv_bfloat16* __restrict__ q_out,
                                __nv_bfloat16* __restrict__ k_cache, __nv_bfloat16* __restrict__ v_cache, int T_max,
-                               int* status) {
+                               int rope_half, int* status) {
   pdl_trigger();
   pdl_wait();
   const int N = (H + 2 * G) * D;
@@ -60,9 +62,30 @@ __global__ void fix_qkv_kernel(const float* __restrict__ P, int splits, int n_to
     if (col == 0) report(status, LLAMA_ERR_DEVICE_BOUNDS);
     return;
   }
-  const float4 v = split_sum4(P, splits, static_cast<long long>(n_tok) * N, static_cast<long long>(t) * N + col);
-  float e0 = v.x, o0 = v.y, e1 = v.z, o1 = v.w;
   const int hh = col / D, j = col - hh * D;
+  __nv_bfloat16* dst;
+  if (hh < H) dst = q_out + (static_cast<long long>(t) * H + hh) * D;
+  else if (hh < H + G) dst = k_cache + ((static_cast<long long>(t) * G + (hh - H)) * T_max + pos) * D;
+  else dst = v_cache + ((static_cast<long long>(t) * G + (hh - H - G)) * T_max + pos) * D;
+  const long long stride = static_cast<long long>(n_tok) * N, at = static_cast<long long>(t) * N + col;
+  if (rope_half && hh < H + G) {   // pairs (j + i, j + i + D/2), angle index j + i
+    if (j >= D / 2) return;
+    const float4 x1 = split_sum4(P, splits, stride, at), x2 = split_sum4(P, splits, stride, at + D / 2);
+    const float* cr = cos + static_cast<long long>(pos) * (D / 2) + j;
+    const float* sr = sin + static_cast<long long>(pos) * (D / 2) + j;
+    const float a[4] = {x1.x, x1.y, x1.z, x1.w}, b[4] = {x2.x, x2.y, x2.z, x2.w};
+    float lo[4], hi[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      lo[i] = a[i] * cr[i] - b[i] * sr[i];
+      hi[i] = b[i] * cr[i] + a[i] * sr[i];
+    }
+    store_bf16x4(dst + j, lo[0], lo[1], lo[2], lo[3]);
+    store_bf16x4(dst + j + D / 2, hi[0], hi[1], hi[2], hi[3]);
+    return;
+  }
+  const float4 v = split_sum4(P, splits, stride, at);
+  float e0 = v.x, o0 = v.y, e1 = v.z, o1 = v.w;
   if (hh < H + G) {   // RoPE at the token's own position, pairs (j, j+1) and (j+2, j+3)
     const float* cr = cos + static_cast<long long>(pos) * (D / 2) + j / 2;
     const float* sr = sin + static_cast<long long>(pos) * (D / 2) + j / 2;
@@ -71,10 +94,6 @@ __global__ void fix_qkv_kernel(const float* __restrict__ P, int splits, int n_to
     const float r2 = e1 * c1 - o1 * s1, r3 = e1 * s1 + o1 * c1;
     e0 = r0; o0 = r1; e1 = r2; o1 = r3;
   }
-  __nv_bfloat16* dst;
-  if (hh < H) dst = q_out + (static_cast<long long>(t) * H + hh) * D;
-  else if (hh < H + G) dst = k_cache + ((static_cast<long long>(t) * G + (hh - H)) * T_max + pos) * D;
-  else dst = v_cache + ((static_cast<long long>(t) * G + (hh - H - G)) * T_max + pos) * D;
   store_bf16x4(dst + j, e0, o0, e1, o1);
 }
 
@@ -169,12 +188,12 @@ int embed_gather(const Ctx& c, const int32_t* tokens, const void* table, void* x
 
 int fix_qkv_rope(const Ctx& c, const float* P, int splits, int n_tok, int H, int G, int D, const int32_t* positions,
                  int max_pos, const float* cos, const float* sin, void* q_out, void* k_cache, void* v_cache,
-                 int T_max) {
+                 int T_max, int rope_half) {
   const int N = (H + 2 * G) * D;
   if (n_tok == 0) return LLAMA_OK;
   launch_pdl(c, fix_qkv_kernel, dim3((N / 4 + 255) / 256, n_tok), dim3(256), 0,
       P, splits, n_tok, H, G, D, positions, max_pos, cos, sin, static_cast<__nv_bfloat16*>(q_out),
-      static_cast<__nv_bfloat16*>(k_cache), static_cast<__nv_bfloat16*>(v_cache), T_max, c.status);
+      static_cast<__nv_bfloat16*>(k_cache), static_cast<__nv_bfloat16*>(v_cache), T_max, rope_half, c.status);
   return after_launch(c);
 }
 

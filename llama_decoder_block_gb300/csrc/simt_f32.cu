@@ -29,12 +29,14 @@ __global__ void simt_linear_kernel(int mode, const float* __restrict__ X, const 
   out[idx] = a;
 }
 
-// One thread per (token row m, column pair (2i, 2i+1) of [q heads | k heads | v heads]).
+// One thread per (token row m, column pair of [q heads | k heads | v heads]): pair i of a head
+// is the columns (2i, 2i+1), or (i, i + D/2) with rope_half.
 __global__ void simt_qkv_kernel(const float* __restrict__ X, const float* __restrict__ Wq,
                                 const float* __restrict__ Wk, const float* __restrict__ Wv, int B, int S, int K,
                                 int H, int G, int D, const float* __restrict__ cos, const float* __restrict__ sin,
                                 const int32_t* __restrict__ positions, int max_pos, float* __restrict__ q_out,
-                                float* __restrict__ k_cache, float* __restrict__ v_cache, int T_max, int* status) {
+                                float* __restrict__ k_cache, float* __restrict__ v_cache, int T_max, int rope_half,
+                                int* status) {
   const int pairs = (H + 2 * G) * D / 2;
   const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= static_cast<long long>(B) * S * pairs) return;
@@ -46,20 +48,23 @@ __global__ void simt_qkv_kernel(const float* __restrict__ X, const float* __rest
     report(status, LLAMA_ERR_DEVICE_BOUNDS);
     return;
   }
-  const int hh = col / D, j = col % D;
+  const int hh = col / D, i = (col % D) / 2;
+  const int j0 = rope_half ? i : 2 * i, j1 = rope_half ? i + D / 2 : 2 * i + 1;
   const float* w;
-  if (hh < H) w = Wq + static_cast<long long>(hh * D + j) * K;
-  else if (hh < H + G) w = Wk + static_cast<long long>((hh - H) * D + j) * K;
-  else w = Wv + static_cast<long long>((hh - H - G) * D + j) * K;
+  if (hh < H) w = Wq + static_cast<long long>(hh * D) * K;
+  else if (hh < H + G) w = Wk + static_cast<long long>((hh - H) * D) * K;
+  else w = Wv + static_cast<long long>((hh - H - G) * D) * K;
+  const float* w0 = w + static_cast<long long>(j0) * K;
+  const float* w1 = w + static_cast<long long>(j1) * K;
   const float* x = X + static_cast<long long>(m) * K;
   float e = 0.f, o = 0.f;
   for (int k = 0; k < K; ++k) {
-    e = fmaf(x[k], w[k], e);
-    o = fmaf(x[k], w[k + K], o);
+    e = fmaf(x[k], w0[k], e);
+    o = fmaf(x[k], w1[k], o);
   }
-  if (hh < H + G) {   // RoPE on q and k: the pair (j, j+1) turns by pos * base^(-j/D)
-    const float c = cos[static_cast<long long>(pos) * (D / 2) + j / 2];
-    const float sn = sin[static_cast<long long>(pos) * (D / 2) + j / 2];
+  if (hh < H + G) {   // RoPE on q and k: the pair (j0, j1) turns by pos * base^(-2i/D)
+    const float c = cos[static_cast<long long>(pos) * (D / 2) + i];
+    const float sn = sin[static_cast<long long>(pos) * (D / 2) + i];
     const float re = e * c - o * sn, ro = e * sn + o * c;
     e = re;
     o = ro;
@@ -68,8 +73,8 @@ __global__ void simt_qkv_kernel(const float* __restrict__ X, const float* __rest
   if (hh < H) dst = q_out + ((static_cast<long long>(b) * H + hh) * S + s) * D;
   else if (hh < H + G) dst = k_cache + ((static_cast<long long>(b) * G + (hh - H)) * T_max + pos) * D;
   else dst = v_cache + ((static_cast<long long>(b) * G + (hh - H - G)) * T_max + pos) * D;
-  dst[j] = e;
-  dst[j + 1] = o;
+  dst[j0] = e;
+  dst[j1] = o;
 }
 
 // One warp per (b, h, s): online softmax over keys 0..pos of KV head h / (H/G).
@@ -146,11 +151,12 @@ int simt_linear(const Ctx& c, int mode, const float* X, const float* W0, const f
 
 int simt_qkv_rope(const Ctx& c, const float* X, const float* Wq, const float* Wk, const float* Wv, int B, int S,
                   int K, int H, int G, int D, const float* cos, const float* sin, const int32_t* positions,
-                  int max_pos, float* q_out, float* k_cache, float* v_cache, int T_max) {
+                  int max_pos, float* q_out, float* k_cache, float* v_cache, int T_max, int rope_half) {
   const long long total = static_cast<long long>(B) * S * ((H + 2 * G) * D / 2);
   if (total == 0) return LLAMA_OK;
   simt_qkv_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, c.stream>>>(
-      X, Wq, Wk, Wv, B, S, K, H, G, D, cos, sin, positions, max_pos, q_out, k_cache, v_cache, T_max, c.status);
+      X, Wq, Wk, Wv, B, S, K, H, G, D, cos, sin, positions, max_pos, q_out, k_cache, v_cache, T_max, rope_half,
+      c.status);
   return after_launch(c);
 }
 

@@ -41,6 +41,7 @@ class LayerShape:
     rope_base: float
     dtype: str            # "f32" or "bf16"
     gamma: str            # "ones" or "noisy" (1 + N(0, 0.1))
+    rope_style: str = "even_odd"   # or "half": RoPE pairs (i, i + D/2)
 
 
 @dataclasses.dataclass(frozen=True)

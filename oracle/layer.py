@@ -90,6 +90,26 @@ def apply_rope(x, cos, sin):
     return y
 
 
+def apply_rope_half(x, cos, sin):
+    """Rotate pairs (x[i], x[i + D/2]) by the angle whose cos/sin are given.
+
+    [T2L] §八 ``apply_rope``: the first and second halves of head_dim form the
+    pairs, first half -> x1 cos - x2 sin, second half -> x2 cos + x1 sin, with
+    the same frequency index i < D/2 as the even/odd form.
+    """
+    assert x.shape[-1] % 2 == 0, "RoPE needs an even head_dim"
+    half = x.shape[-1] // 2
+    x1 = x[..., :half]
+    x2 = x[..., half:]
+    y = np.empty_like(x)
+    y[..., :half] = x1 * cos - x2 * sin
+    y[..., half:] = x2 * cos + x1 * sin
+    return y
+
+
+ROPE_STYLES = {"even_odd": apply_rope, "half": apply_rope_half}
+
+
 def silu(z):
     """SiLU(z) = z * sigmoid(z) = z / (1 + exp(-z)).  [T2L] §5.1; [CORE] §3.2.2."""
     return z / (1.0 + np.exp(-z))
@@ -140,7 +160,7 @@ def attention(q, k, v, q_pos, k_len):
 
 
 def decoder_layer(x, w, cos, sin, *, n_heads, n_kv_heads, head_dim, rms_eps,
-                  past_k=None, past_v=None, past_len=None, store_bf16=False):
+                  past_k=None, past_v=None, past_len=None, store_bf16=False, rope="even_odd"):
     """One pre-norm decoder layer, prefill or incremental.
 
     [L3B] §3.1 and §4.2 (save residual, norm, sublayer, add back, twice, with
@@ -158,6 +178,7 @@ def decoder_layer(x, w, cos, sin, *, n_heads, n_kv_heads, head_dim, rms_eps,
     produced: the normed input, q and k after RoPE, v (the cache), the attention
     output, h, the normed h and the gated MLP activation.  Arithmetic inside a step
     stays exact.
+    ``rope``: "even_odd" ([MOD] §3, the default) or "half" ([T2L] §八) pairing.
     Returns ``(out [B,S,d], k_new [B,G,S,D], v_new [B,G,S,D])``.
     """
     st = round_bf16 if store_bf16 else _keep
@@ -176,8 +197,9 @@ def decoder_layer(x, w, cos, sin, *, n_heads, n_kv_heads, head_dim, rms_eps,
     v = (xn @ w["wv"].T).reshape(B, S, G, D).transpose(0, 2, 1, 3)
     c = cos[pos][:, None, :, :]                                          # [B, 1, S, D/2]
     s = sin[pos][:, None, :, :]
-    q = st(apply_rope(q, c, s))                                          # RoPE on q and k only
-    k = st(apply_rope(k, c, s))
+    rot = ROPE_STYLES[rope]
+    q = st(rot(q, c, s))                                                 # RoPE on q and k only
+    k = st(rot(k, c, s))
     v = st(v)
 
     # keys of sequence b: cached slots [0, past_len[b]) then the S new ones
@@ -203,7 +225,7 @@ def decoder_layer(x, w, cos, sin, *, n_heads, n_kv_heads, head_dim, rms_eps,
 
 
 def stack_forward(tokens, layers, final_norm, embed, lm_head, cos, sin, *, n_heads,
-                  n_kv_heads, head_dim, rms_eps, store_bf16=False):
+                  n_kv_heads, head_dim, rms_eps, store_bf16=False, rope="even_odd"):
     """embed -> layers -> final RMSNorm -> untied LM head ([T2L] §八 ``LlamaModel.forward``).
 
     ``layers`` yields one weight dict per layer (so callers can stream them).
@@ -214,7 +236,7 @@ def stack_forward(tokens, layers, final_norm, embed, lm_head, cos, sin, *, n_hea
     x = embed[tokens]
     for w in layers:
         x, _, _ = decoder_layer(x, w, cos, sin, n_heads=n_heads, n_kv_heads=n_kv_heads,
-                                head_dim=head_dim, rms_eps=rms_eps, store_bf16=store_bf16)
+                                head_dim=head_dim, rms_eps=rms_eps, store_bf16=store_bf16, rope=rope)
         if store_bf16:
             x = round_bf16(x)
     xn = rms_norm(x, final_norm, rms_eps)                                 # the final norm Pre-LN needs

@@ -110,7 +110,7 @@ def gen_layer(args):
 
 def dims_of(layer: synth.LayerShape) -> api.Dims:
     return api.Dims(layer.d_model, layer.n_heads, layer.n_kv_heads, layer.head_dim, layer.d_inter, layer.rms_eps,
-                    TORCH_DT[layer.dtype])
+                    TORCH_DT[layer.dtype], {"even_odd": 0, "half": 1}[layer.rope_style])
 
 
 def tables(layer: synth.LayerShape, max_pos: int, oracle_mod, device="cuda"):
@@ -122,4 +122,5 @@ def tables(layer: synth.LayerShape, max_pos: int, oracle_mod, device="cuda"):
 
 
 def oracle_kw(layer: synth.LayerShape) -> dict:
-    return dict(n_heads=layer.n_heads, n_kv_heads=layer.n_kv_heads, head_dim=layer.head_dim, rms_eps=layer.rms_eps)
+    return dict(n_heads=layer.n_heads, n_kv_heads=layer.n_kv_heads, head_dim=layer.head_dim, rms_eps=layer.rms_eps,
+                rope=layer.rope_style)

@@ -79,6 +79,10 @@ def test_workspace_sizes_and_dims_validation(native):
     assert _bytes(native, _dims(native, dtype=7))[0] == -1
     assert _bytes(native, _dims(native, rms_eps=-1.0))[0] == -1
     assert _bytes(native, _dims(native, n_heads=12, n_kv_heads=4))[0] == -2   # H/G = 3 not a tiled ratio
+    assert _bytes(native, _dims(native, n_heads=24, n_kv_heads=2))[0] == -2   # H/G = 12: not 1, 2, 4 or 8k
+    assert _bytes(native, _dims(native, n_heads=32, n_kv_heads=1))[0] == 0    # MQA: query heads in groups of 8
+    assert _bytes(native, _dims(native, rope_style=1))[0] == 0               # half-split RoPE pairs
+    assert _bytes(native, _dims(native, rope_style=2))[0] == -1
     assert _bytes(native, _dims(native, head_dim=16, d_model=64, n_heads=4, n_kv_heads=2, d_inter=176,
                                 dtype=0))[0] == 0                     # the fp32 path takes any even D
 

@@ -138,7 +138,7 @@ def test_attention_prefill_mask_and_group_map_are_exact(api):
             assert np.allclose(o[i, h][list(expect)], 1.0 / (i + 1), rtol=1e-2)
 
 
-@pytest.mark.parametrize("H,G", [(8, 2), (4, 4), (8, 1), (32, 8)])
+@pytest.mark.parametrize("H,G", [(8, 2), (4, 4), (8, 1), (32, 8), (16, 1), (32, 1), (32, 2)])
 def test_attention_decode(api, H, G):
     rng = _rng(H * 31 + G)
     positions = np.array([0, 1, 127, 128, 511, 512, 1024, 1099], dtype=np.int32)

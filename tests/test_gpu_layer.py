@@ -69,11 +69,27 @@ def test_prefill_tiny_fp32_config(api):
     _check_prefill(api, synth.WORKLOADS["tiny_f32_b1_s16"])
 
 
-@pytest.mark.parametrize("H,G,B,S", [(4, 2, 2, 200), (2, 2, 1, 128), (8, 1, 1, 300), (4, 4, 3, 65)])
+@pytest.mark.parametrize("H,G,B,S", [(4, 2, 2, 200), (2, 2, 1, 128), (8, 1, 1, 300), (4, 4, 3, 65), (16, 1, 1, 140),
+                                     (32, 2, 1, 70)])
 def test_prefill_bf16_small(api, H, G, B, S):
     base = synth.WORKLOADS["gqa8b_bf16_b4_s4096"]
     wl = synth.scaled(base, d_model=256, n_heads=H, n_kv_heads=G, d_inter=384, B=B, S=S,
                       name=f"bf16_d256_h{H}_g{G}_b{B}_s{S}")
+    _check_prefill(api, wl)
+
+
+@pytest.mark.parametrize("H,G", [(4, 2), (16, 1)])
+def test_prefill_bf16_half_split_rope(api, H, G):
+    base = synth.WORKLOADS["gqa8b_bf16_b4_s4096"]
+    wl = synth.scaled(base, d_model=256, n_heads=H, n_kv_heads=G, d_inter=384, B=2, S=150, rope_style="half",
+                      name=f"bf16_half_rope_h{H}_g{G}")
+    _check_prefill(api, wl)
+
+
+def test_prefill_fp32_half_split_rope(api):
+    base = synth.WORKLOADS["tiny_f32_b1_s16"]
+    wl = synth.scaled(base, d_model=96, n_heads=6, n_kv_heads=3, head_dim=16, d_inter=160, B=2, S=37,
+                      rope_style="half", name="f32_half_rope")
     _check_prefill(api, wl)
 
 
@@ -143,6 +159,21 @@ def test_decode_bf16_small_edge_positions(api):
     wl = synth.scaled(base, d_model=256, n_heads=8, n_kv_heads=2, d_inter=384, B=6, T_max=600,
                       name="decode_bf16_d256_b6_t600")
     _run_decode(api, wl, positions=[0, 1, 300, 511, 512, 599])
+
+
+@pytest.mark.parametrize("H,G,rope", [(16, 1, "even_odd"), (8, 2, "half"), (32, 1, "half")])
+def test_decode_bf16_mqa_and_half_split_rope(api, H, G, rope):
+    base = synth.WORKLOADS["decode_gqa8b_bf16_b64_t4096"]
+    wl = synth.scaled(base, d_model=256, n_heads=H, n_kv_heads=G, d_inter=384, B=5, T_max=700, rope_style=rope,
+                      name=f"decode_bf16_h{H}_g{G}_{rope}")
+    _run_decode(api, wl, positions=[0, 130, 511, 650, 699])
+
+
+def test_decode_fp32_half_split_rope(api):
+    base = synth.WORKLOADS["tiny_f32_b1_s16"]
+    wl = synth.scaled(base, kind="decode", B=4, S=0, T_max=40, pos_lo=0, pos_hi=40, rope_style="half",
+                      name="decode_f32_half_rope")
+    _run_decode(api, wl)
 
 
 def test_decode_fp32_small(api):

@@ -20,6 +20,8 @@ MUTANTS = {
                               "return gamma * ((x - mu) / np.sqrt(var + eps) + beta)"),
     "rope_half_split": ("x_even = x[..., 0::2]\n    x_odd = x[..., 1::2]",
                         "x_even = x[..., :x.shape[-1]//2]\n    x_odd = x[..., x.shape[-1]//2:]"),
+    "rope_half_interleaved": ("    x1 = x[..., :half]\n    x2 = x[..., half:]", "    x1 = x[..., 0::2]\n    x2 = x[..., 1::2]"),
+    "rope_half_sign": ("y[..., half:] = x2 * cos + x1 * sin", "y[..., half:] = x2 * cos - x1 * sin"),
     "rope_sign": ("y[..., 0::2] = x_even * cos - x_odd * sin", "y[..., 0::2] = x_even * cos + x_odd * sin"),
     "rope_frequency": ("theta = np.power(float(base), -2.0 * i / head_dim)", "theta = np.power(float(base), -1.0 * i / head_dim)"),
     "rope_on_v": ("    v = st(v)\n", "    v = st(apply_rope(v, c, s))\n"),

@@ -207,6 +207,68 @@ def test_rope_scores_depend_only_on_offset():
         assert abs(a.item() - b.item()) < 1e-12
 
 
+def test_rope_half_pairs_coordinate_i_with_i_plus_half():
+    # "12 · 从 Transformer 到 LLaMA 系列" §八 apply_rope: a one-hot on coordinate 0 rotates into
+    # coordinate D/2 (not 1); on coordinate D/2 + 1 it rotates back into coordinate 1 with
+    # theta_1 = base^(-2/D).
+    D = 8
+    cos, sin = oracle.rope_tables(1e4, D, 5)
+    e0 = np.zeros(D)
+    e0[0] = 1
+    y = oracle.apply_rope_half(e0[None, :], cos[3:4], sin[3:4])[0]
+    assert np.allclose(y, [math.cos(3), 0, 0, 0, math.sin(3), 0, 0, 0], atol=1e-15)
+    e5 = np.zeros(D)
+    e5[5] = 1
+    a = 2 * 1e4 ** (-0.25)
+    y = oracle.apply_rope_half(e5[None, :], cos[2:3], sin[2:3])[0]
+    assert np.allclose(y, [0, -math.sin(a), 0, 0, 0, math.cos(a), 0, 0], atol=1e-15)
+
+
+def test_rope_half_is_even_odd_on_interleaved_coordinates():
+    # moving coordinate i to 2i and i + D/2 to 2i + 1 turns one pairing into the other
+    D = 64
+    cos, sin = oracle.rope_tables(1e4, D, 50)
+    x = RNG.standard_normal((50, D))
+    perm = np.empty(D, dtype=int)
+    perm[0::2] = np.arange(D // 2)
+    perm[1::2] = np.arange(D // 2) + D // 2
+    y_half = oracle.apply_rope_half(x, cos, sin)
+    y_eo = oracle.apply_rope(x[:, perm], cos, sin)
+    assert np.allclose(y_half[:, perm], y_eo, rtol=0, atol=1e-14)
+
+
+def test_rope_half_preserves_norm_and_relative_position():
+    cos, sin = oracle.rope_tables(1e4, 64, 600)
+    x = RNG.standard_normal((600, 64))
+    y = oracle.apply_rope_half(x, cos, sin)
+    assert np.allclose(np.linalg.norm(y, axis=-1), np.linalg.norm(x, axis=-1), rtol=1e-13)
+    assert np.array_equal(y[0], x[0])
+    q, k = RNG.standard_normal(64), RNG.standard_normal(64)
+    r = lambda v, m: oracle.apply_rope_half(v[None], cos[m:m + 1], sin[m:m + 1])
+    for m, n, s in ((5, 2, 100), (3, 250, 77)):
+        assert abs((r(q, m) @ r(k, n).T).item() - (r(q, m + s) @ r(k, n + s).T).item()) < 1e-12
+
+
+def test_layer_with_half_rope_equals_even_odd_layer_with_permuted_projections():
+    # permuting the rows of Wq and Wk inside each head by the interleaving map leaves every
+    # attention score, and so the layer output, unchanged
+    d, H, G, D, I = 64, 4, 2, 16, 96
+    w = _layer_w(d, H, G, D, I)
+    perm = np.empty(D, dtype=int)
+    perm[0::2] = np.arange(D // 2)
+    perm[1::2] = np.arange(D // 2) + D // 2
+    wp = dict(w)
+    wp["wq"] = w["wq"].reshape(H, D, d)[:, perm].reshape(H * D, d)
+    wp["wk"] = w["wk"].reshape(G, D, d)[:, perm].reshape(G * D, d)
+    cos, sin = oracle.rope_tables(1e4, D, 40)
+    x = RNG.standard_normal((2, 40, d))
+    kw = dict(n_heads=H, n_kv_heads=G, head_dim=D, rms_eps=1e-5)
+    out_h, k_h, _ = oracle.decoder_layer(x, w, cos, sin, rope="half", **kw)
+    out_e, k_e, _ = oracle.decoder_layer(x, wp, cos, sin, rope="even_odd", **kw)
+    assert np.allclose(out_h, out_e, rtol=1e-12, atol=1e-12)
+    assert np.allclose(k_h[..., perm], k_e, rtol=1e-12, atol=1e-12)
+
+
 # ------------------------------------------------------------------ attention
 
 def _attn_case(B, H, G, S, D, rng=RNG):
