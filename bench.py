@@ -190,6 +190,68 @@ def bench_stack(api, wl, steps, warmup, dev, pk):
     return res
 
 
+def bench_stack_decode(api, wl, steps, warmup, dev, pk):
+    """One decode step of the whole model (embedding, n_layers layers, final RMSNorm, fp32 LM
+    head) for B sequences, replayed as one CUDA graph; direct calls timed beside it."""
+    import numpy as np
+    import torch
+    from llama_decoder_block_gb300 import synth
+    L = wl.layer
+    B, T, V, d, G, D = wl.B, wl.T_max, wl.vocab, L.d_model, L.n_kv_heads, L.head_dim
+    layers = [dev_weights_random(wl, dev, wl.seed * 1000 + l) for l in range(wl.n_layers)]
+    g = torch.Generator(device=dev).manual_seed(wl.seed)
+    embed = (torch.randn(V, d, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    lm_head = (torch.randn(V, d, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    final_norm = torch.ones(d, dtype=torch.bfloat16, device=dev)
+    caches = []
+    for _ in range(wl.n_layers):
+        k = torch.empty(B, G, T, D, dtype=torch.bfloat16, device=dev).normal_(generator=g)
+        v = torch.empty(B, G, T, D, dtype=torch.bfloat16, device=dev).normal_(generator=g)
+        caches.append((k, v))
+    pos_h = synth.decode_positions(wl)
+    pos = torch.from_numpy(pos_h).to(dev)
+    tokens = torch.randint(0, V, (B,), generator=g, device=dev, dtype=torch.int32)
+    dims = api.Dims(d, L.n_heads, G, D, L.d_inter, L.rms_eps, torch.bfloat16)
+    st = api.StackArgs(dims, layers, final_norm, embed, lm_head)
+    logits = torch.empty(B, V, dtype=torch.float32, device=dev)
+    c, s = api.rope_tables(L.rope_base, D, T)
+    cos, sin = torch.from_numpy(c).to(dev), torch.from_numpy(s).to(dev)
+    ws = api.workspace(api.stack_decode_workspace_bytes(st, B), dev)
+    graph = api.StackDecodeGraph(st, tokens, pos, logits, cos, sin, caches, ws)
+
+    def timed(fn):
+        ts = []
+        for i in range(warmup + steps):   # the step streams ~36 GB, far more than L2
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            e1.synchronize()
+            if i >= warmup:
+                ts.append(e0.elapsed_time(e1))
+        return float(np.median(ts))
+
+    ms_graph = timed(graph.launch)
+    rc = api.device_status()
+    assert rc == 0, f"stack decode graph replays: status {rc} {api.timeout_record()}"
+    ms_direct = timed(lambda: api.stack_decode(st, tokens, pos, logits, cos, sin, caches, ws))
+    rc = api.device_status()
+    assert rc == 0, f"stack decode direct calls: status {rc} {api.timeout_record()}"
+    w_bytes = sum(t.numel() for w in layers for t in w.values()) * 2
+    kv_bytes = wl.n_layers * (int(np.sum(pos_h + 1)) * G * D * 2 * 2)
+    total = w_bytes + kv_bytes + V * d * 2
+    res = {"workload": wl.name, "us_per_step": round(ms_graph * 1e3, 1),
+           "us_per_step_direct_calls": round(ms_direct * 1e3, 1),
+           "tokens_per_s": round(B / (ms_graph * 1e-3), 1), "GB_per_step": round(total / 1e9, 2),
+           "GBps": round(total / (ms_graph * 1e-3) / 1e9, 1),
+           "frac_of_hbm": round(total / (ms_graph * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+           "kernels_per_step": graph.kernel_count}
+    graph.close()
+    del layers, caches, st, logits, ws, graph
+    torch.cuda.empty_cache()
+    return res
+
+
 def prefill_flops(L, B, S):
     M = B * S
     d, H, G, D, I = L.d_model, L.n_heads, L.n_kv_heads, L.head_dim, L.d_inter
@@ -626,6 +688,8 @@ def main():
         line["layernorm"] = bench_norm(api, dev, pk, "layernorm")
         line["layernorm"]["time_vs_rmsnorm"] = round(line["layernorm"]["us"] / line["rmsnorm"]["us"], 3)
         line["stack32_forward"] = bench_stack(api, synth.WORKLOADS["stack32_gqa8b_bf16_s8192_v32000"], 3, 2, dev, pk)
+        line["stack32_decode"] = bench_stack_decode(api, synth.WORKLOADS["stack32_decode_gqa8b_bf16_b64_t4096_v32000"],
+                                                    max(10, args.steps // 2), args.warmup, dev, pk)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tps, n, per = oracle_prefill_sample(wl)
         line["cpu_baseline"] = {"value": round(tps, 2), "unit": "tokens/s", "cores": cores(), "kind": "oracle",

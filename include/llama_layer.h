@@ -133,6 +133,49 @@ int llama_stack_forward(const llama_stack *stack, const int32_t *tokens, float *
                         const float *sin, int32_t max_pos, const llama_kv_cache *caches, int32_t B, int32_t S,
                         void *workspace, size_t ws_bytes, void *cuda_stream);
 
+/* Workspace bytes that llama_stack_decode needs for B sequences. */
+int llama_stack_decode_workspace_bytes(const llama_stack *stack, int32_t B, size_t *bytes);
+
+/* One autoregressive step of the whole model: the token tokens[b] of sequence b sits at
+ * position positions[b]; its K and V go to slot positions[b] of every layer's cache and it
+ * attends to slots 0..positions[b] ("第 10 章：现代 LLaMA 架构" §7 decode through every layer,
+ * then the final RMSNorm and LM head of "12 · 从 Transformer 到 LLaMA 系列" §八
+ * LlamaModel.forward).  tokens, positions: device int32 [B]; logits: device fp32 [B, vocab];
+ * caches: HOST array of n_layers caches, each [B, G, max_T, D] on the device.  Prompt
+ * lengths may differ per sequence.  A position outside a cache or max_pos, or a token
+ * outside [0, vocab), is recorded as LLAMA_ERR_DEVICE_BOUNDS.  Allocation-free and
+ * asynchronous, so it can be captured into a CUDA graph (see llama_stack_decode_graph). */
+int llama_stack_decode(const llama_stack *stack, const int32_t *tokens, const int32_t *positions, float *logits,
+                       const float *cos, const float *sin, int32_t max_pos, const llama_kv_cache *caches, int32_t B,
+                       void *workspace, size_t ws_bytes, void *cuda_stream);
+
+/* ---------------------------------------------------------------- CUDA graphs */
+
+/* A captured decode step (opaque). */
+typedef struct llama_graph llama_graph;
+
+/* Captures one llama_stack_decode call with these arguments into a CUDA graph on the current
+ * device and instantiates it.  Nothing runs: the capture records the kernels (on a private
+ * stream) and validates the arguments exactly as llama_stack_decode does.  The graph keeps
+ * the pointers, so each replay reads the tokens and positions then in those buffers and
+ * writes the logits and cache slots they name; the stack, caches array contents and tables
+ * must stay valid while the graph lives.  Creating a graph allocates the driver's graph
+ * objects (no device buffers).  Not allowed while a trace (llama_trace_begin) is active.
+ * *graph receives the handle, or NULL on error. */
+int llama_stack_decode_graph(const llama_stack *stack, const int32_t *tokens, const int32_t *positions, float *logits,
+                             const float *cos, const float *sin, int32_t max_pos, const llama_kv_cache *caches,
+                             int32_t B, void *workspace, size_t ws_bytes, llama_graph **graph);
+
+/* Replays the graph on cuda_stream (asynchronous); the current device must be the one the
+ * graph was captured on. */
+int llama_graph_launch(llama_graph *graph, void *cuda_stream);
+
+/* Number of the library's kernels in one replay. */
+int32_t llama_graph_kernel_count(const llama_graph *graph);
+
+/* Releases the graph (NULL is a no-op). */
+int llama_graph_destroy(llama_graph *graph);
+
 /* ---------------------------------------------------------------- the steps, one by one
  * The layer entry points are compositions of these; they are exported so that each
  * step can be checked and timed on its own. */
@@ -227,6 +270,12 @@ int llama_get_device_status(void *cuda_stream);
 
 /* Text of a status code (static storage). */
 const char *llama_status_string(int status);
+
+/* The record left by the first device-side wait that timed out since the library was
+ * loaded: out[0] nanoseconds waited, out[1] polls, out[2] blockIdx.x | blockIdx.y << 32,
+ * out[3] threadIdx.x, out[4] SM id, out[5] shared-memory address of the barrier | parity << 32,
+ * out[6] gridDim.x | gridDim.y << 32 (zeros if none).  Copies min(n, 7) fields; synchronous. */
+int llama_debug_timeout_record(int64_t *out, int32_t n);
 
 /* Test of the bounded-wait path: launches one CTA that waits on an mbarrier that
  * nothing arrives at, for at most budget_ns nanoseconds (capped at 10 s), with the

@@ -52,6 +52,14 @@ SIGNATURES = {
     "llama_stack_workspace_bytes": (c_int32, [P(Stack), c_int32, c_int32, P(c_size_t)]),
     "llama_stack_forward": (c_int32, [P(Stack), c_void_p, c_void_p, c_void_p, c_void_p, c_int32, P(KVCache),
                                       c_int32, c_int32, c_void_p, c_size_t, c_void_p]),
+    "llama_stack_decode_workspace_bytes": (c_int32, [P(Stack), c_int32, P(c_size_t)]),
+    "llama_stack_decode": (c_int32, [P(Stack), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int32,
+                                     P(KVCache), c_int32, c_void_p, c_size_t, c_void_p]),
+    "llama_stack_decode_graph": (c_int32, [P(Stack), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int32,
+                                           P(KVCache), c_int32, c_void_p, c_size_t, P(c_void_p)]),
+    "llama_graph_launch": (c_int32, [c_void_p, c_void_p]),
+    "llama_graph_kernel_count": (c_int32, [c_void_p]),
+    "llama_graph_destroy": (c_int32, [c_void_p]),
     "llama_rmsnorm": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_float, c_int32, c_void_p]),
     "llama_layernorm": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_float, c_int32,
                                   c_void_p]),
@@ -71,6 +79,7 @@ SIGNATURES = {
     "llama_get_device_status": (c_int32, [c_void_p]),
     "llama_status_string": (ctypes.c_char_p, [c_int32]),
     "llama_debug_wait_probe": (c_int32, [c_uint64, c_void_p]),
+    "llama_debug_timeout_record": (c_int32, [ctypes.POINTER(ctypes.c_int64), c_int32]),
     "llama_kernel_launch_count": (c_uint64, []),
     "llama_trace_begin": (c_int32, [ctypes.POINTER(c_void_p), c_int32, c_void_p]),
     "llama_trace_end": (c_int32, []),

@@ -119,6 +119,58 @@ def stack_forward(st: StackArgs, tokens, logits, cos, sin, ws, caches=None, stre
             "llama_stack_forward")
 
 
+def stack_decode_workspace_bytes(st: StackArgs, B: int) -> int:
+    n = ctypes.c_size_t()
+    N.check(N.lib().llama_stack_decode_workspace_bytes(ctypes.byref(st.s), B, ctypes.byref(n)), "workspace")
+    return n.value
+
+
+def _cache_array(caches):
+    return (N.KVCache * max(1, len(caches)))(*[cache_struct(k, v) for k, v in caches])
+
+
+def stack_decode(st: StackArgs, tokens, positions, logits, cos, sin, caches, ws, stream=None) -> None:
+    """One decode step of the stack: tokens, positions [B] int32; caches: list of (k, v)."""
+    N.check(N.lib().llama_stack_decode(ctypes.byref(st.s), _ptr(tokens), _ptr(positions), _ptr(logits), _ptr(cos),
+                                       _ptr(sin), cos.shape[0], _cache_array(caches), tokens.shape[0], _ptr(ws),
+                                       ws.numel(), _stream(stream)), "llama_stack_decode")
+
+
+class StackDecodeGraph:
+    """A decode step of the stack captured once as a CUDA graph and replayed with launch().
+
+    The graph reads the tokens and positions in the given buffers at each replay; every
+    tensor passed here must outlive the graph (this object keeps references to them).
+    """
+
+    def __init__(self, st: StackArgs, tokens, positions, logits, cos, sin, caches, ws):
+        self._keep = (st, tokens, positions, logits, cos, sin, list(caches), ws)
+        self._arr = _cache_array(caches)
+        h = ctypes.c_void_p()
+        N.check(N.lib().llama_stack_decode_graph(ctypes.byref(st.s), _ptr(tokens), _ptr(positions), _ptr(logits),
+                                                 _ptr(cos), _ptr(sin), cos.shape[0], self._arr, tokens.shape[0],
+                                                 _ptr(ws), ws.numel(), ctypes.byref(h)), "llama_stack_decode_graph")
+        self._h = h
+
+    @property
+    def kernel_count(self) -> int:
+        return N.lib().llama_graph_kernel_count(self._h)
+
+    def launch(self, stream=None) -> None:
+        N.check(N.lib().llama_graph_launch(self._h, _stream(stream)), "llama_graph_launch")
+
+    def close(self) -> None:
+        if self._h is not None and self._h.value:
+            N.lib().llama_graph_destroy(self._h)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 def rmsnorm(x, gamma, y, eps: float, stream=None) -> None:
     d = x.shape[-1]
     N.check(N.lib().llama_rmsnorm(_ptr(x), _ptr(gamma), _ptr(y), x.numel() // d, d, eps, DTYPES[x.dtype],
@@ -186,6 +238,16 @@ def device_status(stream=None) -> int:
 
 def wait_probe(budget_ns: int, stream=None) -> None:
     N.check(N.lib().llama_debug_wait_probe(budget_ns, _stream(stream)), "llama_debug_wait_probe")
+
+
+def timeout_record() -> dict:
+    """Where the first timed-out device wait gave up (all zeros if none did)."""
+    buf = (ctypes.c_int64 * 7)()
+    N.check(N.lib().llama_debug_timeout_record(buf, 7), "llama_debug_timeout_record")
+    r = list(buf)
+    return {"waited_ns": r[0], "polls": r[1], "block": (r[2] & 0xffffffff, r[2] >> 32), "thread": r[3],
+            "sm": r[4], "barrier_smem": r[5] & 0xffffffff, "parity": r[5] >> 32,
+            "grid": (r[6] & 0xffffffff, r[6] >> 32)}
 
 
 def launch_count() -> int:

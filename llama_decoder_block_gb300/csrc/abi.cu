@@ -3,6 +3,7 @@
 // norm, sublayer, add back -- twice) on top of the kernels of the other files.
 #include <algorithm>
 #include <cstring>
+#include <utility>
 
 #include "common.cuh"
 #include "internal.h"
@@ -177,54 +178,11 @@ int check_prefill_args(const llama_layer_dims* d, const llama_layer_weights* w, 
   return LLAMA_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-int llama_layer_prefill_workspace_bytes(const llama_layer_dims* dims, int32_t B, int32_t S, size_t* bytes) {
-  int rc = check_dims(dims);
-  if (rc) return rc;
-  if (bytes == nullptr || B <= 0 || S <= 0) return LLAMA_ERR_INVALID_ARG;
-  *bytes = prefill_ws(dims, B, S, nullptr, nullptr);
-  return LLAMA_OK;
-}
-
-int llama_layer_prefill(const llama_layer_dims* dims, const llama_layer_weights* w, const void* x, void* out,
-                        const float* cos, const float* sin, int32_t max_pos, llama_kv_cache cache, int32_t B,
-                        int32_t S, void* workspace, size_t ws_bytes, void* cuda_stream) {
-  int rc = check_prefill_args(dims, w, x, out, cos, sin, max_pos, cache, B, S);
-  if (rc) return rc;
-  if (!workspace || !aligned16(workspace) || ws_bytes < prefill_ws(dims, B, S, nullptr, nullptr))
-    return LLAMA_ERR_INVALID_ARG;
-  Ctx c;
-  if ((rc = make_ctx(cuda_stream, &c))) return rc;
-  return prefill_impl(c, dims, w, x, out, cos, sin, max_pos, cache, B, S, workspace);
-}
-
-int llama_layer_decode_workspace_bytes(const llama_layer_dims* dims, int32_t B, int32_t max_T, size_t* bytes) {
-  int rc = check_dims(dims);
-  if (rc) return rc;
-  if (bytes == nullptr || B <= 0 || max_T <= 0) return LLAMA_ERR_INVALID_ARG;
-  int sms = 0;
-  if (dims->dtype == LLAMA_BF16 && (rc = num_sms_current(&sms))) return rc;
-  *bytes = decode_ws(dims, B, max_T, sms, nullptr, nullptr);
-  return LLAMA_OK;
-}
-
-int llama_layer_decode(const llama_layer_dims* dims, const llama_layer_weights* w, const void* x, void* out,
-                       const float* cos, const float* sin, int32_t max_pos, const int32_t* positions,
-                       llama_kv_cache cache, int32_t B, void* workspace, size_t ws_bytes, void* cuda_stream) {
-  int rc = check_dims(dims);
-  if (rc) return rc;
-  if ((rc = check_weights(w))) return rc;
-  if (!x || !out || !cos || !sin || !positions || !cache.k || !cache.v || !workspace) return LLAMA_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(out) || !aligned16(cos) || !aligned16(sin) || !aligned16(cache.k) ||
-      !aligned16(cache.v) || !aligned16(workspace) || x == out)
-    return LLAMA_ERR_INVALID_ARG;
-  if (B <= 0 || max_pos <= 0 || cache.max_T <= 0) return LLAMA_ERR_INVALID_ARG;
-  Ctx c;
-  if ((rc = make_ctx(cuda_stream, &c))) return rc;
-  if (ws_bytes < decode_ws(dims, B, cache.max_T, c.num_sms, nullptr, nullptr)) return LLAMA_ERR_INVALID_ARG;
+// One decode step of one layer; arguments already checked, workspace laid out by decode_ws.
+int decode_impl(const Ctx& c, const llama_layer_dims* dims, const llama_layer_weights* w, const void* x, void* out,
+                const float* cos, const float* sin, int32_t max_pos, const int32_t* positions, llama_kv_cache cache,
+                int32_t B, void* workspace) {
+  int rc;
   DecodeWs p;
   decode_ws(dims, B, cache.max_T, c.num_sms, workspace, &p);
   const int dm = dims->d_model, H = dims->n_heads, G = dims->n_kv_heads, D = dims->head_dim, I = dims->d_inter;
@@ -290,6 +248,128 @@ int llama_layer_decode(const llama_layer_dims* dims, const llama_layer_weights* 
                      dm, I);
 }
 
+// Workspace of llama_stack_decode: ping-pong activations, one layer's decode workspace and
+// the LM head's split-K partials.
+struct StackDecodeWs {
+  void* xa;
+  void* xb;
+  void* layer;
+  float* part;
+};
+
+int lm_head_splits(const llama_stack* st, int B, int num_sms) {
+  if (st->dims.dtype != LLAMA_BF16 || st->vocab % 128 != 0) return 0;   // 0: not the weight-streaming form
+  return choose_splits(num_sms, st->vocab, st->dims.d_model, B);
+}
+
+size_t stack_decode_ws(const llama_stack* st, int B, int num_sms, void* base, StackDecodeWs* out) {
+  const llama_layer_dims* d = &st->dims;
+  const size_t es = esize(d->dtype);
+  Carver cv(base);
+  StackDecodeWs w;
+  w.xa = cv.take(static_cast<size_t>(B) * d->d_model * es);
+  w.xb = cv.take(static_cast<size_t>(B) * d->d_model * es);
+  w.layer = cv.take(decode_ws(d, B, 1, num_sms, nullptr, nullptr));
+  const int s = lm_head_splits(st, B, num_sms);
+  w.part = static_cast<float*>(cv.take(s > 1 ? static_cast<size_t>(s) * B * st->vocab * sizeof(float) : 0));
+  if (out) *out = w;
+  return cv.off;
+}
+
+int check_stack(const llama_stack* st) {
+  if (st == nullptr) return LLAMA_ERR_INVALID_ARG;
+  int rc = check_dims(&st->dims);
+  if (rc) return rc;
+  if (st->n_layers < 0 || st->vocab <= 0 || st->final_norm == nullptr || st->embed == nullptr ||
+      st->lm_head == nullptr || (st->n_layers > 0 && st->layers == nullptr))
+    return LLAMA_ERR_INVALID_ARG;
+  if (!aligned16(st->embed) || !aligned16(st->lm_head) || !aligned16(st->final_norm)) return LLAMA_ERR_INVALID_ARG;
+  if (st->dims.dtype == LLAMA_BF16 && st->vocab % 8 != 0) return LLAMA_ERR_UNSUPPORTED;
+  if ((st->dims.d_model * esize(st->dims.dtype)) % 16 != 0) return LLAMA_ERR_UNSUPPORTED;
+  return LLAMA_OK;
+}
+
+// One decode step of the stack; arguments already checked.
+int stack_decode_impl(const Ctx& c, const llama_stack* st, const int32_t* tokens, const int32_t* positions,
+                      float* logits, const float* cos, const float* sin, int32_t max_pos,
+                      const llama_kv_cache* caches, int32_t B, void* workspace) {
+  const llama_layer_dims* d = &st->dims;
+  const size_t es = esize(d->dtype);
+  StackDecodeWs p;
+  stack_decode_ws(st, B, c.num_sms, workspace, &p);
+  int rc;
+  if ((rc = embed_gather(c, tokens, st->embed, p.xa, B, static_cast<int>(d->d_model * es), st->vocab))) return rc;
+  void* xa = p.xa;
+  void* xb = p.xb;
+  for (int l = 0; l < st->n_layers; ++l) {
+    if ((rc = decode_impl(c, d, &st->layers[l], xa, xb, cos, sin, max_pos, positions, caches[l], B, p.layer)))
+      return rc;
+    std::swap(xa, xb);
+  }
+  // final RMSNorm, then the untied LM head in fp32
+  if ((rc = rmsnorm(c, xa, st->final_norm, xb, B, d->d_model, d->rms_eps, d->dtype))) return rc;
+  if (d->dtype != LLAMA_BF16)
+    return simt_linear(c, 0, static_cast<const float*>(xb), static_cast<const float*>(st->lm_head), nullptr, nullptr,
+                       nullptr, logits, B, st->vocab, d->d_model);
+  const int s = lm_head_splits(st, B, c.num_sms);
+  if (s == 0) return gemm_plain(c, xb, st->lm_head, logits, B, st->vocab, d->d_model, true);
+  const void* W1[1] = {st->lm_head};
+  const int R1[1] = {st->vocab};
+  if ((rc = gemm_tokens_partial(c, W1, R1, 1, xb, B, d->d_model, s, s == 1 ? logits : p.part))) return rc;
+  return s == 1 ? LLAMA_OK : fix_sum_f32(c, p.part, s, B, st->vocab, logits);
+}
+
+}  // namespace
+
+extern "C" {
+
+int llama_layer_prefill_workspace_bytes(const llama_layer_dims* dims, int32_t B, int32_t S, size_t* bytes) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if (bytes == nullptr || B <= 0 || S <= 0) return LLAMA_ERR_INVALID_ARG;
+  *bytes = prefill_ws(dims, B, S, nullptr, nullptr);
+  return LLAMA_OK;
+}
+
+int llama_layer_prefill(const llama_layer_dims* dims, const llama_layer_weights* w, const void* x, void* out,
+                        const float* cos, const float* sin, int32_t max_pos, llama_kv_cache cache, int32_t B,
+                        int32_t S, void* workspace, size_t ws_bytes, void* cuda_stream) {
+  int rc = check_prefill_args(dims, w, x, out, cos, sin, max_pos, cache, B, S);
+  if (rc) return rc;
+  if (!workspace || !aligned16(workspace) || ws_bytes < prefill_ws(dims, B, S, nullptr, nullptr))
+    return LLAMA_ERR_INVALID_ARG;
+  Ctx c;
+  if ((rc = make_ctx(cuda_stream, &c))) return rc;
+  return prefill_impl(c, dims, w, x, out, cos, sin, max_pos, cache, B, S, workspace);
+}
+
+int llama_layer_decode_workspace_bytes(const llama_layer_dims* dims, int32_t B, int32_t max_T, size_t* bytes) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if (bytes == nullptr || B <= 0 || max_T <= 0) return LLAMA_ERR_INVALID_ARG;
+  int sms = 0;
+  if (dims->dtype == LLAMA_BF16 && (rc = num_sms_current(&sms))) return rc;
+  *bytes = decode_ws(dims, B, max_T, sms, nullptr, nullptr);
+  return LLAMA_OK;
+}
+
+int llama_layer_decode(const llama_layer_dims* dims, const llama_layer_weights* w, const void* x, void* out,
+                       const float* cos, const float* sin, int32_t max_pos, const int32_t* positions,
+                       llama_kv_cache cache, int32_t B, void* workspace, size_t ws_bytes, void* cuda_stream) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if ((rc = check_weights(w))) return rc;
+  if (!x || !out || !cos || !sin || !positions || !cache.k || !cache.v || !workspace) return LLAMA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(out) || !aligned16(cos) || !aligned16(sin) || !aligned16(cache.k) ||
+      !aligned16(cache.v) || !aligned16(workspace) || x == out)
+    return LLAMA_ERR_INVALID_ARG;
+  if (B <= 0 || max_pos <= 0 || cache.max_T <= 0) return LLAMA_ERR_INVALID_ARG;
+  Ctx c;
+  if ((rc = make_ctx(cuda_stream, &c))) return rc;
+  if (ws_bytes < decode_ws(dims, B, cache.max_T, c.num_sms, nullptr, nullptr)) return LLAMA_ERR_INVALID_ARG;
+  return decode_impl(c, dims, w, x, out, cos, sin, max_pos, positions, cache, B, workspace);
+}
+
 int llama_stack_workspace_bytes(const llama_stack* st, int32_t B, int32_t S, size_t* bytes) {
   if (st == nullptr || bytes == nullptr || B <= 0 || S <= 0) return LLAMA_ERR_INVALID_ARG;
   int rc = check_dims(&st->dims);
@@ -352,6 +432,36 @@ int llama_stack_forward(const llama_stack* st, const int32_t* tokens, float* log
     return gemm_plain(c, xb, st->lm_head, logits, static_cast<int>(M), st->vocab, d->d_model, true);
   return simt_linear(c, 0, static_cast<const float*>(xb), static_cast<const float*>(st->lm_head), nullptr, nullptr,
                      nullptr, logits, static_cast<int>(M), st->vocab, d->d_model);
+}
+
+int llama_stack_decode_workspace_bytes(const llama_stack* st, int32_t B, size_t* bytes) {
+  int rc = check_stack(st);
+  if (rc) return rc;
+  if (bytes == nullptr || B <= 0) return LLAMA_ERR_INVALID_ARG;
+  int sms = 0;
+  if (st->dims.dtype == LLAMA_BF16 && (rc = num_sms_current(&sms))) return rc;
+  *bytes = stack_decode_ws(st, B, sms, nullptr, nullptr);
+  return LLAMA_OK;
+}
+
+int llama_stack_decode(const llama_stack* st, const int32_t* tokens, const int32_t* positions, float* logits,
+                       const float* cos, const float* sin, int32_t max_pos, const llama_kv_cache* caches, int32_t B,
+                       void* workspace, size_t ws_bytes, void* cuda_stream) {
+  int rc = check_stack(st);
+  if (rc) return rc;
+  if (!tokens || !positions || !logits || !cos || !sin || !workspace || B <= 0 || max_pos <= 0) return LLAMA_ERR_INVALID_ARG;
+  if (st->n_layers > 0 && caches == nullptr) return LLAMA_ERR_INVALID_ARG;
+  if (!aligned16(tokens) || !aligned16(logits) || !aligned16(workspace) || !aligned16(cos) || !aligned16(sin))
+    return LLAMA_ERR_INVALID_ARG;
+  for (int l = 0; l < st->n_layers; ++l) {
+    if ((rc = check_weights(&st->layers[l]))) return rc;
+    const llama_kv_cache& kc = caches[l];
+    if (!kc.k || !kc.v || kc.max_T <= 0 || !aligned16(kc.k) || !aligned16(kc.v)) return LLAMA_ERR_INVALID_ARG;
+  }
+  Ctx c;
+  if ((rc = make_ctx(cuda_stream, &c))) return rc;
+  if (ws_bytes < stack_decode_ws(st, B, c.num_sms, nullptr, nullptr)) return LLAMA_ERR_INVALID_ARG;
+  return stack_decode_impl(c, st, tokens, positions, logits, cos, sin, max_pos, caches, B, workspace);
 }
 
 int llama_rmsnorm(const void* x, const void* gamma, void* y, int32_t rows, int32_t d, float eps, int32_t dtype,

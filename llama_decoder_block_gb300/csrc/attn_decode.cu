@@ -436,6 +436,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
 constexpr size_t kDecSmemBytes = 1024 + 2 * STAGES * KV_TILE + 2 * Q_TILE + 2 * P_TILE + 64 * 4 +
                                  (2 * POS_CACHE + 2) * 4 + (2 * STAGES + 13) * 8 + 16;
 static_assert(kDecSmemBytes <= 232448, "decode attention exceeds the shared memory of one CTA");
+static_assert(kDecSmemBytes >= kTmemKernelMinSmem, "a TMEM-holding kernel must not share an SM with another");
 
 // out[b, h*D + d] = sum_s e^(m_s - M) O_s[d] / sum_s e^(m_s - M) l_s over the segments s of
 // (b, g = h / rep): the CTAs whose ranges meet the tiles [G pre[b] + g n_b, ... + n_b) of the

@@ -301,6 +301,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 constexpr size_t kSmemBytes = 1024 + 6 * TILE + 13 * 8 + 16;
+static_assert(kSmemBytes >= kTmemKernelMinSmem, "a TMEM-holding kernel must not share an SM with another");
 
 }  // namespace
 

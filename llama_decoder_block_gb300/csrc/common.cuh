@@ -14,6 +14,15 @@ namespace llama {
 // Budget of one bounded wait.  A healthy wait in these kernels lasts microseconds;
 // after this long the waiting thread records LLAMA_ERR_TIMEOUT and gives up.
 constexpr uint64_t kWaitBudgetNs = 1000ull * 1000ull * 1000ull;
+// 64-bit fields of the record a timed-out wait leaves after the status word
+constexpr int kTimeoutRecordFields = 7;
+
+// Kernels that hold TMEM allocate it before griddepcontrol.wait, so possibly while the
+// previous kernel of the stream still runs.  A CTA blocked in tcgen05.alloc can then only
+// be waiting for a CTA of an earlier kernel, which never waits on it, as long as no two
+// TMEM-holding CTAs fit on one SM together: each such kernel takes more than half of the
+// SM's 228 KB of shared memory (a static_assert next to each launch checks it).
+constexpr size_t kTmemKernelMinSmem = 228 * 1024 / 2 + 1;
 
 __device__ __forceinline__ void report(int* status, int code) {
   if (status != nullptr) atomicCAS(status, 0, code);
@@ -76,8 +85,22 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
         if (abort_flag != nullptr) *abort_flag = 1;
         return false;
       }
-      if (globaltimer_ns() - t0 > budget_ns) {
-        report(status, LLAMA_ERR_TIMEOUT);
+      const uint64_t now = globaltimer_ns();
+      if (now - t0 > budget_ns) {
+        if (status != nullptr && atomicCAS(status, 0, LLAMA_ERR_TIMEOUT) == 0) {
+          // the first wait to give up leaves a record of itself after the status word
+          long long* rec = reinterpret_cast<long long*>(status + 2);
+          uint32_t smid;
+          asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+          rec[0] = static_cast<long long>(now - t0);
+          rec[1] = it;
+          rec[2] = static_cast<long long>(blockIdx.x) | (static_cast<long long>(blockIdx.y) << 32);
+          rec[3] = threadIdx.x;
+          rec[4] = smid;
+          rec[5] = static_cast<long long>(bar) | (static_cast<long long>(parity) << 32);
+          rec[6] = static_cast<long long>(gridDim.x) | (static_cast<long long>(gridDim.y) << 32);
+          __threadfence();
+        }
         if (abort_flag != nullptr) *abort_flag = 1;
         return false;
       }

@@ -416,6 +416,7 @@ template <int BN, int EPI, int STAGES>
 int launch(const Ctx& c, const TMaps& tm, Params p) {
   auto kern = gemm_tc_kernel<BN, EPI, STAGES>;
   constexpr size_t smem = smem_bytes<BN, EPI, STAGES>();
+  static_assert(smem >= kTmemKernelMinSmem, "a TMEM-holding kernel must not share an SM with another");
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [&] {

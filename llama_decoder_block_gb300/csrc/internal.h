@@ -39,6 +39,8 @@ cudaError_t launch_pdl(const Ctx& c, void (*kern)(KArgs...), dim3 grid, dim3 blo
 }
 // Checks cudaGetLastError after a launch, counts it and records the next trace event.
 int after_launch(const Ctx& c);
+// True while llama_trace_begin's events are being recorded on this thread.
+bool trace_active();
 
 // ---------------------------------------------------------------- tensor maps (tmap.cu)
 // 2-D bf16 row-major matrix [rows, cols] with row stride `ld` elements; box = 64 columns
@@ -111,5 +113,7 @@ int fix_residual(const Ctx& c, const float* P, int splits, int n_tok, int N, con
 int fix_residual_rmsnorm(const Ctx& c, const float* P, int splits, int n_tok, int N, const void* resid,
                          const void* gamma, float eps, void* h_out, void* hn_out);
 int fix_swiglu(const Ctx& c, const float* P, int splits, int n_tok, int I, void* out);
+// out = the sum of the splits (fp32 [n_tok, N]); N % 4 == 0.
+int fix_sum_f32(const Ctx& c, const float* P, int splits, int n_tok, int N, float* out);
 
 }  // namespace llama

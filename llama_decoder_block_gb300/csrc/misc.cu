@@ -197,6 +197,28 @@ int fix_qkv_rope(const Ctx& c, const float* P, int splits, int n_tok, int H, int
   return after_launch(c);
 }
 
+namespace {
+
+// grid (ceil(N / 1024), n_tok): out = sum of the splits in fp32, 4 columns per thread
+__global__ void fix_sum_f32_kernel(const float* __restrict__ P, int splits, int n_tok, int N,
+                                   float* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
+  const int t = blockIdx.y;
+  const int col = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (col >= N) return;
+  const long long at = static_cast<long long>(t) * N + col;
+  *reinterpret_cast<float4*>(out + at) = split_sum4(P, splits, static_cast<long long>(n_tok) * N, at);
+}
+
+}  // namespace
+
+int fix_sum_f32(const Ctx& c, const float* P, int splits, int n_tok, int N, float* out) {
+  if (n_tok == 0) return LLAMA_OK;
+  launch_pdl(c, fix_sum_f32_kernel, dim3((N / 4 + 255) / 256, n_tok), dim3(256), 0, P, splits, n_tok, N, out);
+  return after_launch(c);
+}
+
 int fix_residual(const Ctx& c, const float* P, int splits, int n_tok, int N, const void* resid, void* out) {
   if (n_tok == 0) return LLAMA_OK;
   launch_pdl(c, fix_residual_kernel, dim3((N / 4 + 255) / 256, n_tok), dim3(256), 0,

@@ -11,7 +11,9 @@ namespace llama {
 
 // One status word per device (this is a per-device variable: each device that loads
 // the module has its own copy).  Kernels record the first error with atomicCAS(0, code).
-__device__ int g_status_word;
+// Words 2.. hold the record that the first timed-out wait leaves (see mbar_wait_slow).
+constexpr int kStatusWords = 2 + 2 * kTimeoutRecordFields;
+__device__ __align__(16) int g_status_word[kStatusWords];
 
 namespace {
 
@@ -68,6 +70,8 @@ thread_local void* const* t_events = nullptr;
 thread_local int t_n = 0;
 thread_local int t_next = 0;
 }  // namespace
+
+bool trace_active() { return t_events != nullptr; }
 
 int after_launch(const Ctx& c) {
   g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -151,6 +155,17 @@ const char* llama_status_string(int s) {
     case LLAMA_ERR_SCRATCH_LIMIT: return "request exceeds the fixed scratch of llama_attention_decode_static";
     default: return "unknown status";
   }
+}
+
+int llama_debug_timeout_record(int64_t* out, int32_t n) {
+  if (out == nullptr || n <= 0) return LLAMA_ERR_INVALID_ARG;
+  Ctx c;
+  int rc = make_ctx(nullptr, &c);
+  if (rc != LLAMA_OK) return rc;
+  long long rec[kTimeoutRecordFields];
+  if (cudaMemcpy(rec, c.status + 2, sizeof(rec), cudaMemcpyDeviceToHost) != cudaSuccess) return LLAMA_ERR_CUDA;
+  for (int i = 0; i < n && i < kTimeoutRecordFields; ++i) out[i] = rec[i];
+  return LLAMA_OK;
 }
 
 int llama_debug_wait_probe(uint64_t budget_ns, void* cuda_stream) {

@@ -74,6 +74,9 @@ WORKLOADS = {
                  T_max=4096, pos_lo=1024, pos_hi=4096),
         Workload("stack32_gqa8b_bf16_s8192_v32000", "stack", GQA_8B_LAYER_INIT, 1005, B=1,
                  S=8192, n_layers=32, vocab=32000),
+        # one decode step of that 32-layer model for the decode workload's 64 sequences
+        Workload("stack32_decode_gqa8b_bf16_b64_t4096_v32000", "decode", GQA_8B_LAYER_INIT, 1006, B=64,
+                 S=1, T_max=4096, pos_lo=1024, pos_hi=4096, n_layers=32, vocab=32000),
     )
 }
 
@@ -162,13 +165,13 @@ def decode_positions(wl: Workload) -> np.ndarray:
     return rng(wl.seed, 0, _POSITIONS).integers(wl.pos_lo, wl.pos_hi, size=wl.B).astype(np.int32)
 
 
-def decode_state(wl: Workload) -> tuple[np.ndarray, Stored, Stored]:
-    """positions ``[B]`` int32 and the pre-filled caches K, V ``[B, G, T_max, D]``."""
+def decode_state(wl: Workload, layer: int = 0) -> tuple[np.ndarray, Stored, Stored]:
+    """positions ``[B]`` int32 and layer ``layer``'s pre-filled caches K, V ``[B, G, T_max, D]``."""
     L = wl.layer
     pos = decode_positions(wl)
     shape = (wl.B, L.n_kv_heads, wl.T_max, L.head_dim)
-    k = _store(_normal(rng(wl.seed, 0, _CACHE_K), shape, 1.0, L.dtype), L.dtype)
-    v = _store(_normal(rng(wl.seed, 0, _CACHE_V), shape, 1.0, L.dtype), L.dtype)
+    k = _store(_normal(rng(wl.seed, layer, _CACHE_K), shape, 1.0, L.dtype), L.dtype)
+    v = _store(_normal(rng(wl.seed, layer, _CACHE_V), shape, 1.0, L.dtype), L.dtype)
     return pos, k, v
 
 

@@ -245,6 +245,33 @@ def stack_forward(tokens, layers, final_norm, embed, lm_head, cos, sin, *, n_hea
     return xn @ lm_head.T
 
 
+def stack_decode(tokens, positions, layers, caches, final_norm, embed, lm_head, cos, sin, *, n_heads,
+                 n_kv_heads, head_dim, rms_eps, store_bf16=False, rope="even_odd"):
+    """One autoregressive step of the whole model for B sequences.
+
+    [MOD] §7 decode (one new token per sequence at position_id = past_len,
+    its K/V appended to each layer's cache) through every layer, then the final
+    RMSNorm and the untied LM head of [T2L] §八 ``LlamaModel.forward``.
+    ``tokens``, ``positions``: ``[B]``; ``caches``: one ``(k, v)`` pair
+    ``[B, G, T, D]`` per layer, slots ``[0, positions[b])`` valid.  Returns the
+    logits ``[B, V]`` and, per layer, the new token's ``(k, v)`` ``[B, G, 1, D]``.
+    """
+    positions = np.asarray(positions, dtype=np.int64)
+    x = embed[np.asarray(tokens)][:, None, :]                              # [B, 1, d]
+    new_kv = []
+    for w, (pk, pv) in zip(layers, caches):
+        x, k, v = decoder_layer(x, w, cos, sin, n_heads=n_heads, n_kv_heads=n_kv_heads, head_dim=head_dim,
+                                rms_eps=rms_eps, past_k=pk, past_v=pv, past_len=positions,
+                                store_bf16=store_bf16, rope=rope)
+        if store_bf16:
+            x = round_bf16(x)
+        new_kv.append((k, v))
+    xn = rms_norm(x[:, 0], final_norm, rms_eps)
+    if store_bf16:
+        xn = round_bf16(xn)
+    return xn @ lm_head.T, new_kv
+
+
 def param_count(vocab, d, n_layers, n_heads, n_kv_heads, d_inter, tied=False):
     """Parameters of the model of [T2L] §八: embedding, layers, final norm, LM head.
 

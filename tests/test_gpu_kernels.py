@@ -25,6 +25,9 @@ def test_bounded_wait_gives_up_and_reports(api):
     api.wait_probe(2_000_000)           # 2 ms: the probe waits on an mbarrier nothing arrives at
     assert api.device_status() == -4    # LLAMA_ERR_TIMEOUT
     assert api.device_status() == 0     # read-and-clear
+    rec = api.timeout_record()          # the wait that gave up: the probe's one thread
+    assert 2_000_000 <= rec["waited_ns"] < 1_000_000_000 and rec["polls"] > 0
+    assert rec["thread"] == 0 and rec["block"] == (0, 0) and rec["grid"] == (1, 1)
     x = torch.ones(4, 256, dtype=torch.bfloat16, device="cuda")
     y = torch.empty_like(x)
     api.rmsnorm(x, torch.ones(256, dtype=torch.bfloat16, device="cuda"), y, 1e-5)   # the context still works

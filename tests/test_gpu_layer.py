@@ -263,6 +263,108 @@ def test_stack_fp32_tiny(api):
     _stack_case(api, wl, 2)
 
 
+def _stack_decode_setup(api, wl, positions):
+    """Device stack, per-layer caches (NaN past each position) and the oracle's inputs."""
+    L = wl.layer
+    layers_st = [synth.layer_weights(wl, l) for l in range(wl.n_layers)]
+    glob = synth.stack_globals(wl)
+    nan = NAN_BF16 if L.dtype == "bf16" else np.nan
+    pos = np.asarray(positions, dtype=np.int32)
+    caches_st = []
+    for l in range(wl.n_layers):
+        _, ks, vs = synth.decode_state(wl, l)
+        for b in range(wl.B):
+            ks.data[b, :, pos[b]:] = nan
+            vs.data[b, :, pos[b]:] = nan
+        caches_st.append((ks, vs))
+    dev_layers = [{k: to_dev(v) for k, v in st.items()} for st in layers_st]
+    st = api.StackArgs(dims_of(L), dev_layers, to_dev(glob["final_norm"]), to_dev(glob["embed"]),
+                       to_dev(glob["lm_head"]))
+    caches = [(to_dev(k), to_dev(v)) for k, v in caches_st]
+    tokens = glob["tokens"][:, 0].copy()
+    return st, caches, caches_st, layers_st, glob, tokens, pos
+
+
+def _stack_decode_reference(wl, layers_st, caches_st, glob, tokens, pos):
+    L = wl.layer
+    _, _, c64, s64 = tables(L, wl.T_max, oracle, device="cpu")
+    return oracle.stack_decode(tokens, pos, [{k: v.f64() for k, v in s.items()} for s in layers_st],
+                               [(k.f64(), v.f64()) for k, v in caches_st], glob["final_norm"].f64(),
+                               glob["embed"].f64(), glob["lm_head"].f64(), c64, s64,
+                               store_bf16=(L.dtype == "bf16"), **oracle_kw(L))
+
+
+@pytest.mark.parametrize("vocab,rope", [(512, "even_odd"), (520, "half")])
+def test_stack_decode_bf16_small(api, vocab, rope):
+    # vocab 512: the LM head streams its weights (split-K); 520: the tiled GEMM
+    base = synth.WORKLOADS["stack32_gqa8b_bf16_s8192_v32000"]
+    wl = synth.scaled(base, kind="decode", d_model=256, n_heads=4, n_kv_heads=2, d_inter=384, B=5, S=1,
+                      T_max=300, pos_lo=0, pos_hi=300, vocab=vocab, n_layers=3, gamma="noisy", rope_style=rope,
+                      name=f"stack3_decode_bf16_v{vocab}_{rope}")
+    st, caches, caches_st, layers_st, glob, tokens, pos = _stack_decode_setup(api, wl, [0, 1, 150, 257, 299])
+    L = wl.layer
+    cos, sin, _, _ = tables(L, wl.T_max, oracle)
+    logits = torch.empty(wl.B, wl.vocab, dtype=torch.float32, device="cuda")
+    ws = api.workspace(api.stack_decode_workspace_bytes(st, wl.B), "cuda")
+    api.stack_decode(st, torch.from_numpy(tokens).cuda(), torch.from_numpy(pos).cuda(), logits, cos, sin, caches, ws)
+    assert api.device_status() == 0
+    ref, new_kv = _stack_decode_reference(wl, layers_st, caches_st, glob, tokens, pos)
+    assert_close(f64(logits), ref, TOL["bf16"], "stack decode logits")
+    for l, ((kc, vc), (kn, vn)) in enumerate(zip(caches, new_kv)):
+        for b, p in enumerate(pos):
+            assert_close(f64(kc[b, :, p]), kn[b, :, 0], TOL["bf16"], f"layer {l} K slot b={b}")
+            assert_close(f64(vc[b, :, p]), vn[b, :, 0], TOL["bf16"], f"layer {l} V slot b={b}")
+            # slots past the new one stay untouched (NaN)
+            assert torch.isnan(kc[b, :, p + 1:].float()).all() and torch.isnan(vc[b, :, p + 1:].float()).all()
+
+
+def test_stack_decode_fp32_tiny(api):
+    base = synth.WORKLOADS["tiny_f32_b1_s16"]
+    wl = synth.scaled(base, kind="decode", B=3, S=1, T_max=24, pos_lo=0, pos_hi=24, vocab=96, n_layers=2,
+                      name="stack2_decode_f32")
+    st, caches, caches_st, layers_st, glob, tokens, pos = _stack_decode_setup(api, wl, [0, 9, 23])
+    cos, sin, _, _ = tables(wl.layer, wl.T_max, oracle)
+    logits = torch.empty(wl.B, wl.vocab, dtype=torch.float32, device="cuda")
+    ws = api.workspace(api.stack_decode_workspace_bytes(st, wl.B), "cuda")
+    api.stack_decode(st, torch.from_numpy(tokens).cuda(), torch.from_numpy(pos).cuda(), logits, cos, sin, caches, ws)
+    assert api.device_status() == 0
+    ref, _ = _stack_decode_reference(wl, layers_st, caches_st, glob, tokens, pos)
+    assert_close(f64(logits), ref, TOL["f32"], "fp32 stack decode logits")
+
+
+def test_stack_decode_graph_replay_matches_direct_calls(api):
+    # two consecutive decode steps (positions p, then p + 1 with new tokens written into the
+    # same buffers): the replayed graph and direct calls give identical logits and caches
+    base = synth.WORKLOADS["stack32_gqa8b_bf16_s8192_v32000"]
+    wl = synth.scaled(base, kind="decode", d_model=256, n_heads=8, n_kv_heads=2, d_inter=384, B=4, S=1,
+                      T_max=200, pos_lo=0, pos_hi=200, vocab=512, n_layers=2, name="stack2_decode_graph")
+    st, caches, _, _, _, tokens, pos = _stack_decode_setup(api, wl, [3, 50, 100, 190])
+    caches = [(k.nan_to_num(0.0), v.nan_to_num(0.0)) for k, v in caches]
+    twin = [(k.clone(), v.clone()) for k, v in caches]
+    cos, sin, _, _ = tables(wl.layer, wl.T_max, oracle)
+    tok_d = torch.from_numpy(tokens).cuda()
+    pos_d = torch.from_numpy(pos).cuda()
+    logits_g = torch.empty(wl.B, wl.vocab, dtype=torch.float32, device="cuda")
+    logits_d = torch.empty_like(logits_g)
+    ws_g = api.workspace(api.stack_decode_workspace_bytes(st, wl.B), "cuda")
+    ws_d = api.workspace(api.stack_decode_workspace_bytes(st, wl.B), "cuda")
+    graph = api.StackDecodeGraph(st, tok_d, pos_d, logits_g, cos, sin, caches, ws_g)
+    assert graph.kernel_count > 0
+    tok2 = torch.from_numpy((tokens * 7 + 3) % wl.vocab).to(torch.int32).cuda()
+    for step in range(2):
+        if step == 1:
+            tok_d.copy_(tok2)
+            pos_d.add_(1)
+        graph.launch()
+        api.stack_decode(st, tok_d, pos_d, logits_d, cos, sin, twin, ws_d)
+        torch.cuda.synchronize()
+        assert api.device_status() == 0
+        assert torch.equal(logits_g, logits_d), f"step {step}"
+        for (kg, vg), (kd, vd) in zip(caches, twin):
+            assert torch.equal(kg, kd) and torch.equal(vg, vd)
+    graph.close()
+
+
 def _layer_stream(wl, on_layer=None, window=6):
     """Yields each layer's fp64 weights in order, drawn by a pool of spawned processes
     (a bounded number ahead); `on_layer` also receives the storage-format weights."""

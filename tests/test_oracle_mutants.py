@@ -37,6 +37,9 @@ MUTANTS = {
     "shared_norm_gamma": ("hn = st(rms_norm(h, w[\"ffn_norm\"], rms_eps))",
                           "hn = st(rms_norm(h, w[\"attn_norm\"], rms_eps))"),
     "no_final_norm": ("xn = rms_norm(x, final_norm, rms_eps)", "xn = x"),
+    "stack_decode_no_final_norm": ("xn = rms_norm(x[:, 0], final_norm, rms_eps)", "xn = x[:, 0]"),
+    "stack_decode_cache_of_wrong_layer": ("for w, (pk, pv) in zip(layers, caches):",
+                                          "for w, (pk, pv) in zip(layers, caches[::-1]):"),
     "decode_positions_restart": ("pos = past_len[:, None] + np.arange(S)[None, :]",
                                  "pos = np.zeros_like(past_len)[:, None] + np.arange(S)[None, :]"),
 }

@@ -487,6 +487,41 @@ def test_stack_brute_force_against_torch_statement():
     assert np.allclose(ours, ref.numpy(), rtol=1e-12, atol=1e-12)
 
 
+@pytest.mark.parametrize("store_bf16", [False, True])
+def test_stack_decode_equals_full_forward_last_row(store_bf16):
+    # "第 10 章：现代 LLaMA 架构" §7, the KV-cache check: the logits of full_forward(prompt +
+    # next_token) at the last position equal those of prefill(prompt) followed by
+    # decode_one(next_token, past_kv).  Prompt lengths differ per sequence.
+    rng = np.random.default_rng(21)
+    V, d, H, G, D, I, S, n = 40, 32, 4, 2, 8, 48, 12, 3
+    layers = [_layer_w(d, H, G, D, I, std=0.2, rng=rng) for _ in range(n)]
+    embed = 0.5 * rng.standard_normal((V, d))
+    lm = 0.2 * rng.standard_normal((V, d))
+    fn = 1 + 0.1 * rng.standard_normal(d)
+    tokens = rng.integers(0, V, size=(3, S))
+    cos, sin = oracle.rope_tables(1e4, D, 16)
+    kw = dict(n_heads=H, n_kv_heads=G, head_dim=D, rms_eps=1e-5, store_bf16=store_bf16)
+    full = oracle.stack_forward(tokens, layers, fn, embed, lm, cos, sin, **kw)
+    # prefill: every layer's K/V of the whole prompt; slots at or past each prompt's end are NaN
+    t = np.array([5, 11, 0])
+    caches, x = [], embed[tokens]
+    for w in layers:
+        x, k, v = oracle.decoder_layer(x, w, cos, sin, **kw)
+        if store_bf16:
+            x = oracle.round_bf16(x)
+        k, v = k.copy(), v.copy()
+        for b in range(3):
+            k[b, :, t[b]:] = np.nan
+            v[b, :, t[b]:] = np.nan
+        caches.append((k, v))
+    logits, new_kv = oracle.stack_decode(tokens[np.arange(3), t], t, layers, caches, fn, embed, lm, cos, sin, **kw)
+    assert np.allclose(logits, full[np.arange(3), t], rtol=0, atol=1e-11)
+    assert np.all(np.isfinite(logits))
+    # the new token's K of the first layer is the prefill's K at that slot
+    _, kf, _ = oracle.decoder_layer(embed[tokens], layers[0], cos, sin, **kw)
+    assert np.allclose(new_kv[0][0][:, :, 0], kf[np.arange(3), :, t], rtol=0, atol=1e-12)
+
+
 def test_synth_recipe_is_deterministic_and_shaped():
     wl = synth.WORKLOADS["tiny_f32_b1_s16"]
     a = synth.layer_weights(wl)
