@@ -108,6 +108,21 @@ int llama_layer_prefill(const llama_layer_dims *dims, const llama_layer_weights 
                         const float *cos, const float *sin, int32_t max_pos, llama_kv_cache cache, int32_t B,
                         int32_t S, void *workspace, size_t ws_bytes, void *cuda_stream);
 
+/* Prefill of a chunk on top of what the cache already holds ("第 10 章：现代 LLaMA 架构" §7:
+ * past_kv with position_ids = past_len + arange(T); §3 position_id = past_len): token s of
+ * sequence b sits at position start[b] + s, its rotated K and its V go to cache slot
+ * start[b] + s, and it attends to slots 0 .. start[b] + s (the cached ones as they are).
+ * start: device int32 [B], required; lengths: device int32 [B] or NULL (all S): sequence b
+ * brings lengths[b] <= S tokens and rows s >= lengths[b] of x are padding -- nothing of them
+ * is stored in the cache and their rows of out are unspecified.  A sequence with start[b] < 0,
+ * lengths[b] outside [0, S] or start[b] + lengths[b] beyond cache.max_T or max_pos is
+ * recorded as LLAMA_ERR_DEVICE_BOUNDS and skipped.  Same workspace as llama_layer_prefill
+ * (llama_layer_prefill_workspace_bytes(dims, B, S)). */
+int llama_layer_prefill_chunk(const llama_layer_dims *dims, const llama_layer_weights *w, const void *x, void *out,
+                              const float *cos, const float *sin, int32_t max_pos, const int32_t *start,
+                              const int32_t *lengths, llama_kv_cache cache, int32_t B, int32_t S, void *workspace,
+                              size_t ws_bytes, void *cuda_stream);
+
 /* Workspace bytes that llama_layer_decode needs for B sequences and caches of max_T slots. */
 int llama_layer_decode_workspace_bytes(const llama_layer_dims *dims, int32_t B, int32_t max_T, size_t *bytes);
 

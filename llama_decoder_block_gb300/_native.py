@@ -46,6 +46,9 @@ SIGNATURES = {
     "llama_layer_prefill_workspace_bytes": (c_int32, [P(LayerDims), c_int32, c_int32, P(c_size_t)]),
     "llama_layer_prefill": (c_int32, [P(LayerDims), P(LayerWeights), c_void_p, c_void_p, c_void_p, c_void_p,
                                       c_int32, KVCache, c_int32, c_int32, c_void_p, c_size_t, c_void_p]),
+    "llama_layer_prefill_chunk": (c_int32, [P(LayerDims), P(LayerWeights), c_void_p, c_void_p, c_void_p, c_void_p,
+                                            c_int32, c_void_p, c_void_p, KVCache, c_int32, c_int32, c_void_p,
+                                            c_size_t, c_void_p]),
     "llama_layer_decode_workspace_bytes": (c_int32, [P(LayerDims), c_int32, c_int32, P(c_size_t)]),
     "llama_layer_decode": (c_int32, [P(LayerDims), P(LayerWeights), c_void_p, c_void_p, c_void_p, c_void_p, c_int32,
                                      c_void_p, KVCache, c_int32, c_void_p, c_size_t, c_void_p]),

@@ -86,6 +86,19 @@ def layer_prefill(dims: Dims, w: dict, x, out, cos, sin, cache_k, cache_v, ws, s
                                         _stream(stream)), "llama_layer_prefill")
 
 
+def layer_prefill_chunk(dims: Dims, w: dict, x, out, cos, sin, start, cache_k, cache_v, ws, lengths=None,
+                        stream=None) -> None:
+    """A chunk of S tokens per sequence on top of the cache: token s of sequence b at position
+    start[b] + s (start, lengths: device int32 [B]; lengths None = all S)."""
+    B, S = x.shape[0], x.shape[1]
+    d = dims.c()
+    ww = weights_struct(w)
+    N.check(N.lib().llama_layer_prefill_chunk(ctypes.byref(d), ctypes.byref(ww), _ptr(x), _ptr(out), _ptr(cos),
+                                              _ptr(sin), cos.shape[0], _ptr(start), _ptr(lengths),
+                                              cache_struct(cache_k, cache_v), B, S, _ptr(ws), ws.numel(),
+                                              _stream(stream)), "llama_layer_prefill_chunk")
+
+
 def layer_decode(dims: Dims, w: dict, x, out, cos, sin, positions, cache_k, cache_v, ws, stream=None) -> None:
     d = dims.c()
     ww = weights_struct(w)

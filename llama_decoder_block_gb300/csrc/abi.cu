@@ -122,8 +122,10 @@ int num_sms_current(int* sms) {
   return LLAMA_OK;
 }
 
+// start, lens: null (a prompt from position 0) or device [B] (a chunk on top of the cache).
 int prefill_impl(const Ctx& c, const llama_layer_dims* d, const llama_layer_weights* w, const void* x, void* out,
-                 const float* cos, const float* sin, int max_pos, llama_kv_cache cache, int B, int S, void* ws) {
+                 const float* cos, const float* sin, int max_pos, llama_kv_cache cache, int B, int S, void* ws,
+                 const int32_t* start = nullptr, const int32_t* lens = nullptr) {
   PrefillWs p;
   prefill_ws(d, B, S, ws, &p);
   const int M = B * S, dm = d->d_model, H = d->n_heads, G = d->n_kv_heads, D = d->head_dim, I = d->d_inter;
@@ -131,9 +133,10 @@ int prefill_impl(const Ctx& c, const llama_layer_dims* d, const llama_layer_weig
   if (d->dtype == LLAMA_BF16) {
     if ((rc = rmsnorm(c, x, w->attn_norm, p.xn, M, dm, d->rms_eps, d->dtype))) return rc;
     if ((rc = gemm_qkv_rope(c, p.xn, w->wq, w->wk, w->wv, B, S, dm, H, G, D, cos, sin, p.q, cache.k, cache.v,
-                            cache.max_T, d->rope_style)))
+                            cache.max_T, d->rope_style, start, lens, max_pos)))
       return rc;
-    if ((rc = attn_prefill_tc(c, p.q, cache.k, cache.v, p.o, B, S, H, G, D, cache.max_T))) return rc;
+    if ((rc = attn_prefill_tc(c, p.q, cache.k, cache.v, p.o, B, S, H, G, D, cache.max_T, start, lens, max_pos)))
+      return rc;
     if ((rc = gemm_residual(c, p.o, w->wo, x, p.h, M, dm, H * D))) return rc;
     if ((rc = rmsnorm(c, p.h, w->ffn_norm, p.xn, M, dm, d->rms_eps, d->dtype))) return rc;
     if ((rc = gemm_swiglu(c, p.xn, w->w_gate, w->w_up, p.a, M, I, dm))) return rc;
@@ -145,12 +148,12 @@ int prefill_impl(const Ctx& c, const llama_layer_dims* d, const llama_layer_weig
   float* a = static_cast<float*>(p.a);
   if ((rc = rmsnorm(c, x, w->attn_norm, p.xn, M, dm, d->rms_eps, d->dtype))) return rc;
   if ((rc = simt_qkv_rope(c, xn, static_cast<const float*>(w->wq), static_cast<const float*>(w->wk),
-                          static_cast<const float*>(w->wv), B, S, dm, H, G, D, cos, sin, nullptr, max_pos,
+                          static_cast<const float*>(w->wv), B, S, dm, H, G, D, cos, sin, start, max_pos,
                           static_cast<float*>(p.q), static_cast<float*>(cache.k), static_cast<float*>(cache.v),
-                          cache.max_T, d->rope_style)))
+                          cache.max_T, d->rope_style, lens)))
     return rc;
   if ((rc = simt_attention(c, static_cast<float*>(p.q), static_cast<float*>(cache.k), static_cast<float*>(cache.v),
-                           nullptr, static_cast<float*>(p.o), B, S, H, G, D, cache.max_T, max_pos)))
+                           start, static_cast<float*>(p.o), B, S, H, G, D, cache.max_T, max_pos, lens)))
     return rc;
   if ((rc = simt_linear(c, 1, static_cast<float*>(p.o), static_cast<const float*>(w->wo), nullptr, nullptr, xf, h, M,
                         dm, H * D)))
@@ -341,6 +344,20 @@ int llama_layer_prefill(const llama_layer_dims* dims, const llama_layer_weights*
   Ctx c;
   if ((rc = make_ctx(cuda_stream, &c))) return rc;
   return prefill_impl(c, dims, w, x, out, cos, sin, max_pos, cache, B, S, workspace);
+}
+
+int llama_layer_prefill_chunk(const llama_layer_dims* dims, const llama_layer_weights* w, const void* x, void* out,
+                              const float* cos, const float* sin, int32_t max_pos, const int32_t* start,
+                              const int32_t* lengths, llama_kv_cache cache, int32_t B, int32_t S, void* workspace,
+                              size_t ws_bytes, void* cuda_stream) {
+  int rc = check_prefill_args(dims, w, x, out, cos, sin, max_pos, cache, B, S);
+  if (rc) return rc;
+  if (start == nullptr) return LLAMA_ERR_INVALID_ARG;
+  if (!workspace || !aligned16(workspace) || ws_bytes < prefill_ws(dims, B, S, nullptr, nullptr))
+    return LLAMA_ERR_INVALID_ARG;
+  Ctx c;
+  if ((rc = make_ctx(cuda_stream, &c))) return rc;
+  return prefill_impl(c, dims, w, x, out, cos, sin, max_pos, cache, B, S, workspace, start, lengths);
 }
 
 int llama_layer_decode_workspace_bytes(const llama_layer_dims* dims, int32_t B, int32_t max_T, size_t* bytes) {

@@ -19,6 +19,14 @@
 //               TMEM; O is rescaled only when the running max grows by more than 2^8
 //               (the final O / l uses the same reference max, so the result is exact)
 // fp32 statistics and accumulators; D = 128.
+//
+// A chunk on top of a cache ("第 10 章：现代 LLaMA 架构" §7, past_kv with position_ids =
+// past_len + arange(T)): query s of sequence b sits at position start[b] + s and sees cache
+// slots 0 .. start[b] + s, so a query tile reads the key tiles up to its last query's
+// position and masks the ones its first query does not fully see.  Queries s >= lens[b]
+// pad the chunk: they are computed but not stored, and the V rows of keys at or past
+// start[b] + lens[b] are zeroed in shared memory before P V (stale cache slots may hold
+// anything; 0 * NaN would leak into valid rows).
 #include <mutex>
 
 #include "common.cuh"
@@ -38,6 +46,9 @@ constexpr float kRescaleLog2 = 8.0f;  // rescale O when the max grows by more th
 
 struct AttnParams {
   int B, S, H, G, n_qt, n_pairs;
+  const int32_t* start;               // [B] or null (0)
+  const int32_t* lens;                // [B] or null (S)
+  int T_max, max_pos;
   float scale_log2;                   // log2(e) / sqrt(D)
   __nv_bfloat16* out;                 // [B, S, H*D]
   int* status;
@@ -68,8 +79,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int h = blockIdx.y, b = blockIdx.z;
   const int g = h / (p.H / p.G);
   const int qb[2] = {2 * pair, 2 * pair + 1};
-  const bool hasB = qb[1] < p.n_qt;
-  const int nt = hasB ? qb[1] + 1 : qb[0] + 1;   // key tiles 0 .. last diagonal
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(q_full), 1);
@@ -99,7 +108,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
   pdl_wait();   // inputs written by the previous kernel are read from here on
 
-  if (warp == 0) {
+  // this sequence's chunk: queries [0, len) at positions pos0 + s; keys [0, pos0 + len)
+  int pos0 = 0, len = p.S;
+  if (p.start != nullptr) {
+    pos0 = p.start[b];
+    len = p.lens != nullptr ? p.lens[b] : p.S;
+    if (pos0 < 0 || len < 0 || len > p.S || pos0 + len > p.T_max || pos0 + len > p.max_pos) {
+      if (threadIdx.x == 0 && blockIdx.x == 0 && h == 0) report(p.status, LLAMA_ERR_DEVICE_BOUNDS);
+      len = 0;
+    }
+  }
+  const bool hasA = qb[0] * BQ < len, hasB = qb[1] * BQ < len;
+  // key tiles that tile t reads: up to the position of its last query
+  const int nkt[2] = {hasA ? (pos0 + min(qb[0] * BQ + BQ, len) - 1) / BKV + 1 : 0,
+                      hasB ? (pos0 + min(qb[1] * BQ + BQ, len) - 1) / BKV + 1 : 0};
+  const int nt = hasB ? nkt[1] : nkt[0];
+  const int n_valid = pos0 + len;
+
+  if (!hasA) {
+    // nothing of this sequence falls into these query tiles
+  } else if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ TMA producer
       bool ok = true;
@@ -134,7 +162,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // ------------------------------------------------------------ MMA issuer
       constexpr uint32_t IDESC_QK = idesc_bf16(128, 128, false);
       constexpr uint32_t IDESC_PV = idesc_bf16(128, 128, true);
-      auto active = [&](int t, int j) { return (t == 0 || hasB) && j <= qb[t]; };
+      auto active = [&](int t, int j) { return j < nkt[t]; };
       auto issue_s = [&](int t, int j) {
         const uint32_t aq = smem_u32(sQ + t * TILE), bk = smem_u32(sK + (j & 1) * TILE);
 #pragma unroll
@@ -201,12 +229,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       float m_run = -INFINITY, l_run = 0.f;
       uint32_t r[64];
       bool ok = true;
-      const int n_t = qb[t] + 1;
+      const int n_t = nkt[t];
+      const int qpos = pos0 + qi;                     // this row's position: keys 0 .. qpos
       for (int j = 0; j < n_t; ++j) {
         if (!mbar_wait(smem_u32(s_full + t), j & 1, p.status, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        const bool diag = (j == qb[t]);
         const int kbase = j * BKV;
+        // the tile reaches past the first query's position: mask key > position
+        const bool diag = kbase + BKV - 1 > pos0 + qb[t] * BQ;
         float mx = -INFINITY;
 #pragma unroll 1
         for (int hlf = 0; hlf < 2; ++hlf) {
@@ -215,7 +245,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int i = 0; i < 64; ++i) {
             float s = __uint_as_float(r[i]);
             const int key = kbase + hlf * 64 + i;
-            if (diag && (key > qi || key >= p.S)) s = -INFINITY;
+            if (diag && key > qpos) s = -INFINITY;
             mx = fmaxf(mx, s);
           }
         }
@@ -251,8 +281,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             float p0 = ex2_approx(fmaf(__uint_as_float(r[2 * i]), sl, -m_run));
             float p1 = ex2_approx(fmaf(__uint_as_float(r[2 * i + 1]), sl, -m_run));
             if (diag) {
-              if (key > qi || key >= p.S) p0 = 0.f;
-              if (key + 1 > qi || key + 1 >= p.S) p1 = 0.f;
+              if (key > qpos) p0 = 0.f;
+              if (key + 1 > qpos) p1 = 0.f;
             }
             rowsum += p0 + p1;
             pk[i] = pack_bf16(p0, p1);
@@ -261,6 +291,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_st32(tS + hlf * 32, pk);
         }
         l_run += rowsum;
+        // keys at or past the last valid one: zero their V rows before any P V of this tile
+        // (done by tile 0 if it reads this tile, else by tile 1; the MMA issuer orders tile
+        // 1's product after tile 0's P)
+        if (kbase + BKV > n_valid && (t == 0 || j >= nkt[0]) && kbase + row >= n_valid) {
+          uint8_t* vrow = sV + (j & 1) * TILE + row * 128;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            reinterpret_cast<uint4*>(vrow)[u] = make_uint4(0, 0, 0, 0);
+            reinterpret_cast<uint4*>(vrow + CHUNK)[u] = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(p_full + t));
@@ -274,7 +316,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           tmem_ld32(tO + c * 32, o32);
-          if (qi < p.S) {
+          if (qi < len) {
             uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -306,13 +348,17 @@ static_assert(kSmemBytes >= kTmemKernelMinSmem, "a TMEM-holding kernel must not 
 }  // namespace
 
 int attn_prefill_tc(const Ctx& c, const void* q, const void* k_cache, const void* v_cache, void* out, int B, int S,
-                    int H, int G, int D, int T_max) {
+                    int H, int G, int D, int T_max, const int32_t* start, const int32_t* lens, int max_pos) {
   if (D != HD) return LLAMA_ERR_UNSUPPORTED;
   CUtensorMap tq, tk, tv;
-  // Q [B*H][S][D]; K, V: valid slots [0, S) of [B*G][T_max][D] (rows >= S read as 0)
+  // Q [B*H][S][D]; K, V: [B*G][T_max][D] with the slots a chunk can reach as the extent:
+  // [0, S) from position 0 (rows >= S read as 0), the whole cache on top of one
+  const uint64_t kv_rows = start != nullptr ? static_cast<uint64_t>(T_max) : static_cast<uint64_t>(S);
   if (!make_tmap_3d(&tq, q, HD, S, static_cast<uint64_t>(B) * H, HD, static_cast<uint64_t>(S) * HD, BQ) ||
-      !make_tmap_3d(&tk, k_cache, HD, S, static_cast<uint64_t>(B) * G, HD, static_cast<uint64_t>(T_max) * HD, BKV) ||
-      !make_tmap_3d(&tv, v_cache, HD, S, static_cast<uint64_t>(B) * G, HD, static_cast<uint64_t>(T_max) * HD, BKV))
+      !make_tmap_3d(&tk, k_cache, HD, kv_rows, static_cast<uint64_t>(B) * G, HD, static_cast<uint64_t>(T_max) * HD,
+                    BKV) ||
+      !make_tmap_3d(&tv, v_cache, HD, kv_rows, static_cast<uint64_t>(B) * G, HD, static_cast<uint64_t>(T_max) * HD,
+                    BKV))
     return LLAMA_ERR_INVALID_ARG;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
@@ -328,6 +374,10 @@ int attn_prefill_tc(const Ctx& c, const void* q, const void* k_cache, const void
   p.G = G;
   p.n_qt = (S + BQ - 1) / BQ;
   p.n_pairs = (p.n_qt + 1) / 2;
+  p.start = start;
+  p.lens = lens;
+  p.T_max = T_max;
+  p.max_pos = max_pos;
   p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
   p.out = static_cast<__nv_bfloat16*>(out);
   p.status = c.status;

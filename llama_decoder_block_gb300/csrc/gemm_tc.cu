@@ -53,6 +53,9 @@ struct Params {
   const float* sin;
   int S, H, G, D, T_max;
   int rope_half;                // pairs (i, i + D/2) instead of (2i, 2i+1)
+  const int32_t* start;         // [B] cached length before this chunk (null: 0)
+  const int32_t* lens;          // [B] valid tokens of the chunk (null: S)
+  int max_pos;
   __nv_bfloat16* q_out;
   __nv_bfloat16* k_cache;
   __nv_bfloat16* v_cache;
@@ -314,8 +317,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
       } else if constexpr (EPI == EPI_QKV) {
-        // each 128-column half of the tile is one head of [q heads | k heads | v heads]
-        const int b = m / p.S, s = m - (m / p.S) * p.S;
+        // each 128-column half of the tile is one head of [q heads | k heads | v heads];
+        // token s of sequence b sits at position start[b] + s, and only tokens s < lens[b]
+        // are stored (the others pad the chunk)
+        const int b = m / p.S, s_in = m - (m / p.S) * p.S;
+        int s = s_in;
+        bool keep = m < p.M;
+        if (keep && p.start != nullptr) {
+          const int st = p.start[b], len = p.lens != nullptr ? p.lens[b] : p.S;
+          if (st < 0 || len < 0 || len > p.S || st + len > p.T_max || st + len > p.max_pos) {
+            if (s_in == 0) report(p.status, LLAMA_ERR_DEVICE_BOUNDS);
+            keep = false;
+          }
+          keep = keep && s_in < len;
+          s = st + s_in;
+        }
         const int half_d = p.D >> 1;
 #pragma unroll 1
         for (int hf = 0; hf < 2; ++hf) {
@@ -324,14 +340,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (p.rope_half && hh < p.H + p.G) {
             // half-split pairs: columns 32c + i and 64 + 32c + i, angle index 32c + i
             __nv_bfloat16* dst = hh < p.H
-                ? p.q_out + ((static_cast<long long>(b) * p.H + hh) * p.S + s) * p.D
+                ? p.q_out + ((static_cast<long long>(b) * p.H + hh) * p.S + s_in) * p.D
                 : p.k_cache + ((static_cast<long long>(b) * p.G + (hh - p.H)) * p.T_max + s) * p.D;
 #pragma unroll 1
             for (int c = 0; c < 2; ++c) {
               uint32_t r2[32];
               tmem_ld32(t_acc + hf * 128 + c * 32, r);
               tmem_ld32(t_acc + hf * 128 + 64 + c * 32, r2);
-              if (m >= p.M) continue;
+              if (!keep) continue;
               const float* cr = p.cos + static_cast<long long>(s) * half_d + c * 32;
               const float* sr = p.sin + static_cast<long long>(s) * half_d + c * 32;
               float w2[32];
@@ -350,7 +366,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             tmem_ld32(t_acc + hf * 128 + c * 32, r);
-            if (m >= p.M) continue;
+            if (!keep) continue;
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
             __nv_bfloat16* dst;
@@ -367,7 +383,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               }
             }
             if (hh < p.H)
-              dst = p.q_out + ((static_cast<long long>(b) * p.H + hh) * p.S + s) * p.D;
+              dst = p.q_out + ((static_cast<long long>(b) * p.H + hh) * p.S + s_in) * p.D;
             else if (hh < p.H + p.G)
               dst = p.k_cache + ((static_cast<long long>(b) * p.G + (hh - p.H)) * p.T_max + s) * p.D;
             else
@@ -501,7 +517,8 @@ int gemm_swiglu(const Ctx& c, const void* X, const void* Wg, const void* Wu, voi
 
 int gemm_qkv_rope(const Ctx& c, const void* X, const void* Wq, const void* Wk, const void* Wv, int B, int S, int K,
                   int H, int G, int D, const float* cos, const float* sin, void* q_out, void* k_cache,
-                  void* v_cache, int T_max, int rope_half) {
+                  void* v_cache, int T_max, int rope_half, const int32_t* start, const int32_t* lens,
+                  int max_pos) {
   const int M = B * S;
   TMaps tm{};
   if (!make_tmap_2d(&tm.m[0], X, K, M, K, 128) || !make_tmap_2d(&tm.m[1], Wq, K, H * D, K, 128) ||
@@ -522,6 +539,9 @@ int gemm_qkv_rope(const Ctx& c, const void* X, const void* Wq, const void* Wk, c
   p.D = D;
   p.T_max = T_max;
   p.rope_half = rope_half;
+  p.start = start;
+  p.lens = lens;
+  p.max_pos = max_pos;
   p.q_out = static_cast<__nv_bfloat16*>(q_out);
   p.k_cache = static_cast<__nv_bfloat16*>(k_cache);
   p.v_cache = static_cast<__nv_bfloat16*>(v_cache);

@@ -69,10 +69,13 @@ int gemm_residual(const Ctx& c, const void* X, const void* W, const void* resid,
 int gemm_swiglu(const Ctx& c, const void* X, const void* Wg, const void* Wu, void* out, int M, int I, int K);
 // [q|k|v] = X [Wq;Wk;Wv]^T for B sequences of S tokens at positions 0..S-1; RoPE on q, k;
 // q -> q_out [B, H, S, D]; k, v -> cache slots [0, S) of [B, G, T_max, D].
-// rope_half: pairs (i, i + D/2) instead of (2i, 2i+1).
+// rope_half: pairs (i, i + D/2) instead of (2i, 2i+1).  start (device [B], may be null):
+// token s of sequence b sits at position start[b] + s and goes to that cache slot; lens
+// (device [B], may be null = S): tokens s >= lens[b] are padding and stored nowhere.
 int gemm_qkv_rope(const Ctx& c, const void* X, const void* Wq, const void* Wk, const void* Wv, int B, int S,
                   int K, int H, int G, int D, const float* cos, const float* sin, void* q_out, void* k_cache,
-                  void* v_cache, int T_max, int rope_half);
+                  void* v_cache, int T_max, int rope_half, const int32_t* start = nullptr,
+                  const int32_t* lens = nullptr, int max_pos = 0);
 // Weight-streaming form for few tokens: P[s][t][n] = sum over split s of W[n, k] X[t, k] in fp32,
 // with W the row-concatenation of up to three matrices (rows multiples of 128).
 int gemm_tokens_partial(const Ctx& c, const void* const* W, const int* w_rows, int n_w, const void* X,
@@ -81,8 +84,11 @@ int gemm_tokens_partial(const Ctx& c, const void* const* W, const int* w_rows, i
 int choose_splits(int num_sms, int w_rows_total, int K, int n_tok);
 
 // ---------------------------------------------------------------- attention
+// start / lens as for gemm_qkv_rope: query s of sequence b at position start[b] + s sees
+// cache slots 0 .. start[b] + s; output rows s >= lens[b] are not written.
 int attn_prefill_tc(const Ctx& c, const void* q, const void* k_cache, const void* v_cache, void* out, int B,
-                    int S, int H, int G, int D, int T_max);
+                    int S, int H, int G, int D, int T_max, const int32_t* start = nullptr,
+                    const int32_t* lens = nullptr, int max_pos = 0);
 size_t attn_decode_ws_bytes(int B, int H, int G, int D);
 int attn_decode(const Ctx& c, int dtype, const void* q, const void* k_cache, const void* v_cache,
                 const int32_t* positions, void* out, int B, int H, int G, int D, int T_max, int max_pos,
@@ -90,15 +96,17 @@ int attn_decode(const Ctx& c, int dtype, const void* q, const void* k_cache, con
 
 // ---------------------------------------------------------------- fp32 SIMT path (simt_f32.cu)
 // mode 0: C = X W^T; 1: out = resid + X W^T; 2: out = SiLU(X Wg^T) * (X Wu^T);
-// 3: QKV + RoPE scatter (positions: null -> token m of sequence b at m % S, else positions[b]).
+// 3: QKV + RoPE scatter (positions: null -> token m of sequence b at m % S, else
+// positions[b] + m % S; lens: null, or tokens m % S >= lens[b] are padding and stored nowhere).
 int simt_linear(const Ctx& c, int mode, const float* X, const float* W0, const float* W1, const float* W2,
                 const float* resid, float* out, int M, int N, int K);
 int simt_qkv_rope(const Ctx& c, const float* X, const float* Wq, const float* Wk, const float* Wv, int B, int S,
                   int K, int H, int G, int D, const float* cos, const float* sin, const int32_t* positions,
-                  int max_pos, float* q_out, float* k_cache, float* v_cache, int T_max, int rope_half);
+                  int max_pos, float* q_out, float* k_cache, float* v_cache, int T_max, int rope_half,
+                  const int32_t* lens = nullptr);
 int simt_attention(const Ctx& c, const float* q, const float* k_cache, const float* v_cache,
                    const int32_t* positions, float* out, int B, int S, int H, int G, int D, int T_max,
-                   int max_pos);
+                   int max_pos, const int32_t* lens = nullptr);
 
 // ---------------------------------------------------------------- small kernels (misc.cu)
 // rows of `row_bytes` bytes (a multiple of 16) of any element type

@@ -36,13 +36,18 @@ __global__ void simt_qkv_kernel(const float* __restrict__ X, const float* __rest
                                 int H, int G, int D, const float* __restrict__ cos, const float* __restrict__ sin,
                                 const int32_t* __restrict__ positions, int max_pos, float* __restrict__ q_out,
                                 float* __restrict__ k_cache, float* __restrict__ v_cache, int T_max, int rope_half,
-                                int* status) {
+                                const int32_t* __restrict__ lens, int* status) {
   const int pairs = (H + 2 * G) * D / 2;
   const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= static_cast<long long>(B) * S * pairs) return;
   const int m = static_cast<int>(idx / pairs);
   const int col = static_cast<int>(idx % pairs) * 2;
   const int b = m / S, s = m % S;
+  if (lens != nullptr && (lens[b] < 0 || lens[b] > S)) {
+    report(status, LLAMA_ERR_DEVICE_BOUNDS);
+    return;
+  }
+  if (lens != nullptr && s >= lens[b]) return;   // padding of a shorter sequence: stored nowhere
   const int pos = positions ? positions[b] + s : s;
   if (pos < 0 || pos >= max_pos || pos >= T_max) {
     report(status, LLAMA_ERR_DEVICE_BOUNDS);
@@ -77,11 +82,12 @@ __global__ void simt_qkv_kernel(const float* __restrict__ X, const float* __rest
   dst[j1] = o;
 }
 
-// One warp per (b, h, s): online softmax over keys 0..pos of KV head h / (H/G).
+// One warp per (b, h, s): online softmax over keys 0..pos of KV head h / (H/G).  Rows
+// s >= lens[b] (padding) are not computed and not written.
 __global__ void simt_attention_kernel(const float* __restrict__ q, const float* __restrict__ kc,
                                       const float* __restrict__ vc, const int32_t* __restrict__ positions,
-                                      float* __restrict__ out, int B, int S, int H, int G, int D, int T_max,
-                                      int max_pos, int* status) {
+                                      const int32_t* __restrict__ lens, float* __restrict__ out, int B, int S, int H,
+                                      int G, int D, int T_max, int max_pos, int* status) {
   const long long wid = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (wid >= static_cast<long long>(B) * H * S) return;
@@ -89,6 +95,7 @@ __global__ void simt_attention_kernel(const float* __restrict__ q, const float* 
   const int h = static_cast<int>((wid / S) % H);
   const int b = static_cast<int>(wid / (static_cast<long long>(S) * H));
   const int g = h / (H / G);
+  if (lens != nullptr && (s >= lens[b] || lens[b] > S)) return;
   const int pos = positions ? positions[b] + s : s;
   float* o_row = out + (static_cast<long long>(b) * S + s) * H * D + h * D;
   if (pos < 0 || pos >= max_pos || pos >= T_max) {
@@ -151,23 +158,24 @@ int simt_linear(const Ctx& c, int mode, const float* X, const float* W0, const f
 
 int simt_qkv_rope(const Ctx& c, const float* X, const float* Wq, const float* Wk, const float* Wv, int B, int S,
                   int K, int H, int G, int D, const float* cos, const float* sin, const int32_t* positions,
-                  int max_pos, float* q_out, float* k_cache, float* v_cache, int T_max, int rope_half) {
+                  int max_pos, float* q_out, float* k_cache, float* v_cache, int T_max, int rope_half,
+                  const int32_t* lens) {
   const long long total = static_cast<long long>(B) * S * ((H + 2 * G) * D / 2);
   if (total == 0) return LLAMA_OK;
   simt_qkv_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, c.stream>>>(
       X, Wq, Wk, Wv, B, S, K, H, G, D, cos, sin, positions, max_pos, q_out, k_cache, v_cache, T_max, rope_half,
-      c.status);
+      lens, c.status);
   return after_launch(c);
 }
 
 int simt_attention(const Ctx& c, const float* q, const float* k_cache, const float* v_cache,
                    const int32_t* positions, float* out, int B, int S, int H, int G, int D, int T_max,
-                   int max_pos) {
+                   int max_pos, const int32_t* lens) {
   if (D > 256) return LLAMA_ERR_UNSUPPORTED;
   const long long threads = static_cast<long long>(B) * H * S * 32;
   if (threads == 0) return LLAMA_OK;
   simt_attention_kernel<<<static_cast<unsigned>((threads + 127) / 128), 128, 0, c.stream>>>(
-      q, k_cache, v_cache, positions, out, B, S, H, G, D, T_max, max_pos, c.status);
+      q, k_cache, v_cache, positions, lens, out, B, S, H, G, D, T_max, max_pos, c.status);
   return after_launch(c);
 }
 

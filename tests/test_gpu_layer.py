@@ -6,8 +6,8 @@ import pytest
 import torch
 
 import oracle
-from gpu_util import (NAN_BF16, TOL, assert_close, assert_close_layer_full, dims_of, f64, oracle_kw, tables,
-                      to_dev)
+from gpu_util import (NAN_BF16, TOL, assert_close, assert_close_layer_full, bf16_stored, dims_of, f64, oracle_kw,
+                      tables, to_dev)
 from llama_decoder_block_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -108,6 +108,124 @@ def test_prefill_gqa8b_full_size_causal_prefix(api):
     # the GPU runs B=4, S=4096; rows < 256 depend only on tokens < 256 (causality), so the
     # oracle's 256-token run is their exact reference
     _check_prefill(api, synth.WORKLOADS["gqa8b_bf16_b4_s4096"], prefix=256, full_width=True)
+
+
+def _cache_with_history(wl, T_max, start, seed):
+    """[B, G, T_max, D] K and V caches: N(0,1) in slots < start[b] (the history), NaN elsewhere."""
+    L = wl.layer
+    rng = np.random.default_rng(seed)
+    shape = (wl.B, L.n_kv_heads, T_max, L.head_dim)
+    out = []
+    for _ in range(2):
+        vals = rng.standard_normal(shape)
+        st = bf16_stored(vals) if L.dtype == "bf16" else synth.Stored(vals.astype(np.float32), "f32")
+        for b in range(wl.B):
+            st.data[b, :, start[b]:] = NAN_BF16 if L.dtype == "bf16" else np.nan
+        out.append(st)
+    return out
+
+
+def _check_chunk(api, wl, start, lengths, T_max):
+    L = wl.layer
+    B, S = wl.B, wl.S
+    start = np.asarray(start, dtype=np.int32)
+    lens = np.full(B, S, dtype=np.int32) if lengths is None else np.asarray(lengths, dtype=np.int32)
+    st, w = _weights(wl)
+    xs = synth.activations(wl)
+    x = to_dev(xs)
+    out = torch.empty_like(x)
+    ks, vs = _cache_with_history(wl, T_max, start, wl.seed + 7)
+    kc, vc = to_dev(ks), to_dev(vs)
+    cos, sin, c64, s64 = tables(L, T_max, oracle)
+    dims = dims_of(L)
+    ws = api.workspace(api.prefill_workspace_bytes(dims, B, S), "cuda")
+    api.layer_prefill_chunk(dims, w, x, out, cos, sin, torch.from_numpy(start).cuda(), kc, vc, ws,
+                            lengths=None if lengths is None else torch.from_numpy(lens).cuda())
+    assert api.device_status() == 0
+    w64 = {k: v.f64() for k, v in st.items()}
+    x64, k64, v64 = xs.f64(), ks.f64(), vs.f64()
+    out_h, kc_h, vc_h = f64(out), f64(kc), f64(vc)
+    tol = TOL[L.dtype]
+    for b in range(B):
+        p0, n = int(start[b]), int(lens[b])
+        ref, k_new, v_new = oracle.decoder_layer(x64[b:b + 1, :n], w64, c64, s64, past_k=k64[b:b + 1],
+                                                 past_v=v64[b:b + 1], past_len=np.array([p0]),
+                                                 store_bf16=(L.dtype == "bf16"), **oracle_kw(L))
+        assert_close(out_h[b, :n], ref[0], tol, f"chunk out b={b} start={p0} len={n}")
+        assert_close(kc_h[b, :, p0:p0 + n], k_new[0], tol, f"chunk cache K b={b}")
+        assert_close(vc_h[b, :, p0:p0 + n], v_new[0], tol, f"chunk cache V b={b}")
+        others = np.ones(T_max, bool)
+        others[p0:p0 + n] = False
+        assert np.array_equal(kc_h[b][:, others], k64[b][:, others], equal_nan=True)
+        assert np.array_equal(vc_h[b][:, others], v64[b][:, others], equal_nan=True)
+
+
+@pytest.mark.parametrize("H,G,start,lengths,S,T_max", [
+    (4, 2, [0, 37, 300], [150, 90, 1], 150, 512),      # ragged, one from position 0
+    (8, 1, [130, 5], None, 200, 400),                   # MQA-sized groups, tile-unaligned starts
+    (4, 4, [1000], None, 300, 1400),                    # long history: many key tiles, two masked
+    (2, 2, [256, 128], [128, 100], 128, 400),           # tile-aligned starts
+])
+def test_prefill_chunk_bf16(api, H, G, start, lengths, S, T_max):
+    base = synth.WORKLOADS["gqa8b_bf16_b4_s4096"]
+    wl = synth.scaled(base, d_model=256, n_heads=H, n_kv_heads=G, d_inter=384, B=len(start), S=S,
+                      name=f"chunk_bf16_h{H}_g{G}_s{S}")
+    _check_chunk(api, wl, start, lengths, T_max)
+
+
+def test_prefill_chunk_fp32(api):
+    base = synth.WORKLOADS["tiny_f32_b1_s16"]
+    wl = synth.scaled(base, B=2, S=9, name="chunk_f32_tiny")
+    _check_chunk(api, wl, [0, 20], [9, 4], 40)
+
+
+def test_two_chunks_equal_one_prefill(api):
+    # prefill(prompt[:100]) then the chunk prompt[100:] on top of it: the same outputs and cache
+    # as prefill(prompt) in one call
+    base = synth.WORKLOADS["gqa8b_bf16_b4_s4096"]
+    wl = synth.scaled(base, d_model=256, n_heads=4, n_kv_heads=2, d_inter=384, B=2, S=256, name="two_chunks")
+    L = wl.layer
+    st, w = _weights(wl)
+    x = to_dev(synth.activations(wl))
+    T_max = 300
+    cos, sin, _, _ = tables(L, T_max, oracle)
+    dims = dims_of(L)
+    ws = api.workspace(api.prefill_workspace_bytes(dims, wl.B, wl.S), "cuda")
+    shape = (wl.B, L.n_kv_heads, T_max, L.head_dim)
+    k1, v1 = torch.zeros(shape, dtype=torch.bfloat16, device="cuda"), torch.zeros(shape, dtype=torch.bfloat16,
+                                                                                 device="cuda")
+    k2, v2 = k1.clone(), v1.clone()
+    full = torch.empty_like(x)
+    api.layer_prefill(dims, w, x, full, cos, sin, k1, v1, ws)
+    a = torch.empty(wl.B, 100, L.d_model, dtype=torch.bfloat16, device="cuda")
+    c = torch.empty(wl.B, 156, L.d_model, dtype=torch.bfloat16, device="cuda")
+    zeros = torch.zeros(wl.B, dtype=torch.int32, device="cuda")
+    api.layer_prefill_chunk(dims, w, x[:, :100].contiguous(), a, cos, sin, zeros, k2, v2, ws)
+    api.layer_prefill_chunk(dims, w, x[:, 100:].contiguous(), c, cos, sin, zeros + 100, k2, v2, ws)
+    assert api.device_status() == 0
+    assert_close(f64(torch.cat([a, c], dim=1)), f64(full), TOL["bf16"], "chunked vs whole prefill")
+    assert_close(f64(k2), f64(k1), TOL["bf16"], "chunked vs whole cache K")
+    assert_close(f64(v2), f64(v1), TOL["bf16"], "chunked vs whole cache V")
+
+
+def test_prefill_chunk_out_of_range_is_reported(api):
+    base = synth.WORKLOADS["gqa8b_bf16_b4_s4096"]
+    wl = synth.scaled(base, d_model=256, n_heads=4, n_kv_heads=2, d_inter=384, B=2, S=64, name="chunk_bounds")
+    L = wl.layer
+    _, w = _weights(wl)
+    x = to_dev(synth.activations(wl))
+    out = torch.empty_like(x)
+    T_max = 100
+    cos, sin, _, _ = tables(L, T_max, oracle)
+    dims = dims_of(L)
+    ws = api.workspace(api.prefill_workspace_bytes(dims, wl.B, wl.S), "cuda")
+    kc = torch.zeros(wl.B, L.n_kv_heads, T_max, L.head_dim, dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    start = torch.tensor([10, 50], dtype=torch.int32, device="cuda")   # 50 + 64 > 100
+    api.layer_prefill_chunk(dims, w, x, out, cos, sin, start, kc, vc, ws)
+    assert api.device_status() == -5
+    assert torch.all(kc[1] == 0) and torch.all(vc[1] == 0)             # the bad sequence wrote nothing
+    assert torch.isfinite(out[0].float()).all()
 
 
 def _run_decode(api, wl, positions=None, nan_beyond=True, sample=None, full_width=False):
