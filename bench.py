@@ -294,23 +294,35 @@ def bench_prefill(api, wl, steps, warmup, dev, pk, from_synth):
         step()
     torch.cuda.synchronize()
     assert api.device_status(stream) == 0
-    traces = [api.KernelTrace(len(PREFILL_KERNELS), stream) for _ in range(steps)]
+    # the timed region: one event pair per step, nothing between the layer's kernels (an event
+    # between two kernels would stop the next one from starting under the previous one's tail)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     barrier()
     torch.cuda.synchronize()
     n0 = api.launch_count()
     t0 = time.perf_counter()
-    for tr in traces:
+    for e0, e1 in evs:
         flush.zero_()
-        with tr:
-            step()
+        e0.record(stream)
+        step()
+        e1.record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     launches = api.launch_count() - n0
     barrier()
     assert api.device_status(stream) == 0
+    step_ms = np.array([e0.elapsed_time(e1) for e0, e1 in evs])
+    # kernel by kernel: the same steps again with the library's per-kernel events
+    traces = [api.KernelTrace(len(PREFILL_KERNELS), stream) for _ in range(steps)]
+    for tr in traces:
+        flush.zero_()
+        with tr:
+            step()
+    torch.cuda.synchronize()
+    assert api.device_status(stream) == 0
     per_kernel = np.array([tr.kernel_ms() for tr in traces])           # [steps, kernels]
-    step_ms = per_kernel.sum(axis=1)
     res = {"ms_per_step": float(step_ms.mean()), "tokens_per_step": B * S, "wall_s": wall, "launches": launches,
+           "traced_ms_per_step": float(per_kernel.sum(axis=1).mean()),
            "kernel_ms": {n: float(per_kernel[:, i].mean()) for i, n in enumerate(PREFILL_KERNELS)}}
     flops = prefill_flops(L, B, S)
     res["tflops_total"] = sum(flops.values()) / (res["ms_per_step"] * 1e-3) / 1e12
@@ -380,6 +392,17 @@ def bench_decode(api, wl, steps, warmup, dev, pk):
         step()
     torch.cuda.synchronize()
     assert api.device_status(stream) == 0
+    # one event pair per step (kernels overlap their predecessors' tails), then a traced pass
+    # for the per-kernel times
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    assert api.device_status(stream) == 0
+    step_ms = np.array([e0.elapsed_time(e1) for e0, e1 in evs])
     traces = [api.KernelTrace(len(DECODE_KERNELS), stream) for _ in range(steps)]
     for tr in traces:
         flush.zero_()
@@ -388,7 +411,6 @@ def bench_decode(api, wl, steps, warmup, dev, pk):
     torch.cuda.synchronize()
     assert api.device_status(stream) == 0
     per_kernel = np.array([tr.kernel_ms() for tr in traces])
-    step_ms = per_kernel.sum(axis=1)
     d, H, G, D, I = L.d_model, L.n_heads, L.n_kv_heads, L.head_dim, L.d_inter
     w_bytes = 2 * (d * (H + 2 * G) * D + H * D * d + 3 * d * I + 2 * d)
     kv_read = int(np.sum(pos_h + 1)) * G * D * 2 * 2
@@ -398,6 +420,7 @@ def bench_decode(api, wl, steps, warmup, dev, pk):
     attn_ms = km["attention_decode_split"]
     attn_gbs = kv_read / (attn_ms * 1e-3) / 1e9
     res = {"workload": wl.name, "us_per_step": round(us, 1), "bytes_per_step": step_bytes,
+           "traced_us_per_step": round(float(per_kernel.sum(axis=1).mean() * 1e3), 1),
            "hbm_GBps": round(step_bytes / (us * 1e-6) / 1e9, 1),
            "frac_of_hbm": round(step_bytes / (us * 1e-6) / 1e9 / pk["hbm_gbs"], 4),
            "kernel_us": {k: round(v * 1e3, 1) for k, v in km.items()},

@@ -123,15 +123,18 @@ int num_sms_current(int* sms) {
 }
 
 // start, lens: null (a prompt from position 0) or device [B] (a chunk on top of the cache).
-int prefill_impl(const Ctx& c, const llama_layer_dims* d, const llama_layer_weights* w, const void* x, void* out,
-                 const float* cos, const float* sin, int max_pos, llama_kv_cache cache, int B, int S, void* ws,
-                 const int32_t* start = nullptr, const int32_t* lens = nullptr) {
+// `c0` launches the first kernel (without programmatic serialisation when the call starts
+// a new stream of work), `c` the others.
+int prefill_impl(const Ctx& c0, const Ctx& c_rest, const llama_layer_dims* d, const llama_layer_weights* w,
+                 const void* x, void* out, const float* cos, const float* sin, int max_pos, llama_kv_cache cache,
+                 int B, int S, void* ws, const int32_t* start = nullptr, const int32_t* lens = nullptr) {
   PrefillWs p;
   prefill_ws(d, B, S, ws, &p);
+  const Ctx& c = c_rest;
   const int M = B * S, dm = d->d_model, H = d->n_heads, G = d->n_kv_heads, D = d->head_dim, I = d->d_inter;
   int rc;
+  if ((rc = rmsnorm(c0, x, w->attn_norm, p.xn, M, dm, d->rms_eps, d->dtype))) return rc;
   if (d->dtype == LLAMA_BF16) {
-    if ((rc = rmsnorm(c, x, w->attn_norm, p.xn, M, dm, d->rms_eps, d->dtype))) return rc;
     if ((rc = gemm_qkv_rope(c, p.xn, w->wq, w->wk, w->wv, B, S, dm, H, G, D, cos, sin, p.q, cache.k, cache.v,
                             cache.max_T, d->rope_style, start, lens, max_pos)))
       return rc;
@@ -146,7 +149,6 @@ int prefill_impl(const Ctx& c, const llama_layer_dims* d, const llama_layer_weig
   float* xn = static_cast<float*>(p.xn);
   float* h = static_cast<float*>(p.h);
   float* a = static_cast<float*>(p.a);
-  if ((rc = rmsnorm(c, x, w->attn_norm, p.xn, M, dm, d->rms_eps, d->dtype))) return rc;
   if ((rc = simt_qkv_rope(c, xn, static_cast<const float*>(w->wq), static_cast<const float*>(w->wk),
                           static_cast<const float*>(w->wv), B, S, dm, H, G, D, cos, sin, start, max_pos,
                           static_cast<float*>(p.q), static_cast<float*>(cache.k), static_cast<float*>(cache.v),
@@ -182,9 +184,9 @@ int check_prefill_args(const llama_layer_dims* d, const llama_layer_weights* w, 
 }
 
 // One decode step of one layer; arguments already checked, workspace laid out by decode_ws.
-int decode_impl(const Ctx& c, const llama_layer_dims* dims, const llama_layer_weights* w, const void* x, void* out,
-                const float* cos, const float* sin, int32_t max_pos, const int32_t* positions, llama_kv_cache cache,
-                int32_t B, void* workspace) {
+int decode_impl(const Ctx& c0, const Ctx& c, const llama_layer_dims* dims, const llama_layer_weights* w,
+                const void* x, void* out, const float* cos, const float* sin, int32_t max_pos,
+                const int32_t* positions, llama_kv_cache cache, int32_t B, void* workspace) {
   int rc;
   DecodeWs p;
   decode_ws(dims, B, cache.max_T, c.num_sms, workspace, &p);
@@ -193,7 +195,7 @@ int decode_impl(const Ctx& c, const llama_layer_dims* dims, const llama_layer_we
   if (dims->dtype == LLAMA_BF16) {
     float* P = static_cast<float*>(p.part);
     const int qkv = (H + 2 * G) * D;
-    if ((rc = rmsnorm(c, x, w->attn_norm, p.xn, B, dm, dims->rms_eps, dims->dtype))) return rc;
+    if ((rc = rmsnorm(c0, x, w->attn_norm, p.xn, B, dm, dims->rms_eps, dims->dtype))) return rc;
     {
       const void* W3[3] = {w->wq, w->wk, w->wv};
       const int R3[3] = {H * D, G * D, G * D};
@@ -231,7 +233,7 @@ int decode_impl(const Ctx& c, const llama_layer_dims* dims, const llama_layer_we
   float* xn = static_cast<float*>(p.xn);
   float* h = static_cast<float*>(p.h);
   float* a = static_cast<float*>(p.a);
-  if ((rc = rmsnorm(c, x, w->attn_norm, xn, B, dm, dims->rms_eps, dims->dtype))) return rc;
+  if ((rc = rmsnorm(c0, x, w->attn_norm, xn, B, dm, dims->rms_eps, dims->dtype))) return rc;
   if ((rc = simt_qkv_rope(c, xn, static_cast<const float*>(w->wq), static_cast<const float*>(w->wk),
                           static_cast<const float*>(w->wv), B, 1, dm, H, G, D, cos, sin, positions, max_pos,
                           static_cast<float*>(p.q), static_cast<float*>(cache.k), static_cast<float*>(cache.v), T,
@@ -292,6 +294,16 @@ int check_stack(const llama_stack* st) {
   return LLAMA_OK;
 }
 
+// The contexts of a composite call: its first kernel waits for everything queued before
+// the call (no programmatic serialisation), the rest overlap their predecessors; the
+// weights are the caller's parameters, so GEMMs may prefetch them.
+void call_contexts(const Ctx& base, Ctx* first, Ctx* rest) {
+  *rest = base;
+  rest->static_weights = true;
+  *first = *rest;
+  first->pdl = false;
+}
+
 // One decode step of the stack; arguments already checked.
 int stack_decode_impl(const Ctx& c, const llama_stack* st, const int32_t* tokens, const int32_t* positions,
                       float* logits, const float* cos, const float* sin, int32_t max_pos,
@@ -301,25 +313,27 @@ int stack_decode_impl(const Ctx& c, const llama_stack* st, const int32_t* tokens
   StackDecodeWs p;
   stack_decode_ws(st, B, c.num_sms, workspace, &p);
   int rc;
-  if ((rc = embed_gather(c, tokens, st->embed, p.xa, B, static_cast<int>(d->d_model * es), st->vocab))) return rc;
+  Ctx c0, cr;
+  call_contexts(c, &c0, &cr);
+  if ((rc = embed_gather(c0, tokens, st->embed, p.xa, B, static_cast<int>(d->d_model * es), st->vocab))) return rc;
   void* xa = p.xa;
   void* xb = p.xb;
   for (int l = 0; l < st->n_layers; ++l) {
-    if ((rc = decode_impl(c, d, &st->layers[l], xa, xb, cos, sin, max_pos, positions, caches[l], B, p.layer)))
+    if ((rc = decode_impl(cr, cr, d, &st->layers[l], xa, xb, cos, sin, max_pos, positions, caches[l], B, p.layer)))
       return rc;
     std::swap(xa, xb);
   }
   // final RMSNorm, then the untied LM head in fp32
-  if ((rc = rmsnorm(c, xa, st->final_norm, xb, B, d->d_model, d->rms_eps, d->dtype))) return rc;
+  if ((rc = rmsnorm(cr, xa, st->final_norm, xb, B, d->d_model, d->rms_eps, d->dtype))) return rc;
   if (d->dtype != LLAMA_BF16)
-    return simt_linear(c, 0, static_cast<const float*>(xb), static_cast<const float*>(st->lm_head), nullptr, nullptr,
+    return simt_linear(cr, 0, static_cast<const float*>(xb), static_cast<const float*>(st->lm_head), nullptr, nullptr,
                        nullptr, logits, B, st->vocab, d->d_model);
   const int s = lm_head_splits(st, B, c.num_sms);
-  if (s == 0) return gemm_plain(c, xb, st->lm_head, logits, B, st->vocab, d->d_model, true);
+  if (s == 0) return gemm_plain(cr, xb, st->lm_head, logits, B, st->vocab, d->d_model, true);
   const void* W1[1] = {st->lm_head};
   const int R1[1] = {st->vocab};
-  if ((rc = gemm_tokens_partial(c, W1, R1, 1, xb, B, d->d_model, s, s == 1 ? logits : p.part))) return rc;
-  return s == 1 ? LLAMA_OK : fix_sum_f32(c, p.part, s, B, st->vocab, logits);
+  if ((rc = gemm_tokens_partial(cr, W1, R1, 1, xb, B, d->d_model, s, s == 1 ? logits : p.part))) return rc;
+  return s == 1 ? LLAMA_OK : fix_sum_f32(cr, p.part, s, B, st->vocab, logits);
 }
 
 }  // namespace
@@ -343,7 +357,9 @@ int llama_layer_prefill(const llama_layer_dims* dims, const llama_layer_weights*
     return LLAMA_ERR_INVALID_ARG;
   Ctx c;
   if ((rc = make_ctx(cuda_stream, &c))) return rc;
-  return prefill_impl(c, dims, w, x, out, cos, sin, max_pos, cache, B, S, workspace);
+  Ctx c0, cr;
+  call_contexts(c, &c0, &cr);
+  return prefill_impl(c0, cr, dims, w, x, out, cos, sin, max_pos, cache, B, S, workspace);
 }
 
 int llama_layer_prefill_chunk(const llama_layer_dims* dims, const llama_layer_weights* w, const void* x, void* out,
@@ -357,7 +373,9 @@ int llama_layer_prefill_chunk(const llama_layer_dims* dims, const llama_layer_we
     return LLAMA_ERR_INVALID_ARG;
   Ctx c;
   if ((rc = make_ctx(cuda_stream, &c))) return rc;
-  return prefill_impl(c, dims, w, x, out, cos, sin, max_pos, cache, B, S, workspace, start, lengths);
+  Ctx c0, cr;
+  call_contexts(c, &c0, &cr);
+  return prefill_impl(c0, cr, dims, w, x, out, cos, sin, max_pos, cache, B, S, workspace, start, lengths);
 }
 
 int llama_layer_decode_workspace_bytes(const llama_layer_dims* dims, int32_t B, int32_t max_T, size_t* bytes) {
@@ -384,7 +402,9 @@ int llama_layer_decode(const llama_layer_dims* dims, const llama_layer_weights* 
   Ctx c;
   if ((rc = make_ctx(cuda_stream, &c))) return rc;
   if (ws_bytes < decode_ws(dims, B, cache.max_T, c.num_sms, nullptr, nullptr)) return LLAMA_ERR_INVALID_ARG;
-  return decode_impl(c, dims, w, x, out, cos, sin, max_pos, positions, cache, B, workspace);
+  Ctx c0, cr;
+  call_contexts(c, &c0, &cr);
+  return decode_impl(c0, cr, dims, w, x, out, cos, sin, max_pos, positions, cache, B, workspace);
 }
 
 int llama_stack_workspace_bytes(const llama_stack* st, int32_t B, int32_t S, size_t* bytes) {
@@ -431,14 +451,15 @@ int llama_stack_forward(const llama_stack* st, const int32_t* tokens, float* log
     if ((rc = check_prefill_args(d, &st->layers[l], xa, xb, cos, sin, max_pos, kc, B, S))) return rc;
   }
   if (st->n_layers == 0 && (S > max_pos || !cos || !sin)) return LLAMA_ERR_INVALID_ARG;
-  Ctx c;
-  if ((rc = make_ctx(cuda_stream, &c))) return rc;
-  if ((rc = embed_gather(c, tokens, st->embed, xa, static_cast<int>(M), static_cast<int>(d->d_model * es),
+  Ctx c_base, c0, c;
+  if ((rc = make_ctx(cuda_stream, &c_base))) return rc;
+  call_contexts(c_base, &c0, &c);
+  if ((rc = embed_gather(c0, tokens, st->embed, xa, static_cast<int>(M), static_cast<int>(d->d_model * es),
                          st->vocab)))
     return rc;
   for (int l = 0; l < st->n_layers; ++l) {
     llama_kv_cache kc = caches ? caches[l] : llama_kv_cache{ks, vs, S};
-    if ((rc = prefill_impl(c, d, &st->layers[l], xa, xb, cos, sin, max_pos, kc, B, S, lws))) return rc;
+    if ((rc = prefill_impl(c, c, d, &st->layers[l], xa, xb, cos, sin, max_pos, kc, B, S, lws))) return rc;
     void* t = xa;
     xa = xb;
     xb = t;

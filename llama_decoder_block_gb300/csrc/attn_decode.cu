@@ -108,8 +108,11 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
   uint64_t* q_empty = q_full + 2;            // [2]
   uint64_t* s_full = q_empty + 2;            // [2]
   uint64_t* o_done = s_full + 2;             // [2] by the parity of the tile
+  // [2] by the parity of the tile: the MMA issuer issues S of tile t before it waits for P of
+  // tile t - 1, so the softmax may finish both before that wait looks; with one barrier the
+  // phase of t - 1 could then be overtaken and never seen
   uint64_t* p_full = o_done + 2;
-  uint64_t* o_free = p_full + 1;             // [2] by the parity of the item
+  uint64_t* o_free = p_full + 2;             // [2] by the parity of the item
   uint64_t* drain = o_free + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -128,6 +131,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
       mbar_init(smem_u32(o_done + i), 1);
     }
     mbar_init(smem_u32(p_full), 4);
+    mbar_init(smem_u32(p_full + 1), 4);
     mbar_init(smem_u32(o_free), 4);
     mbar_init(smem_u32(o_free + 1), 4);
     mbar_init(smem_u32(drain), 1);
@@ -229,7 +233,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
       uint32_t tcount = 0, icount = 0;
       bool ok = true, issued = false;
       auto issue_pv = [&](uint32_t tc, bool first, uint32_t ob) -> bool {
-        if (!mbar_wait(smem_u32(p_full), tc & 1, p.status, abort_flag)) return false;
+        if (!mbar_wait(smem_u32(p_full + (tc & 1)), (tc >> 1) & 1, p.status, abort_flag)) return false;
         // O^T buffer ob was last read by the epilogue of the item two before this one
         if (first && icount >= 2 && !mbar_wait(smem_u32(o_free + ob), ((icount - 2) >> 1) & 1, p.status, abort_flag))
           return false;
@@ -387,7 +391,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(p_full));
+        if (lane == 0) mbar_arrive(smem_u32(p_full + pb));
       }
       if (!ok) break;
       // segment epilogue: wait for the last product, write this segment's (m, l, O)
@@ -434,7 +438,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
 }
 
 constexpr size_t kDecSmemBytes = 1024 + 2 * STAGES * KV_TILE + 2 * Q_TILE + 2 * P_TILE + 64 * 4 +
-                                 (2 * POS_CACHE + 2) * 4 + (2 * STAGES + 13) * 8 + 16;
+                                 (2 * POS_CACHE + 2) * 4 + (2 * STAGES + 14) * 8 + 16;
 static_assert(kDecSmemBytes <= 232448, "decode attention exceeds the shared memory of one CTA");
 static_assert(kDecSmemBytes >= kTmemKernelMinSmem, "a TMEM-holding kernel must not share an SM with another");
 

@@ -68,6 +68,24 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
+// Records LLAMA_ERR_TIMEOUT; the first wait to give up also leaves a record of itself after
+// the status word (what it waited on: a barrier address and parity, or a flag address).
+static __device__ __noinline__ void report_timeout(int* status, uint64_t waited, uint32_t polls, uint32_t what,
+                                                   uint32_t parity) {
+  if (status == nullptr || atomicCAS(status, 0, LLAMA_ERR_TIMEOUT) != 0) return;
+  long long* rec = reinterpret_cast<long long*>(status + 2);
+  uint32_t smid;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+  rec[0] = static_cast<long long>(waited);
+  rec[1] = polls;
+  rec[2] = static_cast<long long>(blockIdx.x) | (static_cast<long long>(blockIdx.y) << 32);
+  rec[3] = threadIdx.x;
+  rec[4] = smid;
+  rec[5] = static_cast<long long>(what) | (static_cast<long long>(parity) << 32);
+  rec[6] = static_cast<long long>(gridDim.x) | (static_cast<long long>(gridDim.y) << 32);
+  __threadfence();
+}
+
 // Wait for the phase of parity `parity` to complete, for at most `budget_ns`.
 // Gives up early when another thread of the CTA raised `abort_flag`.  On
 // timeout, records LLAMA_ERR_TIMEOUT in `status`, raises `abort_flag` and
@@ -87,20 +105,7 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
       }
       const uint64_t now = globaltimer_ns();
       if (now - t0 > budget_ns) {
-        if (status != nullptr && atomicCAS(status, 0, LLAMA_ERR_TIMEOUT) == 0) {
-          // the first wait to give up leaves a record of itself after the status word
-          long long* rec = reinterpret_cast<long long*>(status + 2);
-          uint32_t smid;
-          asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-          rec[0] = static_cast<long long>(now - t0);
-          rec[1] = it;
-          rec[2] = static_cast<long long>(blockIdx.x) | (static_cast<long long>(blockIdx.y) << 32);
-          rec[3] = threadIdx.x;
-          rec[4] = smid;
-          rec[5] = static_cast<long long>(bar) | (static_cast<long long>(parity) << 32);
-          rec[6] = static_cast<long long>(gridDim.x) | (static_cast<long long>(gridDim.y) << 32);
-          __threadfence();
-        }
+        report_timeout(status, now - t0, it, bar, parity);
         if (abort_flag != nullptr) *abort_flag = 1;
         return false;
       }

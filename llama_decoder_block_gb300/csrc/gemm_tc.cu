@@ -42,6 +42,8 @@ struct Params {
   int M, N, K;                  // kernel frame: C[M, N] = A[M, K] B[N, K]^T
   int num_mb, num_nb, num_splits, kb_per_split, num_kb;
   int group_m;
+  int weight_first;             // 0, or 1 / 2: operand A / B is a weight that may be loaded before
+                                // griddepcontrol.wait (the first STAGES k-blocks of it are)
   RowMap amap, bmap;
   int a_map0, b_map0;
   void* out;
@@ -173,12 +175,46 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  pdl_wait();   // inputs written by the previous kernel are read from here on
+  // inputs written by the previous kernel are read from here on (the producer waits below,
+  // after issuing the weight tiles that depend on nothing in flight)
+  if (!(warp == 0 && lane == 0)) pdl_wait();
 
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ TMA producer
-      int stage = 0;
+      auto load_a = [&](int stage, int kb, int mb) {
+        int a_map, a_row;
+        resolve_rows(p.amap, mb * BM, a_map, a_row);
+        tma_load_2d(smem_u32(sA + stage * A_TILE_BYTES), &tm.m[p.a_map0 + a_map], smem_u32(full_bar + stage),
+                    kb * BK, a_row);
+      };
+      auto load_b = [&](int stage, int kb, int nb) {
+#pragma unroll
+        for (int bx = 0; bx < B_BOXES; ++bx) {
+          int b_map, b_row;
+          resolve_rows(p.bmap, nb * BN + bx * B_BOX_ROWS, b_map, b_row);
+          tma_load_2d(smem_u32(sB + stage * B_TILE_BYTES + bx * B_BOX_ROWS * 128), &tm.m[p.b_map0 + b_map],
+                      smem_u32(full_bar + stage), kb * BK, b_row);
+        }
+      };
+      // the first STAGES k-blocks' weight tiles go out before the dependency wait: the ring
+      // starts empty, so these stages need no empty-barrier wait
+      int pre = 0;
+      if (p.weight_first != 0) {
+        for (int t = blockIdx.x; t < num_tiles && pre < STAGES; t += gridDim.x) {
+          int mb, nb, split;
+          tile_coords(p, t, mb, nb, split);
+          const int kb0 = split * p.kb_per_split;
+          const int kb1 = min(kb0 + p.kb_per_split, p.num_kb);
+          for (int kb = kb0; kb < kb1 && pre < STAGES; ++kb, ++pre) {
+            mbar_expect_tx(smem_u32(full_bar + pre), STAGE_TX);
+            if (p.weight_first == 1) load_a(pre, kb, mb);
+            else load_b(pre, kb, nb);
+          }
+        }
+      }
+      pdl_wait();
+      int stage = 0, step = 0;
       uint32_t phase = 0;
       uint32_t used_mask = 0, last_parity = 0;
       bool ok = true;
@@ -187,19 +223,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tile_coords(p, t, mb, nb, split);
         const int kb0 = split * p.kb_per_split;
         const int kb1 = min(kb0 + p.kb_per_split, p.num_kb);
-        int a_map, a_row;
-        resolve_rows(p.amap, mb * BM, a_map, a_row);
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(smem_u32(empty_bar + stage), phase ^ 1u, p.status, abort_flag)) { ok = false; break; }
-          const uint32_t fb = smem_u32(full_bar + stage);
-          mbar_expect_tx(fb, STAGE_TX);
-          tma_load_2d(smem_u32(sA + stage * A_TILE_BYTES), &tm.m[p.a_map0 + a_map], fb, kb * BK, a_row);
-#pragma unroll
-          for (int bx = 0; bx < B_BOXES; ++bx) {
-            int b_map, b_row;
-            resolve_rows(p.bmap, nb * BN + bx * B_BOX_ROWS, b_map, b_row);
-            tma_load_2d(smem_u32(sB + stage * B_TILE_BYTES + bx * B_BOX_ROWS * 128), &tm.m[p.b_map0 + b_map], fb,
-                        kb * BK, b_row);
+        for (int kb = kb0; kb < kb1; ++kb, ++step) {
+          if (step < pre) {   // the weight half of this stage is already on its way
+            if (p.weight_first == 1) load_b(stage, kb, nb);
+            else load_a(stage, kb, mb);
+          } else {
+            if (!mbar_wait(smem_u32(empty_bar + stage), phase ^ 1u, p.status, abort_flag)) { ok = false; break; }
+            mbar_expect_tx(smem_u32(full_bar + stage), STAGE_TX);
+            load_a(stage, kb, mb);
+            load_b(stage, kb, nb);
           }
           used_mask |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
@@ -440,6 +472,7 @@ int launch(const Ctx& c, const TMaps& tm, Params p) {
   });
   if (attr_err != cudaSuccess) return LLAMA_ERR_CUDA;
   p.status = c.status;
+  if (!c.static_weights) p.weight_first = 0;
   const int tiles = p.num_mb * p.num_nb * p.num_splits;
   if (tiles == 0) return LLAMA_OK;
   const int grid = std::min(tiles, c.num_sms);
@@ -457,6 +490,7 @@ Params base_params(int M, int N, int K, int BN) {
   p.num_kb = (K + BK - 1) / BK;
   p.num_splits = 1;
   p.kb_per_split = p.num_kb;
+  p.weight_first = 2;   // B holds the weights (kept only when the context says they are static)
   // tile order: a group of group_m row blocks walks all column blocks, so that group's rows
   // of A stay in L2 while the weights stream; take every row block when all of A fits in
   // 48 MB (the weights then stream from DRAM once), else about 32 MB of A per group
@@ -594,6 +628,9 @@ int gemm_tokens_partial(const Ctx& c, const void* const* W, const int* w_rows, i
   if (p.num_splits != splits) return LLAMA_ERR_INVALID_ARG;          // callers pass choose_splits()
   p.out = P;
   p.ldo = total;
+  // No weight loads before griddepcontrol.wait here: measured on the decode step, streaming
+  // weights under the preceding fixup kernel slows that kernel more than it saves.
+  p.weight_first = 0;
   return launch<64, EPI_PARTIAL, 8>(c, tm, p);
 }
 

@@ -16,6 +16,14 @@ struct Ctx {
   int device;
   int num_sms;
   int* status;   // device address of this device's status word
+  // Launch with programmatic stream serialisation (may overlap the previous kernel's tail).
+  // A call's first kernel goes without it, so that everything queued before the call has
+  // finished when any kernel of the call starts.
+  bool pdl = true;
+  // The GEMMs' weight operands are written by nothing that may still run: their producers
+  // may load weight tiles before griddepcontrol.wait.  Set by the composite entry points,
+  // whose weights are the caller's parameters.
+  bool static_weights = false;
 };
 
 // Fills `c` for the current device; returns LLAMA_OK or LLAMA_ERR_CUDA.
@@ -34,7 +42,7 @@ cudaError_t launch_pdl(const Ctx& c, void (*kern)(KArgs...), dim3 grid, dim3 blo
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = c.pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
 }
 // Checks cudaGetLastError after a launch, counts it and records the next trace event.

@@ -122,3 +122,33 @@ def test_steps_full_size(api, name):
     assert_close(f64(out)[rows], ref, tol, "down + residual")
     _one_ulp(f64(out)[rows], ref, "down + residual")
     assert api.device_status() == 0
+
+
+def test_decode_layer_back_to_back_calls_finish_cleanly(api):
+    # 1500 decode steps of the full-size layer queued without a host synchronisation between
+    # them: the kernels overlap each other's tails, so any barrier that a fast producer could
+    # run two phases ahead of its consumer would stall a wait here (LLAMA_ERR_TIMEOUT)
+    wl = synth.WORKLOADS["decode_gqa8b_bf16_b64_t4096"]
+    L = wl.layer
+    B, T = wl.B, wl.T_max
+    g = torch.Generator(device="cuda").manual_seed(11)
+    d, H, G, D, I = L.d_model, L.n_heads, L.n_kv_heads, L.head_dim, L.d_inter
+    shapes = {"wq": (H * D, d), "wk": (G * D, d), "wv": (G * D, d), "wo": (d, H * D), "w_gate": (I, d),
+              "w_up": (I, d), "w_down": (d, I)}
+    w = {k: (torch.randn(s, generator=g, device="cuda") * 0.02).to(torch.bfloat16) for k, s in shapes.items()}
+    w["attn_norm"] = torch.ones(d, dtype=torch.bfloat16, device="cuda")
+    w["ffn_norm"] = torch.ones(d, dtype=torch.bfloat16, device="cuda")
+    kc = torch.randn(B, G, T, D, generator=g, device="cuda").to(torch.bfloat16)
+    vc = torch.randn_like(kc)
+    pos = torch.from_numpy(synth.decode_positions(wl)).cuda()
+    x = torch.randn(B, d, generator=g, device="cuda").to(torch.bfloat16)
+    out = torch.empty_like(x)
+    cos, sin, _, _ = tables(L, T, oracle)
+    dims = dims_of(L)
+    ws = api.workspace(api.decode_workspace_bytes(dims, B, T), "cuda")
+    for _ in range(15):
+        for _ in range(100):
+            api.layer_decode(dims, w, x, out, cos, sin, pos, kc, vc, ws)
+        rc = api.device_status()
+        assert rc == 0, (rc, api.timeout_record())
+    assert torch.isfinite(out.float()).all()
