@@ -184,9 +184,14 @@ int check_prefill_args(const llama_layer_dims* d, const llama_layer_weights* w, 
 }
 
 // One decode step of one layer; arguments already checked, workspace laid out by decode_ws.
+// bf16 layers in a stack: `xn_given` means the workspace's xn already holds RMSNorm₁(x) (the
+// previous layer's last kernel wrote it), and a non-null `next_norm` makes this layer's last
+// kernel also write RMSNorm(out) with that gamma into xn (the next layer's input norm, or the
+// model's final norm).
 int decode_impl(const Ctx& c0, const Ctx& c, const llama_layer_dims* dims, const llama_layer_weights* w,
                 const void* x, void* out, const float* cos, const float* sin, int32_t max_pos,
-                const int32_t* positions, llama_kv_cache cache, int32_t B, void* workspace) {
+                const int32_t* positions, llama_kv_cache cache, int32_t B, void* workspace,
+                const void* next_norm = nullptr, bool xn_given = false) {
   int rc;
   DecodeWs p;
   decode_ws(dims, B, cache.max_T, c.num_sms, workspace, &p);
@@ -195,7 +200,7 @@ int decode_impl(const Ctx& c0, const Ctx& c, const llama_layer_dims* dims, const
   if (dims->dtype == LLAMA_BF16) {
     float* P = static_cast<float*>(p.part);
     const int qkv = (H + 2 * G) * D;
-    if ((rc = rmsnorm(c0, x, w->attn_norm, p.xn, B, dm, dims->rms_eps, dims->dtype))) return rc;
+    if (!xn_given && (rc = rmsnorm(c0, x, w->attn_norm, p.xn, B, dm, dims->rms_eps, dims->dtype))) return rc;
     {
       const void* W3[3] = {w->wq, w->wk, w->wv};
       const int R3[3] = {H * D, G * D, G * D};
@@ -227,6 +232,7 @@ int decode_impl(const Ctx& c0, const Ctx& c, const llama_layer_dims* dims, const
       const int R1[1] = {dm};
       const int s = choose_splits(c.num_sms, dm, I, B);
       if ((rc = gemm_tokens_partial(c, W1, R1, 1, p.a, B, I, s, P))) return rc;
+      if (next_norm != nullptr) return fix_residual_rmsnorm(c, P, s, B, dm, p.h, next_norm, dims->rms_eps, out, p.xn);
       return fix_residual(c, P, s, B, dm, p.h, out);
     }
   }
@@ -318,13 +324,24 @@ int stack_decode_impl(const Ctx& c, const llama_stack* st, const int32_t* tokens
   if ((rc = embed_gather(c0, tokens, st->embed, p.xa, B, static_cast<int>(d->d_model * es), st->vocab))) return rc;
   void* xa = p.xa;
   void* xb = p.xb;
+  // bf16: each layer's last kernel also normalises its output for what follows (the next
+  // layer's attn_norm, the final norm after the last layer) into the layer workspace's xn
+  const bool fuse = d->dtype == LLAMA_BF16 && st->n_layers > 0;
+  DecodeWs lw;
+  decode_ws(d, B, 1, c.num_sms, p.layer, &lw);
   for (int l = 0; l < st->n_layers; ++l) {
-    if ((rc = decode_impl(cr, cr, d, &st->layers[l], xa, xb, cos, sin, max_pos, positions, caches[l], B, p.layer)))
+    const void* nn = !fuse ? nullptr : l + 1 < st->n_layers ? st->layers[l + 1].attn_norm : st->final_norm;
+    if ((rc = decode_impl(cr, cr, d, &st->layers[l], xa, xb, cos, sin, max_pos, positions, caches[l], B, p.layer,
+                          nn, fuse && l > 0)))
       return rc;
     std::swap(xa, xb);
   }
-  // final RMSNorm, then the untied LM head in fp32
-  if ((rc = rmsnorm(cr, xa, st->final_norm, xb, B, d->d_model, d->rms_eps, d->dtype))) return rc;
+  // final RMSNorm (already in the layer workspace when fused), then the untied LM head in fp32
+  if (fuse) {
+    xb = lw.xn;
+  } else if ((rc = rmsnorm(cr, xa, st->final_norm, xb, B, d->d_model, d->rms_eps, d->dtype))) {
+    return rc;
+  }
   if (d->dtype != LLAMA_BF16)
     return simt_linear(cr, 0, static_cast<const float*>(xb), static_cast<const float*>(st->lm_head), nullptr, nullptr,
                        nullptr, logits, B, st->vocab, d->d_model);

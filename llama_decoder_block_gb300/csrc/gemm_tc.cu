@@ -127,7 +127,8 @@ template <int BN, int EPI, int STAGES>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ TMaps tm, const Params p) {
   constexpr int B_TILE_BYTES = BN * BK * 2;
-  constexpr int B_BOX_ROWS = BN >= 128 ? 128 : BN;
+  // B arrives in 128-row boxes, or as one box when BN is not a multiple of 128 (BN <= 256)
+  constexpr int B_BOX_ROWS = BN % 128 == 0 ? 128 : BN;
   constexpr int B_BOXES = BN / B_BOX_ROWS;
   constexpr uint32_t STAGE_TX = A_TILE_BYTES + B_TILE_BYTES;
   constexpr uint32_t TMEM_COLS = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
@@ -480,6 +481,17 @@ int launch(const Ctx& c, const TMaps& tm, Params p) {
   return after_launch(c);
 }
 
+// Tile width (256 or 224 columns) whose rounds of num_sms tiles take the least time, time per
+// round taken as proportional to the width; ties keep 256.
+int tile_width_for(int M, int N, int num_sms) {
+  const long long mb = (M + BM - 1) / BM;
+  auto cost = [&](int bn) {
+    const long long tiles = mb * ((N + bn - 1) / bn);
+    return ((tiles + num_sms - 1) / num_sms) * bn;
+  };
+  return cost(224) < cost(256) ? 224 : 256;
+}
+
 Params base_params(int M, int N, int K, int BN) {
   Params p{};
   p.M = M;
@@ -508,29 +520,35 @@ Params base_params(int M, int N, int K, int BN) {
 }  // namespace
 
 int gemm_plain(const Ctx& c, const void* X, const void* W, void* C, int M, int N, int K, bool c_f32) {
+  const int bn = tile_width_for(M, N, c.num_sms);
   TMaps tm{};
-  if (!make_tmap_2d(&tm.m[0], X, K, M, K, 128) || !make_tmap_2d(&tm.m[1], W, K, N, K, 128))
+  if (!make_tmap_2d(&tm.m[0], X, K, M, K, 128) || !make_tmap_2d(&tm.m[1], W, K, N, K, bn == 256 ? 128 : bn))
     return LLAMA_ERR_INVALID_ARG;
-  Params p = base_params(M, N, K, 256);
+  Params p = base_params(M, N, K, bn);
   p.a_map0 = 0;
   p.b_map0 = 1;
   p.out = C;
   p.ldo = N;
-  return c_f32 ? launch<256, EPI_F32, 4>(c, tm, p) : launch<256, EPI_BF16, 4>(c, tm, p);
+  if (bn == 256) return c_f32 ? launch<256, EPI_F32, 4>(c, tm, p) : launch<256, EPI_BF16, 4>(c, tm, p);
+  return c_f32 ? launch<224, EPI_F32, 5>(c, tm, p) : launch<224, EPI_BF16, 5>(c, tm, p);
 }
 
 int gemm_residual(const Ctx& c, const void* X, const void* W, const void* resid, void* out, int M, int N, int K) {
+  // 224-column tiles when they finish in fewer tile-column rounds (e.g. N = 4096 at M = 2048:
+  // 304 tiles fill 2 rounds of 152 SMs, where 256 tiles of 256 columns leave the second
+  // round two-thirds full)
+  const int bn = tile_width_for(M, N, c.num_sms);
   TMaps tm{};
-  if (!make_tmap_2d(&tm.m[0], X, K, M, K, 128) || !make_tmap_2d(&tm.m[1], W, K, N, K, 128))
+  if (!make_tmap_2d(&tm.m[0], X, K, M, K, 128) || !make_tmap_2d(&tm.m[1], W, K, N, K, bn == 256 ? 128 : bn))
     return LLAMA_ERR_INVALID_ARG;
-  Params p = base_params(M, N, K, 256);
+  Params p = base_params(M, N, K, bn);
   p.a_map0 = 0;
   p.b_map0 = 1;
   p.out = out;
   p.ldo = N;
   p.resid = static_cast<const __nv_bfloat16*>(resid);
   p.ldr = N;
-  return launch<256, EPI_RESID, 4>(c, tm, p);
+  return bn == 256 ? launch<256, EPI_RESID, 4>(c, tm, p) : launch<224, EPI_RESID, 5>(c, tm, p);
 }
 
 int gemm_swiglu(const Ctx& c, const void* X, const void* Wg, const void* Wu, void* out, int M, int I, int K) {

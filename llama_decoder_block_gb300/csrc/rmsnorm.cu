@@ -11,7 +11,7 @@
 namespace llama {
 namespace {
 
-constexpr int kWarpsPerCta = 8;
+constexpr int kWarpsPerCta = 2;   // small CTAs: the last wave of rows is short (measured best of 2, 4, 8, 16)
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
