@@ -241,13 +241,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll 1
         for (int hlf = 0; hlf < 2; ++hlf) {
           tmem_ld64(tS + hlf * 64, r);
+          if (diag) {
 #pragma unroll
-          for (int i = 0; i < 64; ++i) {
-            float s = __uint_as_float(r[i]);
-            const int key = kbase + hlf * 64 + i;
-            if (diag && key > qpos) s = -INFINITY;
-            mx = fmaxf(mx, s);
+            for (int i = 0; i < 64; ++i)
+              if (kbase + hlf * 64 + i > qpos) r[i] = __float_as_uint(-INFINITY);
           }
+          // two scores per max instruction (the ALU pipe is this loop's limit)
+#pragma unroll
+          for (int i = 0; i < 64; i += 2) mx = fmax3(mx, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
         }
         const float mxs = mx * sl;
         const bool need = mxs > m_run + kRescaleLog2;    // also true on the first tile
