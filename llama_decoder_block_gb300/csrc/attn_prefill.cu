@@ -5,8 +5,10 @@
 // repeated along dim 1; "深度学习进阶（三十）…" §1.1; "第 10 章：现代 LLaMA 架构" §6: K/V stay
 // G heads in the cache and are shared logically, never copied H/G times).
 //
-// One CTA per (pair of 128-query blocks 2i and 2i+1, head, sequence), pairs with the most
-// keys first.  Both query tiles read every K/V tile once from shared memory.
+// One CTA per (pair of 128-query blocks 2i and 2i+1, head, sequence).  The pair index is the
+// grid's slowest dimension, counted down, so CTAs are dispatched longest first (the last query
+// pairs read the most keys) and the short pairs fill the tail of the last wave.  Both query
+// tiles read every K/V tile once from shared memory.
 //   warp 0      TMA: both Q tiles once, then K_j, V_j (128 keys each) into a 2-stage ring
 //               straight from the [B, G, max_T, D] cache
 //   warp 1      TMEM allocator and MMA issuer, ping-pong between the two tiles:
@@ -75,8 +77,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int pair = p.n_pairs - 1 - static_cast<int>(blockIdx.x);
-  const int h = blockIdx.y, b = blockIdx.z;
+  const int pair = p.n_pairs - 1 - static_cast<int>(blockIdx.z);
+  const int h = blockIdx.x, b = blockIdx.y;
   const int g = h / (p.H / p.G);
   const int qb[2] = {2 * pair, 2 * pair + 1};
 
@@ -114,7 +116,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     pos0 = p.start[b];
     len = p.lens != nullptr ? p.lens[b] : p.S;
     if (pos0 < 0 || len < 0 || len > p.S || pos0 + len > p.T_max || pos0 + len > p.max_pos) {
-      if (threadIdx.x == 0 && blockIdx.x == 0 && h == 0) report(p.status, LLAMA_ERR_DEVICE_BOUNDS);
+      if (threadIdx.x == 0 && blockIdx.z == 0 && h == 0) report(p.status, LLAMA_ERR_DEVICE_BOUNDS);
       len = 0;
     }
   }
@@ -382,7 +384,8 @@ int attn_prefill_tc(const Ctx& c, const void* q, const void* k_cache, const void
   p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
   p.out = static_cast<__nv_bfloat16*>(out);
   p.status = c.status;
-  launch_pdl(c, attn_prefill_kernel, dim3(p.n_pairs, H, B), dim3(NUM_THREADS), kSmemBytes, tq, tk, tv, p);
+  if (B > 65535 || p.n_pairs > 65535) return LLAMA_ERR_UNSUPPORTED;
+  launch_pdl(c, attn_prefill_kernel, dim3(H, B, p.n_pairs), dim3(NUM_THREADS), kSmemBytes, tq, tk, tv, p);
   return after_launch(c);
 }
 

@@ -31,11 +31,10 @@ enum Epi : int { EPI_BF16 = 0, EPI_F32 = 1, EPI_RESID = 2, EPI_SWIGLU = 3, EPI_Q
 struct RowMap {
   int nseg;          // 1..3 row-concatenated matrices
   int seg_end[3];    // cumulative row ends (multiples of 128)
-  int interleave;    // 1: 256-row block j = [map0 rows 128j.. | map1 rows 128j..]
 };
 
 struct TMaps {
-  CUtensorMap m[4];
+  CUtensorMap m[7];
 };
 
 struct Params {
@@ -46,6 +45,9 @@ struct Params {
                                 // griddepcontrol.wait (the first STAGES k-blocks of it are)
   RowMap amap, bmap;
   int a_map0, b_map0;
+  int b32_map0;                 // QKV on tiles that are not head-aligned: the weight maps again
+                                // with 32-row boxes, for tiles that cross a q|k or k|v boundary
+  int n_maps;                   // tensor maps in use
   void* out;
   long long ldo;
   const __nv_bfloat16* resid;
@@ -65,11 +67,6 @@ struct Params {
 };
 
 __device__ __forceinline__ void resolve_rows(const RowMap& rm, int vrow, int& map, int& row) {
-  if (rm.interleave) {
-    map = (vrow >> 7) & 1;
-    row = (vrow >> 8) << 7;
-    return;
-  }
   map = 0;
   int start = 0;
   if (rm.nseg > 1 && vrow >= rm.seg_end[0]) { map = 1; start = rm.seg_end[0]; }
@@ -91,6 +88,23 @@ __device__ __forceinline__ void tile_coords(const Params& p, int t, int& mb, int
 // ------------------------------------------------------------------ epilogue helpers
 
 __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float* v, int valid) {
+  if (valid < 32 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+    // whole groups of 8 as 16-byte stores, the rest one by one (static register indices)
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+      if (8 * g + 8 <= valid) {
+        uint4 w;
+        w.x = pack_bf16(v[8 * g + 0], v[8 * g + 1]);
+        w.y = pack_bf16(v[8 * g + 2], v[8 * g + 3]);
+        w.z = pack_bf16(v[8 * g + 4], v[8 * g + 5]);
+        w.w = pack_bf16(v[8 * g + 6], v[8 * g + 7]);
+        reinterpret_cast<uint4*>(dst)[g] = w;
+      }
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i >= (valid & ~7) && i < valid) dst[i] = __float2bfloat16_rn(v[i]);
+    return;
+  }
   if (valid >= 32) {
     uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
@@ -127,8 +141,9 @@ template <int BN, int EPI, int STAGES>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ TMaps tm, const Params p) {
   constexpr int B_TILE_BYTES = BN * BK * 2;
-  // B arrives in 128-row boxes, or as one box when BN is not a multiple of 128 (BN <= 256)
-  constexpr int B_BOX_ROWS = BN % 128 == 0 ? 128 : BN;
+  // B arrives in 128-row boxes, or as one box when BN is not a multiple of 128 (BN <= 256);
+  // gate/up tiles as two boxes of BN/2 rows, one from each matrix
+  constexpr int B_BOX_ROWS = EPI == EPI_SWIGLU ? BN / 2 : BN % 128 == 0 ? 128 : BN;
   constexpr int B_BOXES = BN / B_BOX_ROWS;
   constexpr uint32_t STAGE_TX = A_TILE_BYTES + B_TILE_BYTES;
   constexpr uint32_t TMEM_COLS = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
@@ -166,7 +181,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
-    for (int i = 0; i < 4; ++i) tma_prefetch_desc(&tm.m[i]);
+    for (int i = 0; i < p.n_maps; ++i) tma_prefetch_desc(&tm.m[i]);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -190,10 +205,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     kb * BK, a_row);
       };
       auto load_b = [&](int stage, int kb, int nb) {
+        if constexpr (EPI == EPI_QKV && BN % 128 != 0) {
+          int m0, r0, m1, r1;
+          resolve_rows(p.bmap, nb * BN, m0, r0);
+          resolve_rows(p.bmap, nb * BN + BN - 1, m1, r1);
+          if (m0 != m1) {   // the tile crosses a boundary between two of the matrices
+            for (int bx = 0; bx < BN / 32; ++bx) {
+              int b_map, b_row;
+              resolve_rows(p.bmap, nb * BN + bx * 32, b_map, b_row);
+              tma_load_2d(smem_u32(sB + stage * B_TILE_BYTES + bx * 32 * 128), &tm.m[p.b32_map0 + b_map],
+                          smem_u32(full_bar + stage), kb * BK, b_row);
+            }
+            return;
+          }
+        }
 #pragma unroll
         for (int bx = 0; bx < B_BOXES; ++bx) {
+          // (this thread's issue latency bounds the ring's lead over TMA latency: no divisions)
           int b_map, b_row;
-          resolve_rows(p.bmap, nb * BN + bx * B_BOX_ROWS, b_map, b_row);
+          if constexpr (EPI == EPI_SWIGLU) {   // tile nb = [gate rows BN/2*nb.. | the same up rows]
+            b_map = bx;
+            b_row = nb * B_BOX_ROWS;
+          } else {
+            resolve_rows(p.bmap, nb * BN + bx * B_BOX_ROWS, b_map, b_row);
+          }
           tma_load_2d(smem_u32(sB + stage * B_TILE_BYTES + bx * B_BOX_ROWS * 128), &tm.m[p.b_map0 + b_map],
                       smem_u32(full_bar + stage), kb * BK, b_row);
         }
@@ -335,13 +370,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
       } else if constexpr (EPI == EPI_SWIGLU) {
-        // columns [0,128) of the tile are gate rows 128*nb.., [128,256) the matching up rows
+        // columns [0, BN/2) of the tile are gate rows BN/2*nb.., [BN/2, BN) the matching up rows
+        constexpr int HALF = BN / 2;
+        static_assert(HALF % 32 == 0, "gate/up halves of whole 32-column chunks");
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < HALF / 32; ++c) {
           uint32_t u[32];
           tmem_ld32(t_acc + c * 32, r);
-          tmem_ld32(t_acc + 128 + c * 32, u);
-          const int n0 = nb * 128 + c * 32;
+          tmem_ld32(t_acc + HALF + c * 32, u);
+          const int n0 = nb * HALF + c * 32;
           const int valid = min(32, p.N - n0);
           if (m < p.M && valid > 0) {
 #pragma unroll
@@ -350,8 +387,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
       } else if constexpr (EPI == EPI_QKV) {
-        // each 128-column half of the tile is one head of [q heads | k heads | v heads];
-        // token s of sequence b sits at position start[b] + s, and only tokens s < lens[b]
+        // the tile's columns are part of [q heads | k heads | v heads]; token s of sequence b sits at position start[b] + s, and only tokens s < lens[b]
         // are stored (the others pad the chunk)
         const int b = m / p.S, s_in = m - (m / p.S) * p.S;
         int s = s_in;
@@ -366,63 +402,63 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           s = st + s_in;
         }
         const int half_d = p.D >> 1;
+        // 32-column chunks of the tile, each inside one head (D = 128): column col0 of
+        // [q heads | k heads | v heads] is element j0 of head hh
 #pragma unroll 1
-        for (int hf = 0; hf < 2; ++hf) {
-          const int hh = nb * 2 + hf;
+        for (int c = 0; c < BN / 32; ++c) {
+          const int col0 = nb * BN + c * 32;
+          const int hh = col0 / p.D, j0 = col0 - hh * p.D;
           if (hh >= p.H + 2 * p.G) break;
           if (p.rope_half && hh < p.H + p.G) {
-            // half-split pairs: columns 32c + i and 64 + 32c + i, angle index 32c + i
+            // half-split pairs (j, j + D/2), angle index j: the head's two halves are both in
+            // this tile (the host gives this form head-aligned 256-column tiles); the chunks
+            // of the first half take the pairs
+            if (j0 >= half_d) continue;
             __nv_bfloat16* dst = hh < p.H
                 ? p.q_out + ((static_cast<long long>(b) * p.H + hh) * p.S + s_in) * p.D
                 : p.k_cache + ((static_cast<long long>(b) * p.G + (hh - p.H)) * p.T_max + s) * p.D;
-#pragma unroll 1
-            for (int c = 0; c < 2; ++c) {
-              uint32_t r2[32];
-              tmem_ld32(t_acc + hf * 128 + c * 32, r);
-              tmem_ld32(t_acc + hf * 128 + 64 + c * 32, r2);
-              if (!keep) continue;
-              const float* cr = p.cos + static_cast<long long>(s) * half_d + c * 32;
-              const float* sr = p.sin + static_cast<long long>(s) * half_d + c * 32;
-              float w2[32];
+            uint32_t r2[32];
+            tmem_ld32(t_acc + c * 32, r);
+            tmem_ld32(t_acc + c * 32 + half_d, r2);
+            if (!keep) continue;
+            const float* cr = p.cos + static_cast<long long>(s) * half_d + j0;
+            const float* sr = p.sin + static_cast<long long>(s) * half_d + j0;
+            float w2[32];
 #pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                const float cs = cr[i], sn = sr[i];
-                const float x1 = __uint_as_float(r[i]), x2 = __uint_as_float(r2[i]);
-                v[i] = x1 * cs - x2 * sn;
-                w2[i] = x2 * cs + x1 * sn;
-              }
-              store_bf16x32(dst + c * 32, v, 32);
-              store_bf16x32(dst + 64 + c * 32, w2, 32);
+            for (int i = 0; i < 32; ++i) {
+              const float cs = cr[i], sn = sr[i];
+              const float x1 = __uint_as_float(r[i]), x2 = __uint_as_float(r2[i]);
+              v[i] = x1 * cs - x2 * sn;
+              w2[i] = x2 * cs + x1 * sn;
             }
+            store_bf16x32(dst + j0, v, 32);
+            store_bf16x32(dst + j0 + half_d, w2, 32);
             continue;
           }
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            tmem_ld32(t_acc + hf * 128 + c * 32, r);
-            if (!keep) continue;
+          tmem_ld32(t_acc + c * 32, r);
+          if (!keep) continue;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-            __nv_bfloat16* dst;
-            if (hh < p.H + p.G) {
-              // RoPE on q and k: pair (2i, 2i+1) rotated by angle s * base^(-2i/D)
-              const float* cr = p.cos + static_cast<long long>(s) * half_d + c * 16;
-              const float* sr = p.sin + static_cast<long long>(s) * half_d + c * 16;
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+          __nv_bfloat16* dst;
+          if (hh < p.H + p.G) {
+            // RoPE on q and k: pair (2i, 2i+1) rotated by angle s * base^(-2i/D)
+            const float* cr = p.cos + static_cast<long long>(s) * half_d + j0 / 2;
+            const float* sr = p.sin + static_cast<long long>(s) * half_d + j0 / 2;
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const float cs = cr[i], sn = sr[i];
-                const float e = v[2 * i], o = v[2 * i + 1];
-                v[2 * i] = e * cs - o * sn;
-                v[2 * i + 1] = e * sn + o * cs;
-              }
+            for (int i = 0; i < 16; ++i) {
+              const float cs = cr[i], sn = sr[i];
+              const float e = v[2 * i], o = v[2 * i + 1];
+              v[2 * i] = e * cs - o * sn;
+              v[2 * i + 1] = e * sn + o * cs;
             }
-            if (hh < p.H)
-              dst = p.q_out + ((static_cast<long long>(b) * p.H + hh) * p.S + s_in) * p.D;
-            else if (hh < p.H + p.G)
-              dst = p.k_cache + ((static_cast<long long>(b) * p.G + (hh - p.H)) * p.T_max + s) * p.D;
-            else
-              dst = p.v_cache + ((static_cast<long long>(b) * p.G + (hh - p.H - p.G)) * p.T_max + s) * p.D;
-            store_bf16x32(dst + c * 32, v, 32);
           }
+          if (hh < p.H)
+            dst = p.q_out + ((static_cast<long long>(b) * p.H + hh) * p.S + s_in) * p.D;
+          else if (hh < p.H + p.G)
+            dst = p.k_cache + ((static_cast<long long>(b) * p.G + (hh - p.H)) * p.T_max + s) * p.D;
+          else
+            dst = p.v_cache + ((static_cast<long long>(b) * p.G + (hh - p.H - p.G)) * p.T_max + s) * p.D;
+          store_bf16x32(dst + j0, v, 32);
         }
       } else if constexpr (EPI == EPI_PARTIAL) {
         // kernel M = weight rows, N = tokens: P[split][token][row] in fp32
@@ -481,15 +517,16 @@ int launch(const Ctx& c, const TMaps& tm, Params p) {
   return after_launch(c);
 }
 
-// Tile width (256 or 224 columns) whose rounds of num_sms tiles take the least time, time per
-// round taken as proportional to the width; ties keep 256.
+// Rounds of num_sms tiles times the tile width: the time of a GEMM with M rows and n_blocks
+// column blocks of width bn, a round's time taken as proportional to its width.
+long long round_cost(int M, int n_blocks, int bn, int num_sms) {
+  const long long tiles = static_cast<long long>((M + BM - 1) / BM) * n_blocks;
+  return (tiles + num_sms - 1) / num_sms * bn;
+}
+
+// Tile width (256 or 224 columns) with the least round cost for N output columns; ties keep 256.
 int tile_width_for(int M, int N, int num_sms) {
-  const long long mb = (M + BM - 1) / BM;
-  auto cost = [&](int bn) {
-    const long long tiles = mb * ((N + bn - 1) / bn);
-    return ((tiles + num_sms - 1) / num_sms) * bn;
-  };
-  return cost(224) < cost(256) ? 224 : 256;
+  return round_cost(M, (N + 223) / 224, 224, num_sms) < round_cost(M, (N + 255) / 256, 256, num_sms) ? 224 : 256;
 }
 
 Params base_params(int M, int N, int K, int BN) {
@@ -514,6 +551,8 @@ Params base_params(int M, int N, int K, int BN) {
   p.amap.seg_end[0] = 1 << 30;
   p.bmap.nseg = 1;
   p.bmap.seg_end[0] = 1 << 30;
+  p.b32_map0 = 0;
+  p.n_maps = 2;
   return p;
 }
 
@@ -552,16 +591,17 @@ int gemm_residual(const Ctx& c, const void* X, const void* W, const void* resid,
 }
 
 int gemm_swiglu(const Ctx& c, const void* X, const void* Wg, const void* Wu, void* out, int M, int I, int K) {
+  // kernel N runs over 256-column tiles, each = 128 gate rows + the same 128 up rows (measured:
+  // 240-column tiles, which fill the SM-count rounds better at I = 11008, M = 2048, run slower)
   TMaps tm{};
   if (!make_tmap_2d(&tm.m[0], X, K, M, K, 128) || !make_tmap_2d(&tm.m[1], Wg, K, I, K, 128) ||
       !make_tmap_2d(&tm.m[2], Wu, K, I, K, 128))
     return LLAMA_ERR_INVALID_ARG;
-  // kernel N runs over 256-column tiles, each = 128 gate rows + the same 128 up rows
   Params p = base_params(M, 2 * ((I + 127) / 128) * 128, K, 256);
   p.N = I;   // output width (used by the epilogue's bounds)
   p.a_map0 = 0;
   p.b_map0 = 1;
-  p.bmap.interleave = 1;
+  p.n_maps = 3;
   p.out = out;
   p.ldo = I;
   return launch<256, EPI_SWIGLU, 4>(c, tm, p);
@@ -572,13 +612,23 @@ int gemm_qkv_rope(const Ctx& c, const void* X, const void* Wq, const void* Wk, c
                   void* v_cache, int T_max, int rope_half, const int32_t* start, const int32_t* lens,
                   int max_pos) {
   const int M = B * S;
+  // 224-column tiles when they fill the SM-count rounds better (the half-split pairs (j, j+64)
+  // need whole heads in a tile: 256 columns = two heads); a 224-column tile that crosses the
+  // q|k or k|v boundary takes its weights in 32-row boxes from the maps at b32_map0
+  const int bn = rope_half ? 256 : tile_width_for(M, (H + 2 * G) * D, c.num_sms);
+  const int box = bn == 256 ? 128 : bn;
   TMaps tm{};
-  if (!make_tmap_2d(&tm.m[0], X, K, M, K, 128) || !make_tmap_2d(&tm.m[1], Wq, K, H * D, K, 128) ||
-      !make_tmap_2d(&tm.m[2], Wk, K, G * D, K, 128) || !make_tmap_2d(&tm.m[3], Wv, K, G * D, K, 128))
+  if (!make_tmap_2d(&tm.m[0], X, K, M, K, 128) || !make_tmap_2d(&tm.m[1], Wq, K, H * D, K, box) ||
+      !make_tmap_2d(&tm.m[2], Wk, K, G * D, K, box) || !make_tmap_2d(&tm.m[3], Wv, K, G * D, K, box))
     return LLAMA_ERR_INVALID_ARG;
-  Params p = base_params(M, (H + 2 * G) * D, K, 256);
+  if (bn != 256 && (!make_tmap_2d(&tm.m[4], Wq, K, H * D, K, 32) || !make_tmap_2d(&tm.m[5], Wk, K, G * D, K, 32) ||
+                    !make_tmap_2d(&tm.m[6], Wv, K, G * D, K, 32)))
+    return LLAMA_ERR_INVALID_ARG;
+  Params p = base_params(M, (H + 2 * G) * D, K, bn);
   p.a_map0 = 0;
   p.b_map0 = 1;
+  p.b32_map0 = 4;
+  p.n_maps = bn == 256 ? 4 : 7;
   p.bmap.nseg = 3;
   p.bmap.seg_end[0] = H * D;
   p.bmap.seg_end[1] = (H + G) * D;
@@ -597,7 +647,7 @@ int gemm_qkv_rope(const Ctx& c, const void* X, const void* Wq, const void* Wk, c
   p.q_out = static_cast<__nv_bfloat16*>(q_out);
   p.k_cache = static_cast<__nv_bfloat16*>(k_cache);
   p.v_cache = static_cast<__nv_bfloat16*>(v_cache);
-  return launch<256, EPI_QKV, 4>(c, tm, p);
+  return bn == 256 ? launch<256, EPI_QKV, 4>(c, tm, p) : launch<224, EPI_QKV, 5>(c, tm, p);
 }
 
 int choose_splits(int num_sms, int w_rows_total, int K, int n_tok) {
@@ -640,6 +690,7 @@ int gemm_tokens_partial(const Ctx& c, const void* const* W, const int* w_rows, i
   p.amap.nseg = n_w;
   p.a_map0 = 0;
   p.b_map0 = n_w;
+  p.n_maps = n_w + 1;
   splits = std::max(1, std::min(splits, p.num_kb));
   p.kb_per_split = (p.num_kb + splits - 1) / splits;
   p.num_splits = (p.num_kb + p.kb_per_split - 1) / p.kb_per_split;   // every split non-empty
