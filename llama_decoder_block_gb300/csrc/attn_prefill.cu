@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t tO = tmem_base + t_lane + 256 + t * 128;
       const float sl = p.scale_log2;
       float m_run = -INFINITY, l_run = 0.f;
-      uint32_t r[64];
+      uint32_t r[128];   // the row's 128 scores, then (first 64) its P as packed bf16 pairs
       bool ok = true;
       const int n_t = nkt[t];
       const int qpos = pos0 + qi;                     // this row's position: keys 0 .. qpos
@@ -237,28 +237,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!mbar_wait(smem_u32(s_full + t), j & 1, p.status, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const int kbase = j * BKV;
+        // the whole row of S in one TMEM round trip
+        tmem_ld128(tS, r);
         // the tile reaches past the first query's position: mask key > position
         const bool diag = kbase + BKV - 1 > pos0 + qb[t] * BQ;
-        float mx = -INFINITY;
-#pragma unroll 1
-        for (int hlf = 0; hlf < 2; ++hlf) {
-          tmem_ld64(tS + hlf * 64, r);
-          if (diag) {
+        if (diag) {
 #pragma unroll
-            for (int i = 0; i < 64; ++i)
-              if (kbase + hlf * 64 + i > qpos) r[i] = __float_as_uint(-INFINITY);
-          }
-          // two scores per max instruction (the ALU pipe is this loop's limit)
-#pragma unroll
-          for (int i = 0; i < 64; i += 2) mx = fmax3(mx, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+          for (int i = 0; i < 128; ++i)
+            if (kbase + i > qpos) r[i] = __float_as_uint(-INFINITY);
         }
+        // two scores per max instruction (the ALU pipe is this loop's limit)
+        float mx = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 128; i += 2) mx = fmax3(mx, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
         const float mxs = mx * sl;
         const bool need = mxs > m_run + kRescaleLog2;    // also true on the first tile
-        if (__any_sync(0xffffffffu, need)) {
-          const float m_new = need ? mxs : m_run;
-          const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
+        const bool any_need = __any_sync(0xffffffffu, need);
+        const float m_new = need ? mxs : m_run;
+        const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
+        m_run = m_new;
+        // P = 2^(S * scale - m) (masked scores are -inf: P = 0), packed in place: pair i goes
+        // to r[i] once r[2i], r[2i + 1] are read; keys 2c, 2c+1 land in S column c
+        float rowsum = 0.f;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(r[2 * i]), sl, -m_run));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(r[2 * i + 1]), sl, -m_run));
+          rowsum += p0 + p1;
+          r[i] = pack_bf16(p0, p1);
+        }
+        tmem_st64(tS, r);
+        if (any_need) {
           if (j > 0) {
-            // P_{j-1} V_{j-1} must have landed before O is rescaled
+            // P_{j-1} V_{j-1} must have landed before O is rescaled (and O must be rescaled
+            // before this tile's P V, which waits for p_full below)
             if (!mbar_wait(smem_u32(o_done + t), (j - 1) & 1, p.status, abort_flag)) { ok = false; break; }
             tc_fence_after();
             uint32_t o32[32];
@@ -271,27 +283,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
           l_run *= alpha;
-          m_run = m_new;
-        }
-        float rowsum = 0.f;
-#pragma unroll 1
-        for (int hlf = 0; hlf < 2; ++hlf) {
-          tmem_ld64(tS + hlf * 64, r);
-          uint32_t pk[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int key = kbase + hlf * 64 + 2 * i;
-            float p0 = ex2_approx(fmaf(__uint_as_float(r[2 * i]), sl, -m_run));
-            float p1 = ex2_approx(fmaf(__uint_as_float(r[2 * i + 1]), sl, -m_run));
-            if (diag) {
-              if (key > qpos) p0 = 0.f;
-              if (key + 1 > qpos) p1 = 0.f;
-            }
-            rowsum += p0 + p1;
-            pk[i] = pack_bf16(p0, p1);
-          }
-          // keys 64*hlf .. 64*hlf+63 as 32 packed columns over S columns already read
-          tmem_st32(tS + hlf * 32, pk);
         }
         l_run += rowsum;
         // keys at or past the last valid one: zero their V rows before any P V of this tile

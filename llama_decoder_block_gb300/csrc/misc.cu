@@ -26,12 +26,22 @@ __global__ void embed_kernel(const int32_t* __restrict__ tokens, const uint4* __
   for (int i = lane; i < vec_per_row; i += 32) dst[i] = __ldg(src + i);
 }
 
-// Sum over the splits of 4 consecutive fp32 partials (16-byte aligned).
+// Sum over the splits of 4 consecutive fp32 partials (16-byte aligned), in split order.  The
+// loads of the first MAXL splits are all issued before the first add (a fixed, predicated
+// unroll), so a thread waits for one round trip to L2, not one per split.
+template <int MAXL = 4>
 __device__ __forceinline__ float4 split_sum4(const float* P, int splits, long long stride, long long idx) {
-  float4 a = *reinterpret_cast<const float4*>(P + idx);
-  for (int s = 1; s < splits; ++s) {
-    const float4 b = *reinterpret_cast<const float4*>(P + s * stride + idx);
-    a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+  float4 b[MAXL];
+#pragma unroll
+  for (int s = 0; s < MAXL; ++s)
+    if (s < splits) b[s] = __ldcs(reinterpret_cast<const float4*>(P + s * stride + idx));
+  float4 a = b[0];
+#pragma unroll
+  for (int s = 1; s < MAXL; ++s)
+    if (s < splits) { a.x += b[s].x; a.y += b[s].y; a.z += b[s].z; a.w += b[s].w; }
+  for (int s = MAXL; s < splits; ++s) {
+    const float4 c = __ldcs(reinterpret_cast<const float4*>(P + s * stride + idx));
+    a.x += c.x; a.y += c.y; a.z += c.z; a.w += c.w;
   }
   return a;
 }
@@ -113,7 +123,8 @@ __global__ void fix_residual_kernel(const float* __restrict__ P, int splits, int
 
 // One CTA per token: h = resid + sum of the splits (stored in bf16), then hn = RMSNorm(h) from
 // the stored h ("12 · 从 Transformer 到 LLaMA 系列" §八 RMSNorm; fp32 arithmetic).
-__global__ void __launch_bounds__(256) fix_residual_rmsnorm_kernel(const float* __restrict__ P, int splits,
+constexpr int kNormFixThreads = 512;
+__global__ void __launch_bounds__(kNormFixThreads) fix_residual_rmsnorm_kernel(const float* __restrict__ P, int splits,
                                                                    int n_tok, int N,
                                                                    const __nv_bfloat16* __restrict__ resid,
                                                                    const __nv_bfloat16* __restrict__ gamma, float eps,
@@ -121,8 +132,9 @@ __global__ void __launch_bounds__(256) fix_residual_rmsnorm_kernel(const float* 
                                                                    __nv_bfloat16* __restrict__ hn_out) {
   pdl_trigger();
   pdl_wait();
-  constexpr int MAXV = 8;   // 4-column groups per thread: N <= 256 * 4 * 8 = 8192
-  __shared__ float red[8];
+  constexpr int MAXV = 4;   // 4-column groups per thread: N <= 512 * 4 * 4 = 8192
+  constexpr int WARPS = kNormFixThreads / 32;
+  __shared__ float red[WARPS];
   const int t = blockIdx.x;
   const long long row = static_cast<long long>(t) * N;
   float hv[MAXV][4];
@@ -131,7 +143,7 @@ __global__ void __launch_bounds__(256) fix_residual_rmsnorm_kernel(const float* 
   for (int i = 0; i < MAXV; ++i) {
     const int col = (i * blockDim.x + threadIdx.x) * 4;
     if (col < N) {
-      const float4 v = split_sum4(P, splits, static_cast<long long>(n_tok) * N, row + col);
+      const float4 v = split_sum4<8>(P, splits, static_cast<long long>(n_tok) * N, row + col);
       const uint2 r = *reinterpret_cast<const uint2*>(resid + row + col);
       const uint32_t w0 = pack_bf16(bf16_lo(r.x) + v.x, bf16_hi(r.x) + v.y);
       const uint32_t w1 = pack_bf16(bf16_lo(r.y) + v.z, bf16_hi(r.y) + v.w);
@@ -147,7 +159,7 @@ __global__ void __launch_bounds__(256) fix_residual_rmsnorm_kernel(const float* 
   __syncthreads();
   float tot = 0.f;
 #pragma unroll
-  for (int w = 0; w < 8; ++w) tot += red[w];
+  for (int w = 0; w < WARPS; ++w) tot += red[w];
   const float r = rsqrtf(tot / static_cast<float>(N) + eps);
 #pragma unroll
   for (int i = 0; i < MAXV; ++i) {
@@ -229,8 +241,8 @@ int fix_residual(const Ctx& c, const float* P, int splits, int n_tok, int N, con
 int fix_residual_rmsnorm(const Ctx& c, const float* P, int splits, int n_tok, int N, const void* resid,
                          const void* gamma, float eps, void* h_out, void* hn_out) {
   if (n_tok == 0) return LLAMA_OK;
-  if (N % 4 != 0 || N > 256 * 4 * 8) return LLAMA_ERR_UNSUPPORTED;
-  launch_pdl(c, fix_residual_rmsnorm_kernel, dim3(n_tok), dim3(256), 0,
+  if (N % 4 != 0 || N > kNormFixThreads * 4 * 4) return LLAMA_ERR_UNSUPPORTED;
+  launch_pdl(c, fix_residual_rmsnorm_kernel, dim3(n_tok), dim3(kNormFixThreads), 0,
       P, splits, n_tok, N, static_cast<const __nv_bfloat16*>(resid), static_cast<const __nv_bfloat16*>(gamma), eps,
       static_cast<__nv_bfloat16*>(h_out), static_cast<__nv_bfloat16*>(hn_out));
   return after_launch(c);
