@@ -33,6 +33,21 @@ DECODE_KERNELS = ["rmsnorm_attn", "qkv_gemm_stream", "qkv_rope_fixup", "attentio
                   "gate_up_gemm_stream", "swiglu_fixup", "down_gemm_stream", "down_residual_fixup"]
 L2_FLUSH_BYTES = 256 << 20
 
+
+class L2Flush:
+    """Run between timed steps: write a 256 MiB buffer (evicts everything from the 129 MB L2),
+    then read another 256 MiB, so that the write's dirty lines go back to HBM here and not
+    inside the next timed region (where they would cost an HBM-bound kernel ~19 us)."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.sum()
+
 # DRAM bytes (read + write) per launch from ncu captures, keyed by kernel and the sha1 of
 # the source file it was measured on; a changed source makes the figure stale (null).
 NCU_TRAFFIC = {("gate_up_swiglu_gemm", "4257e441288b"): 229686272}   # profiles/gemm_gate_up_mha7b_b1_s2048.md
@@ -167,10 +182,10 @@ def bench_stack(api, wl, steps, warmup, dev, pk):
     c, s = api.rope_tables(L.rope_base, L.head_dim, S)
     cos, sin = torch.from_numpy(c).to(dev), torch.from_numpy(s).to(dev)
     ws = api.workspace(st.workspace_bytes(B, S), dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     ts = []
     for i in range(warmup + steps):
-        flush.zero_()
+        flush()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         api.stack_forward(st, tokens, logits, cos, sin, ws)
@@ -283,14 +298,14 @@ def bench_prefill(api, wl, steps, warmup, dev, pk, from_synth):
     vc = torch.empty_like(kc)
     dims = api.Dims(L.d_model, L.n_heads, L.n_kv_heads, L.head_dim, L.d_inter, L.rms_eps, torch.bfloat16)
     ws = api.workspace(api.prefill_workspace_bytes(dims, B, S), dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
 
     def step():
         api.layer_prefill(dims, w, x, out, cos, sin, kc, vc, ws, stream)
 
     for _ in range(warmup):
-        flush.zero_()
+        flush()
         step()
     torch.cuda.synchronize()
     assert api.device_status(stream) == 0
@@ -302,7 +317,7 @@ def bench_prefill(api, wl, steps, warmup, dev, pk, from_synth):
     n0 = api.launch_count()
     t0 = time.perf_counter()
     for e0, e1 in evs:
-        flush.zero_()
+        flush()
         e0.record(stream)
         step()
         e1.record(stream)
@@ -315,7 +330,7 @@ def bench_prefill(api, wl, steps, warmup, dev, pk, from_synth):
     # kernel by kernel: the same steps again with the library's per-kernel events
     traces = [api.KernelTrace(len(PREFILL_KERNELS), stream) for _ in range(steps)]
     for tr in traces:
-        flush.zero_()
+        flush()
         with tr:
             step()
     torch.cuda.synchronize()
@@ -406,14 +421,14 @@ def bench_decode(api, wl, steps, warmup, dev, pk):
     cos, sin = torch.from_numpy(c).to(dev), torch.from_numpy(s).to(dev)
     dims = api.Dims(L.d_model, L.n_heads, L.n_kv_heads, L.head_dim, L.d_inter, L.rms_eps, torch.bfloat16)
     ws = api.workspace(api.decode_workspace_bytes(dims, B, T), dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
 
     def step():
         api.layer_decode(dims, w, x, out, cos, sin, pos, kc, vc, ws, stream)
 
     for _ in range(warmup):
-        flush.zero_()
+        flush()
         step()
     torch.cuda.synchronize()
     assert api.device_status(stream) == 0
@@ -421,7 +436,7 @@ def bench_decode(api, wl, steps, warmup, dev, pk):
     # for the per-kernel times
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for e0, e1 in evs:
-        flush.zero_()
+        flush()
         e0.record(stream)
         step()
         e1.record(stream)
@@ -430,7 +445,7 @@ def bench_decode(api, wl, steps, warmup, dev, pk):
     step_ms = np.array([e0.elapsed_time(e1) for e0, e1 in evs])
     traces = [api.KernelTrace(len(DECODE_KERNELS), stream) for _ in range(steps)]
     for tr in traces:
-        flush.zero_()
+        flush()
         with tr:
             step()
     torch.cuda.synchronize()
@@ -464,14 +479,14 @@ def bench_norm(api, dev, pk, kind, rows=16384, d=4096, reps=20):
     g = torch.ones(d, dtype=torch.bfloat16, device=dev)
     bt = torch.zeros(d, dtype=torch.bfloat16, device=dev)
     y = torch.empty_like(xs[0])
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     if kind == "rmsnorm":
         fn = lambda x: api.rmsnorm(x, g, y, 1e-5)
     else:
         fn = lambda x: api.layernorm(x, g, bt, y, 1e-5)
     ts = []
     for i in range(reps + 3):
-        flush.zero_()
+        flush()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         fn(xs[i % 2])
@@ -558,10 +573,10 @@ def bench_case(api, case, wl, steps, warmup, dev, pk):
         y = torch.empty_like(x)
         fn = lambda: api.rmsnorm(x, gm, y, L.rms_eps)
         work, unit = 2.0 * M * d * 2, "byte"
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     ts = []
     for i in range(warmup + steps):
-        flush.zero_()
+        flush()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         fn()
@@ -663,7 +678,7 @@ def main():
     cfg = {"workload": MAIN, "B": wl.B, "S": wl.S, "d": L.d_model, "H": L.n_heads, "G": L.n_kv_heads,
            "D": L.head_dim, "d_inter": L.d_inter, "layers": 1, "global_batch": wl.B * max(world, 1),
            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-           "l2": "flushed between timed steps (256 MiB write); weights 404 MB > L2"}
+           "l2": "flushed between timed steps (256 MiB write, then 256 MiB read); weights 404 MB > L2"}
 
     if args.impl == "reference":
         if rank != 0:
