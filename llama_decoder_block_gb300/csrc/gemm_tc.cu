@@ -341,8 +341,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       float v[32];
 
       if constexpr (EPI == EPI_BF16 || EPI == EPI_F32 || EPI == EPI_RESID) {
+        // residual rows of the next chunk are loaded one chunk ahead (their latency then
+        // overlaps this chunk's TMEM load, add and store)
+        uint4 res_n[4];
+        auto load_resid = [&](int c) {
+          if constexpr (EPI == EPI_RESID) {
+            const int n0 = nb * BN + c * 32;
+            if (c < BN / 32 && m < p.M && n0 + 32 <= p.N) {
+              const uint4* src = reinterpret_cast<const uint4*>(p.resid + m * p.ldr + n0);
+#pragma unroll
+              for (int g = 0; g < 4; ++g) res_n[g] = src[g];
+            }
+          }
+        };
+        load_resid(0);
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
+          uint4 res_c[4];
+#pragma unroll
+          for (int g = 0; g < 4; ++g) res_c[g] = res_n[g];
+          load_resid(c + 1);
           tmem_ld32(t_acc + c * 32, r);
           const int n0 = nb * BN + c * 32;
           const int valid = min(32, p.N - n0);
@@ -361,7 +379,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             } else {
               if constexpr (EPI == EPI_RESID) {
                 float rr[32];
-                load_bf16x32(p.resid + m * p.ldr + n0, rr, valid);
+                if (valid >= 32) {
+#pragma unroll
+                  for (int g = 0; g < 4; ++g) {
+                    const uint4 w = res_c[g];
+                    rr[8 * g + 0] = bf16_lo(w.x); rr[8 * g + 1] = bf16_hi(w.x);
+                    rr[8 * g + 2] = bf16_lo(w.y); rr[8 * g + 3] = bf16_hi(w.y);
+                    rr[8 * g + 4] = bf16_lo(w.z); rr[8 * g + 5] = bf16_hi(w.z);
+                    rr[8 * g + 6] = bf16_lo(w.w); rr[8 * g + 7] = bf16_hi(w.w);
+                  }
+                } else {
+                  load_bf16x32(p.resid + m * p.ldr + n0, rr, valid);
+                }
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] += rr[i];
               }
@@ -402,6 +431,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           s = st + s_in;
         }
         const int half_d = p.D >> 1;
+        // even/odd RoPE angles of chunk c (16 pairs) for this row's position, when chunk c is
+        // part of a q or k head of this tile
+        float cs_n[16], sn_n[16];
+        auto load_angles = [&](int c) {
+          const int col0 = nb * BN + c * 32;
+          const int hh = col0 / p.D, j0 = col0 - hh * p.D;
+          if (p.rope_half || !keep || c >= BN / 32 || hh >= p.H + p.G) return;
+          const float4* cr = reinterpret_cast<const float4*>(p.cos + static_cast<long long>(s) * half_d + j0 / 2);
+          const float4* sr = reinterpret_cast<const float4*>(p.sin + static_cast<long long>(s) * half_d + j0 / 2);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float4 cv = cr[i], sv = sr[i];
+            cs_n[4 * i] = cv.x; cs_n[4 * i + 1] = cv.y; cs_n[4 * i + 2] = cv.z; cs_n[4 * i + 3] = cv.w;
+            sn_n[4 * i] = sv.x; sn_n[4 * i + 1] = sv.y; sn_n[4 * i + 2] = sv.z; sn_n[4 * i + 3] = sv.w;
+          }
+        };
+        load_angles(0);
         // 32-column chunks of the tile, each inside one head (D = 128): column col0 of
         // [q heads | k heads | v heads] is element j0 of head hh
 #pragma unroll 1
@@ -435,6 +481,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             store_bf16x32(dst + j0 + half_d, w2, 32);
             continue;
           }
+          // this chunk's angles were loaded during the previous chunk; load the next chunk's
+          // now, so that their L2 latency overlaps this chunk's TMEM load and arithmetic
+          float cs_c[16], sn_c[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            cs_c[i] = cs_n[i];
+            sn_c[i] = sn_n[i];
+          }
+          load_angles(c + 1);
           tmem_ld32(t_acc + c * 32, r);
           if (!keep) continue;
 #pragma unroll
@@ -442,14 +497,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           __nv_bfloat16* dst;
           if (hh < p.H + p.G) {
             // RoPE on q and k: pair (2i, 2i+1) rotated by angle s * base^(-2i/D)
-            const float* cr = p.cos + static_cast<long long>(s) * half_d + j0 / 2;
-            const float* sr = p.sin + static_cast<long long>(s) * half_d + j0 / 2;
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-              const float cs = cr[i], sn = sr[i];
               const float e = v[2 * i], o = v[2 * i + 1];
-              v[2 * i] = e * cs - o * sn;
-              v[2 * i + 1] = e * sn + o * cs;
+              v[2 * i] = e * cs_c[i] - o * sn_c[i];
+              v[2 * i + 1] = e * sn_c[i] + o * cs_c[i];
             }
           }
           if (hh < p.H)
