@@ -42,7 +42,9 @@ class L2Flush:
     def __init__(self, dev):
         import torch
         self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-        self.r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+        # fp32, so that the sum reads the buffer as it is (an integer sum would first widen it
+        # to int64 in a temporary copy: new dirty lines)
+        self.r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
     def __call__(self):
         self.w.zero_()
@@ -50,7 +52,7 @@ class L2Flush:
 
 # DRAM bytes (read + write) per launch from ncu captures, keyed by kernel and the sha1 of
 # the source file it was measured on; a changed source makes the figure stale (null).
-NCU_TRAFFIC = {("gate_up_swiglu_gemm", "4257e441288b"): 229686272}   # profiles/gemm_gate_up_mha7b_b1_s2048.md
+NCU_TRAFFIC = {("gate_up_swiglu_gemm", "c575456b95fd"): 229662976}   # profiles/gemm_gate_up_mha7b_b1_s2048.md
 
 
 def parse():
