@@ -48,6 +48,7 @@ constexpr float kRescaleLog2 = 8.0f;  // rescale O when the max grows by more th
 
 struct AttnParams {
   int B, S, H, G, n_qt, n_pairs;
+  int n_items;                        // n_pairs * H * B work items (one query pair of one head)
   const int32_t* start;               // [B] or null (0)
   const int32_t* lens;                // [B] or null (S)
   int T_max, max_pos;
@@ -55,6 +56,51 @@ struct AttnParams {
   __nv_bfloat16* out;                 // [B, S, H*D]
   int* status;
 };
+
+// Work item i: the (z+1)-th longest query pair (z = i / (H B)) of head h, sequence b (h varies
+// fastest, so the heads that share a KV head sit next to each other).  CTA c takes items
+// c, 2G-1-c, 2G+c, 4G-1-c, ... (G CTAs): a snake over rounds of G items, so a CTA that drew
+// one of the longest pairs in a round draws one of the shortest in the next.
+struct AttnItem {
+  int b, h, g, pair, pos0, len;
+  bool hasA, hasB;
+  int nkt[2], nt, n_valid;
+};
+
+__device__ __forceinline__ int item_of(int c, int r) {
+  const int G = static_cast<int>(gridDim.x);
+  return r * G + ((r & 1) ? G - 1 - c : c);
+}
+
+__device__ __forceinline__ AttnItem make_item(const AttnParams& p, int i, bool report_bounds) {
+  AttnItem it;
+  const int hb = p.H * p.B;
+  const int z = i / hb, rem = i - z * hb;
+  it.b = rem / p.H;
+  it.h = rem - it.b * p.H;
+  it.g = it.h / (p.H / p.G);
+  it.pair = p.n_pairs - 1 - z;
+  // this sequence's chunk: queries [0, len) at positions pos0 + s; keys [0, pos0 + len)
+  it.pos0 = 0;
+  it.len = p.S;
+  if (p.start != nullptr) {
+    it.pos0 = p.start[it.b];
+    it.len = p.lens != nullptr ? p.lens[it.b] : p.S;
+    if (it.pos0 < 0 || it.len < 0 || it.len > p.S || it.pos0 + it.len > p.T_max || it.pos0 + it.len > p.max_pos) {
+      if (report_bounds && z == 0 && it.h == 0) report(p.status, LLAMA_ERR_DEVICE_BOUNDS);
+      it.len = 0;
+    }
+  }
+  const int qa = 2 * it.pair, qb = 2 * it.pair + 1;
+  it.hasA = qa * BQ < it.len;
+  it.hasB = qb * BQ < it.len;
+  // key tiles that tile t reads: up to the position of its last query
+  it.nkt[0] = it.hasA ? (it.pos0 + min(qa * BQ + BQ, it.len) - 1) / BKV + 1 : 0;
+  it.nkt[1] = it.hasB ? (it.pos0 + min(qb * BQ + BQ, it.len) - 1) / BKV + 1 : 0;
+  it.nt = it.hasB ? it.nkt[1] : it.nkt[0];
+  it.n_valid = it.pos0 + it.len;
+  return it;
+}
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -73,17 +119,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* p_full = bars + 7;          // [2] per tile
   uint64_t* o_done = bars + 9;          // [2] per tile
   uint64_t* drain = bars + 11;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  uint64_t* q_empty = bars + 12;        // the Q tiles of an item may be overwritten
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int pair = p.n_pairs - 1 - static_cast<int>(blockIdx.z);
-  const int h = blockIdx.x, b = blockIdx.y;
-  const int g = h / (p.H / p.G);
-  const int qb[2] = {2 * pair, 2 * pair + 1};
+  const int c = static_cast<int>(blockIdx.x);
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(q_full), 1);
+    mbar_init(smem_u32(q_empty), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(kv_full + i), 1);
       mbar_init(smem_u32(kv_empty + i), 1);
@@ -110,53 +155,48 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
   pdl_wait();   // inputs written by the previous kernel are read from here on
 
-  // this sequence's chunk: queries [0, len) at positions pos0 + s; keys [0, pos0 + len)
-  int pos0 = 0, len = p.S;
-  if (p.start != nullptr) {
-    pos0 = p.start[b];
-    len = p.lens != nullptr ? p.lens[b] : p.S;
-    if (pos0 < 0 || len < 0 || len > p.S || pos0 + len > p.T_max || pos0 + len > p.max_pos) {
-      if (threadIdx.x == 0 && blockIdx.z == 0 && h == 0) report(p.status, LLAMA_ERR_DEVICE_BOUNDS);
-      len = 0;
-    }
-  }
-  const bool hasA = qb[0] * BQ < len, hasB = qb[1] * BQ < len;
-  // key tiles that tile t reads: up to the position of its last query
-  const int nkt[2] = {hasA ? (pos0 + min(qb[0] * BQ + BQ, len) - 1) / BKV + 1 : 0,
-                      hasB ? (pos0 + min(qb[1] * BQ + BQ, len) - 1) / BKV + 1 : 0};
-  const int nt = hasB ? nkt[1] : nkt[0];
-  const int n_valid = pos0 + len;
-
-  if (!hasA) {
-    // nothing of this sequence falls into these query tiles
-  } else if (warp == 0) {
+  // Every role walks the same items in the same order; the barrier phases run on across items:
+  // K/V tile g of the CTA (counted over its items) sits in stage g & 1, and S/P of tile t and
+  // the O products of tile t are counted per tile.
+  if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ TMA producer
       bool ok = true;
-      int issued = 0;
-      const uint32_t qbar = smem_u32(q_full);
-      const int qplane = b * p.H + h;
-      mbar_expect_tx(qbar, hasB ? 2 * TILE : TILE);
-      for (int t = 0; t < (hasB ? 2 : 1); ++t) {
-        tma_load_3d(smem_u32(sQ + t * TILE), &tmQ, qbar, 0, qb[t] * BQ, qplane);
-        tma_load_3d(smem_u32(sQ + t * TILE + CHUNK), &tmQ, qbar, 64, qb[t] * BQ, qplane);
-      }
-      for (int j = 0; j < nt; ++j) {
-        const int st = j & 1;
-        if (!mbar_wait(smem_u32(kv_empty + st), ((j >> 1) & 1) ^ 1u, p.status, abort_flag)) { ok = false; break; }
-        const uint32_t fb = smem_u32(kv_full + st);
-        mbar_expect_tx(fb, 2 * TILE);
-        const int row = j * BKV, plane = b * p.G + g;
-        tma_load_3d(smem_u32(sK + st * TILE), &tmK, fb, 0, row, plane);
-        tma_load_3d(smem_u32(sK + st * TILE + CHUNK), &tmK, fb, 64, row, plane);
-        tma_load_3d(smem_u32(sV + st * TILE), &tmV, fb, 0, row, plane);
-        tma_load_3d(smem_u32(sV + st * TILE + CHUNK), &tmV, fb, 64, row, plane);
-        ++issued;
+      uint32_t kvc = 0, qc = 0;
+      for (int r = 0; ok; ++r) {
+        const int i = item_of(c, r);
+        if (i >= p.n_items) break;
+        const AttnItem it = make_item(p, i, true);
+        if (!it.hasA) continue;
+        // the previous item's S products have read its Q tiles
+        if (qc > 0 && !mbar_wait(smem_u32(q_empty), (qc - 1) & 1, p.status, abort_flag)) { ok = false; break; }
+        const uint32_t qbar = smem_u32(q_full);
+        const int qplane = it.b * p.H + it.h;
+        mbar_expect_tx(qbar, it.hasB ? 2 * TILE : TILE);
+        for (int t = 0; t < (it.hasB ? 2 : 1); ++t) {
+          const int qrow = (2 * it.pair + t) * BQ;
+          tma_load_3d(smem_u32(sQ + t * TILE), &tmQ, qbar, 0, qrow, qplane);
+          tma_load_3d(smem_u32(sQ + t * TILE + CHUNK), &tmQ, qbar, 64, qrow, qplane);
+        }
+        ++qc;
+        const int plane = it.b * p.G + it.g;
+        for (int j = 0; j < it.nt; ++j, ++kvc) {
+          const uint32_t st = kvc & 1;
+          if (!mbar_wait(smem_u32(kv_empty + st), ((kvc >> 1) & 1) ^ 1u, p.status, abort_flag)) { ok = false; break; }
+          const uint32_t fb = smem_u32(kv_full + st);
+          mbar_expect_tx(fb, 2 * TILE);
+          const int row = j * BKV;
+          tma_load_3d(smem_u32(sK + st * TILE), &tmK, fb, 0, row, plane);
+          tma_load_3d(smem_u32(sK + st * TILE + CHUNK), &tmK, fb, 64, row, plane);
+          tma_load_3d(smem_u32(sV + st * TILE), &tmV, fb, 0, row, plane);
+          tma_load_3d(smem_u32(sV + st * TILE + CHUNK), &tmV, fb, 64, row, plane);
+        }
       }
       if (!ok) {
-        mbar_wait_slow(qbar, 0, nullptr, nullptr, kWaitBudgetNs);
-        for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j)
-          mbar_wait_slow(smem_u32(kv_full + (j & 1)), (j >> 1) & 1, nullptr, nullptr, kWaitBudgetNs);
+        // leave no copy in flight: the last Q load and the last two K/V loads
+        if (qc > 0) mbar_wait_slow(smem_u32(q_full), (qc - 1) & 1, nullptr, nullptr, kWaitBudgetNs);
+        for (uint32_t g = (kvc > 2 ? kvc - 2 : 0); g < kvc; ++g)
+          mbar_wait_slow(smem_u32(kv_full + (g & 1)), (g >> 1) & 1, nullptr, nullptr, kWaitBudgetNs);
       }
     }
   } else if (warp == 1) {
@@ -164,9 +204,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // ------------------------------------------------------------ MMA issuer
       constexpr uint32_t IDESC_QK = idesc_bf16(128, 128, false);
       constexpr uint32_t IDESC_PV = idesc_bf16(128, 128, true);
-      auto active = [&](int t, int j) { return j < nkt[t]; };
-      auto issue_s = [&](int t, int j) {
-        const uint32_t aq = smem_u32(sQ + t * TILE), bk = smem_u32(sK + (j & 1) * TILE);
+      auto issue_s = [&](int t, uint32_t st) {
+        const uint32_t aq = smem_u32(sQ + t * TILE), bk = smem_u32(sK + st * TILE);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * CHUNK + (kk & 3) * 32;
@@ -175,42 +214,64 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         tc_commit(smem_u32(s_full + t));
       };
-      auto issue_pv = [&](int t, int j) {
-        const uint32_t bv = smem_u32(sV + (j & 1) * TILE);
+      auto issue_pv = [&](int t, uint32_t st, bool first) {
+        const uint32_t bv = smem_u32(sV + st * TILE);
 #pragma unroll
         for (int kk = 0; kk < BKV / 16; ++kk) {
           // V: 128 key rows of 128 bytes per 64-wide d half; K step = 16 rows = 2048 bytes,
           // the second d half is CHUNK bytes further (leading byte offset), 8-row groups 1024 apart
           tc_mma_bf16_ts(tmem_base + 256 + t * 128, tmem_base + t * 128 + kk * 8,
-                         sdesc_sw128(bv + kk * 2048, CHUNK, 1024), IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+                         sdesc_sw128(bv + kk * 2048, CHUNK, 1024), IDESC_PV, (!first || kk > 0) ? 1u : 0u);
         }
         tc_commit(smem_u32(o_done + t));
       };
-      bool ok = mbar_wait(smem_u32(q_full), 0, p.status, abort_flag) &&
-                mbar_wait(smem_u32(kv_full), 0, p.status, abort_flag);
-      bool issued = false;
-      if (ok) {
-        tc_fence_after();
-        issue_s(0, 0);
-        if (hasB) issue_s(1, 0);
-        issued = true;
-      }
-      for (int j = 0; j < nt && ok; ++j) {
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (!active(t, j)) continue;
-          if (!mbar_wait(smem_u32(p_full + t), j & 1, p.status, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-          issue_pv(t, j);
-          if (active(t, j + 1)) {
-            if (!mbar_wait(smem_u32(kv_full + ((j + 1) & 1)), ((j + 1) >> 1) & 1, p.status, abort_flag)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            issue_s(t, j + 1);
-          }
+      bool ok = true, issued = false;
+      uint32_t kvc = 0, qc = 0;
+      uint32_t pc[2] = {0u, 0u};   // P arrivals consumed, per tile
+      for (int r = 0; ok; ++r) {
+        const int i = item_of(c, r);
+        if (i >= p.n_items) break;
+        const AttnItem it = make_item(p, i, false);
+        if (!it.hasA) continue;
+        auto active = [&](int t, int j) { return j < it.nkt[t]; };
+        if (!mbar_wait(smem_u32(q_full), qc & 1, p.status, abort_flag) ||
+            !mbar_wait(smem_u32(kv_full + (kvc & 1)), (kvc >> 1) & 1, p.status, abort_flag)) {
+          ok = false;
+          break;
         }
-        if (ok) tc_commit(smem_u32(kv_empty + (j & 1)));
+        tc_fence_after();
+        // the Q tiles are free for the next item once this item's last S product is done:
+        // commit q_empty right after issuing it
+        int s_left = it.nkt[0] + it.nkt[1];
+        auto issue_s_counted = [&](int t, uint32_t st) {
+          issue_s(t, st);
+          if (--s_left == 0) tc_commit(smem_u32(q_empty));
+        };
+        issue_s_counted(0, kvc & 1);
+        if (it.hasB) issue_s_counted(1, kvc & 1);
+        issued = true;
+        for (int j = 0; j < it.nt && ok; ++j) {
+          const uint32_t g = kvc + j;
+          for (int t = 0; t < 2 && ok; ++t) {
+            if (!active(t, j)) continue;
+            if (!mbar_wait(smem_u32(p_full + t), pc[t] & 1, p.status, abort_flag)) { ok = false; break; }
+            ++pc[t];
+            tc_fence_after();
+            issue_pv(t, g & 1, j == 0);
+            if (active(t, j + 1)) {
+              if (!mbar_wait(smem_u32(kv_full + ((g + 1) & 1)), ((g + 1) >> 1) & 1, p.status, abort_flag)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              issue_s_counted(t, (g + 1) & 1);
+            }
+          }
+          if (ok) tc_commit(smem_u32(kv_empty + (g & 1)));
+        }
+        if (!ok) break;
+        kvc += it.nt;
+        ++qc;
       }
       if (!ok && issued) {
         tc_commit(smem_u32(drain));
@@ -220,66 +281,75 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else if (warp >= 4) {
     // -------------------------------------------------------------- softmax of tile t
     const int t = (warp - 4) >> 2;
-    if (t == 0 || hasB) {
-      const int quarter = warp & 3;
-      const int row = quarter * 32 + lane;
-      const int qi = qb[t] * BQ + row;
-      const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
-      const uint32_t tS = tmem_base + t_lane + t * 128;        // S, and P written over it
-      const uint32_t tO = tmem_base + t_lane + 256 + t * 128;
-      const float sl = p.scale_log2;
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tmem_base + t_lane + t * 128;        // S, and P written over it
+    const uint32_t tO = tmem_base + t_lane + 256 + t * 128;
+    const float sl = p.scale_log2;
+    uint32_t r[128];   // the row's 128 scores, then (first 64) its P as packed bf16 pairs
+    bool ok = true;
+    uint32_t kvc = 0, tc_run = 0;   // K/V tiles of the CTA's items so far; S tiles of tile t so far
+    for (int rr = 0; ok; ++rr) {
+      const int i = item_of(c, rr);
+      if (i >= p.n_items) break;
+      const AttnItem it = make_item(p, i, false);
+      if (!it.hasA) continue;
+      const uint32_t kvbase = kvc;
+      kvc += it.nt;
+      if (t == 1 && !it.hasB) continue;   // this item has no second query tile
+      const int qi = (2 * it.pair + t) * BQ + row;
       float m_run = -INFINITY, l_run = 0.f;
-      uint32_t r[128];   // the row's 128 scores, then (first 64) its P as packed bf16 pairs
-      bool ok = true;
-      const int n_t = nkt[t];
-      const int qpos = pos0 + qi;                     // this row's position: keys 0 .. qpos
+      const int n_t = it.nkt[t];
+      const int qpos = it.pos0 + qi;                 // this row's position: keys 0 .. qpos
       for (int j = 0; j < n_t; ++j) {
-        if (!mbar_wait(smem_u32(s_full + t), j & 1, p.status, abort_flag)) { ok = false; break; }
+        const uint32_t sj = tc_run + j;
+        if (!mbar_wait(smem_u32(s_full + t), sj & 1, p.status, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const int kbase = j * BKV;
         // the whole row of S in one TMEM round trip
         tmem_ld128(tS, r);
         // the tile reaches past the first query's position: mask key > position
-        const bool diag = kbase + BKV - 1 > pos0 + qb[t] * BQ;
+        const bool diag = kbase + BKV - 1 > it.pos0 + (2 * it.pair + t) * BQ;
         if (diag) {
 #pragma unroll
-          for (int i = 0; i < 128; ++i)
-            if (kbase + i > qpos) r[i] = __float_as_uint(-INFINITY);
+          for (int k = 0; k < 128; ++k)
+            if (kbase + k > qpos) r[k] = __float_as_uint(-INFINITY);
         }
         // two scores per max instruction (the ALU pipe is this loop's limit)
         float mx = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < 128; i += 2) mx = fmax3(mx, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+        for (int k = 0; k < 128; k += 2) mx = fmax3(mx, __uint_as_float(r[k]), __uint_as_float(r[k + 1]));
         const float mxs = mx * sl;
         const bool need = mxs > m_run + kRescaleLog2;    // also true on the first tile
         const bool any_need = __any_sync(0xffffffffu, need);
         const float m_new = need ? mxs : m_run;
         const float alpha = need ? ex2_approx(m_run - m_new) : 1.0f;
         m_run = m_new;
-        // P = 2^(S * scale - m) (masked scores are -inf: P = 0), packed in place: pair i goes
-        // to r[i] once r[2i], r[2i + 1] are read; keys 2c, 2c+1 land in S column c
+        // P = 2^(S * scale - m) (masked scores are -inf: P = 0), packed in place: pair k goes
+        // to r[k] once r[2k], r[2k + 1] are read; keys 2c, 2c+1 land in S column c
         float rowsum = 0.f;
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(r[2 * i]), sl, -m_run));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(r[2 * i + 1]), sl, -m_run));
+        for (int k = 0; k < 64; ++k) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(r[2 * k]), sl, -m_run));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(r[2 * k + 1]), sl, -m_run));
           rowsum += p0 + p1;
-          r[i] = pack_bf16(p0, p1);
+          r[k] = pack_bf16(p0, p1);
         }
         tmem_st64(tS, r);
         if (any_need) {
           if (j > 0) {
             // P_{j-1} V_{j-1} must have landed before O is rescaled (and O must be rescaled
             // before this tile's P V, which waits for p_full below)
-            if (!mbar_wait(smem_u32(o_done + t), (j - 1) & 1, p.status, abort_flag)) { ok = false; break; }
+            if (!mbar_wait(smem_u32(o_done + t), (sj - 1) & 1, p.status, abort_flag)) { ok = false; break; }
             tc_fence_after();
             uint32_t o32[32];
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-              tmem_ld32(tO + c * 32, o32);
+            for (int cc = 0; cc < 4; ++cc) {
+              tmem_ld32(tO + cc * 32, o32);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) o32[i] = __float_as_uint(__uint_as_float(o32[i]) * alpha);
-              tmem_st32(tO + c * 32, o32);
+              for (int k = 0; k < 32; ++k) o32[k] = __float_as_uint(__uint_as_float(o32[k]) * alpha);
+              tmem_st32(tO + cc * 32, o32);
             }
           }
           l_run *= alpha;
@@ -288,8 +358,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // keys at or past the last valid one: zero their V rows before any P V of this tile
         // (done by tile 0 if it reads this tile, else by tile 1; the MMA issuer orders tile
         // 1's product after tile 0's P)
-        if (kbase + BKV > n_valid && (t == 0 || j >= nkt[0]) && kbase + row >= n_valid) {
-          uint8_t* vrow = sV + (j & 1) * TILE + row * 128;
+        if (kbase + BKV > it.n_valid && (t == 0 || j >= it.nkt[0]) && kbase + row >= it.n_valid) {
+          uint8_t* vrow = sV + ((kvbase + j) & 1) * TILE + row * 128;
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
             reinterpret_cast<uint4*>(vrow)[u] = make_uint4(0, 0, 0, 0);
@@ -301,29 +371,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(p_full + t));
       }
-      if (ok && mbar_wait(smem_u32(o_done + t), (n_t - 1) & 1, p.status, abort_flag)) {
-        tc_fence_after();
-        const float inv_l = 1.0f / l_run;
-        __nv_bfloat16* dst =
-            p.out + (static_cast<long long>(b) * p.S + qi) * (static_cast<long long>(p.H) * HD) + h * HD;
-        uint32_t o32[32];
+      if (!ok) break;
+      tc_run += n_t;
+      // the item's last product (this thread's reads of O come before the next item's first
+      // P V, which waits for this warp's next arrival on p_full)
+      if (!mbar_wait(smem_u32(o_done + t), (tc_run - 1) & 1, p.status, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      const float inv_l = 1.0f / l_run;
+      __nv_bfloat16* dst =
+          p.out + (static_cast<long long>(it.b) * p.S + qi) * (static_cast<long long>(p.H) * HD) + it.h * HD;
+      uint32_t o32[32];
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          tmem_ld32(tO + c * 32, o32);
-          if (qi < len) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+      for (int cc = 0; cc < 4; ++cc) {
+        tmem_ld32(tO + cc * 32, o32);
+        if (qi < it.len) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + cc * 32);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              uint4 w;
-              w.x = pack_bf16(__uint_as_float(o32[8 * u + 0]) * inv_l, __uint_as_float(o32[8 * u + 1]) * inv_l);
-              w.y = pack_bf16(__uint_as_float(o32[8 * u + 2]) * inv_l, __uint_as_float(o32[8 * u + 3]) * inv_l);
-              w.z = pack_bf16(__uint_as_float(o32[8 * u + 4]) * inv_l, __uint_as_float(o32[8 * u + 5]) * inv_l);
-              w.w = pack_bf16(__uint_as_float(o32[8 * u + 6]) * inv_l, __uint_as_float(o32[8 * u + 7]) * inv_l);
-              d4[u] = w;
-            }
+          for (int u = 0; u < 4; ++u) {
+            uint4 w;
+            w.x = pack_bf16(__uint_as_float(o32[8 * u + 0]) * inv_l, __uint_as_float(o32[8 * u + 1]) * inv_l);
+            w.y = pack_bf16(__uint_as_float(o32[8 * u + 2]) * inv_l, __uint_as_float(o32[8 * u + 3]) * inv_l);
+            w.z = pack_bf16(__uint_as_float(o32[8 * u + 4]) * inv_l, __uint_as_float(o32[8 * u + 5]) * inv_l);
+            w.w = pack_bf16(__uint_as_float(o32[8 * u + 6]) * inv_l, __uint_as_float(o32[8 * u + 7]) * inv_l);
+            d4[u] = w;
           }
         }
       }
+      tc_fence_before();
     }
   }
 
@@ -336,7 +410,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
-constexpr size_t kSmemBytes = 1024 + 6 * TILE + 13 * 8 + 16;
+constexpr size_t kSmemBytes = 1024 + 6 * TILE + 14 * 8 + 16;
 static_assert(kSmemBytes >= kTmemKernelMinSmem, "a TMEM-holding kernel must not share an SM with another");
 
 }  // namespace
@@ -368,6 +442,9 @@ int attn_prefill_tc(const Ctx& c, const void* q, const void* k_cache, const void
   p.G = G;
   p.n_qt = (S + BQ - 1) / BQ;
   p.n_pairs = (p.n_qt + 1) / 2;
+  const long long items = static_cast<long long>(p.n_pairs) * H * B;
+  if (items > (1ll << 30)) return LLAMA_ERR_UNSUPPORTED;
+  p.n_items = static_cast<int>(items);
   p.start = start;
   p.lens = lens;
   p.T_max = T_max;
@@ -375,8 +452,10 @@ int attn_prefill_tc(const Ctx& c, const void* q, const void* k_cache, const void
   p.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HD));
   p.out = static_cast<__nv_bfloat16*>(out);
   p.status = c.status;
-  if (B > 65535 || p.n_pairs > 65535) return LLAMA_ERR_UNSUPPORTED;
-  launch_pdl(c, attn_prefill_kernel, dim3(H, B, p.n_pairs), dim3(NUM_THREADS), kSmemBytes, tq, tk, tv, p);
+  if (p.n_items == 0) return LLAMA_OK;
+  // persistent: one CTA per SM walks its share of the items
+  launch_pdl(c, attn_prefill_kernel, dim3(std::min(p.n_items, c.num_sms)), dim3(NUM_THREADS), kSmemBytes, tq, tk,
+             tv, p);
   return after_launch(c);
 }
 
