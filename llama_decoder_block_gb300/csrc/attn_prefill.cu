@@ -5,10 +5,11 @@
 // repeated along dim 1; "深度学习进阶（三十）…" §1.1; "第 10 章：现代 LLaMA 架构" §6: K/V stay
 // G heads in the cache and are shared logically, never copied H/G times).
 //
-// One CTA per (pair of 128-query blocks 2i and 2i+1, head, sequence).  The pair index is the
-// grid's slowest dimension, counted down, so CTAs are dispatched longest first (the last query
-// pairs read the most keys) and the short pairs fill the tail of the last wave.  Both query
-// tiles read every K/V tile once from shared memory.
+// Persistent: one CTA per SM walks a list of work items, each a pair of 128-query blocks 2i
+// and 2i+1 of one head of one sequence.  The items are ordered longest first (the last query
+// pairs read the most keys) and dealt out in a snake over rounds of one item per CTA, so each
+// CTA's total is close to the mean; the next item's Q and K/V loads overlap the current item's
+// last products.  Both query tiles read every K/V tile once from shared memory.
 //   warp 0      TMA: both Q tiles once, then K_j, V_j (128 keys each) into a 2-stage ring
 //               straight from the [B, G, max_T, D] cache
 //   warp 1      TMEM allocator and MMA issuer, ping-pong between the two tiles:
