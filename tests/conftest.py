@@ -8,6 +8,19 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 
+def pytest_sessionfinish(session, exitstatus):
+    """With LLAMA_PARITY_LOG=<file>: write every GPU-vs-oracle comparison of the session as TSV
+    (what, max and p99 of |gpu-ref|/(1+|ref|), the gate it was held to)."""
+    path = os.environ.get("LLAMA_PARITY_LOG")
+    util = sys.modules.get("gpu_util")
+    if not path or util is None:
+        return
+    with open(path, "w", encoding="utf-8") as f:
+        f.write("what\tmax\tp99\tgate\n")
+        for what, mx, p99, gate in util.PARITY_LOG:
+            f.write(f"{what}\t{mx:.3e}\t{p99:.3e}\t{gate}\n")
+
+
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
 

@@ -26,10 +26,16 @@ def bf16_stored(a: np.ndarray) -> synth.Stored:
     return synth.Stored(synth.f32_to_bf16_bits(a.astype(np.float32)), "bf16")
 
 
+# Every comparison made by the helpers below: (what, max, p99 of |gpu-ref|/(1+|ref|), gate).
+# tests/conftest.py writes them out at the end of the session when LLAMA_PARITY_LOG names a file.
+PARITY_LOG = []
+
+
 def assert_close(gpu: np.ndarray, ref: np.ndarray, tol: float, what: str):
     assert gpu.shape == ref.shape, (what, gpu.shape, ref.shape)
     assert np.all(np.isfinite(gpu)), f"{what}: non-finite values in the GPU result"
     err = np.abs(gpu - ref) / (1.0 + np.abs(ref))
+    PARITY_LOG.append((what, float(err.max()), float(np.quantile(err, 0.99)), f"max <= {tol:.0e}"))
     worst = np.unravel_index(np.argmax(err), err.shape)
     assert err.max() <= tol, (f"{what}: max |gpu-ref|/(1+|ref|) = {err.max():.3e} > {tol:.0e} at {worst} "
                               f"(gpu {gpu[worst]!r}, ref {ref[worst]!r}); p99 {np.quantile(err, 0.99):.3e}")
@@ -53,6 +59,8 @@ def assert_close_layer_full(gpu: np.ndarray, ref: np.ndarray, what: str):
     err = np.abs(gpu - ref) / (1.0 + np.abs(ref))
     frac = float(np.mean(err > g["tol"]))
     norm = float(np.linalg.norm(gpu - ref) / np.linalg.norm(ref))
+    PARITY_LOG.append((what, float(err.max()), float(np.quantile(err, 0.99)),
+                       f"full-width gate: frac over {g['tol']:.0e} = {frac:.2e}, normwise {norm:.2e}"))
     msg = (f"{what}: max {err.max():.3e} (envelope {g['envelope']:.0e}), fraction over {g['tol']:.0e} = {frac:.2e} "
            f"(limit {g['max_frac_over_tol']:.0e}), normwise {norm:.2e} (limit {g['normwise']:.0e}), "
            f"p99 {np.quantile(err, 0.99):.2e}")
