@@ -114,7 +114,10 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
   uint64_t* p_full = o_done + 2;
   uint64_t* o_free = p_full + 2;             // [2] by the parity of the item
   uint64_t* drain = o_free + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  // the softmax warps' own barrier (4 arrivals), waited on with the bounded wait: after a wait
+  // that gave up, no warp is left in a hardware barrier that the others never reach
+  uint64_t* grp = drain + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -135,6 +138,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     mbar_init(smem_u32(o_free), 4);
     mbar_init(smem_u32(o_free + 1), 4);
     mbar_init(smem_u32(drain), 1);
+    mbar_init(smem_u32(grp), 4);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -292,6 +296,14 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     const float sl = p.scale_log2;
     uint32_t tcount = 0, icount = 0;
     bool ok = true;
+    uint32_t gph = 0;   // phases of grp passed
+    auto group_sync = [&]() -> bool {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(grp));
+      const bool r = mbar_wait(smem_u32(grp), gph & 1u, p.status, abort_flag);
+      ++gph;
+      return r;
+    };
     for (long long pos = r0; pos < r1 && ok;) {
       const DecItem d = dec_seg(p, pre_s, pos_s, pos, r1);
       pos += d.ntile;
@@ -329,7 +341,8 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
           for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
           if (lane == 0) rb[sw * 8 + h] = v;
         }
-        named_barrier(1, 128);   // red is double-buffered by tile parity: one barrier per tile
+        // red is double-buffered by tile parity: one barrier per tile
+        if (!group_sync()) { ok = false; break; }
         bool need = false;
         float alpha[REP], pv[REP];
 #pragma unroll
@@ -405,7 +418,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(o_free + (icount & 1)));
       float* rb = red + (last & 1) * 32;   // free: every thread passed this tile's barrier
-      named_barrier(1, 128);
+      if (!group_sync()) { ok = false; break; }
 #pragma unroll
       for (int h = 0; h < REP; ++h) {
         float v = lsum[h];
@@ -413,7 +426,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
         for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
         if (lane == 0) rb[sw * 8 + h] = v;
       }
-      named_barrier(1, 128);
+      if (!group_sync()) { ok = false; break; }
 #pragma unroll
       for (int h = 0; h < REP; ++h) {
         const float o = h < 4 ? __uint_as_float(oa[h]) : __uint_as_float(ob[h - 4]);
@@ -423,7 +436,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
           p.l_part[part + h] = rb[h] + rb[8 + h] + rb[16 + h] + rb[24 + h];
         }
       }
-      named_barrier(1, 128);   // rb is reused by the next segment's first tiles
+      if (!group_sync()) { ok = false; break; }   // rb is reused by the next segment's first tiles
       ++icount;
     }
   }
@@ -438,7 +451,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
 }
 
 constexpr size_t kDecSmemBytes = 1024 + 2 * STAGES * KV_TILE + 2 * Q_TILE + 2 * P_TILE + 64 * 4 +
-                                 (2 * POS_CACHE + 2) * 4 + (2 * STAGES + 14) * 8 + 16;
+                                 (2 * POS_CACHE + 2) * 4 + (2 * STAGES + 15) * 8 + 16;
 static_assert(kDecSmemBytes <= 232448, "decode attention exceeds the shared memory of one CTA");
 static_assert(kDecSmemBytes >= kTmemKernelMinSmem, "a TMEM-holding kernel must not share an SM with another");
 
