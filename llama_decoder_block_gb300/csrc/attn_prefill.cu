@@ -10,16 +10,18 @@
 // pairs read the most keys) and dealt out in a snake over rounds of one item per CTA, so each
 // CTA's total is close to the mean; the next item's Q and K/V loads overlap the current item's
 // last products.  Both query tiles read every K/V tile once from shared memory.
-//   warp 0      TMA: both Q tiles once, then K_j, V_j (128 keys each) into a 2-stage ring
-//               straight from the [B, G, max_T, D] cache
+//   warp 0      TMA: an item's two Q tiles (once the previous item's last S product has read
+//               its own), then K_j, V_j (128 keys each) into a 2-stage ring straight from
+//               the [B, G, max_T, D] cache
 //   warp 1      TMEM allocator and MMA issuer, ping-pong between the two tiles:
 //               S_t = Q_t K_j^T into TMEM; once the softmax of tile t has written P_t,
 //               O_t += P_t V_j with P_t read from TMEM and V as an MN-major smem operand,
 //               then at once S_t for the next K tile, so one tile's softmax overlaps the
 //               other tile's MMAs
-//   warps 4-7   softmax of tile A, warps 8-11 softmax of tile B: one query row per thread;
-//               the row max, exp2 with the scale folded in, P as bf16 written over S in
-//               TMEM; O is rescaled only when the running max grows by more than 2^8
+//   warps 4-7   softmax of tile A, warps 8-11 softmax of tile B: one query row per thread,
+//               read from TMEM in one 128-column load per key tile; the row max, exp2 with
+//               the scale folded in, P as bf16 written over S in TMEM (one 64-column
+//               store); O is rescaled only when the running max grows by more than 2^8
 //               (the final O / l uses the same reference max, so the result is exact)
 // fp32 statistics and accumulators; D = 128.
 //
