@@ -52,7 +52,7 @@ class L2Flush:
 
 # DRAM bytes (read + write) per launch from ncu captures, keyed by kernel and the sha1 of
 # the source file it was measured on; a changed source makes the figure stale (null).
-NCU_TRAFFIC = {("gate_up_swiglu_gemm", "c575456b95fd"): 229662976}   # profiles/gemm_gate_up_mha7b_b1_s2048.md
+NCU_TRAFFIC = {("gate_up_swiglu_gemm", "5f4271c0e9b7"): 229730304}   # profiles/gemm_gate_up_mha7b_b1_s2048.md
 
 
 def parse():
@@ -279,6 +279,69 @@ def prefill_flops(L, B, S):
         "gate_up_swiglu_gemm": 2.0 * M * d * 2 * I,
         "down_residual_gemm": 2.0 * M * I * d,
     }
+
+
+def bench_variants(api, steps, warmup, dev, pk):
+    """The survey's "next" rows timed at benchmark sizes (random weights, L2 flushed before each
+    step, one event pair per step): a 512-token chunk on top of 3584 cached tokens for 4
+    sequences (GQA-8B layer, row f1), and the MHA-7B layer with half-split RoPE and with one KV
+    head for all 32 query heads (row f4)."""
+    import numpy as np
+    import torch
+    from llama_decoder_block_gb300 import synth
+    g8, m7 = synth.WORKLOADS["gqa8b_bf16_b4_s4096"], synth.WORKLOADS["mha7b_bf16_b1_s2048"]
+    cases = [("chunk_gqa8b_b4_s512_after_3584", synth.scaled(g8, S=512, name="chunk"), 3584, 4096),
+             ("mha7b_half_split_rope", synth.scaled(m7, rope_style="half", name="half"), None, None),
+             ("mqa7b_g1_half_split_rope", synth.scaled(m7, n_kv_heads=1, rope_style="half", name="mqa"), None, None)]
+    res = {}
+    for name, wl, start, T in cases:
+        L = wl.layer
+        B, S = wl.B, wl.S
+        T = T or S
+        g = torch.Generator(device=dev).manual_seed(wl.seed + 7)
+        w = dev_weights_random(wl, dev, wl.seed)
+        x = torch.randn(B, S, L.d_model, generator=g, device=dev).to(torch.bfloat16)
+        out = torch.empty_like(x)
+        c, s_ = api.rope_tables(L.rope_base, L.head_dim, T)
+        cos, sin = torch.from_numpy(c).to(dev), torch.from_numpy(s_).to(dev)
+        kc = torch.randn(B, L.n_kv_heads, T, L.head_dim, generator=g, device=dev).to(torch.bfloat16)
+        vc = torch.randn(B, L.n_kv_heads, T, L.head_dim, generator=g, device=dev).to(torch.bfloat16)
+        dims = api.Dims(L.d_model, L.n_heads, L.n_kv_heads, L.head_dim, L.d_inter, L.rms_eps, torch.bfloat16,
+                        rope_style=1 if L.rope_style == "half" else 0)
+        ws = api.workspace(api.prefill_workspace_bytes(dims, B, S), dev)
+        st = torch.full((B,), start or 0, dtype=torch.int32, device=dev)
+        if start is None:
+            fn = lambda: api.layer_prefill(dims, w, x, out, cos, sin, kc, vc, ws)
+        else:
+            fn = lambda: api.layer_prefill_chunk(dims, w, x, out, cos, sin, st, kc, vc, ws)
+        flush = L2Flush(dev)
+        for _ in range(warmup):
+            flush()
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(max(3, steps // 2)):
+            flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        assert api.device_status() == 0
+        ms = float(np.mean(ts))
+        f = prefill_flops(L, B, S)
+        p0 = start or 0
+        # the chunk's queries see the cache before them: sum over s of (p0 + s + 1) keys
+        f["attention_prefill"] = 4.0 * L.head_dim * L.n_heads * B * (S * p0 + S * (S + 1) / 2)
+        tf = sum(f.values()) / (ms * 1e-3) / 1e12
+        res[name] = {"B": B, "S": S, "cached_before": p0, "H": L.n_heads, "G": L.n_kv_heads,
+                     "rope": L.rope_style, "ms_per_step": round(ms, 4),
+                     "tokens_per_s": round(B * S / (ms * 1e-3), 1), "tflops": round(tf, 1),
+                     "frac_of_sustained_peak": round(tf / pk["bf16_sustained"], 4)}
+        del w, x, out, kc, vc, ws, flush
+        torch.cuda.empty_cache()
+    return res
 
 
 def bench_prefill(api, wl, steps, warmup, dev, pk, from_synth):
@@ -757,6 +820,7 @@ def main():
                                  "frac_of_sustained_peak": round(r8["tflops_total"] / pk["bf16_sustained"], 4),
                                  "kernel_ms": {k: round(v, 3) for k, v in r8["kernel_ms"].items()},
                                  "kernel_tflops": r8["kernel_tflops"]}
+        line["next_rows"] = bench_variants(api, args.steps, args.warmup, dev, pk)
         line["rmsnorm"] = bench_norm(api, dev, pk, "rmsnorm")
         line["layernorm"] = bench_norm(api, dev, pk, "layernorm")
         line["layernorm"]["time_vs_rmsnorm"] = round(line["layernorm"]["us"] / line["rmsnorm"]["us"], 3)

@@ -431,17 +431,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           s = st + s_in;
         }
         const int half_d = p.D >> 1;
-        // even/odd RoPE angles of chunk c (16 pairs) for this row's position, when chunk c is
-        // part of a q or k head of this tile
-        float cs_n[16], sn_n[16];
+        // RoPE angles of chunk c for this row's position, when chunk c is part of a q or k head
+        // of this tile: 16 pairs (even/odd: angle index j0/2 ..) or, for a chunk of the first
+        // half of a head, 32 pairs (half-split: angle index j0 ..)
+        float cs_n[32], sn_n[32];
         auto load_angles = [&](int c) {
           const int col0 = nb * BN + c * 32;
           const int hh = col0 / p.D, j0 = col0 - hh * p.D;
-          if (p.rope_half || !keep || c >= BN / 32 || hh >= p.H + p.G) return;
-          const float4* cr = reinterpret_cast<const float4*>(p.cos + static_cast<long long>(s) * half_d + j0 / 2);
-          const float4* sr = reinterpret_cast<const float4*>(p.sin + static_cast<long long>(s) * half_d + j0 / 2);
+          if (!keep || c >= BN / 32 || hh >= p.H + p.G || (p.rope_half && j0 >= half_d)) return;
+          const int first = p.rope_half ? j0 : j0 / 2;
+          const float4* cr = reinterpret_cast<const float4*>(p.cos + static_cast<long long>(s) * half_d + first);
+          const float4* sr = reinterpret_cast<const float4*>(p.sin + static_cast<long long>(s) * half_d + first);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
+          for (int i = 0; i < 8; ++i) {
+            if (i >= 4 && !p.rope_half) break;
             const float4 cv = cr[i], sv = sr[i];
             cs_n[4 * i] = cv.x; cs_n[4 * i + 1] = cv.y; cs_n[4 * i + 2] = cv.z; cs_n[4 * i + 3] = cv.w;
             sn_n[4 * i] = sv.x; sn_n[4 * i + 1] = sv.y; sn_n[4 * i + 2] = sv.z; sn_n[4 * i + 3] = sv.w;
@@ -463,19 +466,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             __nv_bfloat16* dst = hh < p.H
                 ? p.q_out + ((static_cast<long long>(b) * p.H + hh) * p.S + s_in) * p.D
                 : p.k_cache + ((static_cast<long long>(b) * p.G + (hh - p.H)) * p.T_max + s) * p.D;
+            // this chunk's angles came one rope chunk ahead; the next rope chunk is the second
+            // quarter of this head or the first of the next head (the tile is head-aligned)
+            float cs_c[32], sn_c[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              cs_c[i] = cs_n[i];
+              sn_c[i] = sn_n[i];
+            }
+            load_angles(j0 + 32 < half_d ? c + 1 : c + 3);
             uint32_t r2[32];
             tmem_ld32(t_acc + c * 32, r);
             tmem_ld32(t_acc + c * 32 + half_d, r2);
             if (!keep) continue;
-            const float* cr = p.cos + static_cast<long long>(s) * half_d + j0;
-            const float* sr = p.sin + static_cast<long long>(s) * half_d + j0;
             float w2[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-              const float cs = cr[i], sn = sr[i];
               const float x1 = __uint_as_float(r[i]), x2 = __uint_as_float(r2[i]);
-              v[i] = x1 * cs - x2 * sn;
-              w2[i] = x2 * cs + x1 * sn;
+              v[i] = x1 * cs_c[i] - x2 * sn_c[i];
+              w2[i] = x2 * cs_c[i] + x1 * sn_c[i];
             }
             store_bf16x32(dst + j0, v, 32);
             store_bf16x32(dst + j0 + half_d, w2, 32);
