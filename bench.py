@@ -282,10 +282,10 @@ def prefill_flops(L, B, S):
 
 
 def bench_variants(api, steps, warmup, dev, pk):
-    """The survey's "next" rows timed at benchmark sizes (random weights, L2 flushed before each
+    """The layer's variants timed at benchmark sizes (random weights, L2 flushed before each
     step, one event pair per step): a 512-token chunk on top of 3584 cached tokens for 4
-    sequences (GQA-8B layer, row f1), and the MHA-7B layer with half-split RoPE and with one KV
-    head for all 32 query heads (row f4)."""
+    sequences (GQA-8B layer), and the MHA-7B layer with half-split RoPE and with one KV head
+    for all 32 query heads."""
     import numpy as np
     import torch
     from llama_decoder_block_gb300 import synth
@@ -820,7 +820,7 @@ def main():
                                  "frac_of_sustained_peak": round(r8["tflops_total"] / pk["bf16_sustained"], 4),
                                  "kernel_ms": {k: round(v, 3) for k, v in r8["kernel_ms"].items()},
                                  "kernel_tflops": r8["kernel_tflops"]}
-        line["next_rows"] = bench_variants(api, args.steps, args.warmup, dev, pk)
+        line["variants"] = bench_variants(api, args.steps, args.warmup, dev, pk)
         line["rmsnorm"] = bench_norm(api, dev, pk, "rmsnorm")
         line["layernorm"] = bench_norm(api, dev, pk, "layernorm")
         line["layernorm"]["time_vs_rmsnorm"] = round(line["layernorm"]["us"] / line["rmsnorm"]["us"], 3)
