@@ -468,6 +468,19 @@ def test_kv_cache_decode_equals_full_prefill_row(store_bf16):
     h1, k1, v1 = oracle.decoder_layer(x[:, :11], w, cos, sin, **kw)
     h2, _, _ = oracle.decoder_layer(x[:, 11:], w, cos, sin, past_k=k1, past_v=v1, past_len=np.full(B, 11), **kw)
     assert np.allclose(np.concatenate([h1, h2], axis=1), full, rtol=0, atol=1e-12)
+    # per-sequence starts: sequence b's 6-token chunk sits on its own cached length t2[b]
+    # (the cache is the full run's, slots >= t2[b] poisoned) and equals rows t2[b]..t2[b]+5
+    t2 = np.array([3, 14, 9])
+    ck = np.full((B, G, 32, D), np.nan)
+    cv = np.full((B, G, 32, D), np.nan)
+    for b in range(B):
+        ck[b, :, :t2[b]] = kf[b, :, :t2[b]]
+        cv[b, :, :t2[b]] = vf[b, :, :t2[b]]
+    xc = np.stack([x[b, t2[b]:t2[b] + 6] for b in range(B)])
+    hc, kc, _ = oracle.decoder_layer(xc, w, cos, sin, past_k=ck, past_v=cv, past_len=t2, **kw)
+    for b in range(B):
+        assert np.allclose(hc[b], full[b, t2[b]:t2[b] + 6], rtol=0, atol=1e-12)
+        assert np.allclose(kc[b], kf[b, :, t2[b]:t2[b] + 6], rtol=0, atol=1e-12)
 
 
 def test_stack_brute_force_against_torch_statement():
