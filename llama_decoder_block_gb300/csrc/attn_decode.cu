@@ -615,7 +615,7 @@ static __device__ __align__(256) unsigned char g_decode_scratch[kDecodeScratchBy
 
 // Device address of g_decode_scratch, looked up once per device (host code must not use
 // the symbol itself: on the host it only names a stand-in).
-std::atomic<void*> g_decode_scratch_addr[64];
+std::atomic<void*> g_decode_scratch_addr[kMaxDevices];
 
 }  // namespace
 }  // namespace llama

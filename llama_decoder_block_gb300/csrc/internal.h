@@ -10,6 +10,10 @@
 
 namespace llama {
 
+// Devices a process may use with the library (per-device state is kept in arrays of this
+// size; make_ctx refuses a device index beyond it).
+constexpr int kMaxDevices = 64;
+
 // Per-call launch context: the caller's stream and the current device's facts.
 struct Ctx {
   cudaStream_t stream;

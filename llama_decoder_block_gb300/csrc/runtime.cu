@@ -17,7 +17,6 @@ __device__ __align__(16) int g_status_word[kStatusWords];
 
 namespace {
 
-constexpr int kMaxDevices = 64;
 std::atomic<int*> g_status_addr[kMaxDevices];
 std::atomic<int> g_num_sms[kMaxDevices];
 std::atomic<uint64_t> g_launches{0};

@@ -389,7 +389,7 @@ def _tiny_layer_inputs():
     return wl, w, x, cos, sin, kw
 
 
-def test_layer_brute_force_tiny_config_against_torch_sdpa_statement():
+def test_layer_brute_force_tiny_config_against_torch_statement():
     wl, w, x, cos, sin, kw = _tiny_layer_inputs()
     ours, _, _ = oracle.decoder_layer(x, w, cos, sin, **kw)
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a))

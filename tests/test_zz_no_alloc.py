@@ -3,7 +3,9 @@
 llama_attention_decode_static serves callers that cannot allocate device memory: its split
 partials live in a fixed array inside the library instead of a caller workspace.  Two calls in
 a row, on different inputs, must each agree with llama_attention_decode (the workspace form) on
-the same inputs, within the bf16 tolerance of the other tests; an oversized request is refused.
+the same inputs, within the bf16 tolerance of the other tests, and the fp64 oracle's attention on
+those inputs (the cache slots each sequence sees, 0 .. positions[b]); an oversized request is
+refused.
 """
 import ctypes
 
@@ -11,6 +13,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from gpu_util import TOL, assert_close, f64
 
 pytestmark = pytest.mark.gpu
@@ -50,6 +53,11 @@ def test_fixed_scratch_decode_attention_matches_the_workspace_form(api):
         assert _static(api, dims, q, kc, vc, pos, got) == 0
         assert api.device_status() == 0
         assert_close(f64(got), f64(ref), TOL["bf16"], f"fixed-scratch decode attention, call {call + 1}")
+        # the oracle on the same bf16 inputs: one query per sequence at position pos[b], keys 0 .. pos[b]
+        p64 = pos.cpu().numpy().astype(np.int64)
+        want = oracle.attention(f64(q)[:, :, None, :], f64(kc), f64(vc), p64[:, None], p64 + 1)
+        assert_close(f64(got), want[:, :, 0, :].reshape(B, H * 128), TOL["bf16"],
+                     f"fixed-scratch decode attention vs oracle, call {call + 1}")
 
 
 def test_fixed_scratch_refuses_requests_beyond_its_size(api):
