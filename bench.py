@@ -26,7 +26,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = "decoder-layer prefill tokens/s + decode µs/step on 1 GB300; % of TC/HBM roofline"
 MAIN = "mha7b_bf16_b1_s2048"
-PREFILL_KERNELS = ["rmsnorm_attn", "qkv_rope_gemm", "attention_prefill", "o_proj_residual_gemm", "rmsnorm_ffn",
+# the layer's kernels in launch order: both RMSNorms run inside the GEMM that follows them, with
+# the row scales of x from a statistics pass and those of h from the o_proj epilogue
+PREFILL_KERNELS = ["rms_rowscale", "qkv_rope_gemm", "attention_prefill", "o_proj_residual_gemm",
                    "gate_up_swiglu_gemm", "down_residual_gemm"]
 DECODE_KERNELS = ["rmsnorm_attn", "qkv_gemm_stream", "qkv_rope_fixup", "attention_decode_split",
                   "attention_decode_combine", "o_proj_gemm_stream", "o_proj_residual_rmsnorm_fixup",
@@ -65,8 +67,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true", help="only the headline workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", choices=["attention", "gate_up", "down", "qkv", "decode_attention", "decode_layer",
-                                       "rmsnorm", "layernorm"],
+    ap.add_argument("--case", choices=["attention", "gate_up", "down", "o_proj", "qkv", "decode_attention",
+                                       "decode_layer", "rmsnorm", "layernorm"],
                     help="time one step alone (W + K launches, CUDA events) instead of the layer")
     ap.add_argument("--workload", default=MAIN, help="workload whose shapes --case uses")
     return ap.parse_args()
@@ -594,23 +596,29 @@ def bench_case(api, case, wl, steps, warmup, dev, pk):
         fn = lambda: api.attention_prefill(dims, q, k, v, o)
         work, unit = 4.0 * D * H * B * S * (S + 1) / 2, "flop"
     elif case == "gate_up":
-        x, wg, wu = rnd(M, d), rnd(I, d, std=0.02), rnd(I, d, std=0.02)
+        # as in the layer: the FFN RMSNorm inside the gate/up GEMM (row-statistics pass included)
+        x, gm, wg, wu = rnd(M, d), 1 + rnd(d, std=0.1), rnd(I, d, std=0.02), rnd(I, d, std=0.02)
         a = torch.empty(M, I, dtype=torch.bfloat16, device=dev)
-        fn = lambda: api.linear_swiglu(x, wg, wu, a)
+        rs = torch.empty(M, dtype=torch.float32, device=dev)
+        fn = lambda: api.norm_linear_swiglu(x, gm, L.rms_eps, wg, wu, a, rs)
         work, unit = 2.0 * M * d * 2 * I, "flop"
-    elif case == "down":
-        a, wd, r = rnd(M, I), rnd(d, I, std=0.02), rnd(M, d)
+    elif case in ("down", "o_proj"):
+        K = I if case == "down" else H * D
+        a, wd, r = rnd(M, K), rnd(d, K, std=0.02), rnd(M, d)
         out = torch.empty(M, d, dtype=torch.bfloat16, device=dev)
         fn = lambda: api.linear_residual(a, wd, r, out)
-        work, unit = 2.0 * M * I * d, "flop"
+        work, unit = 2.0 * M * K * d, "flop"
     elif case == "qkv":
-        x, wq, wk, wv = rnd(B, S, d), rnd(H * D, d, std=0.02), rnd(G * D, d, std=0.02), rnd(G * D, d, std=0.02)
+        # as in the layer: the attention RMSNorm inside the QKV GEMM (row-statistics pass included)
+        x, gm = rnd(B, S, d), 1 + rnd(d, std=0.1)
+        wq, wk, wv = rnd(H * D, d, std=0.02), rnd(G * D, d, std=0.02), rnd(G * D, d, std=0.02)
         q = torch.empty(B, H, S, D, dtype=torch.bfloat16, device=dev)
         kc = torch.empty(B, G, S, D, dtype=torch.bfloat16, device=dev)
         vc = torch.empty_like(kc)
+        rs = torch.empty(M, dtype=torch.float32, device=dev)
         c, s = api.rope_tables(L.rope_base, D, S)
         cos, sin = torch.from_numpy(c).to(dev), torch.from_numpy(s).to(dev)
-        fn = lambda: api.qkv_rope(dims, x, wq, wk, wv, cos, sin, kc, vc, q)
+        fn = lambda: api.norm_qkv_rope(dims, x, gm, wq, wk, wv, cos, sin, kc, vc, q, rs)
         work, unit = 2.0 * M * d * (H + 2 * G) * D, "flop"
     elif case in ("decode_attention", "decode_layer"):
         dw = wl

@@ -5,7 +5,22 @@
 //   warp 0     TMA producer: 128x64 A tile + BNx64 B tile per stage (128-byte swizzle)
 //   warp 1     TMEM allocator and MMA issuer: tcgen05.mma 128xBNx16 into a TMEM accumulator
 //   warps 2-5  epilogue: tcgen05.ld of the accumulator rows, fused op, stores to HBM
+//   warps 6-9  (RMSNorm-fused form only) operand A: see below
 // Two TMEM accumulators let the epilogue of tile i overlap the main loop of tile i+1.
+//
+// RMSNorm fused into the A operand ("12 · 从 Transformer 到 LLaMA 系列" §八 RMSNorm: y = gamma *
+// x * rsqrt(mean(x^2) + eps); "3.2 核心组件逐一拆解" §3.2.1: the statistics in fp32).  Four norm
+// warps replace the TMA load of A: they read the x tile of each k-block from global memory (two
+// k-blocks ahead), form bf16(gamma_k * (x_mk * r_m)) -- the normalised row rounded where a
+// standalone RMSNorm would store it -- and write it into the swizzled shared-memory stage.  The
+// row scales r_m = rsqrt(mean_k x_mk^2 + eps) come with the input: from a row-statistics pass
+// over the layer input, or from the residual epilogue that produced x (below).  The normalised
+// activation never goes through HBM.
+//
+// Row statistics in the residual epilogue: a tile adds the squares of its rounded outputs of
+// row m into part[nb][m]; the last of the row's column tiles to finish (a per-row ticket)
+// sums part[0..num_nb)[m] in column order and writes r_m, so the result does not depend on
+// which tile finishes last.
 // Epilogues: plain store (bf16 / fp32), residual add (o_proj, down_proj;
 // "05 LLaMA3 Block — 从零件到发动机" §4.2 steps ④ ⑧), SiLU(gate) * up
 // ("3.2 核心组件逐一拆解" §3.2.2; gate and up tiles share one accumulator), QKV with
@@ -24,6 +39,12 @@ constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int A_TILE_BYTES = BM * BK * 2;
 constexpr int NUM_THREADS = 192;
+constexpr int NORM_THREADS = 128;   // the norm warps of the RMSNorm-fused form
+
+template <bool NORM>
+constexpr int threads_of() {
+  return NORM ? NUM_THREADS + NORM_THREADS : NUM_THREADS;
+}
 
 enum Epi : int { EPI_BF16 = 0, EPI_F32 = 1, EPI_RESID = 2, EPI_SWIGLU = 3, EPI_QKV = 4, EPI_PARTIAL = 5 };
 
@@ -63,6 +84,15 @@ struct Params {
   __nv_bfloat16* q_out;
   __nv_bfloat16* k_cache;
   __nv_bfloat16* v_cache;
+  // RMSNorm-fused form: operand A = bf16(norm_gamma_k * (norm_x_mk * norm_r_m))
+  const __nv_bfloat16* norm_x;       // [M, K] row-major
+  const __nv_bfloat16* norm_gamma;   // [K]
+  const float* norm_r;               // [M] rsqrt(mean_k x_mk^2 + eps)
+  // residual epilogue: the row statistics of the output for the next RMSNorm (null: none)
+  float* stat_part;                  // [num_nb][M] sums of squares of each tile's outputs
+  float* stat_r;                     // [M] rsqrt(sum / N + stat_eps), by the row's last tile
+  int* stat_ticket;                  // [M] column tiles done; zero before, reset by the last
+  float stat_inv_n, stat_eps;
   int* status;
 };
 
@@ -137,15 +167,16 @@ __device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float* v,
   }
 }
 
-template <int BN, int EPI, int STAGES>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+template <int BN, int EPI, int STAGES, bool NORM>
+__global__ void __launch_bounds__(threads_of<NORM>())
     gemm_tc_kernel(const __grid_constant__ TMaps tm, const Params p) {
   constexpr int B_TILE_BYTES = BN * BK * 2;
   // B arrives in 128-row boxes, or as one box when BN is not a multiple of 128 (BN <= 256);
   // gate/up tiles as two boxes of BN/2 rows, one from each matrix
   constexpr int B_BOX_ROWS = EPI == EPI_SWIGLU ? BN / 2 : BN % 128 == 0 ? 128 : BN;
   constexpr int B_BOXES = BN / B_BOX_ROWS;
-  constexpr uint32_t STAGE_TX = A_TILE_BYTES + B_TILE_BYTES;
+  // bytes that TMA brings per stage (the norm warps write A themselves)
+  constexpr uint32_t STAGE_TX = NORM ? B_TILE_BYTES : A_TILE_BYTES + B_TILE_BYTES;
   constexpr uint32_t TMEM_COLS = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
   constexpr uint32_t IDESC = idesc_bf16(BM, BN, false);
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
@@ -169,7 +200,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
-      mbar_init(smem_u32(full_bar + i), 1);
+      // the TMA producer's arrival (with the byte count), and in the fused form the four norm warps'
+      mbar_init(smem_u32(full_bar + i), NORM ? 5 : 1);
       mbar_init(smem_u32(empty_bar + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -244,7 +276,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const int kb1 = min(kb0 + p.kb_per_split, p.num_kb);
           for (int kb = kb0; kb < kb1 && pre < STAGES; ++kb, ++pre) {
             mbar_expect_tx(smem_u32(full_bar + pre), STAGE_TX);
-            if (p.weight_first == 1) load_a(pre, kb, mb);
+            if (p.weight_first == 1) load_a(pre, kb, mb);   // (never with NORM: A is the activation)
             else load_b(pre, kb, nb);
           }
         }
@@ -262,11 +294,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int kb = kb0; kb < kb1; ++kb, ++step) {
           if (step < pre) {   // the weight half of this stage is already on its way
             if (p.weight_first == 1) load_b(stage, kb, nb);
-            else load_a(stage, kb, mb);
+            else if (!NORM) load_a(stage, kb, mb);
           } else {
             if (!mbar_wait(smem_u32(empty_bar + stage), phase ^ 1u, p.status, abort_flag)) { ok = false; break; }
             mbar_expect_tx(smem_u32(full_bar + stage), STAGE_TX);
-            load_a(stage, kb, mb);
+            if (!NORM) load_a(stage, kb, mb);
             load_b(stage, kb, nb);
           }
           used_mask |= 1u << stage;
@@ -323,6 +355,108 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_wait_slow(smem_u32(drain_bar), 0, nullptr, nullptr, kWaitBudgetNs);
       }
     }
+  } else if (NORM && warp >= 6) {
+    // -------------------------------------------------------------- norm warps 6..9: operand A
+    // Thread nt owns 16-byte chunk j of the k-block's 128-byte row slice in rows r0 + 16 i of
+    // the tile (a warp reads 4 rows x 128 contiguous bytes per load).  Row r0 + 16 i keeps chunk
+    // j at j ^ (r0 & 7) under the 128-byte swizzle that the MMA descriptors expect.
+    const int nt = threadIdx.x - NUM_THREADS;
+    const int j = nt & 7;
+    const int r0 = nt >> 3;
+    const uint32_t sw_off = static_cast<uint32_t>(r0 * 128 + ((j ^ (r0 & 7)) << 4));
+    const int my_tiles = static_cast<int>(blockIdx.x) < num_tiles
+                             ? (num_tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                                   static_cast<int>(gridDim.x)
+                             : 0;
+    const int total = my_tiles * p.num_kb;   // (tile, k-block) steps of this CTA; no split-K here
+    // x rows of k-block kb of row block mb, and the gamma chunk of that k-block
+    auto fetch = [&](uint4 (&v)[8], uint4& g, int kb, int mb) {
+      const int kcol = kb * BK + j * 8;
+      g = __ldg(reinterpret_cast<const uint4*>(p.norm_gamma + kcol));
+      const __nv_bfloat16* src = p.norm_x + static_cast<long long>(mb * BM + r0) * p.K + kcol;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int m = mb * BM + r0 + 16 * i;
+        v[i] = m < p.M ? __ldcg(reinterpret_cast<const uint4*>(src + static_cast<long long>(16 * i) * p.K))
+                       : make_uint4(0u, 0u, 0u, 0u);
+      }
+    };
+    // row scales of row block mb (rows past M scale zeros: 0)
+    auto fetch_r = [&](float (&r)[8], int mb) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int m = mb * BM + r0 + 16 * i;
+        r[i] = m < p.M ? __ldcg(p.norm_r + m) : 0.f;
+      }
+    };
+    // two cursors over the steps: the one being written and the one being fetched (two ahead)
+    int cur_t = blockIdx.x, cur_kb = 0, cur_mb = 0, pf_t = blockIdx.x, pf_kb = 0, pf_mb = 0;
+    auto coords = [&](int t, int& mb) {
+      int nb, split;
+      if (t < num_tiles) tile_coords(p, t, mb, nb, split);
+    };
+    auto advance = [&](int& t, int& kb, int& mb) {
+      if (++kb == p.num_kb) {
+        kb = 0;
+        t += gridDim.x;
+        coords(t, mb);
+      }
+    };
+    coords(cur_t, cur_mb);
+    pf_mb = cur_mb;
+    uint4 xb[3][8], gb[3];
+    float rc[8], rn[8];   // row scales of the current tile, and of the next one (loaded a tile ahead)
+    if (total > 0) {
+      fetch_r(rc, cur_mb);
+      fetch(xb[0], gb[0], pf_kb, pf_mb);
+      advance(pf_t, pf_kb, pf_mb);
+    }
+    if (total > 1) { fetch(xb[1], gb[1], pf_kb, pf_mb); advance(pf_t, pf_kb, pf_mb); }
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int s0 = 0; s0 < total && ok; s0 += 3) {
+#pragma unroll
+      for (int u = 0; u < 3; ++u) {
+        if (s0 + u >= total) break;
+        if (s0 + u + 2 < total) {   // two steps ahead, into the registers step s0 + u - 1 used
+          fetch(xb[(u + 2) % 3], gb[(u + 2) % 3], pf_kb, pf_mb);
+          advance(pf_t, pf_kb, pf_mb);
+        }
+        if (cur_kb == 0) {
+          // the next tile's row scales: their latency hides behind this tile's k-blocks
+          const int nt_next = cur_t + static_cast<int>(gridDim.x);
+          if (nt_next < num_tiles) {
+            int nmb;
+            coords(nt_next, nmb);
+            fetch_r(rn, nmb);
+          }
+        }
+        if (!mbar_wait(smem_u32(empty_bar + stage), phase ^ 1u, p.status, abort_flag)) { ok = false; break; }
+        const uint32_t gw[4] = {gb[u].x, gb[u].y, gb[u].z, gb[u].w};
+        uint8_t* dst = sA + stage * A_TILE_BYTES + sw_off;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t xw[4] = {xb[u][i].x, xb[u][i].y, xb[u][i].z, xb[u][i].w};
+          const float r = rc[i];
+          uint32_t o[4];
+          // gamma * (x * r) in fp32, rounded once: the value a standalone RMSNorm stores
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            o[q] = pack_bf16(bf16_lo(gw[q]) * (bf16_lo(xw[q]) * r), bf16_hi(gw[q]) * (bf16_hi(xw[q]) * r));
+          *reinterpret_cast<uint4*>(dst + i * 16 * 128) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        fence_proxy_async_smem();   // the tensor core reads the stage through the async proxy
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(full_bar + stage));
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        if (cur_kb == p.num_kb - 1) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) rc[i] = rn[i];
+        }
+        advance(cur_t, cur_kb, cur_mb);
+      }
+    }
   } else {
     // -------------------------------------------------------------- epilogue warps 2..5
     const int quarter = warp & 3;
@@ -355,6 +489,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         };
         load_resid(0);
+        float ss = 0.f;   // row statistics: the sum of squares of this row's rounded outputs
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint4 res_c[4];
@@ -393,8 +528,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] += rr[i];
+                if (p.stat_part != nullptr) {
+#pragma unroll
+                  for (int i = 0; i < 32; ++i) {
+                    const float hb = __bfloat162float(__float2bfloat16_rn(v[i]));   // the stored value
+                    ss = i < valid ? fmaf(hb, hb, ss) : ss;
+                  }
+                }
               }
               store_bf16x32(static_cast<__nv_bfloat16*>(p.out) + m * p.ldo + n0, v, valid);
+            }
+          }
+        }
+        if constexpr (EPI == EPI_RESID) {
+          if (p.stat_part != nullptr && m < p.M) {
+            // this tile's share of row m; the row's last column tile to finish completes r_m
+            p.stat_part[static_cast<long long>(nb) * p.M + m] = ss;
+            __threadfence();
+            if (atomicAdd(p.stat_ticket + m, 1) == p.num_nb - 1) {
+              __threadfence();
+              float tot = 0.f;
+#pragma unroll 4
+              for (int q = 0; q < p.num_nb; ++q) tot += __ldcg(p.stat_part + static_cast<long long>(q) * p.M + m);
+              p.stat_r[m] = rsqrtf(tot * p.stat_inv_n + p.stat_eps);
+              p.stat_ticket[m] = 0;
             }
           }
         }
@@ -466,15 +623,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             __nv_bfloat16* dst = hh < p.H
                 ? p.q_out + ((static_cast<long long>(b) * p.H + hh) * p.S + s_in) * p.D
                 : p.k_cache + ((static_cast<long long>(b) * p.G + (hh - p.H)) * p.T_max + s) * p.D;
-            // this chunk's angles came one rope chunk ahead; the next rope chunk is the second
-            // quarter of this head or the first of the next head (the tile is head-aligned)
-            float cs_c[32], sn_c[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              cs_c[i] = cs_n[i];
-              sn_c[i] = sn_n[i];
-            }
-            load_angles(j0 + 32 < half_d ? c + 1 : c + 3);
+            // this chunk's 32 angles, loaded here (32 pairs per chunk: a look-ahead copy would
+            // not fit the registers of the RMSNorm-fused form)
+            load_angles(c);
             uint32_t r2[32];
             tmem_ld32(t_acc + c * 32, r);
             tmem_ld32(t_acc + c * 32 + half_d, r2);
@@ -483,8 +634,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const float x1 = __uint_as_float(r[i]), x2 = __uint_as_float(r2[i]);
-              v[i] = x1 * cs_c[i] - x2 * sn_c[i];
-              w2[i] = x2 * cs_c[i] + x1 * sn_c[i];
+              v[i] = x1 * cs_n[i] - x2 * sn_n[i];
+              w2[i] = x2 * cs_n[i] + x1 * sn_n[i];
             }
             store_bf16x32(dst + j0, v, 32);
             store_bf16x32(dst + j0 + half_d, w2, 32);
@@ -553,15 +704,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
-template <int BN, int EPI, int STAGES>
+template <int BN, int EPI, int STAGES, bool NORM>
 constexpr size_t smem_bytes() {
+  // alignment slack, the rings, 2 * STAGES + 5 barriers, the TMEM slot and the abort flag
   return 1024 + STAGES * (A_TILE_BYTES + BN * BK * 2) + (2 * STAGES + 5) * 8 + 16;
 }
 
-template <int BN, int EPI, int STAGES>
+template <int BN, int EPI, int STAGES, bool NORM = false>
 int launch(const Ctx& c, const TMaps& tm, Params p) {
-  auto kern = gemm_tc_kernel<BN, EPI, STAGES>;
-  constexpr size_t smem = smem_bytes<BN, EPI, STAGES>();
+  auto kern = gemm_tc_kernel<BN, EPI, STAGES, NORM>;
+  constexpr size_t smem = smem_bytes<BN, EPI, STAGES, NORM>();
+  static_assert(smem <= 227 * 1024, "shared memory per CTA");
   static_assert(smem >= kTmemKernelMinSmem, "a TMEM-holding kernel must not share an SM with another");
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
@@ -573,9 +726,19 @@ int launch(const Ctx& c, const TMaps& tm, Params p) {
   if (!c.static_weights) p.weight_first = 0;
   const int tiles = p.num_mb * p.num_nb * p.num_splits;
   if (tiles == 0) return LLAMA_OK;
+  if (NORM && (p.norm_x == nullptr || p.norm_gamma == nullptr || p.norm_r == nullptr || p.num_splits != 1 ||
+               p.K % BK != 0))
+    return LLAMA_ERR_INVALID_ARG;
   const int grid = std::min(tiles, c.num_sms);
-  launch_pdl(c, kern, dim3(grid), dim3(NUM_THREADS), smem, tm, p);
+  launch_pdl(c, kern, dim3(grid), dim3(threads_of<NORM>()), smem, tm, p);
   return after_launch(c);
+}
+
+// Operand A of the RMSNorm-fused form: x [M, K], gamma [K] and the row scales r [M].
+void set_norm(Params& p, const void* X, const NormIn& n) {
+  p.norm_x = static_cast<const __nv_bfloat16*>(X);
+  p.norm_gamma = static_cast<const __nv_bfloat16*>(n.gamma);
+  p.norm_r = n.r;
 }
 
 // Rounds of num_sms tiles times the tile width: the time of a GEMM with M rows and n_blocks
@@ -619,7 +782,8 @@ Params base_params(int M, int N, int K, int BN) {
 
 }  // namespace
 
-int gemm_plain(const Ctx& c, const void* X, const void* W, void* C, int M, int N, int K, bool c_f32) {
+int gemm_plain(const Ctx& c, const void* X, const void* W, void* C, int M, int N, int K, bool c_f32,
+               const NormIn* norm) {
   const int bn = tile_width_for(M, N, c.num_sms);
   TMaps tm{};
   if (!make_tmap_2d(&tm.m[0], X, K, M, K, 128) || !make_tmap_2d(&tm.m[1], W, K, N, K, bn == 256 ? 128 : bn))
@@ -629,11 +793,22 @@ int gemm_plain(const Ctx& c, const void* X, const void* W, void* C, int M, int N
   p.b_map0 = 1;
   p.out = C;
   p.ldo = N;
+  if (norm != nullptr) {
+    set_norm(p, X, *norm);
+    if (bn == 256) return c_f32 ? launch<256, EPI_F32, 4, true>(c, tm, p) : launch<256, EPI_BF16, 4, true>(c, tm, p);
+    return c_f32 ? launch<224, EPI_F32, 5, true>(c, tm, p) : launch<224, EPI_BF16, 5, true>(c, tm, p);
+  }
   if (bn == 256) return c_f32 ? launch<256, EPI_F32, 4>(c, tm, p) : launch<256, EPI_BF16, 4>(c, tm, p);
   return c_f32 ? launch<224, EPI_F32, 5>(c, tm, p) : launch<224, EPI_BF16, 5>(c, tm, p);
 }
 
-int gemm_residual(const Ctx& c, const void* X, const void* W, const void* resid, void* out, int M, int N, int K) {
+int residual_col_tiles(const Ctx& c, int M, int N) {
+  const int bn = tile_width_for(M, N, c.num_sms);
+  return (N + bn - 1) / bn;
+}
+
+int gemm_residual(const Ctx& c, const void* X, const void* W, const void* resid, void* out, int M, int N, int K,
+                  const RowStatsOut* stats) {
   // 224-column tiles when they finish in fewer tile-column rounds (e.g. N = 4096 at M = 2048:
   // 304 tiles fill 2 rounds of 152 SMs, where 256 tiles of 256 columns leave the second
   // round two-thirds full)
@@ -648,10 +823,19 @@ int gemm_residual(const Ctx& c, const void* X, const void* W, const void* resid,
   p.ldo = N;
   p.resid = static_cast<const __nv_bfloat16*>(resid);
   p.ldr = N;
+  if (stats != nullptr) {
+    if (stats->part == nullptr || stats->r == nullptr || stats->ticket == nullptr) return LLAMA_ERR_INVALID_ARG;
+    p.stat_part = stats->part;
+    p.stat_r = stats->r;
+    p.stat_ticket = stats->ticket;
+    p.stat_inv_n = 1.0f / static_cast<float>(N);
+    p.stat_eps = stats->eps;
+  }
   return bn == 256 ? launch<256, EPI_RESID, 4>(c, tm, p) : launch<224, EPI_RESID, 5>(c, tm, p);
 }
 
-int gemm_swiglu(const Ctx& c, const void* X, const void* Wg, const void* Wu, void* out, int M, int I, int K) {
+int gemm_swiglu(const Ctx& c, const void* X, const void* Wg, const void* Wu, void* out, int M, int I, int K,
+                const NormIn* norm) {
   // kernel N runs over 256-column tiles, each = 128 gate rows + the same 128 up rows (measured:
   // 240-column tiles, which fill the SM-count rounds better at I = 11008, M = 2048, run slower)
   TMaps tm{};
@@ -665,13 +849,17 @@ int gemm_swiglu(const Ctx& c, const void* X, const void* Wg, const void* Wu, voi
   p.n_maps = 3;
   p.out = out;
   p.ldo = I;
+  if (norm != nullptr) {
+    set_norm(p, X, *norm);
+    return launch<256, EPI_SWIGLU, 4, true>(c, tm, p);
+  }
   return launch<256, EPI_SWIGLU, 4>(c, tm, p);
 }
 
 int gemm_qkv_rope(const Ctx& c, const void* X, const void* Wq, const void* Wk, const void* Wv, int B, int S, int K,
                   int H, int G, int D, const float* cos, const float* sin, void* q_out, void* k_cache,
                   void* v_cache, int T_max, int rope_half, const int32_t* start, const int32_t* lens,
-                  int max_pos) {
+                  int max_pos, const NormIn* norm) {
   const int M = B * S;
   // 224-column tiles when they fill the SM-count rounds better (the half-split pairs (j, j+64)
   // need whole heads in a tile: 256 columns = two heads); a 224-column tile that crosses the
@@ -708,6 +896,10 @@ int gemm_qkv_rope(const Ctx& c, const void* X, const void* Wq, const void* Wk, c
   p.q_out = static_cast<__nv_bfloat16*>(q_out);
   p.k_cache = static_cast<__nv_bfloat16*>(k_cache);
   p.v_cache = static_cast<__nv_bfloat16*>(v_cache);
+  if (norm != nullptr) {
+    set_norm(p, X, *norm);
+    return bn == 256 ? launch<256, EPI_QKV, 4, true>(c, tm, p) : launch<224, EPI_QKV, 5, true>(c, tm, p);
+  }
   return bn == 256 ? launch<256, EPI_QKV, 4>(c, tm, p) : launch<224, EPI_QKV, 5>(c, tm, p);
 }
 

@@ -218,3 +218,91 @@ def test_attention_decode_reports_out_of_range_positions(api):
     api.attention_decode(dims, q, kc, vc, pos, out, ws)
     assert api.device_status() == -5
     assert torch.all(out[1] == 0) and torch.all(torch.isfinite(out.float()))
+
+
+def _one_ulp(gpu, ref, what):
+    """A bf16 result of one fp32-accumulated step: within one bf16 ulp (2^-8 relative) plus the
+    accumulation error, which 1e-3 of the row's rms bounds generously."""
+    scale = np.sqrt(np.mean(ref * ref, axis=-1, keepdims=True))
+    bad = np.abs(gpu - ref) > 2.0 ** -8 * np.abs(ref) + 1e-3 * scale
+    assert not bad.any(), f"{what}: {bad.sum()} elements beyond one bf16 ulp, first at {np.argwhere(bad)[0]}"
+
+
+def _norm_inputs(rng, M, K, scale=3.0):
+    x = bf16_stored(scale * rng.standard_normal((M, K)))
+    g = bf16_stored(1 + 0.1 * rng.standard_normal(K))
+    return x, g
+
+
+def _check_row_scales(r, x64, eps):
+    ref = 1.0 / np.sqrt(np.mean(x64 * x64, axis=-1) + eps)
+    assert np.allclose(f64(r), ref, rtol=1e-5, atol=0), "row scales"
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (300, 520, 256), (1000, 2048, 4096), (7, 32000, 4096)])
+@pytest.mark.parametrize("out_f32", [False, True])
+def test_norm_linear_fused(api, M, N, K, out_f32):
+    # RMSNorm inside the GEMM: the tensor cores multiply bf16(gamma * (x * r)), the value a
+    # standalone RMSNorm stores, so the result is the oracle's RMSNorm (rounded where it stores
+    # its output) followed by the product
+    rng = _rng(M * 3 + N + K)
+    x, g = _norm_inputs(rng, M, K)
+    w = bf16_stored(0.02 * rng.standard_normal((N, K)))
+    c = torch.empty(M, N, dtype=torch.float32 if out_f32 else torch.bfloat16, device="cuda")
+    r = api.norm_linear_bf16(to_dev(x), to_dev(g), 1e-5, to_dev(w), c)
+    assert api.device_status() == 0
+    xn = oracle.round_bf16(oracle.rms_norm(x.f64(), g.f64(), 1e-5))
+    ref = oracle.linear(xn, w.f64())
+    assert_close(f64(c), ref, 1e-3 if out_f32 else TOL["bf16"], f"norm + linear {M}x{N}x{K}")
+    if not out_f32:
+        _one_ulp(f64(c), ref, f"norm + linear {M}x{N}x{K}")
+    _check_row_scales(r, x.f64(), 1e-5)
+
+
+@pytest.mark.parametrize("M,I,K", [(130, 384, 256), (1000, 11008, 4096), (64, 1024, 4096)])
+def test_norm_linear_swiglu_fused(api, M, I, K):
+    rng = _rng(M + I + K)
+    x, g = _norm_inputs(rng, M, K)
+    wg = bf16_stored(0.02 * rng.standard_normal((I, K)))
+    wu = bf16_stored(0.02 * rng.standard_normal((I, K)))
+    a = torch.empty(M, I, dtype=torch.bfloat16, device="cuda")
+    r = api.norm_linear_swiglu(to_dev(x), to_dev(g), 1e-6, to_dev(wg), to_dev(wu), a)
+    assert api.device_status() == 0
+    xn = oracle.round_bf16(oracle.rms_norm(x.f64(), g.f64(), 1e-6))
+    ref = oracle.silu(oracle.linear(xn, wg.f64())) * oracle.linear(xn, wu.f64())
+    assert_close(f64(a), ref, TOL["bf16"], f"norm + gate/up {M}x{I}x{K}")
+    _one_ulp(f64(a), ref, f"norm + gate/up {M}x{I}x{K}")
+    _check_row_scales(r, x.f64(), 1e-6)
+
+
+@pytest.mark.parametrize("d,H,G,B,S,rope", [(256, 4, 2, 2, 130, "even_odd"), (512, 8, 1, 1, 300, "even_odd"),
+                                            (256, 4, 2, 2, 150, "half"), (4096, 32, 8, 1, 256, "even_odd")])
+def test_norm_qkv_rope_fused(api, d, H, G, B, S, rope):
+    rng = _rng(d + H * 7 + G + B * 13 + S)
+    D, T_max = 128, S + 9
+    x, g = _norm_inputs(rng, B * S, d, scale=1.0)
+    wq = bf16_stored(0.02 * rng.standard_normal((H * D, d)))
+    wk = bf16_stored(0.02 * rng.standard_normal((G * D, d)))
+    wv = bf16_stored(0.02 * rng.standard_normal((G * D, d)))
+    c64, s64 = oracle.rope_tables(1e4, D, T_max)
+    c32, s32 = c64.astype(np.float32), s64.astype(np.float32)
+    cos, sin = torch.from_numpy(c32).cuda(), torch.from_numpy(s32).cuda()
+    kc = torch.full((B, G, T_max, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    vc = torch.full_like(kc, float("nan"))
+    q = torch.empty(B, H, S, D, dtype=torch.bfloat16, device="cuda")
+    dims = api.Dims(d, H, G, D, 128, 1e-5, torch.bfloat16, 1 if rope == "half" else 0)
+    r = api.norm_qkv_rope(dims, to_dev(x).view(B, S, d), to_dev(g), to_dev(wq), to_dev(wk), to_dev(wv), cos, sin,
+                          kc, vc, q)
+    assert api.device_status() == 0
+    xn = oracle.round_bf16(oracle.rms_norm(x.f64(), g.f64(), 1e-5)).reshape(B, S, d)
+    rot = oracle.layer.ROPE_STYLES[rope]
+    cc, ss = c32.astype(np.float64)[:S][None, None], s32.astype(np.float64)[:S][None, None]
+    q_ref = rot(oracle.linear(xn, wq.f64()).reshape(B, S, H, D).transpose(0, 2, 1, 3), cc, ss)
+    k_ref = rot(oracle.linear(xn, wk.f64()).reshape(B, S, G, D).transpose(0, 2, 1, 3), cc, ss)
+    v_ref = oracle.linear(xn, wv.f64()).reshape(B, S, G, D).transpose(0, 2, 1, 3)
+    assert_close(f64(q), q_ref, TOL["bf16"], "norm + qkv: q")
+    _one_ulp(f64(q), q_ref, "norm + qkv: q")
+    assert_close(f64(kc)[:, :, :S], k_ref, TOL["bf16"], "norm + qkv: k in the cache")
+    assert_close(f64(vc)[:, :, :S], v_ref, TOL["bf16"], "norm + qkv: v in the cache")
+    assert torch.isnan(kc[:, :, S:].float()).all() and torch.isnan(vc[:, :, S:].float()).all()
+    _check_row_scales(r, x.f64(), 1e-5)
