@@ -183,7 +183,7 @@ def test_stack_layers_teacher_forced(api):
         del caches[:]
         if l == check_at[-1]:
             # final RMSNorm + LM head (one fused GEMM on the GPU), from the GPU's last output
-            xn = oracle.round_bf16(oracle.rms_norm(gpu["out"][b_idx, s_idx], glob["final_norm"].f64(), L.rms_eps))
+            xn = oracle.round_bf16(oracle.rms_norm(gpu["out"], glob["final_norm"].f64(), L.rms_eps))
             ref = oracle.linear(xn, glob["lm_head"].f64())
             assert_close(f64(logits)[b_idx, s_idx], ref, TOL["bf16"], "stack: final norm + LM head")
         del ws, st
