@@ -9,10 +9,10 @@
 // Two TMEM accumulators let the epilogue of tile i overlap the main loop of tile i+1.
 //
 // RMSNorm fused into the A operand ("12 · 从 Transformer 到 LLaMA 系列" §八 RMSNorm: y = gamma *
-// x * rsqrt(mean(x^2) + eps); "3.2 核心组件逐一拆解" §3.2.1: the statistics in fp32).  Four norm
-// warps replace the TMA load of A: they read the x tile of each k-block from global memory (two
-// k-blocks ahead), form bf16(gamma_k * (x_mk * r_m)) -- the normalised row rounded where a
-// standalone RMSNorm would store it -- and write it into the swizzled shared-memory stage.  The
+// x * rsqrt(mean(x^2) + eps); "3.2 核心组件逐一拆解" §3.2.1: the statistics in fp32).  TMA brings
+// the raw x tile of each k-block (and that k-block's 64 gammas) into the stage; four norm warps
+// turn it in place into bf16(gamma_k * (x_mk * r_m)) -- the normalised row rounded where a
+// standalone RMSNorm would store it -- and only then release the stage to the MMA issuer.  The
 // row scales r_m = rsqrt(mean_k x_mk^2 + eps) come with the input: from a row-statistics pass
 // over the layer input, or from the residual epilogue that produced x (below).  The normalised
 // activation never goes through HBM.
@@ -84,8 +84,7 @@ struct Params {
   __nv_bfloat16* q_out;
   __nv_bfloat16* k_cache;
   __nv_bfloat16* v_cache;
-  // RMSNorm-fused form: operand A = bf16(norm_gamma_k * (norm_x_mk * norm_r_m))
-  const __nv_bfloat16* norm_x;       // [M, K] row-major
+  // RMSNorm-fused form: operand A = bf16(norm_gamma_k * (x_mk * norm_r_m)), x the A operand
   const __nv_bfloat16* norm_gamma;   // [K]
   const float* norm_r;               // [M] rsqrt(mean_k x_mk^2 + eps)
   // residual epilogue: the row statistics of the output for the next RMSNorm (null: none)
@@ -175,8 +174,10 @@ __global__ void __launch_bounds__(threads_of<NORM>())
   // gate/up tiles as two boxes of BN/2 rows, one from each matrix
   constexpr int B_BOX_ROWS = EPI == EPI_SWIGLU ? BN / 2 : BN % 128 == 0 ? 128 : BN;
   constexpr int B_BOXES = BN / B_BOX_ROWS;
-  // bytes that TMA brings per stage (the norm warps write A themselves)
+  // bytes that TMA brings per stage towards the MMA barrier (in the RMSNorm-fused form the raw A
+  // tile and its gammas arrive on a barrier of their own, for the norm warps)
   constexpr uint32_t STAGE_TX = NORM ? B_TILE_BYTES : A_TILE_BYTES + B_TILE_BYTES;
+  constexpr uint32_t A_TX = A_TILE_BYTES + BK * 2;
   constexpr uint32_t TMEM_COLS = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
   constexpr uint32_t IDESC = idesc_bf16(BM, BN, false);
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
@@ -192,8 +193,11 @@ __global__ void __launch_bounds__(threads_of<NORM>())
   uint64_t* tfull_bar = bars + 2 * STAGES;
   uint64_t* tempty_bar = bars + 2 * STAGES + 2;
   uint64_t* drain_bar = bars + 2 * STAGES + 4;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  uint64_t* afull_bar = bars + 2 * STAGES + 5;    // [STAGES] raw A tile + gammas landed (RMSNorm-fused form)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // [STAGES][BK] gammas (RMSNorm-fused form), 16-byte aligned for the bulk copy
+  uint8_t* sG = reinterpret_cast<uint8_t*>(bars + ((3 * STAGES + 7) & ~1));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int num_tiles = p.num_mb * p.num_nb * p.num_splits;
@@ -203,6 +207,7 @@ __global__ void __launch_bounds__(threads_of<NORM>())
       // the TMA producer's arrival (with the byte count), and in the fused form the four norm warps'
       mbar_init(smem_u32(full_bar + i), NORM ? 5 : 1);
       mbar_init(smem_u32(empty_bar + i), 1);
+      mbar_init(smem_u32(afull_bar + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(tfull_bar + i), 1);
@@ -233,8 +238,16 @@ __global__ void __launch_bounds__(threads_of<NORM>())
       auto load_a = [&](int stage, int kb, int mb) {
         int a_map, a_row;
         resolve_rows(p.amap, mb * BM, a_map, a_row);
-        tma_load_2d(smem_u32(sA + stage * A_TILE_BYTES), &tm.m[p.a_map0 + a_map], smem_u32(full_bar + stage),
-                    kb * BK, a_row);
+        if constexpr (NORM) {
+          // the raw x tile and its gammas, for the norm warps
+          const uint32_t ab = smem_u32(afull_bar + stage);
+          mbar_expect_tx(ab, A_TX);
+          tma_load_2d(smem_u32(sA + stage * A_TILE_BYTES), &tm.m[p.a_map0 + a_map], ab, kb * BK, a_row);
+          bulk_load(smem_u32(sG + stage * BK * 2), p.norm_gamma + kb * BK, BK * 2, ab);
+        } else {
+          tma_load_2d(smem_u32(sA + stage * A_TILE_BYTES), &tm.m[p.a_map0 + a_map], smem_u32(full_bar + stage),
+                      kb * BK, a_row);
+        }
       };
       auto load_b = [&](int stage, int kb, int nb) {
         if constexpr (EPI == EPI_QKV && BN % 128 != 0) {
@@ -294,11 +307,11 @@ __global__ void __launch_bounds__(threads_of<NORM>())
         for (int kb = kb0; kb < kb1; ++kb, ++step) {
           if (step < pre) {   // the weight half of this stage is already on its way
             if (p.weight_first == 1) load_b(stage, kb, nb);
-            else if (!NORM) load_a(stage, kb, mb);
+            else load_a(stage, kb, mb);
           } else {
             if (!mbar_wait(smem_u32(empty_bar + stage), phase ^ 1u, p.status, abort_flag)) { ok = false; break; }
             mbar_expect_tx(smem_u32(full_bar + stage), STAGE_TX);
-            if (!NORM) load_a(stage, kb, mb);
+            load_a(stage, kb, mb);
             load_b(stage, kb, nb);
           }
           used_mask |= 1u << stage;
@@ -307,10 +320,12 @@ __global__ void __launch_bounds__(threads_of<NORM>())
         }
       }
       if (!ok) {
-        // leave no copy in flight: wait (bounded) for the last load into every stage used
+        // leave no copy in flight: wait (bounded) for the last load into every stage used (in the
+        // fused form the MMA barrier also counts the norm warps: the A copies have their own)
         for (int s = 0; s < STAGES; ++s)
           if (used_mask & (1u << s))
-            mbar_wait_slow(smem_u32(full_bar + s), (last_parity >> s) & 1u, nullptr, nullptr, kWaitBudgetNs);
+            mbar_wait_slow(smem_u32((NORM ? afull_bar : full_bar) + s), (last_parity >> s) & 1u, nullptr, nullptr,
+                           kWaitBudgetNs);
       }
     }
   } else if (warp == 1) {
@@ -358,8 +373,9 @@ __global__ void __launch_bounds__(threads_of<NORM>())
   } else if (NORM && warp >= 6) {
     // -------------------------------------------------------------- norm warps 6..9: operand A
     // Thread nt owns 16-byte chunk j of the k-block's 128-byte row slice in rows r0 + 16 i of
-    // the tile (a warp reads 4 rows x 128 contiguous bytes per load).  Row r0 + 16 i keeps chunk
-    // j at j ^ (r0 & 7) under the 128-byte swizzle that the MMA descriptors expect.
+    // the tile.  Row r0 + 16 i keeps chunk j at j ^ (r0 & 7) under the 128-byte swizzle of the
+    // TMA box, which is also the layout the MMA descriptors expect, so the chunk is rewritten
+    // where it lies.
     const int nt = threadIdx.x - NUM_THREADS;
     const int j = nt & 7;
     const int r0 = nt >> 3;
@@ -368,20 +384,7 @@ __global__ void __launch_bounds__(threads_of<NORM>())
                              ? (num_tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
                                    static_cast<int>(gridDim.x)
                              : 0;
-    const int total = my_tiles * p.num_kb;   // (tile, k-block) steps of this CTA; no split-K here
-    // x rows of k-block kb of row block mb, and the gamma chunk of that k-block
-    auto fetch = [&](uint4 (&v)[8], uint4& g, int kb, int mb) {
-      const int kcol = kb * BK + j * 8;
-      g = __ldg(reinterpret_cast<const uint4*>(p.norm_gamma + kcol));
-      const __nv_bfloat16* src = p.norm_x + static_cast<long long>(mb * BM + r0) * p.K + kcol;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int m = mb * BM + r0 + 16 * i;
-        v[i] = m < p.M ? __ldcg(reinterpret_cast<const uint4*>(src + static_cast<long long>(16 * i) * p.K))
-                       : make_uint4(0u, 0u, 0u, 0u);
-      }
-    };
-    // row scales of row block mb (rows past M scale zeros: 0)
+    // row scales of row block mb (rows past M hold TMA's zeros: any scale)
     auto fetch_r = [&](float (&r)[8], int mb) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -389,73 +392,43 @@ __global__ void __launch_bounds__(threads_of<NORM>())
         r[i] = m < p.M ? __ldcg(p.norm_r + m) : 0.f;
       }
     };
-    // two cursors over the steps: the one being written and the one being fetched (two ahead)
-    int cur_t = blockIdx.x, cur_kb = 0, cur_mb = 0, pf_t = blockIdx.x, pf_kb = 0, pf_mb = 0;
-    auto coords = [&](int t, int& mb) {
-      int nb, split;
+    auto tile_mb = [&](int t) {
+      int mb = 0, nb, split;
       if (t < num_tiles) tile_coords(p, t, mb, nb, split);
+      return mb;
     };
-    auto advance = [&](int& t, int& kb, int& mb) {
-      if (++kb == p.num_kb) {
-        kb = 0;
-        t += gridDim.x;
-        coords(t, mb);
-      }
-    };
-    coords(cur_t, cur_mb);
-    pf_mb = cur_mb;
-    uint4 xb[3][8], gb[3];
-    float rc[8], rn[8];   // row scales of the current tile, and of the next one (loaded a tile ahead)
-    if (total > 0) {
-      fetch_r(rc, cur_mb);
-      fetch(xb[0], gb[0], pf_kb, pf_mb);
-      advance(pf_t, pf_kb, pf_mb);
-    }
-    if (total > 1) { fetch(xb[1], gb[1], pf_kb, pf_mb); advance(pf_t, pf_kb, pf_mb); }
+    float rc[8], rn[8];   // row scales of the current tile and of the next one (loaded a tile ahead)
+    if (my_tiles > 0) fetch_r(rc, tile_mb(blockIdx.x));
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int s0 = 0; s0 < total && ok; s0 += 3) {
-#pragma unroll
-      for (int u = 0; u < 3; ++u) {
-        if (s0 + u >= total) break;
-        if (s0 + u + 2 < total) {   // two steps ahead, into the registers step s0 + u - 1 used
-          fetch(xb[(u + 2) % 3], gb[(u + 2) % 3], pf_kb, pf_mb);
-          advance(pf_t, pf_kb, pf_mb);
-        }
-        if (cur_kb == 0) {
-          // the next tile's row scales: their latency hides behind this tile's k-blocks
-          const int nt_next = cur_t + static_cast<int>(gridDim.x);
-          if (nt_next < num_tiles) {
-            int nmb;
-            coords(nt_next, nmb);
-            fetch_r(rn, nmb);
-          }
-        }
-        if (!mbar_wait(smem_u32(empty_bar + stage), phase ^ 1u, p.status, abort_flag)) { ok = false; break; }
-        const uint32_t gw[4] = {gb[u].x, gb[u].y, gb[u].z, gb[u].w};
-        uint8_t* dst = sA + stage * A_TILE_BYTES + sw_off;
+    for (int t = blockIdx.x, n = 0; n < my_tiles && ok; t += gridDim.x, ++n) {
+      if (n + 1 < my_tiles) fetch_r(rn, tile_mb(t + gridDim.x));
+      for (int kb = 0; kb < p.num_kb; ++kb) {
+        if (!mbar_wait(smem_u32(afull_bar + stage), phase, p.status, abort_flag)) { ok = false; break; }
+        const uint4 g = *reinterpret_cast<const uint4*>(sG + stage * BK * 2 + j * 16);
+        const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+        uint8_t* base = sA + stage * A_TILE_BYTES + sw_off;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const uint32_t xw[4] = {xb[u][i].x, xb[u][i].y, xb[u][i].z, xb[u][i].w};
+          uint4* cell = reinterpret_cast<uint4*>(base + i * 16 * 128);
+          const uint4 xv = *cell;
+          const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
           const float r = rc[i];
           uint32_t o[4];
           // gamma * (x * r) in fp32, rounded once: the value a standalone RMSNorm stores
 #pragma unroll
           for (int q = 0; q < 4; ++q)
             o[q] = pack_bf16(bf16_lo(gw[q]) * (bf16_lo(xw[q]) * r), bf16_hi(gw[q]) * (bf16_hi(xw[q]) * r));
-          *reinterpret_cast<uint4*>(dst + i * 16 * 128) = make_uint4(o[0], o[1], o[2], o[3]);
+          *cell = make_uint4(o[0], o[1], o[2], o[3]);
         }
         fence_proxy_async_smem();   // the tensor core reads the stage through the async proxy
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(full_bar + stage));
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-        if (cur_kb == p.num_kb - 1) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) rc[i] = rn[i];
-        }
-        advance(cur_t, cur_kb, cur_mb);
       }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) rc[i] = rn[i];
     }
   } else {
     // -------------------------------------------------------------- epilogue warps 2..5
@@ -706,8 +679,9 @@ __global__ void __launch_bounds__(threads_of<NORM>())
 
 template <int BN, int EPI, int STAGES, bool NORM>
 constexpr size_t smem_bytes() {
-  // alignment slack, the rings, 2 * STAGES + 5 barriers, the TMEM slot and the abort flag
-  return 1024 + STAGES * (A_TILE_BYTES + BN * BK * 2) + (2 * STAGES + 5) * 8 + 16;
+  // alignment slack, the rings, 3 * STAGES + 5 barriers, the TMEM slot and the abort flag (padded
+  // to 16 bytes), the gammas of each stage
+  return 1024 + STAGES * (A_TILE_BYTES + BN * BK * 2) + ((3 * STAGES + 7) & ~1) * 8 + STAGES * BK * 2;
 }
 
 template <int BN, int EPI, int STAGES, bool NORM = false>
@@ -726,17 +700,16 @@ int launch(const Ctx& c, const TMaps& tm, Params p) {
   if (!c.static_weights) p.weight_first = 0;
   const int tiles = p.num_mb * p.num_nb * p.num_splits;
   if (tiles == 0) return LLAMA_OK;
-  if (NORM && (p.norm_x == nullptr || p.norm_gamma == nullptr || p.norm_r == nullptr || p.num_splits != 1 ||
-               p.K % BK != 0))
+  if (NORM && (p.norm_gamma == nullptr || p.norm_r == nullptr || p.num_splits != 1 || p.K % BK != 0 ||
+               p.amap.nseg != 1 || p.weight_first == 1 || (reinterpret_cast<uintptr_t>(p.norm_gamma) & 15) != 0))
     return LLAMA_ERR_INVALID_ARG;
   const int grid = std::min(tiles, c.num_sms);
   launch_pdl(c, kern, dim3(grid), dim3(threads_of<NORM>()), smem, tm, p);
   return after_launch(c);
 }
 
-// Operand A of the RMSNorm-fused form: x [M, K], gamma [K] and the row scales r [M].
-void set_norm(Params& p, const void* X, const NormIn& n) {
-  p.norm_x = static_cast<const __nv_bfloat16*>(X);
+// RMSNorm-fused form: operand A (its tensor map) is x [M, K]; gamma [K] and the row scales r [M].
+void set_norm(Params& p, const NormIn& n) {
   p.norm_gamma = static_cast<const __nv_bfloat16*>(n.gamma);
   p.norm_r = n.r;
 }
@@ -794,7 +767,7 @@ int gemm_plain(const Ctx& c, const void* X, const void* W, void* C, int M, int N
   p.out = C;
   p.ldo = N;
   if (norm != nullptr) {
-    set_norm(p, X, *norm);
+    set_norm(p, *norm);
     if (bn == 256) return c_f32 ? launch<256, EPI_F32, 4, true>(c, tm, p) : launch<256, EPI_BF16, 4, true>(c, tm, p);
     return c_f32 ? launch<224, EPI_F32, 5, true>(c, tm, p) : launch<224, EPI_BF16, 5, true>(c, tm, p);
   }
@@ -850,7 +823,7 @@ int gemm_swiglu(const Ctx& c, const void* X, const void* Wg, const void* Wu, voi
   p.out = out;
   p.ldo = I;
   if (norm != nullptr) {
-    set_norm(p, X, *norm);
+    set_norm(p, *norm);
     return launch<256, EPI_SWIGLU, 4, true>(c, tm, p);
   }
   return launch<256, EPI_SWIGLU, 4>(c, tm, p);
@@ -897,7 +870,7 @@ int gemm_qkv_rope(const Ctx& c, const void* X, const void* Wq, const void* Wk, c
   p.k_cache = static_cast<__nv_bfloat16*>(k_cache);
   p.v_cache = static_cast<__nv_bfloat16*>(v_cache);
   if (norm != nullptr) {
-    set_norm(p, X, *norm);
+    set_norm(p, *norm);
     return bn == 256 ? launch<256, EPI_QKV, 4, true>(c, tm, p) : launch<224, EPI_QKV, 5, true>(c, tm, p);
   }
   return bn == 256 ? launch<256, EPI_QKV, 4>(c, tm, p) : launch<224, EPI_QKV, 5>(c, tm, p);
