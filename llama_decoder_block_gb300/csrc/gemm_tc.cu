@@ -166,10 +166,18 @@ __device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float* v,
   }
 }
 
+// Stages of the A ring: in the RMSNorm-fused form the raw x tiles run ahead of the weight ring
+// (the norm warps' transform sits between a tile's arrival and its MMAs).
+template <bool NORM, int STAGES>
+constexpr int a_stages_of() {
+  return NORM ? 6 : STAGES;
+}
+
 template <int BN, int EPI, int STAGES, bool NORM>
 __global__ void __launch_bounds__(threads_of<NORM>())
     gemm_tc_kernel(const __grid_constant__ TMaps tm, const Params p) {
   constexpr int B_TILE_BYTES = BN * BK * 2;
+  constexpr int SA = a_stages_of<NORM, STAGES>();
   // B arrives in 128-row boxes, or as one box when BN is not a multiple of 128 (BN <= 256);
   // gate/up tiles as two boxes of BN/2 rows, one from each matrix
   constexpr int B_BOX_ROWS = EPI == EPI_SWIGLU ? BN / 2 : BN % 128 == 0 ? 128 : BN;
@@ -186,28 +194,37 @@ __global__ void __launch_bounds__(threads_of<NORM>())
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = smem + STAGES * A_TILE_BYTES;
+  uint8_t* sB = smem + SA * A_TILE_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_TILE_BYTES);
-  uint64_t* full_bar = bars;
-  uint64_t* empty_bar = bars + STAGES;
+  uint64_t* full_bar = bars;                      // [STAGES] A and B landed (fused form: B)
+  uint64_t* empty_bar = bars + STAGES;            // [STAGES] the stage's MMAs are done
   uint64_t* tfull_bar = bars + 2 * STAGES;
   uint64_t* tempty_bar = bars + 2 * STAGES + 2;
   uint64_t* drain_bar = bars + 2 * STAGES + 4;
-  uint64_t* afull_bar = bars + 2 * STAGES + 5;    // [STAGES] raw A tile + gammas landed (RMSNorm-fused form)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * STAGES + 5);
+  // fused form, per A stage: raw tile + gammas landed; normalised by the norm warps; MMAs done
+  uint64_t* araw_bar = bars + 2 * STAGES + 5;
+  uint64_t* aready_bar = araw_bar + SA;
+  uint64_t* aempty_bar = aready_bar + SA;
+  constexpr int BAR_WORDS = 2 * STAGES + 5 + (NORM ? 3 * SA : 0);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + BAR_WORDS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  // [STAGES][BK] gammas (RMSNorm-fused form), 16-byte aligned for the bulk copy
-  uint8_t* sG = reinterpret_cast<uint8_t*>(bars + ((3 * STAGES + 7) & ~1));
+  // [SA][BK] gammas of each A stage (fused form), 16-byte aligned for the bulk copy
+  uint8_t* sG = reinterpret_cast<uint8_t*>(bars + ((BAR_WORDS + 2) & ~1));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int num_tiles = p.num_mb * p.num_nb * p.num_splits;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
-      // the TMA producer's arrival (with the byte count), and in the fused form the four norm warps'
-      mbar_init(smem_u32(full_bar + i), NORM ? 5 : 1);
+      mbar_init(smem_u32(full_bar + i), 1);
       mbar_init(smem_u32(empty_bar + i), 1);
-      mbar_init(smem_u32(afull_bar + i), 1);
+    }
+    if constexpr (NORM) {
+      for (int i = 0; i < SA; ++i) {
+        mbar_init(smem_u32(araw_bar + i), 1);
+        mbar_init(smem_u32(aready_bar + i), 4);
+        mbar_init(smem_u32(aempty_bar + i), 1);
+      }
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(tfull_bar + i), 1);
@@ -232,6 +249,22 @@ __global__ void __launch_bounds__(threads_of<NORM>())
   // after issuing the weight tiles that depend on nothing in flight)
   if (!(warp == 0 && lane == 0)) pdl_wait();
 
+  // The (tile, k-block) steps of this CTA in order, walked by cursors (no divisions per step).
+  struct Cursor {
+    int t, kb, kb1, mb, nb, split;
+  };
+  auto cursor_at_tile = [&](Cursor& c, int t) {
+    c.t = t;
+    if (t < num_tiles) {
+      tile_coords(p, t, c.mb, c.nb, c.split);
+      c.kb = c.split * p.kb_per_split;
+      c.kb1 = min(c.kb + p.kb_per_split, p.num_kb);
+    }
+  };
+  auto cursor_next = [&](Cursor& c) {
+    if (++c.kb == c.kb1) cursor_at_tile(c, c.t + static_cast<int>(gridDim.x));
+  };
+
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ TMA producer
@@ -240,7 +273,7 @@ __global__ void __launch_bounds__(threads_of<NORM>())
         resolve_rows(p.amap, mb * BM, a_map, a_row);
         if constexpr (NORM) {
           // the raw x tile and its gammas, for the norm warps
-          const uint32_t ab = smem_u32(afull_bar + stage);
+          const uint32_t ab = smem_u32(araw_bar + stage);
           mbar_expect_tx(ab, A_TX);
           tma_load_2d(smem_u32(sA + stage * A_TILE_BYTES), &tm.m[p.a_map0 + a_map], ab, kb * BK, a_row);
           bulk_load(smem_u32(sG + stage * BK * 2), p.norm_gamma + kb * BK, BK * 2, ab);
@@ -295,44 +328,81 @@ __global__ void __launch_bounds__(threads_of<NORM>())
         }
       }
       pdl_wait();
-      int stage = 0, step = 0;
-      uint32_t phase = 0;
-      uint32_t used_mask = 0, last_parity = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-        int mb, nb, split;
-        tile_coords(p, t, mb, nb, split);
-        const int kb0 = split * p.kb_per_split;
-        const int kb1 = min(kb0 + p.kb_per_split, p.num_kb);
-        for (int kb = kb0; kb < kb1; ++kb, ++step) {
-          if (step < pre) {   // the weight half of this stage is already on its way
-            if (p.weight_first == 1) load_b(stage, kb, nb);
-            else load_a(stage, kb, mb);
-          } else {
-            if (!mbar_wait(smem_u32(empty_bar + stage), phase ^ 1u, p.status, abort_flag)) { ok = false; break; }
-            mbar_expect_tx(smem_u32(full_bar + stage), STAGE_TX);
-            load_a(stage, kb, mb);
-            load_b(stage, kb, nb);
+      if constexpr (NORM) {
+        // A runs SA - STAGES steps ahead of B: before the weight tile of step s goes out, the raw
+        // x tiles of steps up to s + SA - STAGES do (each into a stage whose MMAs are done)
+        constexpr int LEAD = SA - STAGES;
+        Cursor ca, cb;
+        cursor_at_tile(ca, blockIdx.x);
+        cursor_at_tile(cb, blockIdx.x);
+        int sa = 0, sb = 0, stage_a = 0, stage_b = 0;
+        uint32_t phase_a = 0, phase_b = 0;
+        uint32_t used_a = 0, par_a = 0, used_b = 0, par_b = 0;
+        for (; cb.t < num_tiles && ok; cursor_next(cb), ++sb) {
+          for (; ca.t < num_tiles && sa <= sb + LEAD; cursor_next(ca), ++sa) {
+            if (!mbar_wait(smem_u32(aempty_bar + stage_a), phase_a ^ 1u, p.status, abort_flag)) { ok = false; break; }
+            load_a(stage_a, ca.kb, ca.mb);
+            used_a |= 1u << stage_a;
+            par_a = (par_a & ~(1u << stage_a)) | (phase_a << stage_a);
+            if (++stage_a == SA) { stage_a = 0; phase_a ^= 1u; }
           }
-          used_mask |= 1u << stage;
-          last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          if (!ok) break;
+          if (sb >= pre) {
+            if (!mbar_wait(smem_u32(empty_bar + stage_b), phase_b ^ 1u, p.status, abort_flag)) { ok = false; break; }
+            mbar_expect_tx(smem_u32(full_bar + stage_b), STAGE_TX);
+            load_b(stage_b, cb.kb, cb.nb);
+          }
+          used_b |= 1u << stage_b;
+          par_b = (par_b & ~(1u << stage_b)) | (phase_b << stage_b);
+          if (++stage_b == STAGES) { stage_b = 0; phase_b ^= 1u; }
         }
-      }
-      if (!ok) {
-        // leave no copy in flight: wait (bounded) for the last load into every stage used (in the
-        // fused form the MMA barrier also counts the norm warps: the A copies have their own)
-        for (int s = 0; s < STAGES; ++s)
-          if (used_mask & (1u << s))
-            mbar_wait_slow(smem_u32((NORM ? afull_bar : full_bar) + s), (last_parity >> s) & 1u, nullptr, nullptr,
-                           kWaitBudgetNs);
+        if (!ok) {
+          // leave no copy in flight: wait (bounded) for the last load into every stage used
+          for (int s = 0; s < SA; ++s)
+            if (used_a & (1u << s))
+              mbar_wait_slow(smem_u32(araw_bar + s), (par_a >> s) & 1u, nullptr, nullptr, kWaitBudgetNs);
+          for (int s = 0; s < STAGES; ++s)
+            if (used_b & (1u << s))
+              mbar_wait_slow(smem_u32(full_bar + s), (par_b >> s) & 1u, nullptr, nullptr, kWaitBudgetNs);
+        }
+      } else {
+        int stage = 0, step = 0;
+        uint32_t phase = 0;
+        uint32_t used_mask = 0, last_parity = 0;
+        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+          int mb, nb, split;
+          tile_coords(p, t, mb, nb, split);
+          const int kb0 = split * p.kb_per_split;
+          const int kb1 = min(kb0 + p.kb_per_split, p.num_kb);
+          for (int kb = kb0; kb < kb1; ++kb, ++step) {
+            if (step < pre) {   // the weight half of this stage is already on its way
+              if (p.weight_first == 1) load_b(stage, kb, nb);
+              else load_a(stage, kb, mb);
+            } else {
+              if (!mbar_wait(smem_u32(empty_bar + stage), phase ^ 1u, p.status, abort_flag)) { ok = false; break; }
+              mbar_expect_tx(smem_u32(full_bar + stage), STAGE_TX);
+              load_a(stage, kb, mb);
+              load_b(stage, kb, nb);
+            }
+            used_mask |= 1u << stage;
+            last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          }
+        }
+        if (!ok) {
+          // leave no copy in flight: wait (bounded) for the last load into every stage used
+          for (int s = 0; s < STAGES; ++s)
+            if (used_mask & (1u << s))
+              mbar_wait_slow(smem_u32(full_bar + s), (last_parity >> s) & 1u, nullptr, nullptr, kWaitBudgetNs);
+        }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
-      int stage = 0;
-      uint32_t phase = 0;
+      int stage = 0, stage_a = 0;
+      uint32_t phase = 0, phase_a = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
@@ -347,8 +417,11 @@ __global__ void __launch_bounds__(threads_of<NORM>())
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(smem_u32(full_bar + stage), phase, p.status, abort_flag)) { ok = false; break; }
+          if constexpr (NORM) {
+            if (!mbar_wait(smem_u32(aready_bar + stage_a), phase_a, p.status, abort_flag)) { ok = false; break; }
+          }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(sA + stage * A_TILE_BYTES);
+          const uint32_t a_addr = smem_u32(sA + (NORM ? stage_a : stage) * A_TILE_BYTES);
           const uint32_t b_addr = smem_u32(sB + stage * B_TILE_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
@@ -359,6 +432,10 @@ __global__ void __launch_bounds__(threads_of<NORM>())
           issued = true;
           tc_commit(smem_u32(empty_bar + stage));
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          if constexpr (NORM) {
+            tc_commit(smem_u32(aempty_bar + stage_a));
+            if (++stage_a == SA) { stage_a = 0; phase_a ^= 1u; }
+          }
         }
         if (!ok) break;
         tc_commit(smem_u32(tfull_bar + acc));
@@ -380,10 +457,6 @@ __global__ void __launch_bounds__(threads_of<NORM>())
     const int j = nt & 7;
     const int r0 = nt >> 3;
     const uint32_t sw_off = static_cast<uint32_t>(r0 * 128 + ((j ^ (r0 & 7)) << 4));
-    const int my_tiles = static_cast<int>(blockIdx.x) < num_tiles
-                             ? (num_tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
-                                   static_cast<int>(gridDim.x)
-                             : 0;
     // row scales of row block mb (rows past M hold TMA's zeros: any scale)
     auto fetch_r = [&](float (&r)[8], int mb) {
 #pragma unroll
@@ -392,20 +465,22 @@ __global__ void __launch_bounds__(threads_of<NORM>())
         r[i] = m < p.M ? __ldcg(p.norm_r + m) : 0.f;
       }
     };
-    auto tile_mb = [&](int t) {
-      int mb = 0, nb, split;
-      if (t < num_tiles) tile_coords(p, t, mb, nb, split);
-      return mb;
-    };
     float rc[8], rn[8];   // row scales of the current tile and of the next one (loaded a tile ahead)
-    if (my_tiles > 0) fetch_r(rc, tile_mb(blockIdx.x));
+    Cursor c;
+    cursor_at_tile(c, blockIdx.x);
+    if (c.t < num_tiles) fetch_r(rc, c.mb);
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int t = blockIdx.x, n = 0; n < my_tiles && ok; t += gridDim.x, ++n) {
-      if (n + 1 < my_tiles) fetch_r(rn, tile_mb(t + gridDim.x));
-      for (int kb = 0; kb < p.num_kb; ++kb) {
-        if (!mbar_wait(smem_u32(afull_bar + stage), phase, p.status, abort_flag)) { ok = false; break; }
+    while (c.t < num_tiles && ok) {
+      const int t_next = c.t + static_cast<int>(gridDim.x);
+      if (t_next < num_tiles) {
+        int mb, nb, split;
+        tile_coords(p, t_next, mb, nb, split);
+        fetch_r(rn, mb);
+      }
+      for (; c.kb < c.kb1; ++c.kb) {
+        if (!mbar_wait(smem_u32(araw_bar + stage), phase, p.status, abort_flag)) { ok = false; break; }
         const uint4 g = *reinterpret_cast<const uint4*>(sG + stage * BK * 2 + j * 16);
         const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
         uint8_t* base = sA + stage * A_TILE_BYTES + sw_off;
@@ -424,11 +499,13 @@ __global__ void __launch_bounds__(threads_of<NORM>())
         }
         fence_proxy_async_smem();   // the tensor core reads the stage through the async proxy
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(full_bar + stage));
-        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        if (lane == 0) mbar_arrive(smem_u32(aready_bar + stage));
+        if (++stage == SA) { stage = 0; phase ^= 1u; }
       }
+      if (!ok) break;
 #pragma unroll
       for (int i = 0; i < 8; ++i) rc[i] = rn[i];
+      cursor_at_tile(c, t_next);
     }
   } else {
     // -------------------------------------------------------------- epilogue warps 2..5
@@ -679,9 +756,11 @@ __global__ void __launch_bounds__(threads_of<NORM>())
 
 template <int BN, int EPI, int STAGES, bool NORM>
 constexpr size_t smem_bytes() {
-  // alignment slack, the rings, 3 * STAGES + 5 barriers, the TMEM slot and the abort flag (padded
-  // to 16 bytes), the gammas of each stage
-  return 1024 + STAGES * (A_TILE_BYTES + BN * BK * 2) + ((3 * STAGES + 7) & ~1) * 8 + STAGES * BK * 2;
+  // alignment slack, the rings, the barriers, the TMEM slot and the abort flag (padded to 16
+  // bytes), the gammas of each A stage
+  constexpr int SA = a_stages_of<NORM, STAGES>();
+  constexpr int bar_words = 2 * STAGES + 5 + (NORM ? 3 * SA : 0);
+  return 1024 + SA * A_TILE_BYTES + STAGES * BN * BK * 2 + ((bar_words + 2) & ~1) * 8 + (NORM ? SA * BK * 2 : 0);
 }
 
 template <int BN, int EPI, int STAGES, bool NORM = false>
@@ -769,7 +848,7 @@ int gemm_plain(const Ctx& c, const void* X, const void* W, void* C, int M, int N
   if (norm != nullptr) {
     set_norm(p, *norm);
     if (bn == 256) return c_f32 ? launch<256, EPI_F32, 4, true>(c, tm, p) : launch<256, EPI_BF16, 4, true>(c, tm, p);
-    return c_f32 ? launch<224, EPI_F32, 5, true>(c, tm, p) : launch<224, EPI_BF16, 5, true>(c, tm, p);
+    return c_f32 ? launch<224, EPI_F32, 4, true>(c, tm, p) : launch<224, EPI_BF16, 4, true>(c, tm, p);
   }
   if (bn == 256) return c_f32 ? launch<256, EPI_F32, 4>(c, tm, p) : launch<256, EPI_BF16, 4>(c, tm, p);
   return c_f32 ? launch<224, EPI_F32, 5>(c, tm, p) : launch<224, EPI_BF16, 5>(c, tm, p);
@@ -871,7 +950,7 @@ int gemm_qkv_rope(const Ctx& c, const void* X, const void* Wq, const void* Wk, c
   p.v_cache = static_cast<__nv_bfloat16*>(v_cache);
   if (norm != nullptr) {
     set_norm(p, *norm);
-    return bn == 256 ? launch<256, EPI_QKV, 4, true>(c, tm, p) : launch<224, EPI_QKV, 5, true>(c, tm, p);
+    return bn == 256 ? launch<256, EPI_QKV, 4, true>(c, tm, p) : launch<224, EPI_QKV, 4, true>(c, tm, p);
   }
   return bn == 256 ? launch<256, EPI_QKV, 4>(c, tm, p) : launch<224, EPI_QKV, 5>(c, tm, p);
 }
