@@ -10,12 +10,16 @@
 //
 // RMSNorm fused into the A operand ("12 · 从 Transformer 到 LLaMA 系列" §八 RMSNorm: y = gamma *
 // x * rsqrt(mean(x^2) + eps); "3.2 核心组件逐一拆解" §3.2.1: the statistics in fp32).  TMA brings
-// the raw x tile of each k-block (and that k-block's 64 gammas) into the stage; four norm warps
-// turn it in place into bf16(gamma_k * (x_mk * r_m)) -- the normalised row rounded where a
-// standalone RMSNorm would store it -- and only then release the stage to the MMA issuer.  The
-// row scales r_m = rsqrt(mean_k x_mk^2 + eps) come with the input: from a row-statistics pass
-// over the layer input, or from the residual epilogue that produced x (below).  The normalised
-// activation never goes through HBM.
+// the raw x tile of each k-block (and that k-block's 64 gammas) into a shared-memory ring of its
+// own; four norm warps read it once, each thread one row, form bf16(gamma_k * (x_mk * r_m)) --
+// the normalised row rounded where a standalone RMSNorm would store it -- and store it into one
+// of two A slots in tensor memory, from which the MMAs read their A operand.  Shared memory
+// carries the same bytes as in the plain form (the tensor cores' own A reads move to TMEM), which
+// matters because these GEMMs are bound by shared-memory bandwidth: a transform written back to
+// shared memory cost a third more time.  The row scales r_m = rsqrt(mean_k x_mk^2 + eps) come
+// with the input: from a row-statistics pass over the layer input, or from the residual
+// epilogue that produced x (below).  The normalised activation never goes through HBM.
+// Tensor memory: the two accumulators (2 x 224 columns) and the two A slots (32 columns each).
 //
 // Row statistics in the residual epilogue: a tile adds the squares of its rounded outputs of
 // row m into part[nb][m]; the last of the row's column tiles to finish (a per-row ticket)
@@ -166,12 +170,12 @@ __device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float* v,
   }
 }
 
-// Stages of the A ring: in the RMSNorm-fused form the raw x tiles run ahead of the weight ring
-// (the norm warps' transform sits between a tile's arrival and its MMAs).
+// Stages of the shared-memory A ring (the raw x tiles of the RMSNorm-fused form), and TMEM A slots.
 template <bool NORM, int STAGES>
 constexpr int a_stages_of() {
-  return NORM ? 6 : STAGES;
+  return NORM ? 4 : STAGES;
 }
+constexpr int kNormASlots = 2;
 
 template <int BN, int EPI, int STAGES, bool NORM>
 __global__ void __launch_bounds__(threads_of<NORM>())
@@ -186,9 +190,11 @@ __global__ void __launch_bounds__(threads_of<NORM>())
   // tile and its gammas arrive on a barrier of their own, for the norm warps)
   constexpr uint32_t STAGE_TX = NORM ? B_TILE_BYTES : A_TILE_BYTES + B_TILE_BYTES;
   constexpr uint32_t A_TX = A_TILE_BYTES + BK * 2;
-  constexpr uint32_t TMEM_COLS = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
+  constexpr uint32_t ACC_COLS = 2 * BN + (NORM ? kNormASlots * BK / 2 : 0);
+  constexpr uint32_t TMEM_COLS = ACC_COLS <= 32 ? 32 : ACC_COLS <= 64 ? 64 : ACC_COLS <= 128 ? 128 : ACC_COLS <= 256 ? 256 : 512;
   constexpr uint32_t IDESC = idesc_bf16(BM, BN, false);
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
+  static_assert(ACC_COLS <= 512, "two accumulators (and the A slots) in tensor memory");
 
   pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
@@ -201,11 +207,13 @@ __global__ void __launch_bounds__(threads_of<NORM>())
   uint64_t* tfull_bar = bars + 2 * STAGES;
   uint64_t* tempty_bar = bars + 2 * STAGES + 2;
   uint64_t* drain_bar = bars + 2 * STAGES + 4;
-  // fused form, per A stage: raw tile + gammas landed; normalised by the norm warps; MMAs done
+  // fused form: per raw A stage, landed / read by the norm warps; per TMEM A slot, written by the
+  // norm warps / read by the MMAs
   uint64_t* araw_bar = bars + 2 * STAGES + 5;
-  uint64_t* aready_bar = araw_bar + SA;
-  uint64_t* aempty_bar = aready_bar + SA;
-  constexpr int BAR_WORDS = 2 * STAGES + 5 + (NORM ? 3 * SA : 0);
+  uint64_t* afree_bar = araw_bar + SA;
+  uint64_t* tready_bar = afree_bar + SA;
+  uint64_t* tfree_bar = tready_bar + kNormASlots;
+  constexpr int BAR_WORDS = 2 * STAGES + 5 + (NORM ? 2 * SA + 2 * kNormASlots : 0);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + BAR_WORDS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   // [SA][BK] gammas of each A stage (fused form), 16-byte aligned for the bulk copy
@@ -222,8 +230,11 @@ __global__ void __launch_bounds__(threads_of<NORM>())
     if constexpr (NORM) {
       for (int i = 0; i < SA; ++i) {
         mbar_init(smem_u32(araw_bar + i), 1);
-        mbar_init(smem_u32(aready_bar + i), 4);
-        mbar_init(smem_u32(aempty_bar + i), 1);
+        mbar_init(smem_u32(afree_bar + i), 4);
+      }
+      for (int i = 0; i < kNormASlots; ++i) {
+        mbar_init(smem_u32(tready_bar + i), 4);
+        mbar_init(smem_u32(tfree_bar + i), 1);
       }
     }
     for (int i = 0; i < 2; ++i) {
@@ -245,6 +256,7 @@ __global__ void __launch_bounds__(threads_of<NORM>())
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  const uint32_t tmem_a = tmem_base + 2 * BN;      // the A slots of the fused form
   // inputs written by the previous kernel are read from here on (the producer waits below,
   // after issuing the weight tiles that depend on nothing in flight)
   if (!(warp == 0 && lane == 0)) pdl_wait();
@@ -330,9 +342,10 @@ __global__ void __launch_bounds__(threads_of<NORM>())
       pdl_wait();
       bool ok = true;
       if constexpr (NORM) {
-        // A runs SA - STAGES steps ahead of B: before the weight tile of step s goes out, the raw
-        // x tiles of steps up to s + SA - STAGES do (each into a stage whose MMAs are done)
-        constexpr int LEAD = SA - STAGES;
+        // Before the weight tile of step s goes out, the raw x tiles of steps up to s + SA - 1 do,
+        // each into a stage that the norm warps have read (they run ahead of the MMAs by the
+        // TMEM A slots).
+        constexpr int LEAD = SA - 1;
         Cursor ca, cb;
         cursor_at_tile(ca, blockIdx.x);
         cursor_at_tile(cb, blockIdx.x);
@@ -341,7 +354,7 @@ __global__ void __launch_bounds__(threads_of<NORM>())
         uint32_t used_a = 0, par_a = 0, used_b = 0, par_b = 0;
         for (; cb.t < num_tiles && ok; cursor_next(cb), ++sb) {
           for (; ca.t < num_tiles && sa <= sb + LEAD; cursor_next(ca), ++sa) {
-            if (!mbar_wait(smem_u32(aempty_bar + stage_a), phase_a ^ 1u, p.status, abort_flag)) { ok = false; break; }
+            if (!mbar_wait(smem_u32(afree_bar + stage_a), phase_a ^ 1u, p.status, abort_flag)) { ok = false; break; }
             load_a(stage_a, ca.kb, ca.mb);
             used_a |= 1u << stage_a;
             par_a = (par_a & ~(1u << stage_a)) | (phase_a << stage_a);
@@ -401,8 +414,8 @@ __global__ void __launch_bounds__(threads_of<NORM>())
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
-      int stage = 0, stage_a = 0;
-      uint32_t phase = 0, phase_a = 0;
+      int stage = 0, slot = 0;
+      uint32_t phase = 0, slot_phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
@@ -418,23 +431,32 @@ __global__ void __launch_bounds__(threads_of<NORM>())
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(smem_u32(full_bar + stage), phase, p.status, abort_flag)) { ok = false; break; }
           if constexpr (NORM) {
-            if (!mbar_wait(smem_u32(aready_bar + stage_a), phase_a, p.status, abort_flag)) { ok = false; break; }
+            if (!mbar_wait(smem_u32(tready_bar + slot), slot_phase, p.status, abort_flag)) { ok = false; break; }
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(sA + (NORM ? stage_a : stage) * A_TILE_BYTES);
           const uint32_t b_addr = smem_u32(sB + stage * B_TILE_BYTES);
+          if constexpr (NORM) {
+            // A from its TMEM slot: row m in lane m, k-block columns packed two per 32-bit column
+            const uint32_t a_tmem = tmem_a + static_cast<uint32_t>(slot * (BK / 2));
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            const uint64_t ad = sdesc_sw128(a_addr + k * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(b_addr + k * 32, 16, 1024);
-            tc_mma_bf16(d_tmem, ad, bd, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < BK / 16; ++k)
+              tc_mma_bf16_ts(d_tmem, a_tmem + k * 8, sdesc_sw128(b_addr + k * 32, 16, 1024), IDESC,
+                             (kb > kb0 || k > 0) ? 1u : 0u);
+          } else {
+            const uint32_t a_addr = smem_u32(sA + stage * A_TILE_BYTES);
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k) {
+              const uint64_t ad = sdesc_sw128(a_addr + k * 32, 16, 1024);
+              const uint64_t bd = sdesc_sw128(b_addr + k * 32, 16, 1024);
+              tc_mma_bf16(d_tmem, ad, bd, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+            }
           }
           issued = true;
           tc_commit(smem_u32(empty_bar + stage));
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
           if constexpr (NORM) {
-            tc_commit(smem_u32(aempty_bar + stage_a));
-            if (++stage_a == SA) { stage_a = 0; phase_a ^= 1u; }
+            tc_commit(smem_u32(tfree_bar + slot));
+            if (++slot == kNormASlots) { slot = 0; slot_phase ^= 1u; }
           }
         }
         if (!ok) break;
@@ -449,62 +471,57 @@ __global__ void __launch_bounds__(threads_of<NORM>())
     }
   } else if (NORM && warp >= 6) {
     // -------------------------------------------------------------- norm warps 6..9: operand A
-    // Thread nt owns 16-byte chunk j of the k-block's 128-byte row slice in rows r0 + 16 i of
-    // the tile.  Row r0 + 16 i keeps chunk j at j ^ (r0 & 7) under the 128-byte swizzle of the
-    // TMA box, which is also the layout the MMA descriptors expect, so the chunk is rewritten
-    // where it lies.
-    const int nt = threadIdx.x - NUM_THREADS;
-    const int j = nt & 7;
-    const int r0 = nt >> 3;
-    const uint32_t sw_off = static_cast<uint32_t>(r0 * 128 + ((j ^ (r0 & 7)) << 4));
-    // row scales of row block mb (rows past M hold TMA's zeros: any scale)
-    auto fetch_r = [&](float (&r)[8], int mb) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int m = mb * BM + r0 + 16 * i;
-        r[i] = m < p.M ? __ldcg(p.norm_r + m) : 0.f;
-      }
-    };
-    float rc[8], rn[8];   // row scales of the current tile and of the next one (loaded a tile ahead)
+    // A warp may only reach the TMEM lanes of its quarter (warp % 4): thread `lane` of warp w
+    // owns row 32 (w % 4) + lane of the tile and writes its 64 k-values of each k-block, packed
+    // two per 32-bit column, into the 32 columns of the step's A slot.  In the raw tile the row's
+    // 16-byte chunk j lies at j ^ (row & 7) (the 128-byte swizzle of the TMA box).
+    const int row = (warp & 3) * 32 + lane;
+    const uint32_t t_lane = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    float rc = 0.f, rn = 0.f;   // this row's scale in the current tile and in the next one
     Cursor c;
     cursor_at_tile(c, blockIdx.x);
-    if (c.t < num_tiles) fetch_r(rc, c.mb);
-    int stage = 0;
-    uint32_t phase = 0;
+    if (c.t < num_tiles) rc = c.mb * BM + row < p.M ? __ldcg(p.norm_r + c.mb * BM + row) : 0.f;
+    int stage = 0, slot = 0;
+    uint32_t phase = 0, slot_phase = 0;
     bool ok = true;
     while (c.t < num_tiles && ok) {
       const int t_next = c.t + static_cast<int>(gridDim.x);
-      if (t_next < num_tiles) {
+      if (t_next < num_tiles) {   // the next tile's scale: its latency hides behind this tile
         int mb, nb, split;
         tile_coords(p, t_next, mb, nb, split);
-        fetch_r(rn, mb);
+        rn = mb * BM + row < p.M ? __ldcg(p.norm_r + mb * BM + row) : 0.f;
       }
       for (; c.kb < c.kb1; ++c.kb) {
         if (!mbar_wait(smem_u32(araw_bar + stage), phase, p.status, abort_flag)) { ok = false; break; }
-        const uint4 g = *reinterpret_cast<const uint4*>(sG + stage * BK * 2 + j * 16);
-        const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
-        uint8_t* base = sA + stage * A_TILE_BYTES + sw_off;
+        const uint8_t* xrow = sA + stage * A_TILE_BYTES + row * 128;
+        const uint8_t* grow = sG + stage * BK * 2;
+        uint32_t o[32];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          uint4* cell = reinterpret_cast<uint4*>(base + i * 16 * 128);
-          const uint4 xv = *cell;
+        for (int jj = 0; jj < 8; ++jj) {
+          const uint4 xv = *reinterpret_cast<const uint4*>(xrow + ((jj ^ (row & 7)) << 4));
+          const uint4 gv = *reinterpret_cast<const uint4*>(grow + jj * 16);
           const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-          const float r = rc[i];
-          uint32_t o[4];
+          const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
           // gamma * (x * r) in fp32, rounded once: the value a standalone RMSNorm stores
 #pragma unroll
           for (int q = 0; q < 4; ++q)
-            o[q] = pack_bf16(bf16_lo(gw[q]) * (bf16_lo(xw[q]) * r), bf16_hi(gw[q]) * (bf16_hi(xw[q]) * r));
-          *cell = make_uint4(o[0], o[1], o[2], o[3]);
+            o[4 * jj + q] = pack_bf16(bf16_lo(gw[q]) * (bf16_lo(xw[q]) * rc), bf16_hi(gw[q]) * (bf16_hi(xw[q]) * rc));
         }
-        fence_proxy_async_smem();   // the tensor core reads the stage through the async proxy
+        // the raw stage is no longer needed
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(aready_bar + stage));
+        if (lane == 0) mbar_arrive(smem_u32(afree_bar + stage));
         if (++stage == SA) { stage = 0; phase ^= 1u; }
+        // the slot's previous MMAs are done: overwrite it
+        if (!mbar_wait(smem_u32(tfree_bar + slot), slot_phase ^ 1u, p.status, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        tmem_st32(tmem_a + t_lane + static_cast<uint32_t>(slot * (BK / 2)), o);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(tready_bar + slot));
+        if (++slot == kNormASlots) { slot = 0; slot_phase ^= 1u; }
       }
       if (!ok) break;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) rc[i] = rn[i];
+      rc = rn;
       cursor_at_tile(c, t_next);
     }
   } else {
@@ -606,16 +623,32 @@ __global__ void __launch_bounds__(threads_of<NORM>())
           }
         }
       } else if constexpr (EPI == EPI_SWIGLU) {
-        // columns [0, BN/2) of the tile are gate rows BN/2*nb.., [BN/2, BN) the matching up rows
+        // columns [0, BN/2) of the tile are gate rows BN/2*nb.., [BN/2, BN) the matching up rows.
+        // Every TMEM load covers 32 columns starting at a multiple of 32; when the halves are not
+        // (BN/2 = 112) the up values of an output chunk come from two such loads, 16 apart.
         constexpr int HALF = BN / 2;
-        static_assert(HALF % 32 == 0, "gate/up halves of whole 32-column chunks");
+        constexpr int SHIFT = HALF % 32;
+        static_assert(SHIFT == 0 || SHIFT == 16, "gate/up halves of 16-column multiples");
 #pragma unroll 1
-        for (int c = 0; c < HALF / 32; ++c) {
+        for (int c0 = 0; c0 < HALF; c0 += 32) {
           uint32_t u[32];
-          tmem_ld32(t_acc + c * 32, r);
-          tmem_ld32(t_acc + HALF + c * 32, u);
-          const int n0 = nb * HALF + c * 32;
-          const int valid = min(32, p.N - n0);
+          tmem_ld32(t_acc + c0, r);
+          if constexpr (SHIFT == 0) {
+            tmem_ld32(t_acc + HALF + c0, u);
+          } else {
+            uint32_t u0[32];
+            const int ua = HALF + c0 - SHIFT;   // aligned start of the load holding the first up value
+            tmem_ld32(t_acc + ua, u0);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) u[i] = u0[16 + i];
+            if (c0 + 16 < HALF) {
+              tmem_ld32(t_acc + ua + 32, u0);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) u[16 + i] = u0[i];
+            }
+          }
+          const int n0 = nb * HALF + c0;
+          const int valid = min(min(32, HALF - c0), p.N - n0);
           if (m < p.M && valid > 0) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = silu_f(__uint_as_float(r[i])) * __uint_as_float(u[i]);
@@ -759,7 +792,7 @@ constexpr size_t smem_bytes() {
   // alignment slack, the rings, the barriers, the TMEM slot and the abort flag (padded to 16
   // bytes), the gammas of each A stage
   constexpr int SA = a_stages_of<NORM, STAGES>();
-  constexpr int bar_words = 2 * STAGES + 5 + (NORM ? 3 * SA : 0);
+  constexpr int bar_words = 2 * STAGES + 5 + (NORM ? 2 * SA + 2 * kNormASlots : 0);
   return 1024 + SA * A_TILE_BYTES + STAGES * BN * BK * 2 + ((bar_words + 2) & ~1) * 8 + (NORM ? SA * BK * 2 : 0);
 }
 
@@ -846,9 +879,17 @@ int gemm_plain(const Ctx& c, const void* X, const void* W, void* C, int M, int N
   p.out = C;
   p.ldo = N;
   if (norm != nullptr) {
+    // 224-column tiles: the two accumulators leave tensor memory room for the A slots
+    if (bn != 224) {
+      if (!make_tmap_2d(&tm.m[1], W, K, N, K, 224)) return LLAMA_ERR_INVALID_ARG;
+      p = base_params(M, N, K, 224);
+      p.a_map0 = 0;
+      p.b_map0 = 1;
+      p.out = C;
+      p.ldo = N;
+    }
     set_norm(p, *norm);
-    if (bn == 256) return c_f32 ? launch<256, EPI_F32, 4, true>(c, tm, p) : launch<256, EPI_BF16, 4, true>(c, tm, p);
-    return c_f32 ? launch<224, EPI_F32, 4, true>(c, tm, p) : launch<224, EPI_BF16, 4, true>(c, tm, p);
+    return c_f32 ? launch<224, EPI_F32, 5, true>(c, tm, p) : launch<224, EPI_BF16, 5, true>(c, tm, p);
   }
   if (bn == 256) return c_f32 ? launch<256, EPI_F32, 4>(c, tm, p) : launch<256, EPI_BF16, 4>(c, tm, p);
   return c_f32 ? launch<224, EPI_F32, 5>(c, tm, p) : launch<224, EPI_BF16, 5>(c, tm, p);
@@ -888,6 +929,23 @@ int gemm_residual(const Ctx& c, const void* X, const void* W, const void* resid,
 
 int gemm_swiglu(const Ctx& c, const void* X, const void* Wg, const void* Wu, void* out, int M, int I, int K,
                 const NormIn* norm) {
+  if (norm != nullptr) {
+    // 224-column tiles (112 gate + 112 up rows): the two accumulators leave tensor memory room
+    // for the A slots of the RMSNorm-fused form
+    TMaps tm{};
+    if (!make_tmap_2d(&tm.m[0], X, K, M, K, 128) || !make_tmap_2d(&tm.m[1], Wg, K, I, K, 112) ||
+        !make_tmap_2d(&tm.m[2], Wu, K, I, K, 112))
+      return LLAMA_ERR_INVALID_ARG;
+    Params p = base_params(M, 2 * ((I + 111) / 112) * 112, K, 224);
+    p.N = I;
+    p.a_map0 = 0;
+    p.b_map0 = 1;
+    p.n_maps = 3;
+    p.out = out;
+    p.ldo = I;
+    set_norm(p, *norm);
+    return launch<224, EPI_SWIGLU, 5, true>(c, tm, p);
+  }
   // kernel N runs over 256-column tiles, each = 128 gate rows + the same 128 up rows (measured:
   // 240-column tiles, which fill the SM-count rounds better at I = 11008, M = 2048, run slower)
   TMaps tm{};
@@ -901,10 +959,6 @@ int gemm_swiglu(const Ctx& c, const void* X, const void* Wg, const void* Wu, voi
   p.n_maps = 3;
   p.out = out;
   p.ldo = I;
-  if (norm != nullptr) {
-    set_norm(p, *norm);
-    return launch<256, EPI_SWIGLU, 4, true>(c, tm, p);
-  }
   return launch<256, EPI_SWIGLU, 4>(c, tm, p);
 }
 
@@ -915,8 +969,11 @@ int gemm_qkv_rope(const Ctx& c, const void* X, const void* Wq, const void* Wk, c
   const int M = B * S;
   // 224-column tiles when they fill the SM-count rounds better (the half-split pairs (j, j+64)
   // need whole heads in a tile: 256 columns = two heads); a 224-column tile that crosses the
-  // q|k or k|v boundary takes its weights in 32-row boxes from the maps at b32_map0
-  const int bn = rope_half ? 256 : tile_width_for(M, (H + 2 * G) * D, c.num_sms);
+  // q|k or k|v boundary takes its weights in 32-row boxes from the maps at b32_map0.  The
+  // RMSNorm-fused form always takes 224 columns (tensor memory holds its A slots) and so not the
+  // half-split pairs.
+  if (norm != nullptr && rope_half) return LLAMA_ERR_UNSUPPORTED;
+  const int bn = rope_half ? 256 : norm != nullptr ? 224 : tile_width_for(M, (H + 2 * G) * D, c.num_sms);
   const int box = bn == 256 ? 128 : bn;
   TMaps tm{};
   if (!make_tmap_2d(&tm.m[0], X, K, M, K, 128) || !make_tmap_2d(&tm.m[1], Wq, K, H * D, K, box) ||
@@ -950,7 +1007,7 @@ int gemm_qkv_rope(const Ctx& c, const void* X, const void* Wq, const void* Wk, c
   p.v_cache = static_cast<__nv_bfloat16*>(v_cache);
   if (norm != nullptr) {
     set_norm(p, *norm);
-    return bn == 256 ? launch<256, EPI_QKV, 4, true>(c, tm, p) : launch<224, EPI_QKV, 4, true>(c, tm, p);
+    return launch<224, EPI_QKV, 5, true>(c, tm, p);
   }
   return bn == 256 ? launch<256, EPI_QKV, 4>(c, tm, p) : launch<224, EPI_QKV, 5>(c, tm, p);
 }
