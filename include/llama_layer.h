@@ -241,8 +241,9 @@ int llama_qkv_rope(const llama_layer_dims *dims, const void *xn, const void *wq,
  * "3.2 核心组件逐一拆解" §3.2.1: the statistics in fp32) on its way into the tensor cores: a
  * statistics pass writes the row scales r[m] = rsqrt(mean(A[m]^2) + eps) to row_scale (device
  * fp32 [M], caller-owned, 16-byte aligned; an output of the call), then the GEMM's operand
- * loader forms bf16(gamma * (A * r)) -- the value llama_rmsnorm would store -- in shared memory.
- * The normalised activation is never written to memory.  bf16 data; K % 64 == 0. */
+ * loader forms bf16(gamma * (A * r)) -- the value llama_rmsnorm would store -- and hands it to
+ * the tensor cores through tensor memory.  The normalised activation is never written to
+ * memory.  bf16 data; K % 64 == 0. */
 
 /* C = RMSNorm(A) B^T.  A: device [M, K]; gamma: device [K]; B: device [N, K]; C: device
  * [M, N], bf16 (c_f32 = 0) or fp32 (c_f32 = 1).  N % 8 == 0.  (The stack's final norm and LM
@@ -258,7 +259,8 @@ int llama_norm_linear_swiglu(const void *A, const void *gamma, float eps, const 
 
 /* llama_qkv_rope on RMSNorm(x) with gamma attn_norm and eps dims.rms_eps (the input norm of
  * the attention half, "05 LLaMA3 Block — 从零件到发动机" §4.2 step ②).  x: device [B, S, d];
- * row_scale: device fp32 [B * S]. */
+ * row_scale: device fp32 [B * S].  Even/odd RoPE pairs only (LLAMA_ERR_UNSUPPORTED for the
+ * half-split pairs, whose layer prefill runs llama_rmsnorm and llama_qkv_rope instead). */
 int llama_norm_qkv_rope(const llama_layer_dims *dims, const void *x, const void *attn_norm, const void *wq,
                         const void *wk, const void *wv, const float *cos, const float *sin, int32_t max_pos,
                         llama_kv_cache cache, void *q_out, int32_t B, int32_t S, float *row_scale,

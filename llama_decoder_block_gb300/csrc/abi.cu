@@ -77,8 +77,10 @@ size_t prefill_ws(const llama_layer_dims* d, int B, int S, void* base, PrefillWs
   const size_t M = static_cast<size_t>(B) * S;
   Carver c(base);
   PrefillWs w;
-  // RMSNorm output (both norms); bf16 layers normalise inside the GEMMs that consume it
-  w.xn = c.take(d->dtype == LLAMA_BF16 ? 0 : M * d->d_model * es);
+  // RMSNorm output: fp32 layers (both norms) and the half-split RoPE pairs of bf16 layers (the
+  // attention norm); otherwise bf16 layers normalise inside the GEMMs that consume the norms
+  const bool xn_needed = d->dtype != LLAMA_BF16 || d->rope_style == LLAMA_ROPE_HALF;
+  w.xn = c.take(xn_needed ? M * d->d_model * es : 0);
   w.q = c.take(M * d->n_heads * d->head_dim * es);         // [B, H, S, D]
   w.o = c.take(M * d->n_heads * d->head_dim * es);         // attention output [B, S, H*D]
   w.h = c.take(M * d->d_model * es);                       // attention half output
@@ -156,9 +158,17 @@ int prefill_impl(const Ctx& c0, const Ctx& c_rest, const llama_layer_dims* d, co
     const RowStatsOut stats{p.part, p.r, p.ticket, d->rms_eps};
     if (!r_given && (rc = rms_rowscale(c0, x, p.r, p.ticket, M, dm, d->rms_eps))) return rc;
     const NormIn n1{w->attn_norm, p.r};
-    if ((rc = gemm_qkv_rope(r_given ? c0 : c, x, w->wq, w->wk, w->wv, B, S, dm, H, G, D, cos, sin, p.q, cache.k,
-                            cache.v, cache.max_T, d->rope_style, start, lens, max_pos, &n1)))
+    if (d->rope_style == LLAMA_ROPE_HALF) {
+      // the half-split pairs need head-aligned 256-column QKV tiles, which leave tensor memory no
+      // room for the fused norm's A slots: a standalone RMSNorm, then the plain QKV GEMM
+      if ((rc = rmsnorm(r_given ? c0 : c, x, w->attn_norm, p.xn, M, dm, d->rms_eps, d->dtype))) return rc;
+      if ((rc = gemm_qkv_rope(c, p.xn, w->wq, w->wk, w->wv, B, S, dm, H, G, D, cos, sin, p.q, cache.k, cache.v,
+                              cache.max_T, d->rope_style, start, lens, max_pos)))
+        return rc;
+    } else if ((rc = gemm_qkv_rope(r_given ? c0 : c, x, w->wq, w->wk, w->wv, B, S, dm, H, G, D, cos, sin, p.q,
+                                   cache.k, cache.v, cache.max_T, d->rope_style, start, lens, max_pos, &n1))) {
       return rc;
+    }
     if ((rc = attn_prefill_tc(c, p.q, cache.k, cache.v, p.o, B, S, H, G, D, cache.max_T, start, lens, max_pos)))
       return rc;
     if ((rc = gemm_residual(c, p.o, w->wo, x, p.h, M, dm, H * D, &stats))) return rc;

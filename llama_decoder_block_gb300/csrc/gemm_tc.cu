@@ -507,7 +507,9 @@ __global__ void __launch_bounds__(threads_of<NORM>())
           for (int q = 0; q < 4; ++q)
             o[4 * jj + q] = pack_bf16(bf16_lo(gw[q]) * (bf16_lo(xw[q]) * rc), bf16_hi(gw[q]) * (bf16_hi(xw[q]) * rc));
         }
-        // the raw stage is no longer needed
+        // the raw stage is no longer needed: order these generic-proxy reads before the TMA
+        // (async-proxy) writes that refill it once the producer sees the arrival
+        fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(afree_bar + stage));
         if (++stage == SA) { stage = 0; phase ^= 1u; }

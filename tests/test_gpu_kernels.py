@@ -290,7 +290,7 @@ def test_norm_linear_swiglu_fused(api, M, I, K):
 
 
 @pytest.mark.parametrize("d,H,G,B,S,rope", [(256, 4, 2, 2, 130, "even_odd"), (512, 8, 1, 1, 300, "even_odd"),
-                                            (256, 4, 2, 2, 150, "half"), (4096, 32, 8, 1, 256, "even_odd")])
+                                            (4096, 32, 8, 1, 256, "even_odd"), (4096, 32, 8, 3, 700, "even_odd")])
 def test_norm_qkv_rope_fused(api, d, H, G, B, S, rope):
     rng = _rng(d + H * 7 + G + B * 13 + S)
     D, T_max = 128, S + 9
@@ -322,3 +322,18 @@ def test_norm_qkv_rope_fused(api, d, H, G, B, S, rope):
     xg = _operand_from_gpu_scales(x, g, r).reshape(B, S, d)
     _one_ulp(f64(q), rot(oracle.linear(xg, wq.f64()).reshape(B, S, H, D).transpose(0, 2, 1, 3), cc, ss),
              "norm + qkv: q")
+
+
+def test_norm_qkv_rope_refuses_half_split_pairs(api):
+    # the fused QKV tiles are 224 columns, not head-aligned: the half-split layer runs a standalone
+    # RMSNorm and llama_qkv_rope instead (covered by the half-split layer tests)
+    from llama_decoder_block_gb300 import _native as N
+    dims = api.Dims(256, 4, 2, 128, 128, 1e-5, torch.bfloat16, 1)
+    x = torch.zeros(1, 8, 256, dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros(512, 256, dtype=torch.bfloat16, device="cuda")
+    cos = torch.zeros(8, 64, dtype=torch.float32, device="cuda")
+    kc = torch.zeros(1, 2, 8, 128, dtype=torch.bfloat16, device="cuda")
+    q = torch.empty(1, 4, 8, 128, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(N.LlamaError) as e:
+        api.norm_qkv_rope(dims, x, x[0, 0], w, w[:256], w[:256], cos, cos, kc, kc, q)
+    assert e.value.code == -2
