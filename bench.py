@@ -26,10 +26,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = "decoder-layer prefill tokens/s + decode µs/step on 1 GB300; % of TC/HBM roofline"
 MAIN = "mha7b_bf16_b1_s2048"
-# the layer's kernels in launch order: both RMSNorms run inside the GEMM that follows them, with
-# the row scales of x from a statistics pass and those of h from the o_proj epilogue
-PREFILL_KERNELS = ["rms_rowscale", "qkv_rope_gemm", "attention_prefill", "o_proj_residual_gemm",
-                   "gate_up_swiglu_gemm", "down_residual_gemm"]
+# the layer's kernels in launch order: both RMSNorms run in the prologue of the GEMM after them
+PREFILL_KERNELS = ["qkv_rope_gemm", "attention_prefill", "o_proj_residual_gemm", "gate_up_swiglu_gemm",
+                   "down_residual_gemm"]
 DECODE_KERNELS = ["rmsnorm_attn", "qkv_gemm_stream", "qkv_rope_fixup", "attention_decode_split",
                   "attention_decode_combine", "o_proj_gemm_stream", "o_proj_residual_rmsnorm_fixup",
                   "gate_up_gemm_stream", "swiglu_fixup", "down_gemm_stream", "down_residual_fixup"]
@@ -596,11 +595,11 @@ def bench_case(api, case, wl, steps, warmup, dev, pk):
         fn = lambda: api.attention_prefill(dims, q, k, v, o)
         work, unit = 4.0 * D * H * B * S * (S + 1) / 2, "flop"
     elif case == "gate_up":
-        # as in the layer: the FFN RMSNorm inside the gate/up GEMM (row-statistics pass included)
+        # as in the layer: the FFN RMSNorm in the gate/up GEMM's prologue
         x, gm, wg, wu = rnd(M, d), 1 + rnd(d, std=0.1), rnd(I, d, std=0.02), rnd(I, d, std=0.02)
         a = torch.empty(M, I, dtype=torch.bfloat16, device=dev)
-        rs = torch.empty(M, dtype=torch.float32, device=dev)
-        fn = lambda: api.norm_linear_swiglu(x, gm, L.rms_eps, wg, wu, a, rs)
+        xn, sync = torch.empty_like(x), torch.empty(4, dtype=torch.int32, device=dev)
+        fn = lambda: api.norm_linear_swiglu(x, gm, L.rms_eps, wg, wu, a, xn, sync)
         work, unit = 2.0 * M * d * 2 * I, "flop"
     elif case in ("down", "o_proj"):
         K = I if case == "down" else H * D
@@ -609,16 +608,16 @@ def bench_case(api, case, wl, steps, warmup, dev, pk):
         fn = lambda: api.linear_residual(a, wd, r, out)
         work, unit = 2.0 * M * K * d, "flop"
     elif case == "qkv":
-        # as in the layer: the attention RMSNorm inside the QKV GEMM (row-statistics pass included)
+        # as in the layer: the attention RMSNorm in the QKV GEMM's prologue
         x, gm = rnd(B, S, d), 1 + rnd(d, std=0.1)
         wq, wk, wv = rnd(H * D, d, std=0.02), rnd(G * D, d, std=0.02), rnd(G * D, d, std=0.02)
         q = torch.empty(B, H, S, D, dtype=torch.bfloat16, device=dev)
         kc = torch.empty(B, G, S, D, dtype=torch.bfloat16, device=dev)
         vc = torch.empty_like(kc)
-        rs = torch.empty(M, dtype=torch.float32, device=dev)
+        xn, sync = torch.empty_like(x), torch.empty(4, dtype=torch.int32, device=dev)
         c, s = api.rope_tables(L.rope_base, D, S)
         cos, sin = torch.from_numpy(c).to(dev), torch.from_numpy(s).to(dev)
-        fn = lambda: api.norm_qkv_rope(dims, x, gm, wq, wk, wv, cos, sin, kc, vc, q, rs)
+        fn = lambda: api.norm_qkv_rope(dims, x, gm, wq, wk, wv, cos, sin, kc, vc, q, xn, sync)
         work, unit = 2.0 * M * d * (H + 2 * G) * D, "flop"
     elif case in ("decode_attention", "decode_layer"):
         dw = wl

@@ -236,34 +236,35 @@ int llama_qkv_rope(const llama_layer_dims *dims, const void *xn, const void *wq,
                    int32_t S, void *cuda_stream);
 
 /* RMSNorm fused into the projection that consumes it: the bf16 layers' prefill runs these in
- * place of llama_rmsnorm followed by the plain projection.  Row m of A is normalised as
- * gamma * A[m] * rsqrt(mean(A[m]^2) + eps) ("12 · 从 Transformer 到 LLaMA 系列" §八 RMSNorm;
- * "3.2 核心组件逐一拆解" §3.2.1: the statistics in fp32) on its way into the tensor cores: a
- * statistics pass writes the row scales r[m] = rsqrt(mean(A[m]^2) + eps) to row_scale (device
- * fp32 [M], caller-owned, 16-byte aligned; an output of the call), then the GEMM's operand
- * loader forms bf16(gamma * (A * r)) -- the value llama_rmsnorm would store -- and hands it to
- * the tensor cores through tensor memory.  The normalised activation is never written to
- * memory.  bf16 data; K % 64 == 0. */
+ * place of llama_rmsnorm followed by the plain projection.  The GEMM kernel itself normalises
+ * row m of A as gamma * A[m] * rsqrt(mean(A[m]^2) + eps) ("12 · 从 Transformer 到 LLaMA 系列"
+ * §八 RMSNorm; "3.2 核心组件逐一拆解" §3.2.1: the statistics in fp32) in its prologue -- each of
+ * its CTAs takes a share of the rows, bit for bit what llama_rmsnorm stores -- writes the result
+ * to xn and then multiplies xn: one launch, no separate normalisation kernel.
+ * xn: device [M, K] bf16, caller-owned, 16-byte aligned, not aliasing A; it holds RMSNorm(A)
+ * when the call completes.  sync: device int32, caller-owned scratch (any contents; the call
+ * sets it to zero with a memset before the GEMM and the GEMM's CTAs count themselves in on it);
+ * calls that may overlap on the GPU need separate ones.  The GEMM's CTAs wait for one another
+ * (bounded: LLAMA_ERR_TIMEOUT after about a second), so they must all be resident at once: the
+ * grid is at most one CTA per SM of the device.  bf16 data; K % 8 == 0. */
 
 /* C = RMSNorm(A) B^T.  A: device [M, K]; gamma: device [K]; B: device [N, K]; C: device
  * [M, N], bf16 (c_f32 = 0) or fp32 (c_f32 = 1).  N % 8 == 0.  (The stack's final norm and LM
  * head.) */
 int llama_norm_linear_bf16(const void *A, const void *gamma, float eps, const void *B, void *C, int32_t M, int32_t N,
-                           int32_t K, int32_t c_f32, float *row_scale, void *cuda_stream);
+                           int32_t K, int32_t c_f32, void *xn, int32_t *sync, void *cuda_stream);
 
 /* out = SiLU(RMSNorm(A) W_gate^T) * (RMSNorm(A) W_up^T) (the post-attention norm and the gated
  * MLP's first half, "05 LLaMA3 Block — 从零件到发动机" §4.1-§4.2).  A: device [M, K]; gamma:
  * device [K]; W_gate, W_up: device [I, K]; out: device [M, I].  I % 128 == 0. */
 int llama_norm_linear_swiglu(const void *A, const void *gamma, float eps, const void *W_gate, const void *W_up,
-                             void *out, int32_t M, int32_t I, int32_t K, float *row_scale, void *cuda_stream);
+                             void *out, int32_t M, int32_t I, int32_t K, void *xn, int32_t *sync, void *cuda_stream);
 
 /* llama_qkv_rope on RMSNorm(x) with gamma attn_norm and eps dims.rms_eps (the input norm of
- * the attention half, "05 LLaMA3 Block — 从零件到发动机" §4.2 step ②).  x: device [B, S, d];
- * row_scale: device fp32 [B * S].  Even/odd RoPE pairs only (LLAMA_ERR_UNSUPPORTED for the
- * half-split pairs, whose layer prefill runs llama_rmsnorm and llama_qkv_rope instead). */
+ * the attention half, "05 LLaMA3 Block — 从零件到发动机" §4.2 step ②).  x, xn: device [B, S, d]. */
 int llama_norm_qkv_rope(const llama_layer_dims *dims, const void *x, const void *attn_norm, const void *wq,
                         const void *wk, const void *wv, const float *cos, const float *sin, int32_t max_pos,
-                        llama_kv_cache cache, void *q_out, int32_t B, int32_t S, float *row_scale,
+                        llama_kv_cache cache, void *q_out, int32_t B, int32_t S, void *xn, int32_t *sync,
                         void *cuda_stream);
 
 /* Where llama_layer_prefill and llama_layer_prefill_chunk leave the layer's intermediate
@@ -271,10 +272,8 @@ int llama_norm_qkv_rope(const llama_layer_dims *dims, const void *x, const void 
  * (each is overwritten by the next call that uses the workspace).  offsets receives 5 byte
  * offsets from the workspace start: [0] q after RoPE [B, H, S, D]; [1] attention output
  * [B, S, H*D]; [2] h = x + o_proj(attention) [B, S, d]; [3] the gated MLP activation
- * SiLU(gate) * up [B, S, d_inter]; all of dims.dtype; [4] bf16 layers only: the row scales
- * rsqrt(mean(h^2) + eps) of the stored h, fp32 [B, S], written by the o_proj epilogue for the
- * norm inside the gate/up GEMM.  (The normalised activations of bf16 layers never reach
- * memory; K and V are in the cache.) */
+ * SiLU(gate) * up [B, S, d_inter]; [4] the normalised rows of the last RMSNorm, RMSNorm_2(h)
+ * [B, S, d] (the gate/up GEMM's A operand); all of dims.dtype.  (K and V are in the cache.) */
 int llama_layer_prefill_workspace_layout(const llama_layer_dims *dims, int32_t B, int32_t S, size_t *offsets);
 
 /* Where llama_stack_forward leaves its last layer's data in its workspace (the same

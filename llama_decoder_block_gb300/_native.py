@@ -73,11 +73,12 @@ SIGNATURES = {
     "llama_qkv_rope": (c_int32, [P(LayerDims), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int32,
                                  KVCache, c_void_p, c_int32, c_int32, c_void_p]),
     "llama_norm_linear_bf16": (c_int32, [c_void_p, c_void_p, c_float, c_void_p, c_void_p, c_int32, c_int32, c_int32,
-                                         c_int32, c_void_p, c_void_p]),
+                                         c_int32, c_void_p, c_void_p, c_void_p]),
     "llama_norm_linear_swiglu": (c_int32, [c_void_p, c_void_p, c_float, c_void_p, c_void_p, c_void_p, c_int32,
-                                           c_int32, c_int32, c_void_p, c_void_p]),
+                                           c_int32, c_int32, c_void_p, c_void_p, c_void_p]),
     "llama_norm_qkv_rope": (c_int32, [P(LayerDims), c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
-                                      c_void_p, c_int32, KVCache, c_void_p, c_int32, c_int32, c_void_p, c_void_p]),
+                                      c_void_p, c_int32, KVCache, c_void_p, c_int32, c_int32, c_void_p, c_void_p,
+                                      c_void_p]),
     "llama_layer_prefill_workspace_layout": (c_int32, [P(LayerDims), c_int32, c_int32, P(c_size_t)]),
     "llama_stack_workspace_layout": (c_int32, [P(Stack), c_int32, c_int32, P(c_size_t)]),
     "llama_attention_prefill": (c_int32, [P(LayerDims), c_void_p, KVCache, c_void_p, c_int32, c_int32, c_void_p]),

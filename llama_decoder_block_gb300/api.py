@@ -224,61 +224,61 @@ def qkv_rope(dims: Dims, xn, wq, wk, wv, cos, sin, cache_k, cache_v, q_out, stre
             "llama_qkv_rope")
 
 
-def _row_scale(rows: int, like: torch.Tensor, row_scale):
-    if row_scale is None:
-        row_scale = torch.empty(rows, dtype=torch.float32, device=like.device)
-    return row_scale
+def _norm_buffers(rows: int, K: int, like: torch.Tensor, xn, sync):
+    if xn is None:
+        xn = torch.empty(rows, K, dtype=torch.bfloat16, device=like.device)
+    if sync is None:
+        sync = torch.empty(4, dtype=torch.int32, device=like.device)
+    return xn, sync
 
 
-def norm_linear_bf16(a, gamma, eps: float, b, c, row_scale=None, stream=None) -> torch.Tensor:
-    """c = RMSNorm(a) b^T with the norm inside the GEMM (c bf16 or fp32); returns the row scales
-    rsqrt(mean(a^2) + eps) [M] fp32 that the call computed (into row_scale if given)."""
+def norm_linear_bf16(a, gamma, eps: float, b, c, xn=None, sync=None, stream=None) -> torch.Tensor:
+    """c = RMSNorm(a) b^T, the norm in the GEMM's prologue (c bf16 or fp32); returns xn, the
+    normalised rows the GEMM multiplied (into `xn` if given)."""
     M, K = a.shape
-    row_scale = _row_scale(M, a, row_scale)
+    xn, sync = _norm_buffers(M, K, a, xn, sync)
     N.check(N.lib().llama_norm_linear_bf16(_ptr(a), _ptr(gamma), eps, _ptr(b), _ptr(c), M, b.shape[0], K,
-                                           int(c.dtype == torch.float32), _ptr(row_scale), _stream(stream)),
+                                           int(c.dtype == torch.float32), _ptr(xn), _ptr(sync), _stream(stream)),
             "llama_norm_linear_bf16")
-    return row_scale
+    return xn
 
 
-def norm_linear_swiglu(a, gamma, eps: float, w_gate, w_up, out, row_scale=None, stream=None) -> torch.Tensor:
+def norm_linear_swiglu(a, gamma, eps: float, w_gate, w_up, out, xn=None, sync=None, stream=None) -> torch.Tensor:
     M, K = a.shape
-    row_scale = _row_scale(M, a, row_scale)
+    xn, sync = _norm_buffers(M, K, a, xn, sync)
     N.check(N.lib().llama_norm_linear_swiglu(_ptr(a), _ptr(gamma), eps, _ptr(w_gate), _ptr(w_up), _ptr(out), M,
-                                             w_gate.shape[0], K, _ptr(row_scale), _stream(stream)),
+                                             w_gate.shape[0], K, _ptr(xn), _ptr(sync), _stream(stream)),
             "llama_norm_linear_swiglu")
-    return row_scale
+    return xn
 
 
-def norm_qkv_rope(dims: Dims, x, attn_norm, wq, wk, wv, cos, sin, cache_k, cache_v, q_out, row_scale=None,
+def norm_qkv_rope(dims: Dims, x, attn_norm, wq, wk, wv, cos, sin, cache_k, cache_v, q_out, xn=None, sync=None,
                   stream=None) -> torch.Tensor:
     B, S = x.shape[0], x.shape[1]
-    row_scale = _row_scale(B * S, x, row_scale)
+    xn, sync = _norm_buffers(B * S, x.shape[-1], x, xn, sync)
     d = dims.c()
     N.check(N.lib().llama_norm_qkv_rope(ctypes.byref(d), _ptr(x), _ptr(attn_norm), _ptr(wq), _ptr(wk), _ptr(wv),
                                         _ptr(cos), _ptr(sin), cos.shape[0], cache_struct(cache_k, cache_v),
-                                        _ptr(q_out), B, S, _ptr(row_scale), _stream(stream)), "llama_norm_qkv_rope")
-    return row_scale
+                                        _ptr(q_out), B, S, _ptr(xn), _ptr(sync), _stream(stream)),
+            "llama_norm_qkv_rope")
+    return xn
 
 
 def prefill_intermediates(dims: Dims, ws, B: int, S: int, offset: int = 0) -> dict:
     """Views of the workspace regions where the last llama_layer_prefill(_chunk) call on `ws`
     (its layer workspace starting `offset` bytes in) left q [B, H, S, D], the attention output
-    o [B, S, H*D], h [B, S, d], the gated MLP activation a [B, S, d_inter] and (bf16) the row
-    scales r of h [B, S] fp32.  Read them after that call has completed on its stream."""
+    o [B, S, H*D], h [B, S, d], the gated MLP activation a [B, S, d_inter] and hn =
+    RMSNorm_2(h) [B, S, d].  Read them after that call has completed on its stream."""
     offs = (ctypes.c_size_t * 5)()
     d = dims.c()
     N.check(N.lib().llama_layer_prefill_workspace_layout(ctypes.byref(d), B, S, offs), "workspace layout")
     es = 2 if dims.dtype == torch.bfloat16 else 4
     shapes = {"q": (B, dims.n_heads, S, dims.head_dim), "o": (B, S, dims.n_heads * dims.head_dim),
-              "h": (B, S, dims.d_model), "a": (B, S, dims.d_inter)}
+              "h": (B, S, dims.d_model), "a": (B, S, dims.d_inter), "hn": (B, S, dims.d_model)}
     out = {}
     for off, (name, shape) in zip(offs, shapes.items()):
         n = int(np.prod(shape))
         out[name] = ws[offset + off:offset + off + n * es].view(dims.dtype).view(shape)
-    if dims.dtype == torch.bfloat16:
-        o = offset + offs[4]
-        out["r"] = ws[o:o + B * S * 4].view(torch.float32).view(B, S)
     return out
 
 

@@ -63,32 +63,20 @@ int check_weights(const llama_layer_weights* w) {
 
 struct PrefillWs {
   void *xn, *q, *o, *h, *a;
-  // bf16: row statistics for the RMSNorms inside the GEMMs (row scales [M], the residual
-  // epilogue's partial sums [ceil(d / 224)][M] and per-row tickets [M])
-  float *r, *part;
-  int* ticket;
+  int* sync;   // bf16: the grid-wide counts of the two GEMM prologues that normalise x and h
 };
-
-// Column tiles of a residual GEMM with d output columns, at most (its tiles are 224 or 256 wide).
-int max_residual_tiles(int d) { return (d + 223) / 224; }
 
 size_t prefill_ws(const llama_layer_dims* d, int B, int S, void* base, PrefillWs* out) {
   const size_t es = esize(d->dtype);
   const size_t M = static_cast<size_t>(B) * S;
   Carver c(base);
   PrefillWs w;
-  // RMSNorm output: fp32 layers (both norms) and the half-split RoPE pairs of bf16 layers (the
-  // attention norm); otherwise bf16 layers normalise inside the GEMMs that consume the norms
-  const bool xn_needed = d->dtype != LLAMA_BF16 || d->rope_style == LLAMA_ROPE_HALF;
-  w.xn = c.take(xn_needed ? M * d->d_model * es : 0);
+  w.xn = c.take(M * d->d_model * es);                      // RMSNorm output (both norms)
   w.q = c.take(M * d->n_heads * d->head_dim * es);         // [B, H, S, D]
   w.o = c.take(M * d->n_heads * d->head_dim * es);         // attention output [B, S, H*D]
   w.h = c.take(M * d->d_model * es);                       // attention half output
   w.a = c.take(M * d->d_inter * es);                       // SiLU(gate) * up
-  const bool tc = d->dtype == LLAMA_BF16;
-  w.r = static_cast<float*>(c.take(tc ? M * sizeof(float) : 0));
-  w.part = static_cast<float*>(c.take(tc ? M * max_residual_tiles(d->d_model) * sizeof(float) : 0));
-  w.ticket = static_cast<int*>(c.take(tc ? M * sizeof(int) : 0));
+  w.sync = static_cast<int*>(c.take(d->dtype == LLAMA_BF16 ? 2 * sizeof(int) : 0));
   if (out) *out = w;
   return c.off;
 }
@@ -138,43 +126,34 @@ int num_sms_current(int* sms) {
 
 // start, lens: null (a prompt from position 0) or device [B] (a chunk on top of the cache).
 // `c0` launches the first kernel (without programmatic serialisation when the call starts
-// a new stream of work), `c` the others.  bf16 layers in a stack: `r_given` means the
-// workspace's row scales already hold those of x (the previous layer's down projection wrote
-// them, and the tickets are zero), and `stats_out` makes this layer's down projection write
-// the row scales of its output (for the next layer's input norm or the final norm).
+// a new stream of work), `c` the others.  bf16 layers: `sync` (2 ints, zero) are the counts of
+// the two GEMM prologues; null: the workspace's own, zeroed here.
 int prefill_impl(const Ctx& c0, const Ctx& c_rest, const llama_layer_dims* d, const llama_layer_weights* w,
                  const void* x, void* out, const float* cos, const float* sin, int max_pos, llama_kv_cache cache,
                  int B, int S, void* ws, const int32_t* start = nullptr, const int32_t* lens = nullptr,
-                 bool r_given = false, bool stats_out = false) {
+                 int* sync = nullptr) {
   PrefillWs p;
   prefill_ws(d, B, S, ws, &p);
   const Ctx& c = c_rest;
   const int M = B * S, dm = d->d_model, H = d->n_heads, G = d->n_kv_heads, D = d->head_dim, I = d->d_inter;
   int rc;
   if (d->dtype == LLAMA_BF16) {
-    // Both RMSNorms run inside the GEMM that consumes them (the QKV and the gate/up
-    // projections).  The row scales of x come from a statistics pass (which also zeroes the
-    // per-row tickets), those of h from the o_proj epilogue.
-    const RowStatsOut stats{p.part, p.r, p.ticket, d->rms_eps};
-    if (!r_given && (rc = rms_rowscale(c0, x, p.r, p.ticket, M, dm, d->rms_eps))) return rc;
-    const NormIn n1{w->attn_norm, p.r};
-    if (d->rope_style == LLAMA_ROPE_HALF) {
-      // the half-split pairs need head-aligned 256-column QKV tiles, which leave tensor memory no
-      // room for the fused norm's A slots: a standalone RMSNorm, then the plain QKV GEMM
-      if ((rc = rmsnorm(r_given ? c0 : c, x, w->attn_norm, p.xn, M, dm, d->rms_eps, d->dtype))) return rc;
-      if ((rc = gemm_qkv_rope(c, p.xn, w->wq, w->wk, w->wv, B, S, dm, H, G, D, cos, sin, p.q, cache.k, cache.v,
-                              cache.max_T, d->rope_style, start, lens, max_pos)))
-        return rc;
-    } else if ((rc = gemm_qkv_rope(r_given ? c0 : c, x, w->wq, w->wk, w->wv, B, S, dm, H, G, D, cos, sin, p.q,
-                                   cache.k, cache.v, cache.max_T, d->rope_style, start, lens, max_pos, &n1))) {
-      return rc;
+    // Both RMSNorms run in the prologue of the GEMM that consumes them (the QKV and the gate/up
+    // projections), which normalises the rows into xn and then streams them as its A operand.
+    if (sync == nullptr) {
+      sync = p.sync;
+      if (cudaMemsetAsync(sync, 0, 2 * sizeof(int), c0.stream) != cudaSuccess) return LLAMA_ERR_CUDA;
     }
+    const NormPro n1{w->attn_norm, d->rms_eps, p.xn, sync};
+    const NormPro n2{w->ffn_norm, d->rms_eps, p.xn, sync + 1};
+    if ((rc = gemm_qkv_rope(c0, x, w->wq, w->wk, w->wv, B, S, dm, H, G, D, cos, sin, p.q, cache.k, cache.v,
+                            cache.max_T, d->rope_style, start, lens, max_pos, &n1)))
+      return rc;
     if ((rc = attn_prefill_tc(c, p.q, cache.k, cache.v, p.o, B, S, H, G, D, cache.max_T, start, lens, max_pos)))
       return rc;
-    if ((rc = gemm_residual(c, p.o, w->wo, x, p.h, M, dm, H * D, &stats))) return rc;
-    const NormIn n2{w->ffn_norm, p.r};
+    if ((rc = gemm_residual(c, p.o, w->wo, x, p.h, M, dm, H * D))) return rc;
     if ((rc = gemm_swiglu(c, p.h, w->w_gate, w->w_up, p.a, M, I, dm, &n2))) return rc;
-    return gemm_residual(c, p.a, w->w_down, p.h, out, M, dm, I, stats_out ? &stats : nullptr);
+    return gemm_residual(c, p.a, w->w_down, p.h, out, M, dm, I);
   }
   if ((rc = rmsnorm(c0, x, w->attn_norm, p.xn, M, dm, d->rms_eps, d->dtype))) return rc;
   const float* xf = static_cast<const float*>(x);
@@ -466,6 +445,7 @@ int llama_stack_workspace_bytes(const llama_stack* st, int32_t B, int32_t S, siz
   total += 2 * align_up(M * st->dims.d_model * es);                                           // ping-pong activations
   total += 2 * align_up(M * st->dims.n_kv_heads * st->dims.head_dim * es);                    // K/V if no caches
   total += align_up(prefill_ws(&st->dims, B, S, nullptr, nullptr));
+  total += align_up((2 * static_cast<size_t>(st->n_layers) + 1) * sizeof(int));   // the GEMM prologues' counts
   *bytes = total;
   return LLAMA_OK;
 }
@@ -495,6 +475,7 @@ int llama_stack_forward(const llama_stack* st, const int32_t* tokens, float* log
   void* ks = cv.take(M * d->n_kv_heads * d->head_dim * es);
   void* vs = cv.take(M * d->n_kv_heads * d->head_dim * es);
   void* lws = cv.take(prefill_ws(d, B, S, nullptr, nullptr));
+  int* sync = static_cast<int*>(cv.take((2 * static_cast<size_t>(st->n_layers) + 1) * sizeof(int)));
   for (int l = 0; l < st->n_layers; ++l) {
     llama_kv_cache kc = caches ? caches[l] : llama_kv_cache{ks, vs, S};
     if ((rc = check_prefill_args(d, &st->layers[l], xa, xb, cos, sin, max_pos, kc, B, S))) return rc;
@@ -506,26 +487,26 @@ int llama_stack_forward(const llama_stack* st, const int32_t* tokens, float* log
   if ((rc = embed_gather(c0, tokens, st->embed, xa, static_cast<int>(M), static_cast<int>(d->d_model * es),
                          st->vocab)))
     return rc;
-  // bf16: every RMSNorm runs inside the GEMM after it; the row scales of each layer's input come
-  // from the previous layer's down projection (the first layer's from a statistics pass), and
-  // the last layer's give the final norm's
+  // bf16: every RMSNorm runs in the prologue of the GEMM after it, each with its own count
   const bool tc = d->dtype == LLAMA_BF16;
   PrefillWs pw;
   prefill_ws(d, B, S, lws, &pw);
-  if (tc && (rc = rms_rowscale(c, xa, pw.r, pw.ticket, static_cast<int>(M), d->d_model, d->rms_eps))) return rc;
+  if (tc && cudaMemsetAsync(sync, 0, (2 * static_cast<size_t>(st->n_layers) + 1) * sizeof(int), c.stream) !=
+                cudaSuccess)
+    return LLAMA_ERR_CUDA;
   for (int l = 0; l < st->n_layers; ++l) {
     llama_kv_cache kc = caches ? caches[l] : llama_kv_cache{ks, vs, S};
-    if ((rc = prefill_impl(c, c, d, &st->layers[l], xa, xb, cos, sin, max_pos, kc, B, S, lws, nullptr, nullptr, tc,
-                           tc)))
+    if ((rc = prefill_impl(c, c, d, &st->layers[l], xa, xb, cos, sin, max_pos, kc, B, S, lws, nullptr, nullptr,
+                           tc ? sync + 2 * l : nullptr)))
       return rc;
     void* t = xa;
     xa = xb;
     xb = t;
   }
   // final RMSNorm (required by the pre-norm layout), then the untied LM head in fp32; bf16
-  // stacks normalise inside the LM head's GEMM
+  // stacks normalise in the LM head GEMM's prologue
   if (tc) {
-    const NormIn fn{st->final_norm, pw.r};
+    const NormPro fn{st->final_norm, d->rms_eps, pw.xn, sync + 2 * st->n_layers};
     return gemm_plain(c, xa, st->lm_head, logits, static_cast<int>(M), st->vocab, d->d_model, true, &fn);
   }
   if ((rc = rmsnorm(c, xa, st->final_norm, xb, static_cast<int>(M), d->d_model, d->rms_eps, d->dtype))) return rc;
@@ -643,7 +624,7 @@ int llama_layer_prefill_workspace_layout(const llama_layer_dims* dims, int32_t B
   uint8_t* const base = reinterpret_cast<uint8_t*>(kAlign);
   PrefillWs w;
   prefill_ws(dims, B, S, base, &w);
-  const void* regions[5] = {w.q, w.o, w.h, w.a, w.r};
+  const void* regions[5] = {w.q, w.o, w.h, w.a, w.xn};
   for (int i = 0; i < 5; ++i) offsets[i] = static_cast<size_t>(static_cast<const uint8_t*>(regions[i]) - base);
   return LLAMA_OK;
 }
@@ -672,58 +653,55 @@ int llama_stack_workspace_layout(const llama_stack* st, int32_t B, int32_t S, si
 }
 
 int llama_norm_linear_bf16(const void* A, const void* gamma, float eps, const void* B, void* C, int32_t M, int32_t N,
-                           int32_t K, int32_t c_f32, float* row_scale, void* cuda_stream) {
-  if (!A || !gamma || !B || !C || !row_scale || M <= 0 || N <= 0 || K <= 0 || !(eps >= 0.f))
+                           int32_t K, int32_t c_f32, void* xn, int32_t* sync, void* cuda_stream) {
+  if (!A || !gamma || !B || !C || !xn || !sync || M <= 0 || N <= 0 || K <= 0 || !(eps >= 0.f))
     return LLAMA_ERR_INVALID_ARG;
-  if (!aligned16(A) || !aligned16(gamma) || !aligned16(B) || !aligned16(C)) return LLAMA_ERR_INVALID_ARG;
-  if (K % 64 != 0 || N % 8 != 0) return LLAMA_ERR_UNSUPPORTED;
+  if (!aligned16(A) || !aligned16(gamma) || !aligned16(B) || !aligned16(C) || !aligned16(xn) || A == xn)
+    return LLAMA_ERR_INVALID_ARG;
+  if (K % 8 != 0 || N % 8 != 0) return LLAMA_ERR_UNSUPPORTED;
   Ctx c;
   int rc = make_ctx(cuda_stream, &c);
   if (rc) return rc;
-  Ctx c0, cr;
-  call_contexts(c, &c0, &cr);
-  if ((rc = rms_rowscale(c0, A, row_scale, nullptr, M, K, eps))) return rc;
-  const NormIn n{gamma, row_scale};
-  return gemm_plain(cr, A, B, C, M, N, K, c_f32 != 0, &n);
+  if (cudaMemsetAsync(sync, 0, sizeof(int), c.stream) != cudaSuccess) return LLAMA_ERR_CUDA;
+  const NormPro n{gamma, eps, xn, sync};
+  return gemm_plain(c, A, B, C, M, N, K, c_f32 != 0, &n);
 }
 
 int llama_norm_linear_swiglu(const void* A, const void* gamma, float eps, const void* W_gate, const void* W_up,
-                             void* out, int32_t M, int32_t I, int32_t K, float* row_scale, void* cuda_stream) {
-  if (!A || !gamma || !W_gate || !W_up || !out || !row_scale || M <= 0 || I <= 0 || K <= 0 || !(eps >= 0.f))
+                             void* out, int32_t M, int32_t I, int32_t K, void* xn, int32_t* sync, void* cuda_stream) {
+  if (!A || !gamma || !W_gate || !W_up || !out || !xn || !sync || M <= 0 || I <= 0 || K <= 0 || !(eps >= 0.f))
     return LLAMA_ERR_INVALID_ARG;
-  if (!aligned16(A) || !aligned16(gamma) || !aligned16(W_gate) || !aligned16(W_up) || !aligned16(out))
+  if (!aligned16(A) || !aligned16(gamma) || !aligned16(W_gate) || !aligned16(W_up) || !aligned16(out) ||
+      !aligned16(xn) || A == xn)
     return LLAMA_ERR_INVALID_ARG;
-  if (K % 64 != 0 || I % 128 != 0) return LLAMA_ERR_UNSUPPORTED;
+  if (K % 8 != 0 || I % 128 != 0) return LLAMA_ERR_UNSUPPORTED;
   Ctx c;
   int rc = make_ctx(cuda_stream, &c);
   if (rc) return rc;
-  Ctx c0, cr;
-  call_contexts(c, &c0, &cr);
-  if ((rc = rms_rowscale(c0, A, row_scale, nullptr, M, K, eps))) return rc;
-  const NormIn n{gamma, row_scale};
-  return gemm_swiglu(cr, A, W_gate, W_up, out, M, I, K, &n);
+  if (cudaMemsetAsync(sync, 0, sizeof(int), c.stream) != cudaSuccess) return LLAMA_ERR_CUDA;
+  const NormPro n{gamma, eps, xn, sync};
+  return gemm_swiglu(c, A, W_gate, W_up, out, M, I, K, &n);
 }
 
 int llama_norm_qkv_rope(const llama_layer_dims* dims, const void* x, const void* attn_norm, const void* wq,
                         const void* wk, const void* wv, const float* cos, const float* sin, int32_t max_pos,
-                        llama_kv_cache cache, void* q_out, int32_t B, int32_t S, float* row_scale,
+                        llama_kv_cache cache, void* q_out, int32_t B, int32_t S, void* xn, int32_t* sync,
                         void* cuda_stream) {
   int rc = check_dims(dims);
   if (rc) return rc;
   if (dims->dtype != LLAMA_BF16) return LLAMA_ERR_UNSUPPORTED;
-  if (!x || !attn_norm || !wq || !wk || !wv || !cos || !sin || !cache.k || !cache.v || !q_out || !row_scale)
+  if (!x || !attn_norm || !wq || !wk || !wv || !cos || !sin || !cache.k || !cache.v || !q_out || !xn || !sync)
     return LLAMA_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(attn_norm) || !aligned16(wq) || !aligned16(wk) || !aligned16(wv) ||
-      !aligned16(cos) || !aligned16(sin) || !aligned16(cache.k) || !aligned16(cache.v) || !aligned16(q_out))
+      !aligned16(cos) || !aligned16(sin) || !aligned16(cache.k) || !aligned16(cache.v) || !aligned16(q_out) ||
+      !aligned16(xn) || x == xn)
     return LLAMA_ERR_INVALID_ARG;
   if (B <= 0 || S <= 0 || S > max_pos || S > cache.max_T) return LLAMA_ERR_INVALID_ARG;
   Ctx c;
   if ((rc = make_ctx(cuda_stream, &c))) return rc;
-  Ctx c0, cr;
-  call_contexts(c, &c0, &cr);
-  if ((rc = rms_rowscale(c0, x, row_scale, nullptr, B * S, dims->d_model, dims->rms_eps))) return rc;
-  const NormIn n{attn_norm, row_scale};
-  return gemm_qkv_rope(cr, x, wq, wk, wv, B, S, dims->d_model, dims->n_heads, dims->n_kv_heads, dims->head_dim, cos,
+  if (cudaMemsetAsync(sync, 0, sizeof(int), c.stream) != cudaSuccess) return LLAMA_ERR_CUDA;
+  const NormPro n{attn_norm, dims->rms_eps, xn, sync};
+  return gemm_qkv_rope(c, x, wq, wk, wv, B, S, dims->d_model, dims->n_heads, dims->n_kv_heads, dims->head_dim, cos,
                        sin, q_out, cache.k, cache.v, cache.max_T, dims->rope_style, nullptr, nullptr, max_pos, &n);
 }
 

@@ -5,26 +5,19 @@
 //   warp 0     TMA producer: 128x64 A tile + BNx64 B tile per stage (128-byte swizzle)
 //   warp 1     TMEM allocator and MMA issuer: tcgen05.mma 128xBNx16 into a TMEM accumulator
 //   warps 2-5  epilogue: tcgen05.ld of the accumulator rows, fused op, stores to HBM
-//   warps 6-9  (RMSNorm-fused form only) operand A: see below
 // Two TMEM accumulators let the epilogue of tile i overlap the main loop of tile i+1.
 //
-// RMSNorm fused into the A operand ("12 · 从 Transformer 到 LLaMA 系列" §八 RMSNorm: y = gamma *
-// x * rsqrt(mean(x^2) + eps); "3.2 核心组件逐一拆解" §3.2.1: the statistics in fp32).  TMA brings
-// the raw x tile of each k-block (and that k-block's 64 gammas) into a shared-memory ring of its
-// own; four norm warps read it once, each thread one row, form bf16(gamma_k * (x_mk * r_m)) --
-// the normalised row rounded where a standalone RMSNorm would store it -- and store it into one
-// of two A slots in tensor memory, from which the MMAs read their A operand.  Shared memory
-// carries the same bytes as in the plain form (the tensor cores' own A reads move to TMEM), which
-// matters because these GEMMs are bound by shared-memory bandwidth: a transform written back to
-// shared memory cost a third more time.  The row scales r_m = rsqrt(mean_k x_mk^2 + eps) come
-// with the input: from a row-statistics pass over the layer input, or from the residual
-// epilogue that produced x (below).  The normalised activation never goes through HBM.
-// Tensor memory: the two accumulators (2 x 224 columns) and the two A slots (32 columns each).
-//
-// Row statistics in the residual epilogue: a tile adds the squares of its rounded outputs of
-// row m into part[nb][m]; the last of the row's column tiles to finish (a per-row ticket)
-// sums part[0..num_nb)[m] in column order and writes r_m, so the result does not depend on
-// which tile finishes last.
+// RMSNorm in the prologue ("12 · 从 Transformer 到 LLaMA 系列" §八 RMSNorm: y = gamma * x *
+// rsqrt(mean(x^2) + eps); "3.2 核心组件逐一拆解" §3.2.1: the statistics in fp32).  When the A
+// operand is the normalised activation, the GEMM normalises it itself before its main loop: the
+// epilogue warps, idle until the first accumulator is ready, take the rows of x in turn (one warp
+// per row, the row's sum of squares reduced across the warp in fp32), write gamma * (x * r) as
+// bf16 -- exactly what a standalone RMSNorm stores -- into the A buffer, and count themselves in
+// on a grid-wide counter.  The TMA producer issues the weight tiles of its first stages, waits
+// (bounded) for the count to reach every prologue warp of the grid, and then streams the
+// normalised rows as A as usual.  The main loop is the plain GEMM's: the normalisation touches
+// no shared memory (the GEMMs are bound by shared-memory bandwidth, and every form that
+// rewrote or re-staged the operand between TMA and the tensor cores measured 50-90 % slower).
 // Epilogues: plain store (bf16 / fp32), residual add (o_proj, down_proj;
 // "05 LLaMA3 Block — 从零件到发动机" §4.2 steps ④ ⑧), SiLU(gate) * up
 // ("3.2 核心组件逐一拆解" §3.2.2; gate and up tiles share one accumulator), QKV with
@@ -43,12 +36,6 @@ constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int A_TILE_BYTES = BM * BK * 2;
 constexpr int NUM_THREADS = 192;
-constexpr int NORM_THREADS = 128;   // the norm warps of the RMSNorm-fused form
-
-template <bool NORM>
-constexpr int threads_of() {
-  return NORM ? NUM_THREADS + NORM_THREADS : NUM_THREADS;
-}
 
 enum Epi : int { EPI_BF16 = 0, EPI_F32 = 1, EPI_RESID = 2, EPI_SWIGLU = 3, EPI_QKV = 4, EPI_PARTIAL = 5 };
 
@@ -88,16 +75,108 @@ struct Params {
   __nv_bfloat16* q_out;
   __nv_bfloat16* k_cache;
   __nv_bfloat16* v_cache;
-  // RMSNorm-fused form: operand A = bf16(norm_gamma_k * (x_mk * norm_r_m)), x the A operand
-  const __nv_bfloat16* norm_gamma;   // [K]
-  const float* norm_r;               // [M] rsqrt(mean_k x_mk^2 + eps)
-  // residual epilogue: the row statistics of the output for the next RMSNorm (null: none)
-  float* stat_part;                  // [num_nb][M] sums of squares of each tile's outputs
-  float* stat_r;                     // [M] rsqrt(sum / N + stat_eps), by the row's last tile
-  int* stat_ticket;                  // [M] column tiles done; zero before, reset by the last
-  float stat_inv_n, stat_eps;
+  // RMSNorm in the prologue (null pro_out: none): rows [0, M) of pro_x [M, K] normalised with
+  // pro_gamma [K] into pro_out [M, K], the buffer operand A is read from
+  const __nv_bfloat16* pro_x;
+  const __nv_bfloat16* pro_gamma;
+  __nv_bfloat16* pro_out;
+  float pro_inv_k, pro_eps;
+  int* pro_count;               // prologue warps done (zero before the launch)
   int* status;
 };
+
+__device__ __forceinline__ float warp_sum32(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Rows gw, gw + nw, ... of the prologue's RMSNorm, K = VPL * 256: lane owns 16-byte vectors
+// i * 32 + lane of its row (the order of the standalone RMSNorm kernel, so both give the same
+// bits); the next row's loads are issued before this row's reduction.
+template <int VPL>
+__device__ __forceinline__ void prologue_rows(const Params& p, int gw, int nw, int lane) {
+  const uint4* x = reinterpret_cast<const uint4*>(p.pro_x);
+  const uint4* g = reinterpret_cast<const uint4*>(p.pro_gamma);
+  uint4* y = reinterpret_cast<uint4*>(p.pro_out);
+  uint4 v[VPL], vn[VPL];
+  int row = gw;
+  if (row < p.M) {
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) v[i] = __ldcs(x + static_cast<long long>(row) * (VPL * 32) + i * 32 + lane);
+  }
+  for (; row < p.M; row += nw) {
+    const int nrow = row + nw;
+    if (nrow < p.M) {
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) vn[i] = __ldcs(x + static_cast<long long>(nrow) * (VPL * 32) + i * 32 + lane);
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float a = bf16_lo(w[j]), b = bf16_hi(w[j]);
+        ss = fmaf(a, a, ss);
+        ss = fmaf(b, b, ss);
+      }
+    }
+    ss = warp_sum32(ss);
+    const float r = rsqrtf(ss * p.pro_inv_k + p.pro_eps);
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const uint4 gv = __ldg(g + i * 32 + lane);
+      const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+      const uint32_t gw4[4] = {gv.x, gv.y, gv.z, gv.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        o[j] = pack_bf16(bf16_lo(gw4[j]) * (bf16_lo(w[j]) * r), bf16_hi(gw4[j]) * (bf16_hi(w[j]) * r));
+      y[static_cast<long long>(row) * (VPL * 32) + i * 32 + lane] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) v[i] = vn[i];
+  }
+}
+
+// Any K: lane-strided elements, two passes over the row (the second from L1).
+__device__ __noinline__ void prologue_rows_generic(const Params& p, int gw, int nw, int lane) {
+  for (int row = gw; row < p.M; row += nw) {
+    const __nv_bfloat16* xr = p.pro_x + static_cast<long long>(row) * p.K;
+    float ss = 0.f;
+    for (int i = lane; i < p.K; i += 32) {
+      const float a = __bfloat162float(xr[i]);
+      ss = fmaf(a, a, ss);
+    }
+    ss = warp_sum32(ss);
+    const float r = rsqrtf(ss * p.pro_inv_k + p.pro_eps);
+    __nv_bfloat16* yr = p.pro_out + static_cast<long long>(row) * p.K;
+    for (int i = lane; i < p.K; i += 32)
+      yr[i] = __float2bfloat16_rn(__bfloat162float(p.pro_gamma[i]) * (__bfloat162float(xr[i]) * r));
+  }
+}
+
+// Wait (bounded) until *count reaches target; false (and LLAMA_ERR_TIMEOUT recorded) if it
+// does not within the wait budget or another wait of the CTA gave up.
+__device__ __noinline__ bool wait_count(const int* count, int target, int* status, volatile int* abort_flag) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(count) : "memory");
+    if (v >= target) return true;
+    if ((it & 15u) == 0u) {
+      if (*abort_flag) return false;
+      const uint64_t now = globaltimer_ns();
+      if (now - t0 > kWaitBudgetNs) {
+        report_timeout(status, now - t0, it, 0xFFFFFFFFu, static_cast<uint32_t>(target));
+        *abort_flag = 1;
+        return false;
+      }
+    }
+    __nanosleep(64);
+  }
+}
 
 __device__ __forceinline__ void resolve_rows(const RowMap& rm, int vrow, int& map, int& row) {
   map = 0;
@@ -170,54 +249,32 @@ __device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float* v,
   }
 }
 
-// Stages of the shared-memory A ring (the raw x tiles of the RMSNorm-fused form), and TMEM A slots.
-template <bool NORM, int STAGES>
-constexpr int a_stages_of() {
-  return NORM ? 4 : STAGES;
-}
-constexpr int kNormASlots = 2;
-
-template <int BN, int EPI, int STAGES, bool NORM>
-__global__ void __launch_bounds__(threads_of<NORM>())
+template <int BN, int EPI, int STAGES>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ TMaps tm, const Params p) {
   constexpr int B_TILE_BYTES = BN * BK * 2;
-  constexpr int SA = a_stages_of<NORM, STAGES>();
   // B arrives in 128-row boxes, or as one box when BN is not a multiple of 128 (BN <= 256);
   // gate/up tiles as two boxes of BN/2 rows, one from each matrix
   constexpr int B_BOX_ROWS = EPI == EPI_SWIGLU ? BN / 2 : BN % 128 == 0 ? 128 : BN;
   constexpr int B_BOXES = BN / B_BOX_ROWS;
-  // bytes that TMA brings per stage towards the MMA barrier (in the RMSNorm-fused form the raw A
-  // tile and its gammas arrive on a barrier of their own, for the norm warps)
-  constexpr uint32_t STAGE_TX = NORM ? B_TILE_BYTES : A_TILE_BYTES + B_TILE_BYTES;
-  constexpr uint32_t A_TX = A_TILE_BYTES + BK * 2;
-  constexpr uint32_t ACC_COLS = 2 * BN + (NORM ? kNormASlots * BK / 2 : 0);
-  constexpr uint32_t TMEM_COLS = ACC_COLS <= 32 ? 32 : ACC_COLS <= 64 ? 64 : ACC_COLS <= 128 ? 128 : ACC_COLS <= 256 ? 256 : 512;
+  constexpr uint32_t STAGE_TX = A_TILE_BYTES + B_TILE_BYTES;
+  constexpr uint32_t TMEM_COLS = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
   constexpr uint32_t IDESC = idesc_bf16(BM, BN, false);
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
-  static_assert(ACC_COLS <= 512, "two accumulators (and the A slots) in tensor memory");
 
   pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = smem + SA * A_TILE_BYTES;
+  uint8_t* sB = smem + STAGES * A_TILE_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_TILE_BYTES);
-  uint64_t* full_bar = bars;                      // [STAGES] A and B landed (fused form: B)
-  uint64_t* empty_bar = bars + STAGES;            // [STAGES] the stage's MMAs are done
+  uint64_t* full_bar = bars;
+  uint64_t* empty_bar = bars + STAGES;
   uint64_t* tfull_bar = bars + 2 * STAGES;
   uint64_t* tempty_bar = bars + 2 * STAGES + 2;
   uint64_t* drain_bar = bars + 2 * STAGES + 4;
-  // fused form: per raw A stage, landed / read by the norm warps; per TMEM A slot, written by the
-  // norm warps / read by the MMAs
-  uint64_t* araw_bar = bars + 2 * STAGES + 5;
-  uint64_t* afree_bar = araw_bar + SA;
-  uint64_t* tready_bar = afree_bar + SA;
-  uint64_t* tfree_bar = tready_bar + kNormASlots;
-  constexpr int BAR_WORDS = 2 * STAGES + 5 + (NORM ? 2 * SA + 2 * kNormASlots : 0);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + BAR_WORDS);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  // [SA][BK] gammas of each A stage (fused form), 16-byte aligned for the bulk copy
-  uint8_t* sG = reinterpret_cast<uint8_t*>(bars + ((BAR_WORDS + 2) & ~1));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int num_tiles = p.num_mb * p.num_nb * p.num_splits;
@@ -226,16 +283,6 @@ __global__ void __launch_bounds__(threads_of<NORM>())
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(smem_u32(full_bar + i), 1);
       mbar_init(smem_u32(empty_bar + i), 1);
-    }
-    if constexpr (NORM) {
-      for (int i = 0; i < SA; ++i) {
-        mbar_init(smem_u32(araw_bar + i), 1);
-        mbar_init(smem_u32(afree_bar + i), 4);
-      }
-      for (int i = 0; i < kNormASlots; ++i) {
-        mbar_init(smem_u32(tready_bar + i), 4);
-        mbar_init(smem_u32(tfree_bar + i), 1);
-      }
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(tfull_bar + i), 1);
@@ -256,26 +303,28 @@ __global__ void __launch_bounds__(threads_of<NORM>())
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const uint32_t tmem_a = tmem_base + 2 * BN;      // the A slots of the fused form
   // inputs written by the previous kernel are read from here on (the producer waits below,
   // after issuing the weight tiles that depend on nothing in flight)
   if (!(warp == 0 && lane == 0)) pdl_wait();
-
-  // The (tile, k-block) steps of this CTA in order, walked by cursors (no divisions per step).
-  struct Cursor {
-    int t, kb, kb1, mb, nb, split;
-  };
-  auto cursor_at_tile = [&](Cursor& c, int t) {
-    c.t = t;
-    if (t < num_tiles) {
-      tile_coords(p, t, c.mb, c.nb, c.split);
-      c.kb = c.split * p.kb_per_split;
-      c.kb1 = min(c.kb + p.kb_per_split, p.num_kb);
+  // prologue RMSNorm: the epilogue warps normalise their share of the rows of A (the forms whose A
+  // can be a normalised activation)
+  constexpr bool kPrologue = EPI == EPI_BF16 || EPI == EPI_F32 || EPI == EPI_SWIGLU || EPI == EPI_QKV;
+  if (kPrologue && p.pro_out != nullptr && warp >= 2) {
+    const int gw = static_cast<int>(blockIdx.x) * 4 + (warp - 2), nw = static_cast<int>(gridDim.x) * 4;
+    switch (p.K % 256 == 0 && p.K <= 4096 ? p.K / 256 : 0) {
+      case 1: prologue_rows<1>(p, gw, nw, lane); break;
+      case 2: prologue_rows<2>(p, gw, nw, lane); break;
+      case 4: prologue_rows<4>(p, gw, nw, lane); break;
+      case 8: prologue_rows<8>(p, gw, nw, lane); break;
+      case 16: prologue_rows<16>(p, gw, nw, lane); break;
+      default: prologue_rows_generic(p, gw, nw, lane);
     }
-  };
-  auto cursor_next = [&](Cursor& c) {
-    if (++c.kb == c.kb1) cursor_at_tile(c, c.t + static_cast<int>(gridDim.x));
-  };
+    // the rows go to other CTAs' TMA loads: order the generic stores before them
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) atomicAdd(p.pro_count, 1);
+  }
 
   if (warp == 0) {
     if (lane == 0) {
@@ -283,16 +332,8 @@ __global__ void __launch_bounds__(threads_of<NORM>())
       auto load_a = [&](int stage, int kb, int mb) {
         int a_map, a_row;
         resolve_rows(p.amap, mb * BM, a_map, a_row);
-        if constexpr (NORM) {
-          // the raw x tile and its gammas, for the norm warps
-          const uint32_t ab = smem_u32(araw_bar + stage);
-          mbar_expect_tx(ab, A_TX);
-          tma_load_2d(smem_u32(sA + stage * A_TILE_BYTES), &tm.m[p.a_map0 + a_map], ab, kb * BK, a_row);
-          bulk_load(smem_u32(sG + stage * BK * 2), p.norm_gamma + kb * BK, BK * 2, ab);
-        } else {
-          tma_load_2d(smem_u32(sA + stage * A_TILE_BYTES), &tm.m[p.a_map0 + a_map], smem_u32(full_bar + stage),
-                      kb * BK, a_row);
-        }
+        tma_load_2d(smem_u32(sA + stage * A_TILE_BYTES), &tm.m[p.a_map0 + a_map], smem_u32(full_bar + stage),
+                    kb * BK, a_row);
       };
       auto load_b = [&](int stage, int kb, int nb) {
         if constexpr (EPI == EPI_QKV && BN % 128 != 0) {
@@ -334,88 +375,53 @@ __global__ void __launch_bounds__(threads_of<NORM>())
           const int kb1 = min(kb0 + p.kb_per_split, p.num_kb);
           for (int kb = kb0; kb < kb1 && pre < STAGES; ++kb, ++pre) {
             mbar_expect_tx(smem_u32(full_bar + pre), STAGE_TX);
-            if (p.weight_first == 1) load_a(pre, kb, mb);   // (never with NORM: A is the activation)
+            if (p.weight_first == 1) load_a(pre, kb, mb);
             else load_b(pre, kb, nb);
           }
         }
       }
       pdl_wait();
       bool ok = true;
-      if constexpr (NORM) {
-        // Before the weight tile of step s goes out, the raw x tiles of steps up to s + SA - 1 do,
-        // each into a stage that the norm warps have read (they run ahead of the MMAs by the
-        // TMEM A slots).
-        constexpr int LEAD = SA - 1;
-        Cursor ca, cb;
-        cursor_at_tile(ca, blockIdx.x);
-        cursor_at_tile(cb, blockIdx.x);
-        int sa = 0, sb = 0, stage_a = 0, stage_b = 0;
-        uint32_t phase_a = 0, phase_b = 0;
-        uint32_t used_a = 0, par_a = 0, used_b = 0, par_b = 0;
-        for (; cb.t < num_tiles && ok; cursor_next(cb), ++sb) {
-          for (; ca.t < num_tiles && sa <= sb + LEAD; cursor_next(ca), ++sa) {
-            if (!mbar_wait(smem_u32(afree_bar + stage_a), phase_a ^ 1u, p.status, abort_flag)) { ok = false; break; }
-            load_a(stage_a, ca.kb, ca.mb);
-            used_a |= 1u << stage_a;
-            par_a = (par_a & ~(1u << stage_a)) | (phase_a << stage_a);
-            if (++stage_a == SA) { stage_a = 0; phase_a ^= 1u; }
+      if (kPrologue && p.pro_out != nullptr) {
+        // every CTA's prologue warps have written their rows of A
+        ok = wait_count(p.pro_count, 4 * static_cast<int>(gridDim.x), p.status, abort_flag);
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+      }
+      int stage = 0, step = 0;
+      uint32_t phase = 0;
+      uint32_t used_mask = 0, last_parity = 0;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        int mb, nb, split;
+        tile_coords(p, t, mb, nb, split);
+        const int kb0 = split * p.kb_per_split;
+        const int kb1 = min(kb0 + p.kb_per_split, p.num_kb);
+        for (int kb = kb0; kb < kb1; ++kb, ++step) {
+          if (step < pre) {   // the weight half of this stage is already on its way
+            if (p.weight_first == 1) load_b(stage, kb, nb);
+            else load_a(stage, kb, mb);
+          } else {
+            if (!mbar_wait(smem_u32(empty_bar + stage), phase ^ 1u, p.status, abort_flag)) { ok = false; break; }
+            mbar_expect_tx(smem_u32(full_bar + stage), STAGE_TX);
+            load_a(stage, kb, mb);
+            load_b(stage, kb, nb);
           }
-          if (!ok) break;
-          if (sb >= pre) {
-            if (!mbar_wait(smem_u32(empty_bar + stage_b), phase_b ^ 1u, p.status, abort_flag)) { ok = false; break; }
-            mbar_expect_tx(smem_u32(full_bar + stage_b), STAGE_TX);
-            load_b(stage_b, cb.kb, cb.nb);
-          }
-          used_b |= 1u << stage_b;
-          par_b = (par_b & ~(1u << stage_b)) | (phase_b << stage_b);
-          if (++stage_b == STAGES) { stage_b = 0; phase_b ^= 1u; }
+          used_mask |= 1u << stage;
+          last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
-        if (!ok) {
-          // leave no copy in flight: wait (bounded) for the last load into every stage used
-          for (int s = 0; s < SA; ++s)
-            if (used_a & (1u << s))
-              mbar_wait_slow(smem_u32(araw_bar + s), (par_a >> s) & 1u, nullptr, nullptr, kWaitBudgetNs);
-          for (int s = 0; s < STAGES; ++s)
-            if (used_b & (1u << s))
-              mbar_wait_slow(smem_u32(full_bar + s), (par_b >> s) & 1u, nullptr, nullptr, kWaitBudgetNs);
-        }
-      } else {
-        int stage = 0, step = 0;
-        uint32_t phase = 0;
-        uint32_t used_mask = 0, last_parity = 0;
-        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-          int mb, nb, split;
-          tile_coords(p, t, mb, nb, split);
-          const int kb0 = split * p.kb_per_split;
-          const int kb1 = min(kb0 + p.kb_per_split, p.num_kb);
-          for (int kb = kb0; kb < kb1; ++kb, ++step) {
-            if (step < pre) {   // the weight half of this stage is already on its way
-              if (p.weight_first == 1) load_b(stage, kb, nb);
-              else load_a(stage, kb, mb);
-            } else {
-              if (!mbar_wait(smem_u32(empty_bar + stage), phase ^ 1u, p.status, abort_flag)) { ok = false; break; }
-              mbar_expect_tx(smem_u32(full_bar + stage), STAGE_TX);
-              load_a(stage, kb, mb);
-              load_b(stage, kb, nb);
-            }
-            used_mask |= 1u << stage;
-            last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
-            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-          }
-        }
-        if (!ok) {
-          // leave no copy in flight: wait (bounded) for the last load into every stage used
-          for (int s = 0; s < STAGES; ++s)
-            if (used_mask & (1u << s))
-              mbar_wait_slow(smem_u32(full_bar + s), (last_parity >> s) & 1u, nullptr, nullptr, kWaitBudgetNs);
-        }
+      }
+      if (!ok) {
+        // leave no copy in flight: wait (bounded) for the last load into every stage used
+        for (int s = 0; s < STAGES; ++s)
+          if (used_mask & (1u << s))
+            mbar_wait_slow(smem_u32(full_bar + s), (last_parity >> s) & 1u, nullptr, nullptr, kWaitBudgetNs);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
-      int stage = 0, slot = 0;
-      uint32_t phase = 0, slot_phase = 0;
+      int stage = 0;
+      uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
@@ -430,34 +436,18 @@ __global__ void __launch_bounds__(threads_of<NORM>())
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(smem_u32(full_bar + stage), phase, p.status, abort_flag)) { ok = false; break; }
-          if constexpr (NORM) {
-            if (!mbar_wait(smem_u32(tready_bar + slot), slot_phase, p.status, abort_flag)) { ok = false; break; }
-          }
           tc_fence_after();
+          const uint32_t a_addr = smem_u32(sA + stage * A_TILE_BYTES);
           const uint32_t b_addr = smem_u32(sB + stage * B_TILE_BYTES);
-          if constexpr (NORM) {
-            // A from its TMEM slot: row m in lane m, k-block columns packed two per 32-bit column
-            const uint32_t a_tmem = tmem_a + static_cast<uint32_t>(slot * (BK / 2));
 #pragma unroll
-            for (int k = 0; k < BK / 16; ++k)
-              tc_mma_bf16_ts(d_tmem, a_tmem + k * 8, sdesc_sw128(b_addr + k * 32, 16, 1024), IDESC,
-                             (kb > kb0 || k > 0) ? 1u : 0u);
-          } else {
-            const uint32_t a_addr = smem_u32(sA + stage * A_TILE_BYTES);
-#pragma unroll
-            for (int k = 0; k < BK / 16; ++k) {
-              const uint64_t ad = sdesc_sw128(a_addr + k * 32, 16, 1024);
-              const uint64_t bd = sdesc_sw128(b_addr + k * 32, 16, 1024);
-              tc_mma_bf16(d_tmem, ad, bd, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
-            }
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t ad = sdesc_sw128(a_addr + k * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(b_addr + k * 32, 16, 1024);
+            tc_mma_bf16(d_tmem, ad, bd, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
           }
           issued = true;
           tc_commit(smem_u32(empty_bar + stage));
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-          if constexpr (NORM) {
-            tc_commit(smem_u32(tfree_bar + slot));
-            if (++slot == kNormASlots) { slot = 0; slot_phase ^= 1u; }
-          }
         }
         if (!ok) break;
         tc_commit(smem_u32(tfull_bar + acc));
@@ -468,63 +458,6 @@ __global__ void __launch_bounds__(threads_of<NORM>())
         tc_commit(smem_u32(drain_bar));
         mbar_wait_slow(smem_u32(drain_bar), 0, nullptr, nullptr, kWaitBudgetNs);
       }
-    }
-  } else if (NORM && warp >= 6) {
-    // -------------------------------------------------------------- norm warps 6..9: operand A
-    // A warp may only reach the TMEM lanes of its quarter (warp % 4): thread `lane` of warp w
-    // owns row 32 (w % 4) + lane of the tile and writes its 64 k-values of each k-block, packed
-    // two per 32-bit column, into the 32 columns of the step's A slot.  In the raw tile the row's
-    // 16-byte chunk j lies at j ^ (row & 7) (the 128-byte swizzle of the TMA box).
-    const int row = (warp & 3) * 32 + lane;
-    const uint32_t t_lane = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    float rc = 0.f, rn = 0.f;   // this row's scale in the current tile and in the next one
-    Cursor c;
-    cursor_at_tile(c, blockIdx.x);
-    if (c.t < num_tiles) rc = c.mb * BM + row < p.M ? __ldcg(p.norm_r + c.mb * BM + row) : 0.f;
-    int stage = 0, slot = 0;
-    uint32_t phase = 0, slot_phase = 0;
-    bool ok = true;
-    while (c.t < num_tiles && ok) {
-      const int t_next = c.t + static_cast<int>(gridDim.x);
-      if (t_next < num_tiles) {   // the next tile's scale: its latency hides behind this tile
-        int mb, nb, split;
-        tile_coords(p, t_next, mb, nb, split);
-        rn = mb * BM + row < p.M ? __ldcg(p.norm_r + mb * BM + row) : 0.f;
-      }
-      for (; c.kb < c.kb1; ++c.kb) {
-        if (!mbar_wait(smem_u32(araw_bar + stage), phase, p.status, abort_flag)) { ok = false; break; }
-        const uint8_t* xrow = sA + stage * A_TILE_BYTES + row * 128;
-        const uint8_t* grow = sG + stage * BK * 2;
-        uint32_t o[32];
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-          const uint4 xv = *reinterpret_cast<const uint4*>(xrow + ((jj ^ (row & 7)) << 4));
-          const uint4 gv = *reinterpret_cast<const uint4*>(grow + jj * 16);
-          const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-          const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-          // gamma * (x * r) in fp32, rounded once: the value a standalone RMSNorm stores
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            o[4 * jj + q] = pack_bf16(bf16_lo(gw[q]) * (bf16_lo(xw[q]) * rc), bf16_hi(gw[q]) * (bf16_hi(xw[q]) * rc));
-        }
-        // the raw stage is no longer needed: order these generic-proxy reads before the TMA
-        // (async-proxy) writes that refill it once the producer sees the arrival
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(afree_bar + stage));
-        if (++stage == SA) { stage = 0; phase ^= 1u; }
-        // the slot's previous MMAs are done: overwrite it
-        if (!mbar_wait(smem_u32(tfree_bar + slot), slot_phase ^ 1u, p.status, abort_flag)) { ok = false; break; }
-        tc_fence_after();
-        tmem_st32(tmem_a + t_lane + static_cast<uint32_t>(slot * (BK / 2)), o);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(tready_bar + slot));
-        if (++slot == kNormASlots) { slot = 0; slot_phase ^= 1u; }
-      }
-      if (!ok) break;
-      rc = rn;
-      cursor_at_tile(c, t_next);
     }
   } else {
     // -------------------------------------------------------------- epilogue warps 2..5
@@ -558,7 +491,6 @@ __global__ void __launch_bounds__(threads_of<NORM>())
           }
         };
         load_resid(0);
-        float ss = 0.f;   // row statistics: the sum of squares of this row's rounded outputs
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint4 res_c[4];
@@ -597,60 +529,22 @@ __global__ void __launch_bounds__(threads_of<NORM>())
                 }
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] += rr[i];
-                if (p.stat_part != nullptr) {
-#pragma unroll
-                  for (int i = 0; i < 32; ++i) {
-                    const float hb = __bfloat162float(__float2bfloat16_rn(v[i]));   // the stored value
-                    ss = i < valid ? fmaf(hb, hb, ss) : ss;
-                  }
-                }
               }
               store_bf16x32(static_cast<__nv_bfloat16*>(p.out) + m * p.ldo + n0, v, valid);
             }
           }
         }
-        if constexpr (EPI == EPI_RESID) {
-          if (p.stat_part != nullptr && m < p.M) {
-            // this tile's share of row m; the row's last column tile to finish completes r_m
-            p.stat_part[static_cast<long long>(nb) * p.M + m] = ss;
-            __threadfence();
-            if (atomicAdd(p.stat_ticket + m, 1) == p.num_nb - 1) {
-              __threadfence();
-              float tot = 0.f;
-#pragma unroll 4
-              for (int q = 0; q < p.num_nb; ++q) tot += __ldcg(p.stat_part + static_cast<long long>(q) * p.M + m);
-              p.stat_r[m] = rsqrtf(tot * p.stat_inv_n + p.stat_eps);
-              p.stat_ticket[m] = 0;
-            }
-          }
-        }
       } else if constexpr (EPI == EPI_SWIGLU) {
-        // columns [0, BN/2) of the tile are gate rows BN/2*nb.., [BN/2, BN) the matching up rows.
-        // Every TMEM load covers 32 columns starting at a multiple of 32; when the halves are not
-        // (BN/2 = 112) the up values of an output chunk come from two such loads, 16 apart.
+        // columns [0, BN/2) of the tile are gate rows BN/2*nb.., [BN/2, BN) the matching up rows
         constexpr int HALF = BN / 2;
-        constexpr int SHIFT = HALF % 32;
-        static_assert(SHIFT == 0 || SHIFT == 16, "gate/up halves of 16-column multiples");
+        static_assert(HALF % 32 == 0, "gate/up halves of whole 32-column chunks");
 #pragma unroll 1
-        for (int c0 = 0; c0 < HALF; c0 += 32) {
+        for (int c = 0; c < HALF / 32; ++c) {
           uint32_t u[32];
-          tmem_ld32(t_acc + c0, r);
-          if constexpr (SHIFT == 0) {
-            tmem_ld32(t_acc + HALF + c0, u);
-          } else {
-            uint32_t u0[32];
-            const int ua = HALF + c0 - SHIFT;   // aligned start of the load holding the first up value
-            tmem_ld32(t_acc + ua, u0);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) u[i] = u0[16 + i];
-            if (c0 + 16 < HALF) {
-              tmem_ld32(t_acc + ua + 32, u0);
-#pragma unroll
-              for (int i = 0; i < 16; ++i) u[16 + i] = u0[i];
-            }
-          }
-          const int n0 = nb * HALF + c0;
-          const int valid = min(min(32, HALF - c0), p.N - n0);
+          tmem_ld32(t_acc + c * 32, r);
+          tmem_ld32(t_acc + HALF + c * 32, u);
+          const int n0 = nb * HALF + c * 32;
+          const int valid = min(32, p.N - n0);
           if (m < p.M && valid > 0) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = silu_f(__uint_as_float(r[i])) * __uint_as_float(u[i]);
@@ -708,9 +602,15 @@ __global__ void __launch_bounds__(threads_of<NORM>())
             __nv_bfloat16* dst = hh < p.H
                 ? p.q_out + ((static_cast<long long>(b) * p.H + hh) * p.S + s_in) * p.D
                 : p.k_cache + ((static_cast<long long>(b) * p.G + (hh - p.H)) * p.T_max + s) * p.D;
-            // this chunk's 32 angles, loaded here (32 pairs per chunk: a look-ahead copy would
-            // not fit the registers of the RMSNorm-fused form)
-            load_angles(c);
+            // this chunk's angles came one rope chunk ahead; the next rope chunk is the second
+            // quarter of this head or the first of the next head (the tile is head-aligned)
+            float cs_c[32], sn_c[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              cs_c[i] = cs_n[i];
+              sn_c[i] = sn_n[i];
+            }
+            load_angles(j0 + 32 < half_d ? c + 1 : c + 3);
             uint32_t r2[32];
             tmem_ld32(t_acc + c * 32, r);
             tmem_ld32(t_acc + c * 32 + half_d, r2);
@@ -719,8 +619,8 @@ __global__ void __launch_bounds__(threads_of<NORM>())
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const float x1 = __uint_as_float(r[i]), x2 = __uint_as_float(r2[i]);
-              v[i] = x1 * cs_n[i] - x2 * sn_n[i];
-              w2[i] = x2 * cs_n[i] + x1 * sn_n[i];
+              v[i] = x1 * cs_c[i] - x2 * sn_c[i];
+              w2[i] = x2 * cs_c[i] + x1 * sn_c[i];
             }
             store_bf16x32(dst + j0, v, 32);
             store_bf16x32(dst + j0 + half_d, w2, 32);
@@ -789,20 +689,15 @@ __global__ void __launch_bounds__(threads_of<NORM>())
   }
 }
 
-template <int BN, int EPI, int STAGES, bool NORM>
+template <int BN, int EPI, int STAGES>
 constexpr size_t smem_bytes() {
-  // alignment slack, the rings, the barriers, the TMEM slot and the abort flag (padded to 16
-  // bytes), the gammas of each A stage
-  constexpr int SA = a_stages_of<NORM, STAGES>();
-  constexpr int bar_words = 2 * STAGES + 5 + (NORM ? 2 * SA + 2 * kNormASlots : 0);
-  return 1024 + SA * A_TILE_BYTES + STAGES * BN * BK * 2 + ((bar_words + 2) & ~1) * 8 + (NORM ? SA * BK * 2 : 0);
+  return 1024 + STAGES * (A_TILE_BYTES + BN * BK * 2) + (2 * STAGES + 5) * 8 + 16;
 }
 
-template <int BN, int EPI, int STAGES, bool NORM = false>
+template <int BN, int EPI, int STAGES>
 int launch(const Ctx& c, const TMaps& tm, Params p) {
-  auto kern = gemm_tc_kernel<BN, EPI, STAGES, NORM>;
-  constexpr size_t smem = smem_bytes<BN, EPI, STAGES, NORM>();
-  static_assert(smem <= 227 * 1024, "shared memory per CTA");
+  auto kern = gemm_tc_kernel<BN, EPI, STAGES>;
+  constexpr size_t smem = smem_bytes<BN, EPI, STAGES>();
   static_assert(smem >= kTmemKernelMinSmem, "a TMEM-holding kernel must not share an SM with another");
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
@@ -814,18 +709,12 @@ int launch(const Ctx& c, const TMaps& tm, Params p) {
   if (!c.static_weights) p.weight_first = 0;
   const int tiles = p.num_mb * p.num_nb * p.num_splits;
   if (tiles == 0) return LLAMA_OK;
-  if (NORM && (p.norm_gamma == nullptr || p.norm_r == nullptr || p.num_splits != 1 || p.K % BK != 0 ||
-               p.amap.nseg != 1 || p.weight_first == 1 || (reinterpret_cast<uintptr_t>(p.norm_gamma) & 15) != 0))
+  if (p.pro_out != nullptr && (EPI == EPI_RESID || EPI == EPI_PARTIAL || p.pro_x == nullptr ||
+                              p.pro_gamma == nullptr || p.pro_count == nullptr))
     return LLAMA_ERR_INVALID_ARG;
   const int grid = std::min(tiles, c.num_sms);
-  launch_pdl(c, kern, dim3(grid), dim3(threads_of<NORM>()), smem, tm, p);
+  launch_pdl(c, kern, dim3(grid), dim3(NUM_THREADS), smem, tm, p);
   return after_launch(c);
-}
-
-// RMSNorm-fused form: operand A (its tensor map) is x [M, K]; gamma [K] and the row scales r [M].
-void set_norm(Params& p, const NormIn& n) {
-  p.norm_gamma = static_cast<const __nv_bfloat16*>(n.gamma);
-  p.norm_r = n.r;
 }
 
 // Rounds of num_sms tiles times the tile width: the time of a GEMM with M rows and n_blocks
@@ -838,6 +727,17 @@ long long round_cost(int M, int n_blocks, int bn, int num_sms) {
 // Tile width (256 or 224 columns) with the least round cost for N output columns; ties keep 256.
 int tile_width_for(int M, int N, int num_sms) {
   return round_cost(M, (N + 223) / 224, 224, num_sms) < round_cost(M, (N + 255) / 256, 256, num_sms) ? 224 : 256;
+}
+
+// RMSNorm in the prologue: A (the tensor map at a_map0) is built on n.xn, which the prologue
+// fills with RMSNorm(X).
+void set_prologue(Params& p, const void* X, const NormPro& n) {
+  p.pro_x = static_cast<const __nv_bfloat16*>(X);
+  p.pro_gamma = static_cast<const __nv_bfloat16*>(n.gamma);
+  p.pro_out = static_cast<__nv_bfloat16*>(n.xn);
+  p.pro_inv_k = 1.0f / static_cast<float>(p.K);
+  p.pro_eps = n.eps;
+  p.pro_count = n.count;
 }
 
 Params base_params(int M, int N, int K, int BN) {
@@ -870,40 +770,23 @@ Params base_params(int M, int N, int K, int BN) {
 }  // namespace
 
 int gemm_plain(const Ctx& c, const void* X, const void* W, void* C, int M, int N, int K, bool c_f32,
-               const NormIn* norm) {
+               const NormPro* norm) {
   const int bn = tile_width_for(M, N, c.num_sms);
   TMaps tm{};
-  if (!make_tmap_2d(&tm.m[0], X, K, M, K, 128) || !make_tmap_2d(&tm.m[1], W, K, N, K, bn == 256 ? 128 : bn))
+  if (!make_tmap_2d(&tm.m[0], norm ? norm->xn : X, K, M, K, 128) ||
+      !make_tmap_2d(&tm.m[1], W, K, N, K, bn == 256 ? 128 : bn))
     return LLAMA_ERR_INVALID_ARG;
   Params p = base_params(M, N, K, bn);
+  if (norm != nullptr) set_prologue(p, X, *norm);
   p.a_map0 = 0;
   p.b_map0 = 1;
   p.out = C;
   p.ldo = N;
-  if (norm != nullptr) {
-    // 224-column tiles: the two accumulators leave tensor memory room for the A slots
-    if (bn != 224) {
-      if (!make_tmap_2d(&tm.m[1], W, K, N, K, 224)) return LLAMA_ERR_INVALID_ARG;
-      p = base_params(M, N, K, 224);
-      p.a_map0 = 0;
-      p.b_map0 = 1;
-      p.out = C;
-      p.ldo = N;
-    }
-    set_norm(p, *norm);
-    return c_f32 ? launch<224, EPI_F32, 5, true>(c, tm, p) : launch<224, EPI_BF16, 5, true>(c, tm, p);
-  }
   if (bn == 256) return c_f32 ? launch<256, EPI_F32, 4>(c, tm, p) : launch<256, EPI_BF16, 4>(c, tm, p);
   return c_f32 ? launch<224, EPI_F32, 5>(c, tm, p) : launch<224, EPI_BF16, 5>(c, tm, p);
 }
 
-int residual_col_tiles(const Ctx& c, int M, int N) {
-  const int bn = tile_width_for(M, N, c.num_sms);
-  return (N + bn - 1) / bn;
-}
-
-int gemm_residual(const Ctx& c, const void* X, const void* W, const void* resid, void* out, int M, int N, int K,
-                  const RowStatsOut* stats) {
+int gemm_residual(const Ctx& c, const void* X, const void* W, const void* resid, void* out, int M, int N, int K) {
   // 224-column tiles when they finish in fewer tile-column rounds (e.g. N = 4096 at M = 2048:
   // 304 tiles fill 2 rounds of 152 SMs, where 256 tiles of 256 columns leave the second
   // round two-thirds full)
@@ -918,43 +801,19 @@ int gemm_residual(const Ctx& c, const void* X, const void* W, const void* resid,
   p.ldo = N;
   p.resid = static_cast<const __nv_bfloat16*>(resid);
   p.ldr = N;
-  if (stats != nullptr) {
-    if (stats->part == nullptr || stats->r == nullptr || stats->ticket == nullptr) return LLAMA_ERR_INVALID_ARG;
-    p.stat_part = stats->part;
-    p.stat_r = stats->r;
-    p.stat_ticket = stats->ticket;
-    p.stat_inv_n = 1.0f / static_cast<float>(N);
-    p.stat_eps = stats->eps;
-  }
   return bn == 256 ? launch<256, EPI_RESID, 4>(c, tm, p) : launch<224, EPI_RESID, 5>(c, tm, p);
 }
 
 int gemm_swiglu(const Ctx& c, const void* X, const void* Wg, const void* Wu, void* out, int M, int I, int K,
-                const NormIn* norm) {
-  if (norm != nullptr) {
-    // 224-column tiles (112 gate + 112 up rows): the two accumulators leave tensor memory room
-    // for the A slots of the RMSNorm-fused form
-    TMaps tm{};
-    if (!make_tmap_2d(&tm.m[0], X, K, M, K, 128) || !make_tmap_2d(&tm.m[1], Wg, K, I, K, 112) ||
-        !make_tmap_2d(&tm.m[2], Wu, K, I, K, 112))
-      return LLAMA_ERR_INVALID_ARG;
-    Params p = base_params(M, 2 * ((I + 111) / 112) * 112, K, 224);
-    p.N = I;
-    p.a_map0 = 0;
-    p.b_map0 = 1;
-    p.n_maps = 3;
-    p.out = out;
-    p.ldo = I;
-    set_norm(p, *norm);
-    return launch<224, EPI_SWIGLU, 5, true>(c, tm, p);
-  }
+                const NormPro* norm) {
   // kernel N runs over 256-column tiles, each = 128 gate rows + the same 128 up rows (measured:
   // 240-column tiles, which fill the SM-count rounds better at I = 11008, M = 2048, run slower)
   TMaps tm{};
-  if (!make_tmap_2d(&tm.m[0], X, K, M, K, 128) || !make_tmap_2d(&tm.m[1], Wg, K, I, K, 128) ||
+  if (!make_tmap_2d(&tm.m[0], norm ? norm->xn : X, K, M, K, 128) || !make_tmap_2d(&tm.m[1], Wg, K, I, K, 128) ||
       !make_tmap_2d(&tm.m[2], Wu, K, I, K, 128))
     return LLAMA_ERR_INVALID_ARG;
   Params p = base_params(M, 2 * ((I + 127) / 128) * 128, K, 256);
+  if (norm != nullptr) set_prologue(p, X, *norm);
   p.N = I;   // output width (used by the epilogue's bounds)
   p.a_map0 = 0;
   p.b_map0 = 1;
@@ -967,24 +826,22 @@ int gemm_swiglu(const Ctx& c, const void* X, const void* Wg, const void* Wu, voi
 int gemm_qkv_rope(const Ctx& c, const void* X, const void* Wq, const void* Wk, const void* Wv, int B, int S, int K,
                   int H, int G, int D, const float* cos, const float* sin, void* q_out, void* k_cache,
                   void* v_cache, int T_max, int rope_half, const int32_t* start, const int32_t* lens,
-                  int max_pos, const NormIn* norm) {
+                  int max_pos, const NormPro* norm) {
   const int M = B * S;
   // 224-column tiles when they fill the SM-count rounds better (the half-split pairs (j, j+64)
   // need whole heads in a tile: 256 columns = two heads); a 224-column tile that crosses the
-  // q|k or k|v boundary takes its weights in 32-row boxes from the maps at b32_map0.  The
-  // RMSNorm-fused form always takes 224 columns (tensor memory holds its A slots) and so not the
-  // half-split pairs.
-  if (norm != nullptr && rope_half) return LLAMA_ERR_UNSUPPORTED;
-  const int bn = rope_half ? 256 : norm != nullptr ? 224 : tile_width_for(M, (H + 2 * G) * D, c.num_sms);
+  // q|k or k|v boundary takes its weights in 32-row boxes from the maps at b32_map0
+  const int bn = rope_half ? 256 : tile_width_for(M, (H + 2 * G) * D, c.num_sms);
   const int box = bn == 256 ? 128 : bn;
   TMaps tm{};
-  if (!make_tmap_2d(&tm.m[0], X, K, M, K, 128) || !make_tmap_2d(&tm.m[1], Wq, K, H * D, K, box) ||
+  if (!make_tmap_2d(&tm.m[0], norm ? norm->xn : X, K, M, K, 128) || !make_tmap_2d(&tm.m[1], Wq, K, H * D, K, box) ||
       !make_tmap_2d(&tm.m[2], Wk, K, G * D, K, box) || !make_tmap_2d(&tm.m[3], Wv, K, G * D, K, box))
     return LLAMA_ERR_INVALID_ARG;
   if (bn != 256 && (!make_tmap_2d(&tm.m[4], Wq, K, H * D, K, 32) || !make_tmap_2d(&tm.m[5], Wk, K, G * D, K, 32) ||
                     !make_tmap_2d(&tm.m[6], Wv, K, G * D, K, 32)))
     return LLAMA_ERR_INVALID_ARG;
   Params p = base_params(M, (H + 2 * G) * D, K, bn);
+  if (norm != nullptr) set_prologue(p, X, *norm);
   p.a_map0 = 0;
   p.b_map0 = 1;
   p.b32_map0 = 4;
@@ -1007,10 +864,6 @@ int gemm_qkv_rope(const Ctx& c, const void* X, const void* Wq, const void* Wk, c
   p.q_out = static_cast<__nv_bfloat16*>(q_out);
   p.k_cache = static_cast<__nv_bfloat16*>(k_cache);
   p.v_cache = static_cast<__nv_bfloat16*>(v_cache);
-  if (norm != nullptr) {
-    set_norm(p, *norm);
-    return launch<224, EPI_QKV, 5, true>(c, tm, p);
-  }
   return bn == 256 ? launch<256, EPI_QKV, 4>(c, tm, p) : launch<224, EPI_QKV, 5>(c, tm, p);
 }
 

@@ -66,9 +66,6 @@ bool make_tmap_3d(CUtensorMap* tm, const void* base, uint64_t n0, uint64_t n1, u
 
 // ---------------------------------------------------------------- RMSNorm (rmsnorm.cu)
 int rmsnorm(const Ctx& c, const void* x, const void* gamma, void* y, int rows, int d, float eps, int dtype);
-// Row scales r[m] = rsqrt(mean(x[m]^2) + eps) of bf16 rows x [rows, d] (fp32 statistics), for a
-// GEMM with the RMSNorm fused into its A operand; also zeroes ticket[0..rows) when not null.
-int rms_rowscale(const Ctx& c, const void* x, float* r, int* ticket, int rows, int d, float eps);
 
 // ---------------------------------------------------------------- LayerNorm (layernorm.cu)
 // y = gamma * (x - mean) * rsqrt(biased variance + eps) + beta per row.
@@ -76,35 +73,24 @@ int layernorm(const Ctx& c, const void* x, const void* gamma, const void* beta, 
               int dtype);
 
 // ---------------------------------------------------------------- tcgen05 GEMMs (gemm_tc.cu)
-// RMSNorm of operand A inside a GEMM (see gemm_tc.cu): the GEMM multiplies bf16(gamma * (X * r))
-// with r the row scales rsqrt(mean(X^2) + eps).  K % 64 == 0.
-struct NormIn {
+// RMSNorm of operand A in the GEMM's prologue (see gemm_tc.cu): the GEMM first writes
+// RMSNorm(X) = gamma * X * rsqrt(mean(X^2) + eps) into xn, then multiplies xn.
+struct NormPro {
   const void* gamma;   // device [K]
-  const float* r;      // device [M]
-};
-// Row statistics of a residual GEMM's output for the RMSNorm that follows it: part [tiles][M]
-// (tiles = residual_col_tiles(M, N)), r [M] receives rsqrt(mean(out^2) + eps) of the stored
-// (rounded) outputs, ticket [M] must be zero before the launch (it is zero again after it).
-struct RowStatsOut {
-  float* part;
-  float* r;
-  int* ticket;
   float eps;
+  void* xn;            // device [M, K] bf16, 16-byte aligned: receives RMSNorm(X), the A operand
+  int* count;          // device int, zero before the launch (the prologue's grid-wide count)
 };
 
 // All compute C = X W^T with X [M, K] and W [N, K] bf16 row-major, fp32 accumulation.
 // norm (may be null): X is normalised per row first, RMSNorm(X) W^T.
 int gemm_plain(const Ctx& c, const void* X, const void* W, void* C, int M, int N, int K, bool c_f32,
-               const NormIn* norm = nullptr);
-// out = resid + X W^T  (bf16); resid and out may alias.  stats (may be null): the row
-// statistics of out for the next RMSNorm.
-int gemm_residual(const Ctx& c, const void* X, const void* W, const void* resid, void* out, int M, int N, int K,
-                  const RowStatsOut* stats = nullptr);
-// Column tiles of gemm_residual at this shape (the row of partial sums that stats->part needs).
-int residual_col_tiles(const Ctx& c, int M, int N);
+               const NormPro* norm = nullptr);
+// out = resid + X W^T  (bf16); resid and out may alias.
+int gemm_residual(const Ctx& c, const void* X, const void* W, const void* resid, void* out, int M, int N, int K);
 // out[:, n] = SiLU(X W_gate^T)[:, n] * (X W_up^T)[:, n]  (bf16, [M, I]).
 int gemm_swiglu(const Ctx& c, const void* X, const void* Wg, const void* Wu, void* out, int M, int I, int K,
-                const NormIn* norm = nullptr);
+                const NormPro* norm = nullptr);
 // [q|k|v] = X [Wq;Wk;Wv]^T for B sequences of S tokens at positions 0..S-1; RoPE on q, k;
 // q -> q_out [B, H, S, D]; k, v -> cache slots [0, S) of [B, G, T_max, D].
 // rope_half: pairs (i, i + D/2) instead of (2i, 2i+1).  start (device [B], may be null):
@@ -113,7 +99,7 @@ int gemm_swiglu(const Ctx& c, const void* X, const void* Wg, const void* Wu, voi
 int gemm_qkv_rope(const Ctx& c, const void* X, const void* Wq, const void* Wk, const void* Wv, int B, int S,
                   int K, int H, int G, int D, const float* cos, const float* sin, void* q_out, void* k_cache,
                   void* v_cache, int T_max, int rope_half, const int32_t* start = nullptr,
-                  const int32_t* lens = nullptr, int max_pos = 0, const NormIn* norm = nullptr);
+                  const int32_t* lens = nullptr, int max_pos = 0, const NormPro* norm = nullptr);
 // Weight-streaming form for few tokens: P[s][t][n] = sum over split s of W[n, k] X[t, k] in fp32,
 // with W the row-concatenation of up to three matrices (rows multiples of 128).
 int gemm_tokens_partial(const Ctx& c, const void* const* W, const int* w_rows, int n_w, const void* X,

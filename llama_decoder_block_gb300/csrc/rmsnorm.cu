@@ -83,81 +83,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
     yr[i] = static_cast<T>(static_cast<float>(gamma[i]) * (static_cast<float>(xr[i]) * r));
 }
 
-// Row scales only: r[row] = rsqrt(mean(x^2) + eps) for a GEMM that normalises its A operand
-// itself; reads the row once (bf16), writes one float.  The sum runs in the order of
-// rmsnorm_bf16_kernel, so both give the same scale.  Also zeroes ticket[row] (the per-row
-// counters of the residual epilogues that later produce row statistics).
-template <int VPL>
-__global__ void __launch_bounds__(kWarpsPerCta * 32)
-    rms_rowscale_kernel(const uint4* __restrict__ x, float* __restrict__ r, int* __restrict__ ticket, int rows,
-                        float inv_d, float eps) {
-  pdl_trigger();
-  pdl_wait();
-  const int row = blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  const uint4* xr = x + static_cast<long long>(row) * (VPL * 32);
-  uint4 v[VPL];
-#pragma unroll
-  for (int i = 0; i < VPL; ++i) v[i] = __ldcg(xr + i * 32 + lane);   // the GEMM reads the row again: keep it in L2
-  float ss = 0.f;
-#pragma unroll
-  for (int i = 0; i < VPL; ++i) {
-    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float a = bf16_lo(w[j]), b = bf16_hi(w[j]);
-      ss = fmaf(a, a, ss);
-      ss = fmaf(b, b, ss);
-    }
-  }
-  ss = warp_sum(ss);
-  if (lane == 0) {
-    r[row] = rsqrtf(ss * inv_d + eps);
-    if (ticket != nullptr) ticket[row] = 0;
-  }
-}
-
-__global__ void __launch_bounds__(kWarpsPerCta * 32)
-    rms_rowscale_generic_kernel(const __nv_bfloat16* __restrict__ x, float* __restrict__ r, int* __restrict__ ticket,
-                                int rows, int d, float eps) {
-  pdl_trigger();
-  pdl_wait();
-  const int row = blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  const __nv_bfloat16* xr = x + static_cast<long long>(row) * d;
-  float ss = 0.f;
-  for (int i = lane; i < d; i += 32) {
-    const float a = __bfloat162float(xr[i]);
-    ss = fmaf(a, a, ss);
-  }
-  ss = warp_sum(ss);
-  if (lane == 0) {
-    r[row] = rsqrtf(ss / static_cast<float>(d) + eps);
-    if (ticket != nullptr) ticket[row] = 0;
-  }
-}
-
 }  // namespace
-
-int rms_rowscale(const Ctx& c, const void* x, float* r, int* ticket, int rows, int d, float eps) {
-  if (rows == 0) return LLAMA_OK;
-  const dim3 grid((rows + kWarpsPerCta - 1) / kWarpsPerCta), block(kWarpsPerCta * 32);
-  const uint4* xv = static_cast<const uint4*>(x);
-  const float inv_d = 1.0f / static_cast<float>(d);
-  switch (d % 256 == 0 && d <= 4096 ? d / 256 : 0) {
-    case 1: launch_pdl(c, rms_rowscale_kernel<1>, grid, block, 0, xv, r, ticket, rows, inv_d, eps); break;
-    case 2: launch_pdl(c, rms_rowscale_kernel<2>, grid, block, 0, xv, r, ticket, rows, inv_d, eps); break;
-    case 4: launch_pdl(c, rms_rowscale_kernel<4>, grid, block, 0, xv, r, ticket, rows, inv_d, eps); break;
-    case 8: launch_pdl(c, rms_rowscale_kernel<8>, grid, block, 0, xv, r, ticket, rows, inv_d, eps); break;
-    case 16: launch_pdl(c, rms_rowscale_kernel<16>, grid, block, 0, xv, r, ticket, rows, inv_d, eps); break;
-    default:
-      launch_pdl(c, rms_rowscale_generic_kernel, grid, block, 0, static_cast<const __nv_bfloat16*>(x), r, ticket,
-                 rows, d, eps);
-  }
-  return after_launch(c);
-}
 
 int rmsnorm(const Ctx& c, const void* x, const void* gamma, void* y, int rows, int d, float eps, int dtype) {
   if (rows == 0) return LLAMA_OK;

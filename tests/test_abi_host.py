@@ -71,9 +71,7 @@ def _bytes(native, dims, B=2, S=64):
 
 def test_workspace_sizes_and_dims_validation(native):
     rc, n = _bytes(native, _dims(native))
-    assert rc == 0 and n >= 2 * 2 * 64 * (256 + 2 * 512 + 384)   # h, q, o, a (bf16 norms stay inside the GEMMs)
-    rc32, n32 = _bytes(native, _dims(native, dtype=0))
-    assert rc32 == 0 and n32 >= 4 * 2 * 64 * (2 * 256 + 2 * 512 + 384)   # fp32 adds the normed activation
+    assert rc == 0 and n >= 2 * 2 * 64 * (2 * 256 + 2 * 512 + 384)   # xn, h, q, o, a
     assert _bytes(native, _dims(native, n_kv_heads=3))[0] == -1     # H % G != 0
     assert _bytes(native, _dims(native, head_dim=15, dtype=0))[0] == -1   # odd D
     assert _bytes(native, _dims(native, head_dim=64))[0] == -2      # bf16 tile path needs D = 128
@@ -144,9 +142,8 @@ def test_workspace_layout_names_disjoint_regions_inside_the_workspace(native):
         rc, total = _bytes(native, dims, B, S)
         assert rc == 0
         es = 2 if dt == 1 else 4
-        sizes = [B * 4 * S * 128 * es, B * S * 4 * 128 * es, B * S * 256 * es, B * S * 384 * es]   # q, o, h, a
-        if dt == 1:
-            sizes.append(B * S * 4)                                                           # row scales of h
+        sizes = [B * 4 * S * 128 * es, B * S * 4 * 128 * es, B * S * 256 * es, B * S * 384 * es,
+                 B * S * 256 * es]                                                         # q, o, h, a, hn
         spans = sorted((o, o + n) for o, n in zip(offs, sizes))
         assert all(o % 256 == 0 for o in offs)
         assert all(a_end <= b_start for (_, a_end), (b_start, _) in zip(spans, spans[1:]))
@@ -157,22 +154,25 @@ def test_workspace_layout_names_disjoint_regions_inside_the_workspace(native):
 
 def test_norm_fused_steps_reject_bad_arguments_without_a_gpu(native):
     lib = native.lib()
-    buf = (ctypes.c_uint8 * 4096)()
+    buf = (ctypes.c_uint8 * 8192)()
     p = (ctypes.addressof(buf) + 255) // 256 * 256
-    assert lib.llama_norm_linear_bf16(p, p, 1e-5, p, p, 4, 16, 96, 0, p, None) == -2       # K % 64
-    assert lib.llama_norm_linear_bf16(p, None, 1e-5, p, p, 4, 16, 64, 0, p, None) == -1    # no gamma
-    assert lib.llama_norm_linear_bf16(p, p, 1e-5, p, p, 4, 16, 64, 0, None, None) == -1   # no row scales
-    assert lib.llama_norm_linear_bf16(p, p, -1.0, p, p, 4, 16, 64, 0, p, None) == -1       # eps < 0
-    assert lib.llama_norm_linear_bf16(p, p + 8, 1e-5, p, p, 4, 16, 64, 0, p, None) == -1   # gamma misaligned
-    assert lib.llama_norm_linear_swiglu(p, p, 1e-5, p, p, p, 4, 96, 64, p, None) == -2     # I % 128
-    assert lib.llama_norm_linear_swiglu(p, p, 1e-5, p, p, None, 4, 128, 64, p, None) == -1
+    xn, sy = p + 4096, p + 2048
+    assert lib.llama_norm_linear_bf16(p, p, 1e-5, p, p, 4, 16, 60, 0, xn, sy, None) == -2       # K % 8
+    assert lib.llama_norm_linear_bf16(p, None, 1e-5, p, p, 4, 16, 64, 0, xn, sy, None) == -1    # no gamma
+    assert lib.llama_norm_linear_bf16(p, p, 1e-5, p, p, 4, 16, 64, 0, None, sy, None) == -1     # no xn
+    assert lib.llama_norm_linear_bf16(p, p, 1e-5, p, p, 4, 16, 64, 0, xn, None, None) == -1     # no sync
+    assert lib.llama_norm_linear_bf16(p, p, 1e-5, p, p, 4, 16, 64, 0, p, sy, None) == -1        # xn aliases A
+    assert lib.llama_norm_linear_bf16(p, p, -1.0, p, p, 4, 16, 64, 0, xn, sy, None) == -1       # eps < 0
+    assert lib.llama_norm_linear_bf16(p, p + 8, 1e-5, p, p, 4, 16, 64, 0, xn, sy, None) == -1   # gamma misaligned
+    assert lib.llama_norm_linear_swiglu(p, p, 1e-5, p, p, p, 4, 96, 64, xn, sy, None) == -2     # I % 128
+    assert lib.llama_norm_linear_swiglu(p, p, 1e-5, p, p, None, 4, 128, 64, xn, sy, None) == -1
     dims = _dims(native)
     cache = native.KVCache(p, p, 64)
     call = lambda **kw: lib.llama_norm_qkv_rope(ctypes.byref(kw.get("dims", dims)), p, kw.get("g", p), p, p, p, p, p,
-                                                kw.get("max_pos", 64), cache, p, 1, kw.get("S", 8), kw.get("r", p),
-                                                None)
+                                                kw.get("max_pos", 64), cache, p, 1, kw.get("S", 8), kw.get("xn", xn),
+                                                sy, None)
     assert call(g=None) == -1
-    assert call(r=None) == -1
+    assert call(xn=None) == -1
     assert call(S=65) == -1                      # S > max_T
     assert call(max_pos=4) == -1                 # S > max_pos
     assert call(dims=_dims(native, head_dim=16, d_model=64, n_heads=4, n_kv_heads=2, d_inter=176, dtype=0)) == -2

@@ -234,63 +234,60 @@ def _norm_inputs(rng, M, K, scale=3.0):
     return x, g
 
 
-def _check_row_scales(r, x64, eps):
-    ref = 1.0 / np.sqrt(np.mean(x64 * x64, axis=-1) + eps)
-    assert np.allclose(f64(r), ref, rtol=1e-5, atol=0), "row scales"
+def _check_prologue(api, xd, gd, xn, eps, what):
+    """The GEMM prologue's normalised rows are bit for bit those of the standalone RMSNorm (same
+    arithmetic, same order), and within one rounding of the oracle's."""
+    y = torch.empty_like(xd)
+    api.rmsnorm(xd, gd, y, eps)
+    assert torch.equal(xn.view(-1), y.view(-1)), f"{what}: prologue rows differ from llama_rmsnorm"
 
 
-def _operand_from_gpu_scales(x, g, r):
-    """The bf16 operand the norm-fused GEMM multiplies, rebuilt from the GPU's row scales r:
-    gamma * (x * r) with the two fp32 products rounded as IEEE fp32 multiplies round, then to
-    bf16.  (The oracle's fp64 normalised row rounds to the other bf16 neighbour at ~1e-4 of the
-    elements; a flip of a large element moves the product by more than one ulp, so the one-ulp
-    check of the GEMM itself uses this operand.)"""
-    x32 = x.f64().astype(np.float32)
-    t = (x32 * f64(r).astype(np.float32)[:, None]).astype(np.float32)
-    t = (g.f64().astype(np.float32)[None, :] * t).astype(np.float32)
-    return oracle.round_bf16(t.astype(np.float64))
-
-
-@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (300, 520, 256), (1000, 2048, 4096), (7, 32000, 4096)])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (300, 520, 256), (1000, 2048, 4096), (7, 32000, 4096),
+                                   (2048, 8192, 4096), (130, 264, 200)])
 @pytest.mark.parametrize("out_f32", [False, True])
 def test_norm_linear_fused(api, M, N, K, out_f32):
-    # RMSNorm inside the GEMM: the tensor cores multiply bf16(gamma * (x * r)), the value a
-    # standalone RMSNorm stores, so the result is the oracle's RMSNorm (rounded where it stores
-    # its output) followed by the product
+    # RMSNorm in the GEMM's prologue: the GEMM normalises the rows into xn and multiplies xn, so
+    # the result is the oracle's RMSNorm (rounded where it stores its output) followed by the
+    # product.  (2048 x 8192 x 4096: several tiles per CTA; K = 64, 200: the generic prologue.)
     rng = _rng(M * 3 + N + K)
     x, g = _norm_inputs(rng, M, K)
     w = bf16_stored(0.02 * rng.standard_normal((N, K)))
     c = torch.empty(M, N, dtype=torch.float32 if out_f32 else torch.bfloat16, device="cuda")
-    r = api.norm_linear_bf16(to_dev(x), to_dev(g), 1e-5, to_dev(w), c)
+    xd, gd = to_dev(x), to_dev(g)
+    xn = api.norm_linear_bf16(xd, gd, 1e-5, to_dev(w), c)
     assert api.device_status() == 0
-    xn = oracle.round_bf16(oracle.rms_norm(x.f64(), g.f64(), 1e-5))
-    ref = oracle.linear(xn, w.f64())
+    xn_ref = oracle.round_bf16(oracle.rms_norm(x.f64(), g.f64(), 1e-5))
+    assert_close(f64(xn), xn_ref, TOL["bf16"], f"norm prologue {M}x{K}")
+    ref = oracle.linear(xn_ref, w.f64())
     assert_close(f64(c), ref, 1e-3 if out_f32 else TOL["bf16"], f"norm + linear {M}x{N}x{K}")
-    _check_row_scales(r, x.f64(), 1e-5)
     if not out_f32:
-        _one_ulp(f64(c), oracle.linear(_operand_from_gpu_scales(x, g, r), w.f64()), f"norm + linear {M}x{N}x{K}")
+        _one_ulp(f64(c), oracle.linear(f64(xn), w.f64()), f"norm + linear {M}x{N}x{K}")
+    if K % 256 == 0:
+        _check_prologue(api, xd, gd, xn, 1e-5, f"norm + linear {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("M,I,K", [(130, 384, 256), (1000, 11008, 4096), (64, 1024, 4096)])
+@pytest.mark.parametrize("M,I,K", [(130, 384, 256), (1000, 11008, 4096), (64, 1024, 4096), (2048, 11008, 4096)])
 def test_norm_linear_swiglu_fused(api, M, I, K):
     rng = _rng(M + I + K)
     x, g = _norm_inputs(rng, M, K)
     wg = bf16_stored(0.02 * rng.standard_normal((I, K)))
     wu = bf16_stored(0.02 * rng.standard_normal((I, K)))
     a = torch.empty(M, I, dtype=torch.bfloat16, device="cuda")
-    r = api.norm_linear_swiglu(to_dev(x), to_dev(g), 1e-6, to_dev(wg), to_dev(wu), a)
+    xd, gd = to_dev(x), to_dev(g)
+    xn = api.norm_linear_swiglu(xd, gd, 1e-6, to_dev(wg), to_dev(wu), a)
     assert api.device_status() == 0
-    xn = oracle.round_bf16(oracle.rms_norm(x.f64(), g.f64(), 1e-6))
-    ref = oracle.silu(oracle.linear(xn, wg.f64())) * oracle.linear(xn, wu.f64())
+    xn_ref = oracle.round_bf16(oracle.rms_norm(x.f64(), g.f64(), 1e-6))
+    ref = oracle.silu(oracle.linear(xn_ref, wg.f64())) * oracle.linear(xn_ref, wu.f64())
     assert_close(f64(a), ref, TOL["bf16"], f"norm + gate/up {M}x{I}x{K}")
-    _check_row_scales(r, x.f64(), 1e-6)
-    xg = _operand_from_gpu_scales(x, g, r)
+    xg = f64(xn)
     _one_ulp(f64(a), oracle.silu(oracle.linear(xg, wg.f64())) * oracle.linear(xg, wu.f64()),
              f"norm + gate/up {M}x{I}x{K}")
+    _check_prologue(api, xd, gd, xn, 1e-6, f"norm + gate/up {M}x{I}x{K}")
 
 
 @pytest.mark.parametrize("d,H,G,B,S,rope", [(256, 4, 2, 2, 130, "even_odd"), (512, 8, 1, 1, 300, "even_odd"),
-                                            (4096, 32, 8, 1, 256, "even_odd"), (4096, 32, 8, 3, 700, "even_odd")])
+                                            (256, 4, 2, 2, 150, "half"), (4096, 32, 8, 1, 256, "even_odd"),
+                                            (4096, 32, 8, 3, 700, "even_odd")])
 def test_norm_qkv_rope_fused(api, d, H, G, B, S, rope):
     rng = _rng(d + H * 7 + G + B * 13 + S)
     D, T_max = 128, S + 9
@@ -305,35 +302,20 @@ def test_norm_qkv_rope_fused(api, d, H, G, B, S, rope):
     vc = torch.full_like(kc, float("nan"))
     q = torch.empty(B, H, S, D, dtype=torch.bfloat16, device="cuda")
     dims = api.Dims(d, H, G, D, 128, 1e-5, torch.bfloat16, 1 if rope == "half" else 0)
-    r = api.norm_qkv_rope(dims, to_dev(x).view(B, S, d), to_dev(g), to_dev(wq), to_dev(wk), to_dev(wv), cos, sin,
-                          kc, vc, q)
+    xd, gd = to_dev(x), to_dev(g)
+    xn = api.norm_qkv_rope(dims, xd.view(B, S, d), gd, to_dev(wq), to_dev(wk), to_dev(wv), cos, sin, kc, vc, q)
     assert api.device_status() == 0
-    xn = oracle.round_bf16(oracle.rms_norm(x.f64(), g.f64(), 1e-5)).reshape(B, S, d)
+    xn_ref = oracle.round_bf16(oracle.rms_norm(x.f64(), g.f64(), 1e-5)).reshape(B, S, d)
     rot = oracle.layer.ROPE_STYLES[rope]
     cc, ss = c32.astype(np.float64)[:S][None, None], s32.astype(np.float64)[:S][None, None]
-    q_ref = rot(oracle.linear(xn, wq.f64()).reshape(B, S, H, D).transpose(0, 2, 1, 3), cc, ss)
-    k_ref = rot(oracle.linear(xn, wk.f64()).reshape(B, S, G, D).transpose(0, 2, 1, 3), cc, ss)
-    v_ref = oracle.linear(xn, wv.f64()).reshape(B, S, G, D).transpose(0, 2, 1, 3)
+    q_ref = rot(oracle.linear(xn_ref, wq.f64()).reshape(B, S, H, D).transpose(0, 2, 1, 3), cc, ss)
+    k_ref = rot(oracle.linear(xn_ref, wk.f64()).reshape(B, S, G, D).transpose(0, 2, 1, 3), cc, ss)
+    v_ref = oracle.linear(xn_ref, wv.f64()).reshape(B, S, G, D).transpose(0, 2, 1, 3)
     assert_close(f64(q), q_ref, TOL["bf16"], "norm + qkv: q")
     assert_close(f64(kc)[:, :, :S], k_ref, TOL["bf16"], "norm + qkv: k in the cache")
     assert_close(f64(vc)[:, :, :S], v_ref, TOL["bf16"], "norm + qkv: v in the cache")
     assert torch.isnan(kc[:, :, S:].float()).all() and torch.isnan(vc[:, :, S:].float()).all()
-    _check_row_scales(r, x.f64(), 1e-5)
-    xg = _operand_from_gpu_scales(x, g, r).reshape(B, S, d)
+    xg = f64(xn).reshape(B, S, d)
     _one_ulp(f64(q), rot(oracle.linear(xg, wq.f64()).reshape(B, S, H, D).transpose(0, 2, 1, 3), cc, ss),
              "norm + qkv: q")
-
-
-def test_norm_qkv_rope_refuses_half_split_pairs(api):
-    # the fused QKV tiles are 224 columns, not head-aligned: the half-split layer runs a standalone
-    # RMSNorm and llama_qkv_rope instead (covered by the half-split layer tests)
-    from llama_decoder_block_gb300 import _native as N
-    dims = api.Dims(256, 4, 2, 128, 128, 1e-5, torch.bfloat16, 1)
-    x = torch.zeros(1, 8, 256, dtype=torch.bfloat16, device="cuda")
-    w = torch.zeros(512, 256, dtype=torch.bfloat16, device="cuda")
-    cos = torch.zeros(8, 64, dtype=torch.float32, device="cuda")
-    kc = torch.zeros(1, 2, 8, 128, dtype=torch.bfloat16, device="cuda")
-    q = torch.empty(1, 4, 8, 128, dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(N.LlamaError) as e:
-        api.norm_qkv_rope(dims, x, x[0, 0], w, w[:256], w[:256], cos, cos, kc, kc, q)
-    assert e.value.code == -2
+    _check_prologue(api, xd, gd, xn, 1e-5, "norm + qkv")
