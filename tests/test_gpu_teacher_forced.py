@@ -82,11 +82,15 @@ def check_layer_steps(L, w64, x_rows, gpu, c64, s64, b_idx, s_idx, what):
     h_ref = x_rows + oracle.linear(gpu["o"], w64["wo"])
     assert_close(gpu["h"], h_ref, tol, f"{what}: o_proj + residual")
 
-    # ffn RMSNorm (the gate/up GEMM's prologue), from the GPU's h
+    # ffn RMSNorm (the gate/up GEMM's prologue), from the GPU's h; then gate/up + SiLU * up from
+    # the GPU's normalised h (or, where those rows were overwritten, from the oracle's)
     hn_ref = oracle.rms_norm(gpu["h"], w64["ffn_norm"], eps)
-    assert_close(gpu["hn"], hn_ref, tol, f"{what}: ffn RMSNorm (GEMM prologue)")
-    # gate/up + SiLU * up, from the GPU's normalised h
-    a_ref = oracle.silu(oracle.linear(gpu["hn"], w64["w_gate"])) * oracle.linear(gpu["hn"], w64["w_up"])
+    if gpu.get("hn") is not None:
+        assert_close(gpu["hn"], hn_ref, tol, f"{what}: ffn RMSNorm (GEMM prologue)")
+        hn = gpu["hn"]
+    else:
+        hn = oracle.round_bf16(hn_ref)
+    a_ref = oracle.silu(oracle.linear(hn, w64["w_gate"])) * oracle.linear(hn, w64["w_up"])
     assert_close(gpu["a"], a_ref, tol, f"{what}: gate/up + SiLU*up")
 
     # down + residual, from the GPU's h and a
@@ -179,12 +183,15 @@ def test_stack_layers_teacher_forced(api):
         if l == 0:   # the embedding gather is exact
             assert np.array_equal(x_in, glob["embed"].f64()[glob["tokens"][b_idx, s_idx]])
         gpu = gpu_rows(inter, kc, vc, inter["out"], b_idx, s_idx)
+        fn_rows = gpu.pop("hn")   # after the stack: the final norm's rows (the LM head's prologue wrote last)
         check_layer_steps(L, host_layers[l], x_in, gpu, c64, s64, b_idx, s_idx, f"stack layer {l}")
         del caches[:]
         if l == check_at[-1]:
-            # final RMSNorm + LM head (one fused GEMM on the GPU), from the GPU's last output
-            xn = oracle.round_bf16(oracle.rms_norm(gpu["out"], glob["final_norm"].f64(), L.rms_eps))
-            ref = oracle.linear(xn, glob["lm_head"].f64())
-            assert_close(f64(logits)[b_idx, s_idx], ref, TOL["bf16"], "stack: final norm + LM head")
+            # final RMSNorm (the LM head GEMM's prologue) from the GPU's last output, then the LM
+            # head from the GPU's normalised rows
+            fn_ref = oracle.rms_norm(gpu["out"], glob["final_norm"].f64(), L.rms_eps)
+            assert_close(fn_rows, fn_ref, TOL["bf16"], "stack: final RMSNorm (GEMM prologue)")
+            ref = oracle.linear(fn_rows, glob["lm_head"].f64())
+            assert_close(f64(logits)[b_idx, s_idx], ref, TOL["bf16"], "stack: LM head")
         del ws, st
         torch.cuda.empty_cache()
