@@ -95,7 +95,7 @@ __device__ __forceinline__ float warp_sum32(float v) {
 // i * 32 + lane of its row (the order of the standalone RMSNorm kernel, so both give the same
 // bits); the next row's loads are issued before this row's reduction.
 template <int VPL>
-__device__ __forceinline__ void prologue_rows(const Params& p, int gw, int nw, int lane) {
+__device__ __noinline__ void prologue_rows(const Params& p, int gw, int nw, int lane) {
   const uint4* x = reinterpret_cast<const uint4*>(p.pro_x);
   const uint4* g = reinterpret_cast<const uint4*>(p.pro_gamma);
   uint4* y = reinterpret_cast<uint4*>(p.pro_out);
@@ -306,11 +306,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // inputs written by the previous kernel are read from here on (the producer waits below,
   // after issuing the weight tiles that depend on nothing in flight)
   if (!(warp == 0 && lane == 0)) pdl_wait();
-  // prologue RMSNorm: the epilogue warps normalise their share of the rows of A (the forms whose A
-  // can be a normalised activation)
+  // Prologue RMSNorm (the forms whose A can be a normalised activation): every warp of the CTA
+  // normalises its share of the rows of A before taking up its role (the producer after issuing
+  // its first weight tiles), then counts itself in.
   constexpr bool kPrologue = EPI == EPI_BF16 || EPI == EPI_F32 || EPI == EPI_SWIGLU || EPI == EPI_QKV;
-  if (kPrologue && p.pro_out != nullptr && warp >= 2) {
-    const int gw = static_cast<int>(blockIdx.x) * 4 + (warp - 2), nw = static_cast<int>(gridDim.x) * 4;
+  const bool prologue = kPrologue && p.pro_out != nullptr;
+  auto run_prologue = [&]() {
+    const int gw = static_cast<int>(blockIdx.x) * (NUM_THREADS / 32) + warp;
+    const int nw = static_cast<int>(gridDim.x) * (NUM_THREADS / 32);
     switch (p.K % 256 == 0 && p.K <= 4096 ? p.K / 256 : 0) {
       case 1: prologue_rows<1>(p, gw, nw, lane); break;
       case 2: prologue_rows<2>(p, gw, nw, lane); break;
@@ -324,11 +327,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __threadfence();
     __syncwarp();
     if (lane == 0) atomicAdd(p.pro_count, 1);
-  }
+  };
+  if (prologue && warp >= 1) run_prologue();
 
   if (warp == 0) {
-    if (lane == 0) {
-      // ------------------------------------------------------------ TMA producer
+    {
+      // ------------------------------------------------------------ TMA producer (lane 0)
       auto load_a = [&](int stage, int kb, int mb) {
         int a_map, a_row;
         resolve_rows(p.amap, mb * BM, a_map, a_row);
@@ -367,7 +371,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // the first STAGES k-blocks' weight tiles go out before the dependency wait: the ring
       // starts empty, so these stages need no empty-barrier wait
       int pre = 0;
-      if (p.weight_first != 0) {
+      if (lane == 0 && p.weight_first != 0) {
         for (int t = blockIdx.x; t < num_tiles && pre < STAGES; t += gridDim.x) {
           int mb, nb, split;
           tile_coords(p, t, mb, nb, split);
@@ -380,41 +384,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
       }
-      pdl_wait();
-      bool ok = true;
-      if (kPrologue && p.pro_out != nullptr) {
-        // every CTA's prologue warps have written their rows of A
-        ok = wait_count(p.pro_count, 4 * static_cast<int>(gridDim.x), p.status, abort_flag);
-        asm volatile("fence.proxy.async.global;" ::: "memory");
-      }
-      int stage = 0, step = 0;
-      uint32_t phase = 0;
-      uint32_t used_mask = 0, last_parity = 0;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-        int mb, nb, split;
-        tile_coords(p, t, mb, nb, split);
-        const int kb0 = split * p.kb_per_split;
-        const int kb1 = min(kb0 + p.kb_per_split, p.num_kb);
-        for (int kb = kb0; kb < kb1; ++kb, ++step) {
-          if (step < pre) {   // the weight half of this stage is already on its way
-            if (p.weight_first == 1) load_b(stage, kb, nb);
-            else load_a(stage, kb, mb);
-          } else {
-            if (!mbar_wait(smem_u32(empty_bar + stage), phase ^ 1u, p.status, abort_flag)) { ok = false; break; }
-            mbar_expect_tx(smem_u32(full_bar + stage), STAGE_TX);
-            load_a(stage, kb, mb);
-            load_b(stage, kb, nb);
-          }
-          used_mask |= 1u << stage;
-          last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      if (lane == 0) pdl_wait();
+      __syncwarp();
+      if (prologue) run_prologue();
+      if (lane == 0) {
+        bool ok = true;
+        if (prologue) {
+          // every warp of the grid has written its rows of A
+          ok = wait_count(p.pro_count, (NUM_THREADS / 32) * static_cast<int>(gridDim.x), p.status, abort_flag);
+          asm volatile("fence.proxy.async.global;" ::: "memory");
         }
-      }
-      if (!ok) {
-        // leave no copy in flight: wait (bounded) for the last load into every stage used
-        for (int s = 0; s < STAGES; ++s)
-          if (used_mask & (1u << s))
-            mbar_wait_slow(smem_u32(full_bar + s), (last_parity >> s) & 1u, nullptr, nullptr, kWaitBudgetNs);
+        int stage = 0, step = 0;
+        uint32_t phase = 0;
+        uint32_t used_mask = 0, last_parity = 0;
+        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+          int mb, nb, split;
+          tile_coords(p, t, mb, nb, split);
+          const int kb0 = split * p.kb_per_split;
+          const int kb1 = min(kb0 + p.kb_per_split, p.num_kb);
+          for (int kb = kb0; kb < kb1; ++kb, ++step) {
+            if (step < pre) {   // the weight half of this stage is already on its way
+              if (p.weight_first == 1) load_b(stage, kb, nb);
+              else load_a(stage, kb, mb);
+            } else {
+              if (!mbar_wait(smem_u32(empty_bar + stage), phase ^ 1u, p.status, abort_flag)) { ok = false; break; }
+              mbar_expect_tx(smem_u32(full_bar + stage), STAGE_TX);
+              load_a(stage, kb, mb);
+              load_b(stage, kb, nb);
+            }
+            used_mask |= 1u << stage;
+            last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          }
+        }
+        if (!ok) {
+          // leave no copy in flight: wait (bounded) for the last load into every stage used
+          for (int s = 0; s < STAGES; ++s)
+            if (used_mask & (1u << s))
+              mbar_wait_slow(smem_u32(full_bar + s), (last_parity >> s) & 1u, nullptr, nullptr, kWaitBudgetNs);
+        }
       }
     }
   } else if (warp == 1) {
