@@ -11,8 +11,12 @@
 // CTA's total is close to the mean; the next item's Q and K/V loads overlap the current item's
 // last products.  Both query tiles read every K/V tile once from shared memory.
 //   warp 0      TMA: an item's two Q tiles (once the previous item's last S product has read
-//               its own), then K_j, V_j (128 keys each) into a 2-stage ring straight from
-//               the [B, G, max_T, D] cache
+//               its own), then K_j, V_j (128 keys each) into 2-stage rings straight from the
+//               [B, G, max_T, D] cache: K and V into 2-stage rings of their own, each stage
+//               released as soon as its last reader is done (K_j after the S products of key
+//               tile j, V_j after its P V products), so each K tile goes out well ahead of its
+//               S products (the wait for the next S was half of a softmax warp's time with one
+//               2-stage ring for both)
 //   warp 1      TMEM allocator and MMA issuer, ping-pong between the two tiles:
 //               S_t = Q_t K_j^T into TMEM; once the softmax of tile t has written P_t,
 //               O_t += P_t V_j with P_t read from TMEM and V as an MN-major smem operand,
@@ -46,6 +50,7 @@ constexpr int HD = 128;
 constexpr int CHUNK = 128 * 128;      // one 64-column half of a 128-row bf16 tile
 constexpr int TILE = 2 * CHUNK;       // 128 rows x 128 columns bf16
 constexpr int NUM_THREADS = 384;
+constexpr int K_STAGES = 2;           // K ring (3 stages measured no faster); V ring: 2 stages
 constexpr uint32_t TMEM_COLS = 512;   // S/P of tile t at [128t, 128t+128), O of tile t at 256 + 128t
 constexpr float kRescaleLog2 = 8.0f;  // rescale O when the max grows by more than 2^8
 
@@ -111,19 +116,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem;                   // 2 tiles
-  uint8_t* sK = smem + 2 * TILE;        // 2 stages
-  uint8_t* sV = smem + 4 * TILE;        // 2 stages
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 6 * TILE);
+  uint8_t* sQ = smem;                               // 2 tiles
+  uint8_t* sK = smem + 2 * TILE;                    // K_STAGES stages
+  uint8_t* sV = smem + (2 + K_STAGES) * TILE;       // 2 stages
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (4 + K_STAGES) * TILE);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;         // [2] per stage
-  uint64_t* kv_empty = bars + 3;        // [2] per stage
-  uint64_t* s_full = bars + 5;          // [2] per tile
-  uint64_t* p_full = bars + 7;          // [2] per tile
-  uint64_t* o_done = bars + 9;          // [2] per tile
-  uint64_t* drain = bars + 11;
-  uint64_t* q_empty = bars + 12;        // the Q tiles of an item may be overwritten
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
+  uint64_t* s_full = bars + 1;          // [2] per tile
+  uint64_t* p_full = bars + 3;          // [2] per tile
+  uint64_t* o_done = bars + 5;          // [2] per tile
+  uint64_t* drain = bars + 7;
+  uint64_t* q_empty = bars + 8;         // the Q tiles of an item may be overwritten
+  uint64_t* v_full = bars + 9;          // [2] per V stage
+  uint64_t* v_empty = bars + 11;        // [2] per V stage
+  uint64_t* k_full = bars + 13;         // [K_STAGES] per K stage
+  uint64_t* k_empty = bars + 13 + K_STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13 + 2 * K_STAGES);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -132,9 +139,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(q_full), 1);
     mbar_init(smem_u32(q_empty), 1);
+    for (int i = 0; i < K_STAGES; ++i) {
+      mbar_init(smem_u32(k_full + i), 1);
+      mbar_init(smem_u32(k_empty + i), 1);
+    }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(kv_full + i), 1);
-      mbar_init(smem_u32(kv_empty + i), 1);
+      mbar_init(smem_u32(v_full + i), 1);
+      mbar_init(smem_u32(v_empty + i), 1);
       mbar_init(smem_u32(s_full + i), 1);
       mbar_init(smem_u32(p_full + i), 4);
       mbar_init(smem_u32(o_done + i), 1);
@@ -165,7 +176,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       // ------------------------------------------------------------ TMA producer
       bool ok = true;
-      uint32_t kvc = 0, qc = 0;
+      uint32_t kvc = 0, qc = 0, kc_issued = 0, vc_issued = 0;
       for (int r = 0; ok; ++r) {
         const int i = item_of(c, r);
         if (i >= p.n_items) break;
@@ -184,22 +195,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ++qc;
         const int plane = it.b * p.G + it.g;
         for (int j = 0; j < it.nt; ++j, ++kvc) {
-          const uint32_t st = kvc & 1;
-          if (!mbar_wait(smem_u32(kv_empty + st), ((kvc >> 1) & 1) ^ 1u, p.status, abort_flag)) { ok = false; break; }
-          const uint32_t fb = smem_u32(kv_full + st);
-          mbar_expect_tx(fb, 2 * TILE);
+          const uint32_t st = kvc & 1, ph = ((kvc >> 1) & 1) ^ 1u;
+          const uint32_t kst = kvc % K_STAGES, kph = ((kvc / K_STAGES) & 1) ^ 1u;
           const int row = j * BKV;
-          tma_load_3d(smem_u32(sK + st * TILE), &tmK, fb, 0, row, plane);
-          tma_load_3d(smem_u32(sK + st * TILE + CHUNK), &tmK, fb, 64, row, plane);
-          tma_load_3d(smem_u32(sV + st * TILE), &tmV, fb, 0, row, plane);
-          tma_load_3d(smem_u32(sV + st * TILE + CHUNK), &tmV, fb, 64, row, plane);
+          if (!mbar_wait(smem_u32(k_empty + kst), kph, p.status, abort_flag)) { ok = false; break; }
+          const uint32_t kb = smem_u32(k_full + kst);
+          mbar_expect_tx(kb, TILE);
+          tma_load_3d(smem_u32(sK + kst * TILE), &tmK, kb, 0, row, plane);
+          tma_load_3d(smem_u32(sK + kst * TILE + CHUNK), &tmK, kb, 64, row, plane);
+          ++kc_issued;
+          if (!mbar_wait(smem_u32(v_empty + st), ph, p.status, abort_flag)) { ok = false; break; }
+          const uint32_t vb = smem_u32(v_full + st);
+          mbar_expect_tx(vb, TILE);
+          tma_load_3d(smem_u32(sV + st * TILE), &tmV, vb, 0, row, plane);
+          tma_load_3d(smem_u32(sV + st * TILE + CHUNK), &tmV, vb, 64, row, plane);
+          ++vc_issued;
         }
       }
       if (!ok) {
-        // leave no copy in flight: the last Q load and the last two K/V loads
+        // leave no copy in flight: the last Q load and the last two K and V loads
         if (qc > 0) mbar_wait_slow(smem_u32(q_full), (qc - 1) & 1, nullptr, nullptr, kWaitBudgetNs);
-        for (uint32_t g = (kvc > 2 ? kvc - 2 : 0); g < kvc; ++g)
-          mbar_wait_slow(smem_u32(kv_full + (g & 1)), (g >> 1) & 1, nullptr, nullptr, kWaitBudgetNs);
+        for (uint32_t g = (kc_issued > K_STAGES ? kc_issued - K_STAGES : 0); g < kc_issued; ++g)
+          mbar_wait_slow(smem_u32(k_full + g % K_STAGES), (g / K_STAGES) & 1, nullptr, nullptr, kWaitBudgetNs);
+        for (uint32_t g = (vc_issued > 2 ? vc_issued - 2 : 0); g < vc_issued; ++g)
+          mbar_wait_slow(smem_u32(v_full + (g & 1)), (g >> 1) & 1, nullptr, nullptr, kWaitBudgetNs);
       }
     }
   } else if (warp == 1) {
@@ -207,8 +226,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // ------------------------------------------------------------ MMA issuer
       constexpr uint32_t IDESC_QK = idesc_bf16(128, 128, false);
       constexpr uint32_t IDESC_PV = idesc_bf16(128, 128, true);
-      auto issue_s = [&](int t, uint32_t st) {
-        const uint32_t aq = smem_u32(sQ + t * TILE), bk = smem_u32(sK + st * TILE);
+      auto issue_s = [&](int t, uint32_t kst) {
+        const uint32_t aq = smem_u32(sQ + t * TILE), bk = smem_u32(sK + kst * TILE);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * CHUNK + (kk & 3) * 32;
@@ -238,23 +257,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!it.hasA) continue;
         auto active = [&](int t, int j) { return j < it.nkt[t]; };
         if (!mbar_wait(smem_u32(q_full), qc & 1, p.status, abort_flag) ||
-            !mbar_wait(smem_u32(kv_full + (kvc & 1)), (kvc >> 1) & 1, p.status, abort_flag)) {
+            !mbar_wait(smem_u32(k_full + kvc % K_STAGES), (kvc / K_STAGES) & 1, p.status, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
         // the Q tiles are free for the next item once this item's last S product is done:
-        // commit q_empty right after issuing it
+        // commit q_empty right after issuing it; K_j is free once the S products of key tile j
+        // are (the last one is tile B's when B reads key tile j, else tile A's)
         int s_left = it.nkt[0] + it.nkt[1];
-        auto issue_s_counted = [&](int t, uint32_t st) {
-          issue_s(t, st);
+        auto issue_s_counted = [&](int t, int j, uint32_t kst) {
+          issue_s(t, kst);
           if (--s_left == 0) tc_commit(smem_u32(q_empty));
+          if (t == 1 || !active(1, j)) tc_commit(smem_u32(k_empty + kst));
         };
-        issue_s_counted(0, kvc & 1);
-        if (it.hasB) issue_s_counted(1, kvc & 1);
+        issue_s_counted(0, 0, kvc % K_STAGES);
+        if (it.hasB) issue_s_counted(1, 0, kvc % K_STAGES);
         issued = true;
         for (int j = 0; j < it.nt && ok; ++j) {
           const uint32_t g = kvc + j;
+          if (!mbar_wait(smem_u32(v_full + (g & 1)), (g >> 1) & 1, p.status, abort_flag)) { ok = false; break; }
           for (int t = 0; t < 2 && ok; ++t) {
             if (!active(t, j)) continue;
             if (!mbar_wait(smem_u32(p_full + t), pc[t] & 1, p.status, abort_flag)) { ok = false; break; }
@@ -262,15 +284,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_after();
             issue_pv(t, g & 1, j == 0);
             if (active(t, j + 1)) {
-              if (!mbar_wait(smem_u32(kv_full + ((g + 1) & 1)), ((g + 1) >> 1) & 1, p.status, abort_flag)) {
+              const uint32_t gn = g + 1;
+              if (!mbar_wait(smem_u32(k_full + gn % K_STAGES), (gn / K_STAGES) & 1, p.status, abort_flag)) {
                 ok = false;
                 break;
               }
               tc_fence_after();
-              issue_s_counted(t, (g + 1) & 1);
+              issue_s_counted(t, j + 1, gn % K_STAGES);
             }
           }
-          if (ok) tc_commit(smem_u32(kv_empty + (g & 1)));
+          if (ok) tc_commit(smem_u32(v_empty + (g & 1)));
         }
         if (!ok) break;
         kvc += it.nt;
@@ -360,8 +383,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         l_run += rowsum;
         // keys at or past the last valid one: zero their V rows before any P V of this tile
         // (done by tile 0 if it reads this tile, else by tile 1; the MMA issuer orders tile
-        // 1's product after tile 0's P)
-        if (kbase + BKV > it.n_valid && (t == 0 || j >= it.nkt[0]) && kbase + row >= it.n_valid) {
+        // 1's product after tile 0's P), once the tile's V has landed
+        const bool zero_v = kbase + BKV > it.n_valid && (t == 0 || j >= it.nkt[0]);
+        if (zero_v) {
+          const uint32_t g = kvbase + j;
+          if (!mbar_wait(smem_u32(v_full + (g & 1)), (g >> 1) & 1, p.status, abort_flag)) { ok = false; break; }
+        }
+        if (zero_v && kbase + row >= it.n_valid) {
           uint8_t* vrow = sV + ((kvbase + j) & 1) * TILE + row * 128;
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
@@ -413,7 +441,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
-constexpr size_t kSmemBytes = 1024 + 6 * TILE + 14 * 8 + 16;
+constexpr size_t kSmemBytes = 1024 + (4 + K_STAGES) * TILE + (13 + 2 * K_STAGES) * 8 + 16;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 static_assert(kSmemBytes >= kTmemKernelMinSmem, "a TMEM-holding kernel must not share an SM with another");
 
 }  // namespace
