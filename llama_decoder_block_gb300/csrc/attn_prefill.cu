@@ -226,29 +226,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // ------------------------------------------------------------ MMA issuer
       constexpr uint32_t IDESC_QK = idesc_bf16(128, 128, false);
       constexpr uint32_t IDESC_PV = idesc_bf16(128, 128, true);
+      const uint64_t dQ = sdesc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t dK = sdesc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t dV = sdesc_sw128(smem_u32(sV), CHUNK, 1024);
       auto issue_s = [&](int t, uint32_t kst) {
-        const uint32_t aq = smem_u32(sQ + t * TILE), bk = smem_u32(sK + kst * TILE);
+        const uint64_t aq = dQ + static_cast<uint64_t>((t * TILE) >> 4);
+        const uint64_t bk = dK + static_cast<uint64_t>((kst * TILE) >> 4);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * CHUNK + (kk & 3) * 32;
-          tc_mma_bf16(tmem_base + t * 128, sdesc_sw128(aq + off, 16, 1024), sdesc_sw128(bk + off, 16, 1024),
-                      IDESC_QK, kk > 0 ? 1u : 0u);
+          const uint32_t off = ((kk >> 2) * CHUNK + (kk & 3) * 32) >> 4;
+          tc_mma_bf16(tmem_base + t * 128, aq + off, bk + off, IDESC_QK, kk > 0 ? 1u : 0u);
         }
         tc_commit(smem_u32(s_full + t));
       };
-      auto issue_pv = [&](int t, uint32_t st, bool first) {
-        const uint32_t bv = smem_u32(sV + st * TILE);
+      // O_t += P_t V_j; o_done[t] only after the item's last one (the softmax's rescale of O
+      // before P_t V_j needs P_t V_{j-1} complete, which s_full[t] for S_t(j) already implies:
+      // S_t(j) is issued after it, and a commit tracks all earlier products of this thread)
+      auto issue_pv = [&](int t, uint32_t st, bool first, bool last) {
+        const uint64_t bv = dV + static_cast<uint64_t>((st * TILE) >> 4);
 #pragma unroll
         for (int kk = 0; kk < BKV / 16; ++kk) {
           // V: 128 key rows of 128 bytes per 64-wide d half; K step = 16 rows = 2048 bytes,
           // the second d half is CHUNK bytes further (leading byte offset), 8-row groups 1024 apart
           tc_mma_bf16_ts(tmem_base + 256 + t * 128, tmem_base + t * 128 + kk * 8,
-                         sdesc_sw128(bv + kk * 2048, CHUNK, 1024), IDESC_PV, (!first || kk > 0) ? 1u : 0u);
+                         bv + static_cast<uint64_t>((kk * 2048) >> 4), IDESC_PV, (!first || kk > 0) ? 1u : 0u);
         }
-        tc_commit(smem_u32(o_done + t));
+        if (last) tc_commit(smem_u32(o_done + t));
       };
       bool ok = true, issued = false;
-      uint32_t kvc = 0, qc = 0;
+      uint32_t kvc = 0, qc = 0, k_seen = ~0u;
       uint32_t pc[2] = {0u, 0u};   // P arrivals consumed, per tile
       for (int r = 0; ok; ++r) {
         const int i = item_of(c, r);
@@ -282,14 +288,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (!mbar_wait(smem_u32(p_full + t), pc[t] & 1, p.status, abort_flag)) { ok = false; break; }
             ++pc[t];
             tc_fence_after();
-            issue_pv(t, g & 1, j == 0);
+            issue_pv(t, g & 1, j == 0, !active(t, j + 1));
             if (active(t, j + 1)) {
               const uint32_t gn = g + 1;
-              if (!mbar_wait(smem_u32(k_full + gn % K_STAGES), (gn / K_STAGES) & 1, p.status, abort_flag)) {
-                ok = false;
-                break;
+              // K_{j+1} once per key tile (tile B's S follows tile A's)
+              if (gn != k_seen) {
+                if (!mbar_wait(smem_u32(k_full + gn % K_STAGES), (gn / K_STAGES) & 1, p.status, abort_flag)) {
+                  ok = false;
+                  break;
+                }
+                k_seen = gn;
+                tc_fence_after();
               }
-              tc_fence_after();
               issue_s_counted(t, j + 1, gn % K_STAGES);
             }
           }
@@ -315,7 +325,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const float sl = p.scale_log2;
     uint32_t r[128];   // the row's 128 scores, then (first 64) its P as packed bf16 pairs
     bool ok = true;
-    uint32_t kvc = 0, tc_run = 0;   // K/V tiles of the CTA's items so far; S tiles of tile t so far
+    // K/V tiles of the CTA's items so far; S tiles of tile t so far; items of tile t so far
+    uint32_t kvc = 0, tc_run = 0, oc = 0;
     for (int rr = 0; ok; ++rr) {
       const int i = item_of(c, rr);
       if (i >= p.n_items) break;
@@ -342,10 +353,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int k = 0; k < 128; ++k)
             if (kbase + k > qpos) r[k] = __float_as_uint(-INFINITY);
         }
-        // two scores per max instruction (the ALU pipe is this loop's limit)
-        float mx = -INFINITY;
+        // two scores per max instruction, in four independent chains (only the two softmax
+        // warps of a sub-partition share its issue slots: a single chain would wait on latency)
+        float m4[4];
 #pragma unroll
-        for (int k = 0; k < 128; k += 2) mx = fmax3(mx, __uint_as_float(r[k]), __uint_as_float(r[k + 1]));
+        for (int u = 0; u < 4; ++u) m4[u] = fmaxf(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
+#pragma unroll
+        for (int k = 8; k < 128; k += 8)
+#pragma unroll
+          for (int u = 0; u < 4; ++u) m4[u] = fmax3(m4[u], __uint_as_float(r[k + 2 * u]), __uint_as_float(r[k + 2 * u + 1]));
+        const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
         const float mxs = mx * sl;
         const bool need = mxs > m_run + kRescaleLog2;    // also true on the first tile
         const bool any_need = __any_sync(0xffffffffu, need);
@@ -354,21 +371,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         m_run = m_new;
         // P = 2^(S * scale - m) (masked scores are -inf: P = 0), packed in place: pair k goes
         // to r[k] once r[2k], r[2k + 1] are read; keys 2c, 2c+1 land in S column c
-        float rowsum = 0.f;
+        // S * scale - m two scores per instruction; the row sum in two packed accumulators
+        float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int k = 0; k < 64; ++k) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(r[2 * k]), sl, -m_run));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(r[2 * k + 1]), sl, -m_run));
-          rowsum += p0 + p1;
+          float x0, x1;
+          fma2(x0, x1, __uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1]), sl, sl, -m_run, -m_run);
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          const int a = 2 * (k & 1);
+          add2(sum4[a], sum4[a + 1], sum4[a], sum4[a + 1], p0, p1);
           r[k] = pack_bf16(p0, p1);
         }
+        add2(sum4[0], sum4[1], sum4[0], sum4[1], sum4[2], sum4[3]);
+        const float rowsum = sum4[0] + sum4[1];
         tmem_st64(tS, r);
         if (any_need) {
           if (j > 0) {
-            // P_{j-1} V_{j-1} must have landed before O is rescaled (and O must be rescaled
-            // before this tile's P V, which waits for p_full below)
-            if (!mbar_wait(smem_u32(o_done + t), (sj - 1) & 1, p.status, abort_flag)) { ok = false; break; }
-            tc_fence_after();
+            // O is rescaled before this tile's P V (which waits for p_full below); P_{j-1} V_{j-1}
+            // has landed: it was issued before S_j, whose completion s_full signalled
             uint32_t o32[32];
 #pragma unroll 1
             for (int cc = 0; cc < 4; ++cc) {
@@ -406,7 +426,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_run += n_t;
       // the item's last product (this thread's reads of O come before the next item's first
       // P V, which waits for this warp's next arrival on p_full)
-      if (!mbar_wait(smem_u32(o_done + t), (tc_run - 1) & 1, p.status, abort_flag)) { ok = false; break; }
+      if (!mbar_wait(smem_u32(o_done + t), oc & 1, p.status, abort_flag)) { ok = false; break; }
+      ++oc;
       tc_fence_after();
       const float inv_l = 1.0f / l_run;
       __nv_bfloat16* dst =
