@@ -222,97 +222,102 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ------------------------------------------------------------ MMA issuer
-      constexpr uint32_t IDESC_QK = idesc_bf16(128, 128, false);
-      constexpr uint32_t IDESC_PV = idesc_bf16(128, 128, true);
-      const uint64_t dQ = sdesc_sw128(smem_u32(sQ), 16, 1024);
-      const uint64_t dK = sdesc_sw128(smem_u32(sK), 16, 1024);
-      const uint64_t dV = sdesc_sw128(smem_u32(sV), CHUNK, 1024);
-      auto issue_s = [&](int t, uint32_t kst) {
-        const uint64_t aq = dQ + static_cast<uint64_t>((t * TILE) >> 4);
-        const uint64_t bk = dK + static_cast<uint64_t>((kst * TILE) >> 4);
+    // -------------------------------------------------------------- MMA issuer
+    // The whole warp walks the loop (its operands stay warp-uniform) and one elected lane
+    // issues each product and commit: from a single diverged lane an issue costs about as
+    // long as a 128 x 128 x 16 product runs, and the bookkeeping between products would
+    // leave the tensor core idle.
+    constexpr uint32_t IDESC_QK = idesc_bf16(128, 128, false);
+    constexpr uint32_t IDESC_PV = idesc_bf16(128, 128, true);
+    const uint64_t dQ = sdesc_sw128(smem_u32(sQ), 16, 1024);
+    const uint64_t dK = sdesc_sw128(smem_u32(sK), 16, 1024);
+    const uint64_t dV = sdesc_sw128(smem_u32(sV), CHUNK, 1024);
+    // every lane waits (they stay in step); a timeout or abort seen by any lane ends the loop
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+      const bool r = mbar_wait(smem_u32(bar), parity, p.status, abort_flag);
+      return __all_sync(0xffffffffu, r) != 0;
+    };
+    auto issue_s = [&](int t, uint32_t kst) {
+      const uint64_t aq = dQ + static_cast<uint64_t>((t * TILE) >> 4);
+      const uint64_t bk = dK + static_cast<uint64_t>((kst * TILE) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * CHUNK + (kk & 3) * 32) >> 4;
-          tc_mma_bf16(tmem_base + t * 128, aq + off, bk + off, IDESC_QK, kk > 0 ? 1u : 0u);
-        }
-        tc_commit(smem_u32(s_full + t));
-      };
-      // O_t += P_t V_j; o_done[t] only after the item's last one (the softmax's rescale of O
-      // before P_t V_j needs P_t V_{j-1} complete, which s_full[t] for S_t(j) already implies:
-      // S_t(j) is issued after it, and a commit tracks all earlier products of this thread)
-      auto issue_pv = [&](int t, uint32_t st, bool first, bool last) {
-        const uint64_t bv = dV + static_cast<uint64_t>((st * TILE) >> 4);
+      for (int kk = 0; kk < HD / 16; ++kk) {
+        const uint32_t off = ((kk >> 2) * CHUNK + (kk & 3) * 32) >> 4;
+        tc_mma_bf16_warp(tmem_base + t * 128, aq + off, bk + off, IDESC_QK, kk > 0 ? 1u : 0u);
+      }
+      tc_commit_warp(smem_u32(s_full + t));
+    };
+    // O_t += P_t V_j; o_done[t] only after the item's last one (the softmax's rescale of O
+    // before P_t V_j needs P_t V_{j-1} complete, which s_full[t] for S_t(j) already implies:
+    // S_t(j) is issued after it, and a commit tracks all earlier products of its thread)
+    auto issue_pv = [&](int t, uint32_t st, bool first, bool last) {
+      const uint64_t bv = dV + static_cast<uint64_t>((st * TILE) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < BKV / 16; ++kk) {
-          // V: 128 key rows of 128 bytes per 64-wide d half; K step = 16 rows = 2048 bytes,
-          // the second d half is CHUNK bytes further (leading byte offset), 8-row groups 1024 apart
-          tc_mma_bf16_ts(tmem_base + 256 + t * 128, tmem_base + t * 128 + kk * 8,
-                         bv + static_cast<uint64_t>((kk * 2048) >> 4), IDESC_PV, (!first || kk > 0) ? 1u : 0u);
-        }
-        if (last) tc_commit(smem_u32(o_done + t));
+      for (int kk = 0; kk < BKV / 16; ++kk) {
+        // V: 128 key rows of 128 bytes per 64-wide d half; K step = 16 rows = 2048 bytes,
+        // the second d half is CHUNK bytes further (leading byte offset), 8-row groups 1024 apart
+        tc_mma_bf16_ts_warp(tmem_base + 256 + t * 128, tmem_base + t * 128 + kk * 8,
+                            bv + static_cast<uint64_t>((kk * 2048) >> 4), IDESC_PV, (!first || kk > 0) ? 1u : 0u);
+      }
+      if (last) tc_commit_warp(smem_u32(o_done + t));
+    };
+    bool ok = true, issued = false;
+    uint32_t kvc = 0, qc = 0, k_seen = ~0u;
+    uint32_t pc[2] = {0u, 0u};   // P arrivals consumed, per tile
+    for (int r = 0; ok; ++r) {
+      const int i = item_of(c, r);
+      if (i >= p.n_items) break;
+      const AttnItem it = make_item(p, i, false);
+      if (!it.hasA) continue;
+      auto active = [&](int t, int j) { return j < it.nkt[t]; };
+      if (!wait_all(q_full, qc & 1) || !wait_all(k_full + kvc % K_STAGES, (kvc / K_STAGES) & 1)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // the Q tiles are free for the next item once this item's last S product is done:
+      // commit q_empty right after issuing it; K_j is free once the S products of key tile j
+      // are (the last one is tile B's when B reads key tile j, else tile A's)
+      int s_left = it.nkt[0] + it.nkt[1];
+      auto issue_s_counted = [&](int t, int j, uint32_t kst) {
+        issue_s(t, kst);
+        if (--s_left == 0) tc_commit_warp(smem_u32(q_empty));
+        if (t == 1 || !active(1, j)) tc_commit_warp(smem_u32(k_empty + kst));
       };
-      bool ok = true, issued = false;
-      uint32_t kvc = 0, qc = 0, k_seen = ~0u;
-      uint32_t pc[2] = {0u, 0u};   // P arrivals consumed, per tile
-      for (int r = 0; ok; ++r) {
-        const int i = item_of(c, r);
-        if (i >= p.n_items) break;
-        const AttnItem it = make_item(p, i, false);
-        if (!it.hasA) continue;
-        auto active = [&](int t, int j) { return j < it.nkt[t]; };
-        if (!mbar_wait(smem_u32(q_full), qc & 1, p.status, abort_flag) ||
-            !mbar_wait(smem_u32(k_full + kvc % K_STAGES), (kvc / K_STAGES) & 1, p.status, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        // the Q tiles are free for the next item once this item's last S product is done:
-        // commit q_empty right after issuing it; K_j is free once the S products of key tile j
-        // are (the last one is tile B's when B reads key tile j, else tile A's)
-        int s_left = it.nkt[0] + it.nkt[1];
-        auto issue_s_counted = [&](int t, int j, uint32_t kst) {
-          issue_s(t, kst);
-          if (--s_left == 0) tc_commit(smem_u32(q_empty));
-          if (t == 1 || !active(1, j)) tc_commit(smem_u32(k_empty + kst));
-        };
-        issue_s_counted(0, 0, kvc % K_STAGES);
-        if (it.hasB) issue_s_counted(1, 0, kvc % K_STAGES);
-        issued = true;
-        for (int j = 0; j < it.nt && ok; ++j) {
-          const uint32_t g = kvc + j;
-          if (!mbar_wait(smem_u32(v_full + (g & 1)), (g >> 1) & 1, p.status, abort_flag)) { ok = false; break; }
-          for (int t = 0; t < 2 && ok; ++t) {
-            if (!active(t, j)) continue;
-            if (!mbar_wait(smem_u32(p_full + t), pc[t] & 1, p.status, abort_flag)) { ok = false; break; }
-            ++pc[t];
-            tc_fence_after();
-            issue_pv(t, g & 1, j == 0, !active(t, j + 1));
-            if (active(t, j + 1)) {
-              const uint32_t gn = g + 1;
-              // K_{j+1} once per key tile (tile B's S follows tile A's)
-              if (gn != k_seen) {
-                if (!mbar_wait(smem_u32(k_full + gn % K_STAGES), (gn / K_STAGES) & 1, p.status, abort_flag)) {
-                  ok = false;
-                  break;
-                }
-                k_seen = gn;
-                tc_fence_after();
-              }
-              issue_s_counted(t, j + 1, gn % K_STAGES);
+      issue_s_counted(0, 0, kvc % K_STAGES);
+      if (it.hasB) issue_s_counted(1, 0, kvc % K_STAGES);
+      issued = true;
+      for (int j = 0; j < it.nt && ok; ++j) {
+        const uint32_t g = kvc + j;
+        if (!wait_all(v_full + (g & 1), (g >> 1) & 1)) { ok = false; break; }
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (!active(t, j)) continue;
+          if (!wait_all(p_full + t, pc[t] & 1)) { ok = false; break; }
+          ++pc[t];
+          tc_fence_after();
+          issue_pv(t, g & 1, j == 0, !active(t, j + 1));
+          if (active(t, j + 1)) {
+            const uint32_t gn = g + 1;
+            // K_{j+1} once per key tile (tile B's S follows tile A's)
+            if (gn != k_seen) {
+              if (!wait_all(k_full + gn % K_STAGES, (gn / K_STAGES) & 1)) { ok = false; break; }
+              k_seen = gn;
+              tc_fence_after();
             }
+            issue_s_counted(t, j + 1, gn % K_STAGES);
           }
-          if (ok) tc_commit(smem_u32(v_empty + (g & 1)));
         }
-        if (!ok) break;
-        kvc += it.nt;
-        ++qc;
+        if (ok) tc_commit_warp(smem_u32(v_empty + (g & 1)));
       }
-      if (!ok && issued) {
-        tc_commit(smem_u32(drain));
-        mbar_wait_slow(smem_u32(drain), 0, nullptr, nullptr, kWaitBudgetNs);
-      }
+      if (!ok) break;
+      kvc += it.nt;
+      ++qc;
+    }
+    if (!ok && issued) {
+      // all products of the issuing lane must finish before the TMEM is released
+      tc_commit_warp(smem_u32(drain));
+      if (lane == 0) mbar_wait_slow(smem_u32(drain), 0, nullptr, nullptr, kWaitBudgetNs);
+      __syncwarp();
     }
   } else if (warp >= 4) {
     // -------------------------------------------------------------- softmax of tile t
