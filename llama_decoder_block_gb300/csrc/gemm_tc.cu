@@ -426,46 +426,51 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ------------------------------------------------------------ MMA issuer
-      int stage = 0;
-      uint32_t phase = 0;
-      int acc = 0;
-      uint32_t acc_phase = 0;
-      bool ok = true;
-      bool issued = false;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-        int mb, nb, split;
-        tile_coords(p, t, mb, nb, split);
-        const int kb0 = split * p.kb_per_split;
-        const int kb1 = min(kb0 + p.kb_per_split, p.num_kb);
-        if (!mbar_wait(smem_u32(tempty_bar + acc), acc_phase ^ 1u, p.status, abort_flag)) { ok = false; break; }
+    // -------------------------------------------------------------- MMA issuer
+    // The whole warp walks the loop (operands stay warp-uniform) and one elected lane issues
+    // each product and commit: issued from a single diverged lane a product costs about half
+    // of what a 128 x 256 x 16 product runs, leaving little time for the waits between stages.
+    const uint64_t dA = sdesc_sw128(smem_u32(sA), 16, 1024);
+    const uint64_t dB = sdesc_sw128(smem_u32(sB), 16, 1024);
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+      const bool r = mbar_wait(smem_u32(bar), parity, p.status, abort_flag);
+      return __all_sync(0xffffffffu, r) != 0;
+    };
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    bool issued = false;
+    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      int mb, nb, split;
+      tile_coords(p, t, mb, nb, split);
+      const int kb0 = split * p.kb_per_split;
+      const int kb1 = min(kb0 + p.kb_per_split, p.num_kb);
+      if (!wait_all(tempty_bar + acc, acc_phase ^ 1u)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!wait_all(full_bar + stage, phase)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(smem_u32(full_bar + stage), phase, p.status, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t a_addr = smem_u32(sA + stage * A_TILE_BYTES);
-          const uint32_t b_addr = smem_u32(sB + stage * B_TILE_BYTES);
+        const uint64_t ad = dA + static_cast<uint64_t>((stage * A_TILE_BYTES) >> 4);
+        const uint64_t bd = dB + static_cast<uint64_t>((stage * B_TILE_BYTES) >> 4);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            const uint64_t ad = sdesc_sw128(a_addr + k * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(b_addr + k * 32, 16, 1024);
-            tc_mma_bf16(d_tmem, ad, bd, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
-          }
-          issued = true;
-          tc_commit(smem_u32(empty_bar + stage));
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-        }
-        if (!ok) break;
-        tc_commit(smem_u32(tfull_bar + acc));
-        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        for (int k = 0; k < BK / 16; ++k)   // 16 K elements = 32 bytes further along the row
+          tc_mma_bf16_warp(d_tmem, ad + 2 * k, bd + 2 * k, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+        issued = true;
+        tc_commit_warp(smem_u32(empty_bar + stage));
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
-      if (!ok && issued) {
-        // all MMAs of this thread must finish before the TMEM is released
-        tc_commit(smem_u32(drain_bar));
-        mbar_wait_slow(smem_u32(drain_bar), 0, nullptr, nullptr, kWaitBudgetNs);
-      }
+      if (!ok) break;
+      tc_commit_warp(smem_u32(tfull_bar + acc));
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+    if (!ok && issued) {
+      // all products of the issuing lane must finish before the TMEM is released
+      tc_commit_warp(smem_u32(drain_bar));
+      if (lane == 0) mbar_wait_slow(smem_u32(drain_bar), 0, nullptr, nullptr, kWaitBudgetNs);
+      __syncwarp();
     }
   } else {
     // -------------------------------------------------------------- epilogue warps 2..5
