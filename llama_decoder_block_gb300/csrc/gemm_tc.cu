@@ -186,14 +186,19 @@ __device__ __forceinline__ void resolve_rows(const RowMap& rm, int vrow, int& ma
   row = vrow - start;
 }
 
-__device__ __forceinline__ void tile_coords(const Params& p, int t, int& mb, int& nb, int& split) {
-  split = t % p.num_splits;
-  t /= p.num_splits;
-  const int per_group = p.group_m * p.num_nb;
-  const int g = t / per_group, r = t % per_group;
-  const int first_m = g * p.group_m;
-  const int gm = min(p.group_m, p.num_mb - first_m);
-  mb = first_m + r % gm;
+// Work unit u of a launch with clusters of CM CTAs along M: the CM CTAs of a cluster take the
+// row blocks CM * i + rank of the same column block (and split), so they share its weight
+// tile.  The order is tile_coords' over CM-row-block units (CM = 1: the same tiles).
+template <int CM>
+__device__ __forceinline__ void unit_coords(const Params& p, int u, int rank, int& mb, int& nb, int& split) {
+  split = u % p.num_splits;
+  u /= p.num_splits;
+  const int units_m = p.num_mb / CM, gmm = max(1, p.group_m / CM);
+  const int per_group = gmm * p.num_nb;
+  const int g = u / per_group, r = u % per_group;
+  const int first_m = g * gmm;
+  const int gm = min(gmm, units_m - first_m);
+  mb = (first_m + r % gm) * CM + rank;
   nb = r / gm;
 }
 
@@ -249,14 +254,23 @@ __device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float* v,
   }
 }
 
-template <int BN, int EPI, int STAGES>
+// CM = 2: clusters of two CTAs on consecutive row blocks of one column block.  Each CTA loads
+// its own A tile and half of the shared B (weight) tile, which TMA multicast writes into both
+// CTAs' shared memory: a third less operand traffic into each SM per k-block (the 128 x 256
+// tiles are bound by that traffic, not by the tensor cores).  A stage is refilled only once
+// both CTAs' products have read it (empty barriers count one commit from each).
+template <int BN, int EPI, int STAGES, int CM>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ TMaps tm, const Params p) {
   constexpr int B_TILE_BYTES = BN * BK * 2;
-  // B arrives in 128-row boxes, or as one box when BN is not a multiple of 128 (BN <= 256);
-  // gate/up tiles as two boxes of BN/2 rows, one from each matrix
-  constexpr int B_BOX_ROWS = EPI == EPI_SWIGLU ? BN / 2 : BN % 128 == 0 ? 128 : BN;
+  // B arrives in 128-row boxes, or as one box when BN is not a multiple of 128 (BN <= 256),
+  // two boxes of BN/2 rows in clusters; gate/up tiles as two boxes of BN/2 rows, one from each
+  // matrix
+  constexpr int B_BOX_ROWS = EPI == EPI_SWIGLU ? BN / 2 : BN % 128 == 0 ? 128 : (CM == 2 ? BN / 2 : BN);
   constexpr int B_BOXES = BN / B_BOX_ROWS;
+  static_assert(CM == 1 || (CM == 2 && B_BOXES % 2 == 0 && B_BOX_ROWS % 8 == 0 && EPI != EPI_PARTIAL),
+                "clusters split B into whole 8-row swizzle groups, one half per CTA");
+  constexpr uint16_t kClusterMask = (1u << CM) - 1u;
   constexpr uint32_t STAGE_TX = A_TILE_BYTES + B_TILE_BYTES;
   constexpr uint32_t TMEM_COLS = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
   constexpr uint32_t IDESC = idesc_bf16(BM, BN, false);
@@ -277,12 +291,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int num_tiles = p.num_mb * p.num_nb * p.num_splits;
+  // work units (tiles, or tile pairs in clusters) walked by this CTA's cluster
+  const int num_units = p.num_mb / CM * p.num_nb * p.num_splits;
+  const int unit0 = static_cast<int>(blockIdx.x) / CM, unit_step = static_cast<int>(gridDim.x) / CM;
+  const int rank = CM == 1 ? 0 : static_cast<int>(cluster_ctarank());
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(smem_u32(full_bar + i), 1);
-      mbar_init(smem_u32(empty_bar + i), 1);
+      mbar_init(smem_u32(empty_bar + i), CM);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(tfull_bar + i), 1);
@@ -300,7 +317,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (CM > 1)
+    cluster_sync();   // the peer's barriers are initialised before any multicast reaches them
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   // inputs written by the previous kernel are read from here on (the producer waits below,
@@ -339,23 +359,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tma_load_2d(smem_u32(sA + stage * A_TILE_BYTES), &tm.m[p.a_map0 + a_map], smem_u32(full_bar + stage),
                     kb * BK, a_row);
       };
+      // a box of B: into this CTA's stage, or (clusters) into the same stage of both CTAs
+      auto load_b_box = [&](uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1) {
+        if constexpr (CM > 1)
+          tma_load_2d_mc(dst, map, bar, c0, c1, kClusterMask);
+        else
+          tma_load_2d(dst, map, bar, c0, c1);
+      };
       auto load_b = [&](int stage, int kb, int nb) {
         if constexpr (EPI == EPI_QKV && BN % 128 != 0) {
           int m0, r0, m1, r1;
           resolve_rows(p.bmap, nb * BN, m0, r0);
           resolve_rows(p.bmap, nb * BN + BN - 1, m1, r1);
           if (m0 != m1) {   // the tile crosses a boundary between two of the matrices
-            for (int bx = 0; bx < BN / 32; ++bx) {
+            for (int bx = rank; bx < BN / 32; bx += CM) {
               int b_map, b_row;
               resolve_rows(p.bmap, nb * BN + bx * 32, b_map, b_row);
-              tma_load_2d(smem_u32(sB + stage * B_TILE_BYTES + bx * 32 * 128), &tm.m[p.b32_map0 + b_map],
-                          smem_u32(full_bar + stage), kb * BK, b_row);
+              load_b_box(smem_u32(sB + stage * B_TILE_BYTES + bx * 32 * 128), &tm.m[p.b32_map0 + b_map],
+                         smem_u32(full_bar + stage), kb * BK, b_row);
             }
             return;
           }
         }
 #pragma unroll
         for (int bx = 0; bx < B_BOXES; ++bx) {
+          if (CM > 1 && bx % CM != rank) continue;   // the other CTA of the cluster loads this box
           // (this thread's issue latency bounds the ring's lead over TMA latency: no divisions)
           int b_map, b_row;
           if constexpr (EPI == EPI_SWIGLU) {   // tile nb = [gate rows BN/2*nb.. | the same up rows]
@@ -364,17 +392,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           } else {
             resolve_rows(p.bmap, nb * BN + bx * B_BOX_ROWS, b_map, b_row);
           }
-          tma_load_2d(smem_u32(sB + stage * B_TILE_BYTES + bx * B_BOX_ROWS * 128), &tm.m[p.b_map0 + b_map],
-                      smem_u32(full_bar + stage), kb * BK, b_row);
+          load_b_box(smem_u32(sB + stage * B_TILE_BYTES + bx * B_BOX_ROWS * 128), &tm.m[p.b_map0 + b_map],
+                     smem_u32(full_bar + stage), kb * BK, b_row);
         }
       };
       // the first STAGES k-blocks' weight tiles go out before the dependency wait: the ring
       // starts empty, so these stages need no empty-barrier wait
       int pre = 0;
       if (lane == 0 && p.weight_first != 0) {
-        for (int t = blockIdx.x; t < num_tiles && pre < STAGES; t += gridDim.x) {
+        for (int u = unit0; u < num_units && pre < STAGES; u += unit_step) {
           int mb, nb, split;
-          tile_coords(p, t, mb, nb, split);
+          unit_coords<CM>(p, u, rank, mb, nb, split);
           const int kb0 = split * p.kb_per_split;
           const int kb1 = min(kb0 + p.kb_per_split, p.num_kb);
           for (int kb = kb0; kb < kb1 && pre < STAGES; ++kb, ++pre) {
@@ -397,9 +425,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int stage = 0, step = 0;
         uint32_t phase = 0;
         uint32_t used_mask = 0, last_parity = 0;
-        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        for (int u = unit0; u < num_units && ok; u += unit_step) {
           int mb, nb, split;
-          tile_coords(p, t, mb, nb, split);
+          unit_coords<CM>(p, u, rank, mb, nb, split);
           const int kb0 = split * p.kb_per_split;
           const int kb1 = min(kb0 + p.kb_per_split, p.num_kb);
           for (int kb = kb0; kb < kb1; ++kb, ++step) {
@@ -414,6 +442,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             used_mask |= 1u << stage;
             last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          }
+        }
+        if constexpr (CM > 1) {
+          // every stage's last fill released by both CTAs' products: no commit of the other
+          // CTA is still on its way to this CTA's barriers when it leaves
+          for (int i = 0; i < STAGES && ok; ++i) {
+            if (!mbar_wait(smem_u32(empty_bar + stage), phase ^ 1u, p.status, abort_flag)) ok = false;
             if (++stage == STAGES) { stage = 0; phase ^= 1u; }
           }
         }
@@ -442,9 +478,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t acc_phase = 0;
     bool ok = true;
     bool issued = false;
-    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+    for (int u = unit0; u < num_units && ok; u += unit_step) {
       int mb, nb, split;
-      tile_coords(p, t, mb, nb, split);
+      unit_coords<CM>(p, u, rank, mb, nb, split);
       const int kb0 = split * p.kb_per_split;
       const int kb1 = min(kb0 + p.kb_per_split, p.num_kb);
       if (!wait_all(tempty_bar + acc, acc_phase ^ 1u)) { ok = false; break; }
@@ -459,7 +495,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int k = 0; k < BK / 16; ++k)   // 16 K elements = 32 bytes further along the row
           tc_mma_bf16_warp(d_tmem, ad + 2 * k, bd + 2 * k, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
         issued = true;
-        tc_commit_warp(smem_u32(empty_bar + stage));
+        if constexpr (CM > 1)
+          tc_commit_mc_warp(smem_u32(empty_bar + stage), kClusterMask);   // both CTAs' stage
+        else
+          tc_commit_warp(smem_u32(empty_bar + stage));
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
@@ -479,9 +518,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t t_lane = static_cast<uint32_t>(quarter * 32) << 16;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+    for (int u = unit0; u < num_units; u += unit_step) {
       int mb, nb, split;
-      tile_coords(p, t, mb, nb, split);
+      unit_coords<CM>(p, u, rank, mb, nb, split);
       if (!mbar_wait(smem_u32(tfull_bar + acc), acc_phase, p.status, abort_flag)) break;
       tc_fence_after();
       const uint32_t t_acc = tmem_base + t_lane + static_cast<uint32_t>(acc * BN);
@@ -694,7 +733,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  if constexpr (CM > 1)
+    cluster_sync();   // no CTA leaves while the other may still write its shared memory
+  else
+    __syncthreads();
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
@@ -707,28 +749,60 @@ constexpr size_t smem_bytes() {
   return 1024 + STAGES * (A_TILE_BYTES + BN * BK * 2) + (2 * STAGES + 5) * 8 + 16;
 }
 
-template <int BN, int EPI, int STAGES>
+template <int BN, int EPI, int STAGES, int CM = 1>
 int launch(const Ctx& c, const TMaps& tm, Params p) {
-  auto kern = gemm_tc_kernel<BN, EPI, STAGES>;
+  auto kern = gemm_tc_kernel<BN, EPI, STAGES, CM>;
   constexpr size_t smem = smem_bytes<BN, EPI, STAGES>();
   static_assert(smem >= kTmemKernelMinSmem, "a TMEM-holding kernel must not share an SM with another");
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
+  static int max_clusters = 0;   // clusters of CM CTAs that can be resident at once
   std::call_once(once, [&] {
     attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (attr_err == cudaSuccess && CM > 1) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(c.num_sms / CM * CM);
+      cfg.blockDim = dim3(NUM_THREADS);
+      cfg.dynamicSmemBytes = smem;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = CM;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
+      if (attr_err == cudaSuccess && max_clusters < 1) attr_err = cudaErrorInvalidConfiguration;
+    }
   });
   if (attr_err != cudaSuccess) return LLAMA_ERR_CUDA;
   p.status = c.status;
   if (!c.static_weights) p.weight_first = 0;
-  const int tiles = p.num_mb * p.num_nb * p.num_splits;
-  if (tiles == 0) return LLAMA_OK;
+  if (p.num_mb % CM != 0 || (CM > 1 && p.num_splits != 1)) return LLAMA_ERR_INVALID_ARG;
+  const int units = p.num_mb / CM * p.num_nb * p.num_splits;
+  if (units == 0) return LLAMA_OK;
   if (p.pro_out != nullptr && (EPI == EPI_RESID || EPI == EPI_PARTIAL || p.pro_x == nullptr ||
                               p.pro_gamma == nullptr || p.pro_count == nullptr))
     return LLAMA_ERR_INVALID_ARG;
-  const int grid = std::min(tiles, c.num_sms);
-  launch_pdl(c, kern, dim3(grid), dim3(NUM_THREADS), smem, tm, p);
+  if constexpr (CM == 1) {
+    launch_pdl(c, kern, dim3(std::min(units, c.num_sms)), dim3(NUM_THREADS), smem, tm, p);
+  } else {
+    const int clusters = std::min(units, std::min(max_clusters, c.num_sms / CM));
+    launch_pdl_cluster(c, kern, dim3(clusters * CM), dim3(NUM_THREADS), smem, CM, tm, p);
+  }
   return after_launch(c);
 }
+
+// Clusters of two CTAs sharing each weight tile, where the row blocks pair up.
+bool use_clusters(int M) { return (M + BM - 1) / BM % 2 == 0; }
+
+template <int BN, int EPI, int STAGES>
+int launch_cl(const Ctx& c, const TMaps& tm, const Params& p, bool clusters) {
+  return clusters ? launch<BN, EPI, STAGES, 2>(c, tm, p) : launch<BN, EPI, STAGES, 1>(c, tm, p);
+}
+
+// Rows of the weight boxes: 128, or the whole tile width (BN < 256), halved in clusters.
+uint32_t weight_box_rows(int bn, bool clusters) { return bn == 256 ? 128u : clusters ? bn / 2 : bn; }
 
 // Rounds of num_sms tiles times the tile width: the time of a GEMM with M rows and n_blocks
 // column blocks of width bn, a round's time taken as proportional to its width.
@@ -785,9 +859,10 @@ Params base_params(int M, int N, int K, int BN) {
 int gemm_plain(const Ctx& c, const void* X, const void* W, void* C, int M, int N, int K, bool c_f32,
                const NormPro* norm) {
   const int bn = tile_width_for(M, N, c.num_sms);
+  const bool cl = use_clusters(M);
   TMaps tm{};
   if (!make_tmap_2d(&tm.m[0], norm ? norm->xn : X, K, M, K, 128) ||
-      !make_tmap_2d(&tm.m[1], W, K, N, K, bn == 256 ? 128 : bn))
+      !make_tmap_2d(&tm.m[1], W, K, N, K, weight_box_rows(bn, cl)))
     return LLAMA_ERR_INVALID_ARG;
   Params p = base_params(M, N, K, bn);
   if (norm != nullptr) set_prologue(p, X, *norm);
@@ -795,8 +870,8 @@ int gemm_plain(const Ctx& c, const void* X, const void* W, void* C, int M, int N
   p.b_map0 = 1;
   p.out = C;
   p.ldo = N;
-  if (bn == 256) return c_f32 ? launch<256, EPI_F32, 4>(c, tm, p) : launch<256, EPI_BF16, 4>(c, tm, p);
-  return c_f32 ? launch<224, EPI_F32, 5>(c, tm, p) : launch<224, EPI_BF16, 5>(c, tm, p);
+  if (bn == 256) return c_f32 ? launch_cl<256, EPI_F32, 4>(c, tm, p, cl) : launch_cl<256, EPI_BF16, 4>(c, tm, p, cl);
+  return c_f32 ? launch_cl<224, EPI_F32, 5>(c, tm, p, cl) : launch_cl<224, EPI_BF16, 5>(c, tm, p, cl);
 }
 
 int gemm_residual(const Ctx& c, const void* X, const void* W, const void* resid, void* out, int M, int N, int K) {
@@ -804,8 +879,9 @@ int gemm_residual(const Ctx& c, const void* X, const void* W, const void* resid,
   // 304 tiles fill 2 rounds of 152 SMs, where 256 tiles of 256 columns leave the second
   // round two-thirds full)
   const int bn = tile_width_for(M, N, c.num_sms);
+  const bool cl = use_clusters(M);
   TMaps tm{};
-  if (!make_tmap_2d(&tm.m[0], X, K, M, K, 128) || !make_tmap_2d(&tm.m[1], W, K, N, K, bn == 256 ? 128 : bn))
+  if (!make_tmap_2d(&tm.m[0], X, K, M, K, 128) || !make_tmap_2d(&tm.m[1], W, K, N, K, weight_box_rows(bn, cl)))
     return LLAMA_ERR_INVALID_ARG;
   Params p = base_params(M, N, K, bn);
   p.a_map0 = 0;
@@ -814,7 +890,7 @@ int gemm_residual(const Ctx& c, const void* X, const void* W, const void* resid,
   p.ldo = N;
   p.resid = static_cast<const __nv_bfloat16*>(resid);
   p.ldr = N;
-  return bn == 256 ? launch<256, EPI_RESID, 4>(c, tm, p) : launch<224, EPI_RESID, 5>(c, tm, p);
+  return bn == 256 ? launch_cl<256, EPI_RESID, 4>(c, tm, p, cl) : launch_cl<224, EPI_RESID, 5>(c, tm, p, cl);
 }
 
 int gemm_swiglu(const Ctx& c, const void* X, const void* Wg, const void* Wu, void* out, int M, int I, int K,
@@ -833,7 +909,7 @@ int gemm_swiglu(const Ctx& c, const void* X, const void* Wg, const void* Wu, voi
   p.n_maps = 3;
   p.out = out;
   p.ldo = I;
-  return launch<256, EPI_SWIGLU, 4>(c, tm, p);
+  return launch_cl<256, EPI_SWIGLU, 4>(c, tm, p, use_clusters(M));
 }
 
 int gemm_qkv_rope(const Ctx& c, const void* X, const void* Wq, const void* Wk, const void* Wv, int B, int S, int K,
@@ -845,7 +921,8 @@ int gemm_qkv_rope(const Ctx& c, const void* X, const void* Wq, const void* Wk, c
   // need whole heads in a tile: 256 columns = two heads); a 224-column tile that crosses the
   // q|k or k|v boundary takes its weights in 32-row boxes from the maps at b32_map0
   const int bn = rope_half ? 256 : tile_width_for(M, (H + 2 * G) * D, c.num_sms);
-  const int box = bn == 256 ? 128 : bn;
+  const bool cl = use_clusters(M);
+  const uint32_t box = weight_box_rows(bn, cl);
   TMaps tm{};
   if (!make_tmap_2d(&tm.m[0], norm ? norm->xn : X, K, M, K, 128) || !make_tmap_2d(&tm.m[1], Wq, K, H * D, K, box) ||
       !make_tmap_2d(&tm.m[2], Wk, K, G * D, K, box) || !make_tmap_2d(&tm.m[3], Wv, K, G * D, K, box))
@@ -877,7 +954,7 @@ int gemm_qkv_rope(const Ctx& c, const void* X, const void* Wq, const void* Wk, c
   p.q_out = static_cast<__nv_bfloat16*>(q_out);
   p.k_cache = static_cast<__nv_bfloat16*>(k_cache);
   p.v_cache = static_cast<__nv_bfloat16*>(v_cache);
-  return bn == 256 ? launch<256, EPI_QKV, 4>(c, tm, p) : launch<224, EPI_QKV, 5>(c, tm, p);
+  return bn == 256 ? launch_cl<256, EPI_QKV, 4>(c, tm, p, cl) : launch_cl<224, EPI_QKV, 5>(c, tm, p, cl);
 }
 
 int choose_splits(int num_sms, int w_rows_total, int K, int n_tok) {

@@ -49,6 +49,31 @@ cudaError_t launch_pdl(const Ctx& c, void (*kern)(KArgs...), dim3 grid, dim3 blo
   cfg.numAttrs = c.pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
 }
+// The same with thread-block clusters of cluster_x CTAs along x (grid.x a multiple of it).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_cluster(const Ctx& c, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                               unsigned cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = c.stream;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeClusterDimension;
+  attr[n].val.clusterDim.x = cluster_x;
+  attr[n].val.clusterDim.y = 1;
+  attr[n].val.clusterDim.z = 1;
+  ++n;
+  if (c.pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
 // Checks cudaGetLastError after a launch, counts it and records the next trace event.
 int after_launch(const Ctx& c);
 // True while llama_trace_begin's events are being recorded on this thread.
