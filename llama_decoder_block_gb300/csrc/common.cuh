@@ -56,15 +56,28 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// kCluster: the barrier also receives arrivals from other CTAs of the cluster (released at
+// cluster scope); the wait acquires at cluster scope.
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred P;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
-      "selp.b32 %0, 1, 0, P;\n\t}"
-      : "=r"(done)
-      : "r"(bar), "r"(parity)
-      : "memory");
+  if constexpr (kCluster) {
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 P, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, P;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, P;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  }
   return done != 0;
 }
 
@@ -91,11 +104,12 @@ static __device__ __noinline__ void report_timeout(int* status, uint64_t waited,
 // timeout, records LLAMA_ERR_TIMEOUT in `status`, raises `abort_flag` and
 // returns false; the caller must then leave its loop and go to the CTA's
 // common exit.
+template <bool kCluster = false>
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, int* status,
                                             volatile int* abort_flag, uint64_t budget_ns) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_test(bar, parity)) return true;
+    if (mbar_test<kCluster>(bar, parity)) return true;
     if ((it & 31u) == 0u) {
       if (abort_flag != nullptr && *abort_flag) return false;
       // once any wait on this device has timed out, later ones give up at once
@@ -113,10 +127,11 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
   }
 }
 
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* status,
                                           volatile int* abort_flag) {
-  if (mbar_test(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, status, abort_flag, kWaitBudgetNs);
+  if (mbar_test<kCluster>(bar, parity)) return true;
+  return mbar_wait_slow<kCluster>(bar, parity, status, abort_flag, kWaitBudgetNs);
 }
 
 // ------------------------------------------------------------------ TMA
@@ -153,12 +168,35 @@ __device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void* tmap, u
       : "memory");
 }
 
+// Two-SM form of tma_load_2d: the copy lands in this CTA's shared memory and completes on the
+// mbarrier at `cluster_bar` (a cluster_map address), which may be the even CTA's of the pair.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap, uint32_t cluster_bar, int c0,
+                                                 int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(tmap), "r"(cluster_bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+
 // ------------------------------------------------------------------ thread-block clusters
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
+}
+// The shared::cluster address of shared-memory offset `saddr` (a shared::cta address) in CTA
+// `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+// Arrive once on an mbarrier of any CTA of the cluster (a cluster_map address), releasing this
+// thread's earlier writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 // Every thread of every CTA of the cluster: shared-memory writes before it (mbarrier inits
 // included) are visible cluster-wide after it.
@@ -247,6 +285,41 @@ __device__ __forceinline__ void tc_commit_warp(uint32_t bar) {
       "elect.sync _|e, 0xffffffff;\n\t"
       "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
       : "memory");
+}
+
+// Two-SM forms (every tcgen05 instruction of such a kernel uses .cta_group::2): one product
+// M = 256 issued by the even CTA of a CTA pair reads A rows 0..127 from its own shared memory
+// and rows 128..255 from the peer's (same offset), B's first N/2 rows from its own and the
+// last N/2 from the peer's, and writes D rows 0..127 to its own TMEM, 128..255 to the peer's
+// (same TMEM address).  The warp is converged and one elected lane issues, as above.
+__device__ __forceinline__ void tc_mma2_bf16_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                  uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit2_mc_warp(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
+}
+// The pair's TMEM: one warp of each CTA of the pair takes part; both get the same address.
+__device__ __forceinline__ void tmem_alloc2(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish2() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
 // tc_commit_warp arriving on the mbarrier at offset `bar` in every CTA of the cluster named in

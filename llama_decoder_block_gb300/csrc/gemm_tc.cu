@@ -38,6 +38,10 @@ constexpr int A_TILE_BYTES = BM * BK * 2;
 constexpr int NUM_THREADS = 192;
 
 enum Epi : int { EPI_BF16 = 0, EPI_F32 = 1, EPI_RESID = 2, EPI_SWIGLU = 3, EPI_QKV = 4, EPI_PARTIAL = 5 };
+// How the CTAs of a launch share weight tiles: one CTA per tile; clusters of two CTAs on
+// consecutive row blocks whose B tile reaches both through TMA multicast; or pairs of CTAs
+// whose even CTA issues two-SM products over both CTAs' halves of B.
+enum TileMode : int { kSingle = 0, kShareB = 1, kPair = 2 };
 
 // How a 128-row block of an operand maps to one of the kernel's tensor maps.
 struct RowMap {
@@ -254,27 +258,41 @@ __device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float* v,
   }
 }
 
-// CM = 2: clusters of two CTAs on consecutive row blocks of one column block.  Each CTA loads
-// its own A tile and half of the shared B (weight) tile, which TMA multicast writes into both
-// CTAs' shared memory: a third less operand traffic into each SM per k-block (the 128 x 256
-// tiles are bound by that traffic, not by the tensor cores).  A stage is refilled only once
-// both CTAs' products have read it (empty barriers count one commit from each).
-template <int BN, int EPI, int STAGES, int CM>
+// MODE kShareB: clusters of two CTAs on consecutive row blocks of one column block.  Each CTA
+// loads its own A tile and half of the B (weight) tile's boxes, which TMA multicast writes into
+// both CTAs' stage: half the weight reads from L2.  A stage is refilled once both CTAs'
+// products have read it (each empty barrier counts one commit from each).
+// MODE kPair: two-SM products.  The pair takes the two row blocks as one 256 x BN tile: each
+// CTA loads its own A tile and half of B's rows, and the even CTA issues M = 256 products
+// (.cta_group::2) that read both CTAs' shared memory and write each CTA's 128 rows of D into
+// its own TMEM: a third less operand traffic into each SM per k-block than either form above
+// (the 128 x 256 tiles are bound by that traffic, not by the tensor cores), and deeper rings in
+// the same shared memory.  The odd CTA's copies complete on the even CTA's full barriers; the
+// even CTA's commits reach both CTAs' empty and accumulator-full barriers; both CTAs'
+// epilogues release the even CTA's accumulators.  (Measured faster than kShareB at 256-column
+// tiles, slower at 224: those take kShareB.)
+template <int BN, int EPI, int STAGES, int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ TMaps tm, const Params p) {
-  constexpr int B_TILE_BYTES = BN * BK * 2;
-  // B arrives in 128-row boxes, or as one box when BN is not a multiple of 128 (BN <= 256),
-  // two boxes of BN/2 rows in clusters; gate/up tiles as two boxes of BN/2 rows, one from each
-  // matrix
-  constexpr int B_BOX_ROWS = EPI == EPI_SWIGLU ? BN / 2 : BN % 128 == 0 ? 128 : (CM == 2 ? BN / 2 : BN);
-  constexpr int B_BOXES = BN / B_BOX_ROWS;
-  static_assert(CM == 1 || (CM == 2 && B_BOXES % 2 == 0 && B_BOX_ROWS % 8 == 0 && EPI != EPI_PARTIAL),
-                "clusters split B into whole 8-row swizzle groups, one half per CTA");
-  constexpr uint16_t kClusterMask = (1u << CM) - 1u;
+  constexpr int CM = MODE == kSingle ? 1 : 2;   // CTAs per cluster
+  constexpr bool kPairMma = MODE == kPair;
+  // B rows this CTA holds per stage: the whole tile, or its half in a pair
+  constexpr int B_ROWS = kPairMma ? BN / 2 : BN;
+  constexpr int B_TILE_BYTES = B_ROWS * BK * 2;
+  // B arrives in 128-row boxes, or as one box of all its rows when that is not a multiple of
+  // 128 (<= 256), as two halves in kShareB clusters (each CTA loads one for both); gate/up
+  // tiles: 128 gate rows, then the same 128 up rows (in a pair, the even CTA holds the gate
+  // rows, the odd one the up rows)
+  constexpr int B_BOX_ROWS =
+      EPI == EPI_SWIGLU ? BN / 2 : B_ROWS % 128 == 0 ? 128 : (MODE == kShareB ? BN / 2 : B_ROWS);
+  constexpr int B_BOXES = B_ROWS / B_BOX_ROWS;
+  static_assert(MODE == kSingle || (EPI != EPI_PARTIAL && (MODE == kShareB ? B_BOXES % 2 == 0 : BN % 128 == 0)),
+                "clusters split B into whole boxes, one half per CTA");
+  constexpr uint16_t kBoth = 3;                 // cluster ranks 0 and 1
   constexpr uint32_t STAGE_TX = A_TILE_BYTES + B_TILE_BYTES;
   constexpr uint32_t TMEM_COLS = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
-  constexpr uint32_t IDESC = idesc_bf16(BM, BN, false);
-  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
+  constexpr uint32_t IDESC = idesc_bf16(kPairMma ? 2 * BM : BM, BN, false);
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128 and 256");
 
   pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
@@ -299,11 +317,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(smem_u32(full_bar + i), 1);
-      mbar_init(smem_u32(empty_bar + i), CM);
+      mbar_init(smem_u32(empty_bar + i), MODE == kShareB ? 2 : 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(tfull_bar + i), 1);
-      mbar_init(smem_u32(tempty_bar + i), 4);
+      mbar_init(smem_u32(tempty_bar + i), kPairMma ? 8 : 4);   // the epilogue warps of every CTA of a pair
     }
     mbar_init(smem_u32(drain_bar), 1);
     *abort_flag = 0;
@@ -313,12 +331,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int i = 0; i < p.n_maps; ++i) tma_prefetch_desc(&tm.m[i]);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (kPairMma) {
+      tmem_alloc2(smem_u32(tmem_slot), TMEM_COLS);   // the same columns in both CTAs
+      tmem_relinquish2();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   if constexpr (CM > 1)
-    cluster_sync();   // the peer's barriers are initialised before any multicast reaches them
+    cluster_sync();   // the peer's barriers are initialised before any signal reaches them
   else
     __syncthreads();
   tc_fence_after();
@@ -353,47 +376,58 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 0) {
     {
       // ------------------------------------------------------------ TMA producer (lane 0)
+      // one box into this CTA's stage; in a pair the odd CTA's copies complete on the even
+      // CTA's full barrier (the even CTA's products read both CTAs' stages)
+      // (kShareB: B boxes go to the same stage of both CTAs of the cluster)
+      const uint32_t full_pair0 = kPairMma ? cluster_map(smem_u32(full_bar), 0) : 0u;
+      auto load_box = [&](uint32_t dst, const CUtensorMap* map, int stage, int c0, int c1, bool b_box) {
+        if (kPairMma && rank == 1)
+          tma_load_2d_pair(dst, map, full_pair0 + static_cast<uint32_t>(stage) * 8u, c0, c1);
+        else if (MODE == kShareB && b_box)
+          tma_load_2d_mc(dst, map, smem_u32(full_bar + stage), c0, c1, kBoth);
+        else
+          tma_load_2d(dst, map, smem_u32(full_bar + stage), c0, c1);
+      };
+      // the bytes a stage's full barrier waits for (kShareB: this CTA's A and all of B; pairs:
+      // the even CTA's counts both CTAs' copies, the odd CTA's is not used)
+      auto expect_stage = [&](int stage) {
+        if (!kPairMma || rank == 0) mbar_expect_tx(smem_u32(full_bar + stage), kPairMma ? 2 * STAGE_TX : STAGE_TX);
+      };
       auto load_a = [&](int stage, int kb, int mb) {
         int a_map, a_row;
         resolve_rows(p.amap, mb * BM, a_map, a_row);
-        tma_load_2d(smem_u32(sA + stage * A_TILE_BYTES), &tm.m[p.a_map0 + a_map], smem_u32(full_bar + stage),
-                    kb * BK, a_row);
+        load_box(smem_u32(sA + stage * A_TILE_BYTES), &tm.m[p.a_map0 + a_map], stage, kb * BK, a_row, false);
       };
-      // a box of B: into this CTA's stage, or (clusters) into the same stage of both CTAs
-      auto load_b_box = [&](uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1) {
-        if constexpr (CM > 1)
-          tma_load_2d_mc(dst, map, bar, c0, c1, kClusterMask);
-        else
-          tma_load_2d(dst, map, bar, c0, c1);
-      };
+      // this CTA's B rows of tile nb: all of them, or its half in a pair
       auto load_b = [&](int stage, int kb, int nb) {
+        const int row0 = nb * BN + (kPairMma ? rank * B_ROWS : 0);
         if constexpr (EPI == EPI_QKV && BN % 128 != 0) {
           int m0, r0, m1, r1;
-          resolve_rows(p.bmap, nb * BN, m0, r0);
-          resolve_rows(p.bmap, nb * BN + BN - 1, m1, r1);
-          if (m0 != m1) {   // the tile crosses a boundary between two of the matrices
-            for (int bx = rank; bx < BN / 32; bx += CM) {
+          resolve_rows(p.bmap, row0, m0, r0);
+          resolve_rows(p.bmap, row0 + B_ROWS - 1, m1, r1);
+          if (m0 != m1) {   // the rows cross a boundary between two of the matrices: 32-row boxes
+            for (int bx = MODE == kShareB ? rank : 0; bx < B_ROWS / 32; bx += CM) {
               int b_map, b_row;
-              resolve_rows(p.bmap, nb * BN + bx * 32, b_map, b_row);
-              load_b_box(smem_u32(sB + stage * B_TILE_BYTES + bx * 32 * 128), &tm.m[p.b32_map0 + b_map],
-                         smem_u32(full_bar + stage), kb * BK, b_row);
+              resolve_rows(p.bmap, row0 + bx * 32, b_map, b_row);
+              load_box(smem_u32(sB + stage * B_TILE_BYTES + bx * 32 * 128), &tm.m[p.b32_map0 + b_map], stage,
+                       kb * BK, b_row, true);
             }
             return;
           }
         }
 #pragma unroll
         for (int bx = 0; bx < B_BOXES; ++bx) {
-          if (CM > 1 && bx % CM != rank) continue;   // the other CTA of the cluster loads this box
+          if (MODE == kShareB && bx % 2 != rank) continue;   // the other CTA loads this box for both
           // (this thread's issue latency bounds the ring's lead over TMA latency: no divisions)
           int b_map, b_row;
           if constexpr (EPI == EPI_SWIGLU) {   // tile nb = [gate rows BN/2*nb.. | the same up rows]
-            b_map = bx;
+            b_map = kPairMma ? rank : bx;
             b_row = nb * B_BOX_ROWS;
           } else {
-            resolve_rows(p.bmap, nb * BN + bx * B_BOX_ROWS, b_map, b_row);
+            resolve_rows(p.bmap, row0 + bx * B_BOX_ROWS, b_map, b_row);
           }
-          load_b_box(smem_u32(sB + stage * B_TILE_BYTES + bx * B_BOX_ROWS * 128), &tm.m[p.b_map0 + b_map],
-                     smem_u32(full_bar + stage), kb * BK, b_row);
+          load_box(smem_u32(sB + stage * B_TILE_BYTES + bx * B_BOX_ROWS * 128), &tm.m[p.b_map0 + b_map], stage,
+                   kb * BK, b_row, true);
         }
       };
       // the first STAGES k-blocks' weight tiles go out before the dependency wait: the ring
@@ -406,7 +440,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const int kb0 = split * p.kb_per_split;
           const int kb1 = min(kb0 + p.kb_per_split, p.num_kb);
           for (int kb = kb0; kb < kb1 && pre < STAGES; ++kb, ++pre) {
-            mbar_expect_tx(smem_u32(full_bar + pre), STAGE_TX);
+            expect_stage(pre);
             if (p.weight_first == 1) load_a(pre, kb, mb);
             else load_b(pre, kb, nb);
           }
@@ -436,7 +470,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               else load_a(stage, kb, mb);
             } else {
               if (!mbar_wait(smem_u32(empty_bar + stage), phase ^ 1u, p.status, abort_flag)) { ok = false; break; }
-              mbar_expect_tx(smem_u32(full_bar + stage), STAGE_TX);
+              expect_stage(stage);
               load_a(stage, kb, mb);
               load_b(stage, kb, nb);
             }
@@ -453,14 +487,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (++stage == STAGES) { stage = 0; phase ^= 1u; }
           }
         }
-        if (!ok) {
-          // leave no copy in flight: wait (bounded) for the last load into every stage used
+        if (!ok && !(kPairMma && rank == 1)) {
+          // leave no copy in flight: wait (bounded) for the last load into every stage used (in
+          // a pair the even CTA's full barriers count the odd CTA's copies too, and the cluster
+          // barrier at the end keeps the odd CTA until then)
           for (int s = 0; s < STAGES; ++s)
             if (used_mask & (1u << s))
               mbar_wait_slow(smem_u32(full_bar + s), (last_parity >> s) & 1u, nullptr, nullptr, kWaitBudgetNs);
         }
       }
     }
+  } else if (warp == 1 && kPairMma && rank == 1) {
+    // the odd CTA of a pair: its products are issued by the even CTA
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA issuer
     // The whole warp walks the loop (operands stay warp-uniform) and one elected lane issues
@@ -468,8 +506,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // of what a 128 x 256 x 16 product runs, leaving little time for the waits between stages.
     const uint64_t dA = sdesc_sw128(smem_u32(sA), 16, 1024);
     const uint64_t dB = sdesc_sw128(smem_u32(sB), 16, 1024);
-    auto wait_all = [&](uint64_t* bar, uint32_t parity) {
-      const bool r = mbar_wait(smem_u32(bar), parity, p.status, abort_flag);
+    // remote = the barrier also receives arrivals from the other CTA of the pair (the wait
+    // acquires at cluster scope)
+    auto wait_all = [&](uint64_t* bar, uint32_t parity, bool remote = false) {
+      const bool r = kPairMma && remote ? mbar_wait<true>(smem_u32(bar), parity, p.status, abort_flag)
+                                      : mbar_wait(smem_u32(bar), parity, p.status, abort_flag);
       return __all_sync(0xffffffffu, r) != 0;
     };
     int stage = 0;
@@ -483,31 +524,43 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       unit_coords<CM>(p, u, rank, mb, nb, split);
       const int kb0 = split * p.kb_per_split;
       const int kb1 = min(kb0 + p.kb_per_split, p.num_kb);
-      if (!wait_all(tempty_bar + acc, acc_phase ^ 1u)) { ok = false; break; }
+      if (!wait_all(tempty_bar + acc, acc_phase ^ 1u, true)) { ok = false; break; }
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
       for (int kb = kb0; kb < kb1; ++kb) {
-        if (!wait_all(full_bar + stage, phase)) { ok = false; break; }
+        if (!wait_all(full_bar + stage, phase, true)) { ok = false; break; }
         tc_fence_after();
         const uint64_t ad = dA + static_cast<uint64_t>((stage * A_TILE_BYTES) >> 4);
         const uint64_t bd = dB + static_cast<uint64_t>((stage * B_TILE_BYTES) >> 4);
 #pragma unroll
-        for (int k = 0; k < BK / 16; ++k)   // 16 K elements = 32 bytes further along the row
-          tc_mma_bf16_warp(d_tmem, ad + 2 * k, bd + 2 * k, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+        for (int k = 0; k < BK / 16; ++k) {   // 16 K elements = 32 bytes further along the row
+          if constexpr (kPairMma)
+            tc_mma2_bf16_warp(d_tmem, ad + 2 * k, bd + 2 * k, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+          else
+            tc_mma_bf16_warp(d_tmem, ad + 2 * k, bd + 2 * k, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+        }
         issued = true;
-        if constexpr (CM > 1)
-          tc_commit_mc_warp(smem_u32(empty_bar + stage), kClusterMask);   // both CTAs' stage
+        if constexpr (kPairMma)
+          tc_commit2_mc_warp(smem_u32(empty_bar + stage), kBoth);   // both CTAs' stage is free
+        else if constexpr (MODE == kShareB)
+          tc_commit_mc_warp(smem_u32(empty_bar + stage), kBoth);    // both CTAs' copy of B read
         else
           tc_commit_warp(smem_u32(empty_bar + stage));
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
       if (!ok) break;
-      tc_commit_warp(smem_u32(tfull_bar + acc));
+      if constexpr (kPairMma)
+        tc_commit2_mc_warp(smem_u32(tfull_bar + acc), kBoth);   // both CTAs' rows are done
+      else
+        tc_commit_warp(smem_u32(tfull_bar + acc));
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
     if (!ok && issued) {
       // all products of the issuing lane must finish before the TMEM is released
-      tc_commit_warp(smem_u32(drain_bar));
+      if constexpr (kPairMma)
+        tc_commit2_mc_warp(smem_u32(drain_bar), 1);
+      else
+        tc_commit_warp(smem_u32(drain_bar));
       if (lane == 0) mbar_wait_slow(smem_u32(drain_bar), 0, nullptr, nullptr, kWaitBudgetNs);
       __syncwarp();
     }
@@ -727,7 +780,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(tempty_bar + acc));
+      if (lane == 0) {
+        if constexpr (kPairMma)
+          mbar_arrive_cluster(cluster_map(smem_u32(tempty_bar + acc), 0));   // the even CTA's
+        else
+          mbar_arrive(smem_u32(tempty_bar + acc));
+      }
       if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
     }
   }
@@ -740,19 +798,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    if constexpr (kPairMma)
+      tmem_dealloc2(tmem_base, TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 
-template <int BN, int EPI, int STAGES>
+template <int BN, int EPI, int STAGES, int MODE>
 constexpr size_t smem_bytes() {
-  return 1024 + STAGES * (A_TILE_BYTES + BN * BK * 2) + (2 * STAGES + 5) * 8 + 16;
+  return 1024 + STAGES * (A_TILE_BYTES + (MODE == kPair ? BN / 2 : BN) * BK * 2) + (2 * STAGES + 5) * 8 + 16;
 }
 
-template <int BN, int EPI, int STAGES, int CM = 1>
+template <int BN, int EPI, int STAGES, int MODE = kSingle>
 int launch(const Ctx& c, const TMaps& tm, Params p) {
-  auto kern = gemm_tc_kernel<BN, EPI, STAGES, CM>;
-  constexpr size_t smem = smem_bytes<BN, EPI, STAGES>();
+  constexpr int CM = MODE == kSingle ? 1 : 2;
+  auto kern = gemm_tc_kernel<BN, EPI, STAGES, MODE>;
+  constexpr size_t smem = smem_bytes<BN, EPI, STAGES, MODE>();
+  static_assert(smem <= 227 * 1024, "shared memory per CTA");
   static_assert(smem >= kTmemKernelMinSmem, "a TMEM-holding kernel must not share an SM with another");
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
@@ -793,12 +856,18 @@ int launch(const Ctx& c, const TMaps& tm, Params p) {
   return after_launch(c);
 }
 
-// Clusters of two CTAs sharing each weight tile, where the row blocks pair up.
+// Clusters of two CTAs on consecutive row blocks, where the row blocks pair up.
 bool use_clusters(int M) { return (M + BM - 1) / BM % 2 == 0; }
 
+// Clusters where the row blocks pair up: two-SM products at 256 columns (their rings hold
+// half of each B tile per stage, so 6 stages), multicast clusters at 224.
 template <int BN, int EPI, int STAGES>
 int launch_cl(const Ctx& c, const TMaps& tm, const Params& p, bool clusters) {
-  return clusters ? launch<BN, EPI, STAGES, 2>(c, tm, p) : launch<BN, EPI, STAGES, 1>(c, tm, p);
+  if (!clusters) return launch<BN, EPI, STAGES, kSingle>(c, tm, p);
+  if constexpr (BN == 256)
+    return launch<BN, EPI, 6, kPair>(c, tm, p);
+  else
+    return launch<BN, EPI, STAGES, kShareB>(c, tm, p);
 }
 
 // Rows of the weight boxes: 128, or the whole tile width (BN < 256), halved in clusters.
