@@ -90,6 +90,57 @@ def test_linear_bf16(api, M, N, K, out_f32):
     assert api.device_status() == 0
 
 
+# Shapes that select each tile form on a 152-SM GB300 (the row blocks pair up when M is a
+# multiple of 256): two-SM products on 256-column tiles (M = 256, N = 17448: 69 tiles of 256
+# in one round against 78 of 224 in two; the last tile holds 40 columns), B shared by
+# multicast on 224-column tiles (M = 256, N = 456: two full tiles and an 8-column one), and
+# one CTA per tile (M = 384: three row blocks).
+TILE_FORM_SHAPES = [(256, 17448, 256), (256, 456, 256), (384, 456, 256)]
+
+
+@pytest.mark.parametrize("M,N,K", TILE_FORM_SHAPES)
+@pytest.mark.parametrize("out_f32", [False, True])
+def test_linear_tile_forms(api, M, N, K, out_f32):
+    rng = _rng(M * 3 + N + K)
+    a = bf16_stored(rng.standard_normal((M, K)))
+    b = bf16_stored(0.02 * rng.standard_normal((N, K)))
+    c = torch.empty(M, N, dtype=torch.float32 if out_f32 else torch.bfloat16, device="cuda")
+    api.linear_bf16(to_dev(a), to_dev(b), c)
+    ref = oracle.linear(a.f64(), b.f64())
+    assert_close(f64(c), ref, 1e-3 if out_f32 else TOL["bf16"], f"linear {M}x{N}x{K}")
+    assert api.device_status() == 0
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 17408, 256), (256, 384, 256), (384, 384, 256)])
+def test_linear_residual_tile_forms(api, M, N, K):
+    # the same three forms with N % 128 == 0, as this entry point requires (17408: 68 tiles of
+    # 256 in one round against 78 of 224 in two; 384: a 224-column tile and a 160-column one)
+    rng = _rng(M * 5 + N + K)
+    a = bf16_stored(rng.standard_normal((M, K)))
+    b = bf16_stored(0.02 * rng.standard_normal((N, K)))
+    r = bf16_stored(rng.standard_normal((M, N)))
+    out = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    api.linear_residual(to_dev(a), to_dev(b), to_dev(r), out)
+    ref = r.f64() + oracle.linear(a.f64(), b.f64())
+    assert_close(f64(out), ref, TOL["bf16"], f"linear + residual {M}x{N}x{K}")
+    assert api.device_status() == 0
+
+
+@pytest.mark.parametrize("M,I,K", [(256, 384, 256), (384, 384, 256)])
+def test_linear_swiglu_tile_forms(api, M, I, K):
+    # M = 256: two-SM products (the even CTA holds the gate rows, the odd one the up rows);
+    # M = 384: one CTA per tile
+    rng = _rng(M * 7 + I + K)
+    x = bf16_stored(rng.standard_normal((M, K)))
+    wg = bf16_stored(0.05 * rng.standard_normal((I, K)))
+    wu = bf16_stored(0.05 * rng.standard_normal((I, K)))
+    a = torch.empty(M, I, dtype=torch.bfloat16, device="cuda")
+    api.linear_swiglu(to_dev(x), to_dev(wg), to_dev(wu), a)
+    ref = oracle.silu(oracle.linear(x.f64(), wg.f64())) * oracle.linear(x.f64(), wu.f64())
+    assert_close(f64(a), ref, TOL["bf16"], f"gate/up + SiLU*up {M}x{I}x{K}")
+    assert api.device_status() == 0
+
+
 def _attn_dims(api, H, G):
     return api.Dims(H * 128, H, G, 128, 128, 1e-5, torch.bfloat16)
 
