@@ -71,7 +71,7 @@ def test_prefill_tiny_fp32_config(api):
 
 
 @pytest.mark.parametrize("H,G,B,S", [(4, 2, 2, 200), (2, 2, 1, 128), (8, 1, 1, 300), (4, 4, 3, 65), (16, 1, 1, 140),
-                                     (32, 2, 1, 70)])
+                                     (32, 2, 1, 70), (4, 2, 3, 1), (4, 2, 1, 129)])
 def test_prefill_bf16_small(api, H, G, B, S):
     base = synth.WORKLOADS["gqa8b_bf16_b4_s4096"]
     wl = synth.scaled(base, d_model=256, n_heads=H, n_kv_heads=G, d_inter=384, B=B, S=S,
@@ -296,6 +296,16 @@ def test_decode_bf16_mqa_and_half_split_rope(api, H, G, rope):
     wl = synth.scaled(base, d_model=256, n_heads=H, n_kv_heads=G, d_inter=384, B=5, T_max=700, rope_style=rope,
                       name=f"decode_bf16_h{H}_g{G}_{rope}")
     _run_decode(api, wl, positions=[0, 130, 511, 650, 699])
+
+
+@pytest.mark.parametrize("B", [1, 70])
+def test_decode_bf16_token_tiles(api, B):
+    # the weight-streaming GEMMs take the tokens as the N = 64 operand: one token, and two token
+    # tiles with a ragged second one (70 = 64 + 6); positions over the whole cache, 0 included
+    base = synth.WORKLOADS["decode_gqa8b_bf16_b64_t4096"]
+    wl = synth.scaled(base, d_model=256, n_heads=8, n_kv_heads=2, d_inter=384, B=B, T_max=300, pos_lo=0, pos_hi=300,
+                      name=f"decode_bf16_b{B}_t300")
+    _run_decode(api, wl, positions=[0] if B == 1 else None)
 
 
 def test_decode_fp32_half_split_rope(api):
