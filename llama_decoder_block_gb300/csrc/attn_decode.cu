@@ -193,6 +193,9 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ TMA producer
+      // the cache is read once per step: evict-first keeps the segment partials and the step's
+      // activations in L2 while it streams through
+      const uint64_t kv_policy = l2_evict_first_policy();
       uint32_t tcount = 0, icount = 0;
       bool ok = true;
       for (long long pos = r0; pos < r1 && ok;) {
@@ -214,10 +217,10 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
           const uint32_t fb = smem_u32(kv_full + st);
           mbar_expect_tx(fb, 2 * KV_TILE);
           const int row = d.k_begin + t * KT;
-          tma_load_3d(smem_u32(sK + st * KV_TILE), &tmK, fb, 0, row, plane);
-          tma_load_3d(smem_u32(sK + st * KV_TILE + KV_CHUNK), &tmK, fb, 64, row, plane);
-          tma_load_3d(smem_u32(sV + st * KV_TILE), &tmV, fb, 0, row, plane);
-          tma_load_3d(smem_u32(sV + st * KV_TILE + KV_CHUNK), &tmV, fb, 64, row, plane);
+          tma_load_3d_hint(smem_u32(sK + st * KV_TILE), &tmK, fb, 0, row, plane, kv_policy);
+          tma_load_3d_hint(smem_u32(sK + st * KV_TILE + KV_CHUNK), &tmK, fb, 64, row, plane, kv_policy);
+          tma_load_3d_hint(smem_u32(sV + st * KV_TILE), &tmV, fb, 0, row, plane, kv_policy);
+          tma_load_3d_hint(smem_u32(sV + st * KV_TILE + KV_CHUNK), &tmV, fb, 64, row, plane, kv_policy);
         }
         ++icount;
       }

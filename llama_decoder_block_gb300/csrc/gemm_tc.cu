@@ -380,7 +380,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // CTA's full barrier (the even CTA's products read both CTAs' stages)
       // (kShareB: B boxes go to the same stage of both CTAs of the cluster)
       const uint32_t full_pair0 = kPairMma ? cluster_map(smem_u32(full_bar), 0) : 0u;
+      const uint64_t evict_first = EPI == EPI_PARTIAL ? l2_evict_first_policy() : 0;
       auto load_box = [&](uint32_t dst, const CUtensorMap* map, int stage, int c0, int c1, bool b_box) {
+        if (EPI == EPI_PARTIAL && !b_box) {
+          // the weight-streaming form reads each weight once per call: evict-first, so that the
+          // stream does not push the split partials out of L2 before the fixup kernel reads them
+          // (as dirty lines they would also be written back to HBM: ~8 µs of a decode step)
+          tma_load_2d_hint(dst, map, smem_u32(full_bar + stage), c0, c1, evict_first);
+          return;
+        }
         if (kPairMma && rank == 1)
           tma_load_2d_pair(dst, map, full_pair0 + static_cast<uint32_t>(stage) * 8u, c0, c1);
         else if (MODE == kShareB && b_box)
