@@ -2,7 +2,7 @@
 
 The GPU runs every step over all rows in the launch shape the benchmark uses; the oracle
 recomputes sampled rows (GEMM rows are independent, attention rows need only their own keys).
-One step at a time there is a single bf16 rounding between oracle and GPU, so the north-star
+One step at a time there is a single bf16 rounding between oracle and GPU, so the bf16
 tolerance 2e-2 * (1 + |ref|) holds elementwise, and so does the tighter one-ulp bound below.
 """
 import numpy as np
