@@ -286,11 +286,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   constexpr int B_BOX_ROWS =
       EPI == EPI_SWIGLU ? BN / 2 : B_ROWS % 128 == 0 ? 128 : (MODE == kShareB ? BN / 2 : B_ROWS);
   constexpr int B_BOXES = B_ROWS / B_BOX_ROWS;
-  static_assert(MODE == kSingle || (EPI != EPI_PARTIAL && (MODE == kShareB ? B_BOXES % 2 == 0 : BN % 128 == 0)),
+  static_assert(MODE == kSingle || (EPI != EPI_PARTIAL && (MODE == kShareB ? B_BOXES % 2 == 0
+                                                                           : (BN % 128 == 0 || EPI == EPI_SWIGLU))),
                 "clusters split B into whole boxes, one half per CTA");
   constexpr uint16_t kBoth = 3;                 // cluster ranks 0 and 1
   constexpr uint32_t STAGE_TX = A_TILE_BYTES + B_TILE_BYTES;
-  constexpr uint32_t TMEM_COLS = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
+  // columns per accumulator: the tile width rounded up to 32, so that the second accumulator
+  // starts on a 32-column boundary (256 for 240-column tiles)
+  constexpr int ACC_COLS = (BN + 31) / 32 * 32;
+  constexpr uint32_t TMEM_COLS = 2 * ACC_COLS <= 32    ? 32
+                                 : 2 * ACC_COLS <= 64  ? 64
+                                 : 2 * ACC_COLS <= 128 ? 128
+                                 : 2 * ACC_COLS <= 256 ? 256
+                                                       : 512;
   constexpr uint32_t IDESC = idesc_bf16(kPairMma ? 2 * BM : BM, BN, false);
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128 and 256");
 
@@ -534,7 +542,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int kb1 = min(kb0 + p.kb_per_split, p.num_kb);
       if (!wait_all(tempty_bar + acc, acc_phase ^ 1u, true)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * ACC_COLS);
       for (int kb = kb0; kb < kb1; ++kb) {
         if (!wait_all(full_bar + stage, phase, true)) { ok = false; break; }
         tc_fence_after();
@@ -584,7 +592,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       unit_coords<CM>(p, u, rank, mb, nb, split);
       if (!mbar_wait(smem_u32(tfull_bar + acc), acc_phase, p.status, abort_flag)) break;
       tc_fence_after();
-      const uint32_t t_acc = tmem_base + t_lane + static_cast<uint32_t>(acc * BN);
+      const uint32_t t_acc = tmem_base + t_lane + static_cast<uint32_t>(acc * ACC_COLS);
       const int m = mb * BM + row;
       uint32_t r[32];
       float v[32];
@@ -650,9 +658,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       } else if constexpr (EPI == EPI_SWIGLU) {
         // columns [0, BN/2) of the tile are gate rows BN/2*nb.., [BN/2, BN) the matching up rows
         constexpr int HALF = BN / 2;
-        static_assert(HALF % 32 == 0, "gate/up halves of whole 32-column chunks");
+        static_assert(HALF % 8 == 0, "gate/up halves of whole 8-column chunks");
+        if constexpr (HALF % 32 != 0) {
+          // 120-column halves (240-column tiles): 8 columns at a time, the up half starting at
+          // column 120 of the accumulator
 #pragma unroll 1
-        for (int c = 0; c < HALF / 32; ++c) {
+          for (int c = 0; c < HALF / 8; ++c) {
+            uint32_t g8[8], u8[8];
+            tmem_ld8(t_acc + c * 8, g8);
+            tmem_ld8(t_acc + HALF + c * 8, u8);
+            const int n0 = nb * HALF + c * 8;
+            const int valid = min(8, p.N - n0);
+            if (m < p.M && valid > 0) {
+              float w8[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) w8[i] = silu_f(__uint_as_float(g8[i])) * __uint_as_float(u8[i]);
+              __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + m * p.ldo + n0;
+              if (valid == 8 && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+                uint4 w;
+                w.x = pack_bf16(w8[0], w8[1]);
+                w.y = pack_bf16(w8[2], w8[3]);
+                w.z = pack_bf16(w8[4], w8[5]);
+                w.w = pack_bf16(w8[6], w8[7]);
+                *reinterpret_cast<uint4*>(dst) = w;
+              } else {
+                for (int i = 0; i < valid; ++i) dst[i] = __float2bfloat16_rn(w8[i]);
+              }
+            }
+          }
+        }
+#pragma unroll 1
+        for (int c = 0; c < (HALF % 32 == 0 ? HALF / 32 : 0); ++c) {
           uint32_t u[32];
           tmem_ld32(t_acc + c * 32, r);
           tmem_ld32(t_acc + HALF + c * 32, u);
@@ -893,6 +929,17 @@ int tile_width_for(int M, int N, int num_sms) {
   return round_cost(M, (N + 223) / 224, 224, num_sms) < round_cost(M, (N + 255) / 256, 256, num_sms) ? 224 : 256;
 }
 
+// Gate/up tile width in two-SM pairs: 240 (120 gate + 120 up columns) when its rounds of pair
+// units are at least 3 % narrower in total than those of 256-column tiles, else 256.
+int swiglu_pair_width(int M, int I, int num_sms) {
+  const long long pairs_m = (M + BM - 1) / BM / 2, clusters = std::max(1, num_sms / 2);
+  auto cost = [&](int half) {
+    const long long units = pairs_m * ((I + half - 1) / half);
+    return (units + clusters - 1) / clusters * (2 * half);
+  };
+  return cost(120) * 100 <= cost(128) * 97 ? 240 : 256;
+}
+
 // RMSNorm in the prologue: A (the tensor map at a_map0) is built on n.xn, which the prologue
 // fills with RMSNorm(X).
 void set_prologue(Params& p, const void* X, const NormPro& n) {
@@ -972,13 +1019,19 @@ int gemm_residual(const Ctx& c, const void* X, const void* W, const void* resid,
 
 int gemm_swiglu(const Ctx& c, const void* X, const void* Wg, const void* Wu, void* out, int M, int I, int K,
                 const NormPro* norm) {
-  // kernel N runs over 256-column tiles, each = 128 gate rows + the same 128 up rows (measured:
-  // 240-column tiles, which fill the SM-count rounds better at I = 11008, M = 2048, run slower)
+  // kernel N runs over tiles of `half` gate rows + the same `half` up rows: 256 columns, or in
+  // two-SM pairs 240 when that saves at least 3 % of the rounds' width (I = 11008, M = 2048: 10
+  // rounds of 736 pair units at 240 against 10 of 688 at 256, the last one nearly empty;
+  // measured 217.9-218.1 against 218.6-220.4 us).  Without pairs 240-column tiles ran slower
+  // (each CTA then takes all 240 weight rows per k-block).
+  const bool cl = use_clusters(M);
+  const int bn = cl && swiglu_pair_width(M, I, c.num_sms) == 240 ? 240 : 256;
+  const int half = bn / 2;
   TMaps tm{};
-  if (!make_tmap_2d(&tm.m[0], norm ? norm->xn : X, K, M, K, 128) || !make_tmap_2d(&tm.m[1], Wg, K, I, K, 128) ||
-      !make_tmap_2d(&tm.m[2], Wu, K, I, K, 128))
+  if (!make_tmap_2d(&tm.m[0], norm ? norm->xn : X, K, M, K, 128) || !make_tmap_2d(&tm.m[1], Wg, K, I, K, half) ||
+      !make_tmap_2d(&tm.m[2], Wu, K, I, K, half))
     return LLAMA_ERR_INVALID_ARG;
-  Params p = base_params(M, 2 * ((I + 127) / 128) * 128, K, 256);
+  Params p = base_params(M, 2 * ((I + half - 1) / half) * half, K, bn);
   if (norm != nullptr) set_prologue(p, X, *norm);
   p.N = I;   // output width (used by the epilogue's bounds)
   p.a_map0 = 0;
@@ -986,7 +1039,8 @@ int gemm_swiglu(const Ctx& c, const void* X, const void* Wg, const void* Wu, voi
   p.n_maps = 3;
   p.out = out;
   p.ldo = I;
-  return launch_cl<256, EPI_SWIGLU, 4>(c, tm, p, use_clusters(M));
+  if (bn == 240) return launch<240, EPI_SWIGLU, 7, kPair>(c, tm, p);
+  return launch_cl<256, EPI_SWIGLU, 4>(c, tm, p, cl);
 }
 
 int gemm_qkv_rope(const Ctx& c, const void* X, const void* Wq, const void* Wk, const void* Wv, int B, int S, int K,

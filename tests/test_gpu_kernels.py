@@ -126,9 +126,11 @@ def test_linear_residual_tile_forms(api, M, N, K):
     assert api.device_status() == 0
 
 
-@pytest.mark.parametrize("M,I,K", [(256, 384, 256), (384, 384, 256)])
+@pytest.mark.parametrize("M,I,K", [(256, 384, 256), (256, 9728, 256), (384, 384, 256)])
 def test_linear_swiglu_tile_forms(api, M, I, K):
-    # M = 256: two-SM products (the even CTA holds the gate rows, the odd one the up rows);
+    # M = 256: two-SM products (the even CTA holds the gate rows, the odd one the up rows), in
+    # 240-column tiles at I = 384 (4 tiles, the last with 24 of its 120 columns valid) and in
+    # 256-column tiles at I = 9728 (76 tiles: one round of pairs, where 240 would take two);
     # M = 384: one CTA per tile
     rng = _rng(M * 7 + I + K)
     x = bf16_stored(rng.standard_normal((M, K)))
