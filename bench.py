@@ -55,7 +55,7 @@ class L2Flush:
 # dram__bytes_write.sum from one ncu capture of that kernel alone at the headline shapes
 # (`bench.py --case NAME`), keyed by kernel and the sha1 of the source file it was measured
 # on; a changed source makes the figure stale (reported as null).
-NCU_TRAFFIC = {("gate_up_swiglu_gemm", "9f992eb3b4b6"): 232772608}
+NCU_TRAFFIC = {("gate_up_swiglu_gemm", "004dd89b26bf"): 232772608}
 
 
 def parse():

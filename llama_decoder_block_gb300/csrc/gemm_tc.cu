@@ -281,8 +281,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   constexpr int B_TILE_BYTES = B_ROWS * BK * 2;
   // B arrives in 128-row boxes, or as one box of all its rows when that is not a multiple of
   // 128 (<= 256), as two halves in kShareB clusters (each CTA loads one for both); gate/up
-  // tiles: 128 gate rows, then the same 128 up rows (in a pair, the even CTA holds the gate
-  // rows, the odd one the up rows)
+  // tiles: BN/2 gate rows (128, or 120 in 240-column pairs), then the same up rows (in a pair,
+  // the even CTA holds the gate rows, the odd one the up rows)
   constexpr int B_BOX_ROWS =
       EPI == EPI_SWIGLU ? BN / 2 : B_ROWS % 128 == 0 ? 128 : (MODE == kShareB ? BN / 2 : B_ROWS);
   constexpr int B_BOXES = B_ROWS / B_BOX_ROWS;
